@@ -1,0 +1,272 @@
+/*
+ * tp.h -- C ABI of the GB300 tensor-parallel sharded projection library (libtp.so).
+ *
+ * The method (diffusers documentation, "Tensor parallelism" page): every
+ * weight matrix of a transformer block is split across tp_degree ranks,
+ * either "colwise" (output features, weight dim 0: each rank computes a slice
+ * of the output) or "rowwise" (input features, weight dim 1: each rank
+ * computes a partial sum).  Fused projections are split block by block.  The
+ * slices are joined at the layer boundary: concatenation (AllGather) for
+ * colwise, summation (AllReduce) for rowwise.
+ *
+ * This library runs all tp_degree logical ranks on ONE GPU.  Every rank's
+ * shard lives in its own buffer, every rank's GEMM runs inside one kernel
+ * launch, and the joins happen in device memory inside the kernels.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - Layout: every matrix is row-major and dense unless a leading dimension is
+ *   given.  Weights use the nn.Linear layout [out_features, in_features];
+ *   activations are [tokens, features].  Elements are bf16 (raw 16-bit
+ *   patterns) unless stated; fp32 where stated.
+ * - Ownership: the caller allocates and owns every buffer (inputs, outputs and
+ *   workspace).  The library allocates no memory and keeps no pointer after a
+ *   call returns.
+ * - Asynchrony: kernels are enqueued on `stream` (a cudaStream_t; NULL is the
+ *   legacy default stream) and the call returns without waiting.  Buffers
+ *   must stay valid until the stream reaches that point.
+ * - Validation: every argument is checked on the host before anything is
+ *   copied or launched; a rejected call has no effect on device memory.  The
+ *   plan checks follow the page's §Constraints and verification ("check both
+ *   before loading or sharding any weight").
+ * - Errors: a call returns a tp_status; TP_OK means the work was enqueued.
+ *   tp_last_error() gives a message for the calling thread's last failure.
+ *   Nothing falls back silently to another path (§Limitations: unsupported
+ *   options raise instead of quietly doing something else).
+ * - Device: the current CUDA device of the calling thread.  Requires sm_103a
+ *   (GB300) for the GEMM entry points.
+ */
+#ifndef TP_H_
+#define TP_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define TP_API __attribute__((visibility("default")))
+#else
+#define TP_API
+#endif
+
+typedef struct CUstream_st* tp_stream_t; /* same type as cudaStream_t */
+
+typedef enum {
+  TP_OK = 0,
+  TP_ERR_INVALID_ARG = 1,         /* null pointer, negative size, rank outside [0, tp_degree), ... */
+  TP_ERR_HEADS_NOT_DIVISIBLE = 2, /* tp_degree does not divide the attention-head count */
+  TP_ERR_SPLIT_NOT_DIVISIBLE = 3, /* a packed block is not divisible by tp_degree on its own */
+  TP_ERR_SPLIT_SUM = 4,           /* packed block sizes do not add up to the sharded dimension */
+  TP_ERR_NOT_WHOLE_HEADS = 5,     /* a rank's part of a head-structured block is not whole heads */
+  TP_ERR_ALIGNMENT = 6,           /* a pointer or row stride the kernels need 16-byte aligned is not */
+  TP_ERR_NOT_PINNED = 7,          /* a host source pointer is pageable (not page-locked) memory */
+  TP_ERR_WORKSPACE = 8,           /* workspace missing or smaller than tp_rowwise_workspace_bytes() */
+  TP_ERR_CUDA = 9,                /* a CUDA runtime call failed (message in tp_last_error) */
+  TP_ERR_TIMEOUT = 10,            /* a kernel gave up waiting on an internal barrier (tp_device_status) */
+  TP_ERR_UNSUPPORTED = 11         /* valid plan outside what this build implements (e.g. tp_degree > 16) */
+} tp_status;
+
+typedef enum { TP_COLWISE = 0, TP_ROWWISE = 1 } tp_style;
+typedef enum { TP_GATHER = 0, TP_REDUCE = 1 } tp_combine_mode;
+typedef enum { TP_ACT_NONE = 0, TP_ACT_GELU_TANH = 1, TP_ACT_SWIGLU = 2 } tp_act;
+typedef enum {
+  TP_REDUCE_NONE = 0,      /* write every rank's fp32 partial; join later with tp_combine(TP_REDUCE) */
+  TP_REDUCE_WORKSPACE = 1, /* fp32 partials to a workspace; the last rank to finish a tile sums them */
+  TP_REDUCE_ACCUM = 2      /* each tile's ranks accumulate in turn into one fp32 on-chip accumulator */
+} tp_reduce_mode;
+
+#define TP_MAX_DEGREE 16 /* largest tp_degree the GEMM entry points accept */
+#define TP_MAX_SPLITS 16 /* largest number of packed blocks in one weight */
+
+/* ------------------------------------------------------------------------ */
+/* Plan                                                                      */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * tp_validate -- check a sharding plan for one weight [rows, cols].
+ *
+ * "Tensor parallelism" page: §Load a sharded model (tp_degree must divide the
+ * number of attention heads), §Fused projections (packed blocks, absolute
+ * sizes as stored in _tp_packed_col_blocks / _tp_packed_row_blocks) and
+ * §Constraints and verification (every packed block divisible by tp_degree
+ * on its own).  Checks, in order:
+ *   1. TP_ERR_INVALID_ARG: tp_degree >= 1, rows/cols/num_heads/head_dim >= 0,
+ *      style valid, 0 <= n_splits <= TP_MAX_SPLITS, fused_splits non-NULL when
+ *      n_splits > 0, every split > 0.
+ *   2. TP_ERR_HEADS_NOT_DIVISIBLE: num_heads > 0 and num_heads % tp_degree != 0.
+ *   3. TP_ERR_SPLIT_SUM: the splits do not add up to the sharded dimension
+ *      (rows for TP_COLWISE, cols for TP_ROWWISE).
+ *   4. TP_ERR_SPLIT_NOT_DIVISIBLE: some split % tp_degree != 0.
+ *   5. TP_ERR_NOT_WHOLE_HEADS: head_dim > 0 and some (split / tp_degree) %
+ *      head_dim != 0 (the sharded dimension is made of heads of head_dim).
+ * fused_splits: host array of n_splits absolute block sizes along the sharded
+ * dimension, in packed order; NULL/0 means one block (a plain split).
+ * Pure host function; touches no device.
+ */
+TP_API tp_status tp_validate(int64_t rows, int64_t cols, tp_style style, int tp_degree, int64_t num_heads,
+                      int64_t head_dim, const int64_t* fused_splits, int n_splits);
+
+/*
+ * tp_shard_shape -- shape of every rank's dense shard after tp_validate's
+ * checks 1, 3 and 4: [rows / tp_degree, cols] for TP_COLWISE, [rows, cols /
+ * tp_degree] for TP_ROWWISE.  out_rows/out_cols: host pointers, written on
+ * TP_OK only.  Pure host function.
+ */
+TP_API tp_status tp_shard_shape(int64_t rows, int64_t cols, tp_style style, int tp_degree,
+                         const int64_t* fused_splits, int n_splits, int64_t* out_rows, int64_t* out_cols);
+
+/* ------------------------------------------------------------------------ */
+/* Shard extraction                                                          */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * tp_plan_shard -- copy rank `rank`'s slice of a bf16 weight into a dense
+ * device buffer.
+ *
+ * "Tensor parallelism" page, §Load a sharded model: each rank reads only its
+ * own slice of every weight and places it directly on its device, so no
+ * full-size weight is ever staged there; §Limitations: enable_parallelism()
+ * shards a model already in memory.  Both are this call: `weight` may be
+ * page-locked host memory (the slice is read over the CPU-GPU link straight
+ * into `dev_out`; nothing else reaches the device) or device memory (a
+ * device-to-device copy).  Pageable host memory is rejected with
+ * TP_ERR_NOT_PINNED.
+ *
+ * Slice definition (§Colwise and rowwise, §Fused projections): with packed
+ * blocks of sizes s_0..s_{n-1} at offsets o_b along the sharded dimension,
+ * block b contributes [o_b + rank*s_b/p, o_b + (rank+1)*s_b/p) and the parts
+ * are concatenated in block order.  TP_COLWISE slices rows, TP_ROWWISE slices
+ * columns.  A fused QKV weight with splits {H,H,H} thus gives rank r the rows
+ * [Q_r; K_r; V_r] of whole heads; a gate/up weight with {F,F} gives
+ * [gate_r; up_r].
+ *
+ * weight:  bf16 [rows, cols] row-major (host page-locked or device).
+ * dev_out: device buffer of tp_shard_shape() elements, dense row-major.
+ * num_heads/head_dim: as in tp_validate (0 to skip those checks).
+ * The copy is bit-exact (any 16-bit pattern, NaN payloads included).
+ * Errors: everything tp_validate returns, TP_ERR_INVALID_ARG for NULL
+ * pointers with a non-empty shard or a dev_out that is not device memory,
+ * TP_ERR_NOT_PINNED, TP_ERR_CUDA.
+ */
+TP_API tp_status tp_plan_shard(const void* weight, int64_t rows, int64_t cols, tp_style style, int tp_degree, int rank,
+                        const int64_t* fused_splits, int n_splits, int64_t num_heads, int64_t head_dim,
+                        void* dev_out, tp_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Sharded projections                                                       */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * tp_linear_colwise -- every rank's colwise projection in one launch:
+ *     Y_r = act(X . W_r^T + b_r)      for r = 0 .. tp_degree-1
+ *
+ * "Tensor parallelism" page, §Colwise and rowwise: the input X is replicated
+ * and each rank computes its slice of the output features; the output stays
+ * sharded for the rowwise projection that follows.
+ *
+ * x:           device bf16 [T, K] (shared by every rank).
+ * w_shards:    host array of tp_degree device pointers, each bf16 [N_r, K]
+ *              (the dense shards tp_plan_shard writes).
+ * bias_shards: NULL, or host array of tp_degree device pointers (each NULL or
+ *              bf16 [N_r], sharded like the weight's rows).
+ * act:         TP_ACT_NONE / TP_ACT_GELU_TANH (0.5x(1+tanh(sqrt(2/pi)(x+0.044715x^3))))
+ *              / TP_ACT_SWIGLU (the shard is [gate_r; up_r], N_r even, and
+ *              Y_r = silu(gate) * up has N_r/2 columns).  The activation is
+ *              applied to the fp32 accumulator before rounding to bf16.
+ * y_shards:    host array of tp_degree device pointers, each bf16 [T, N_out]
+ *              with row stride ldy elements (N_out = N_r, or N_r/2 for SwiGLU).
+ *              ldy = 0 means N_out (dense).  Passing y_shards[r] = Y + r*N_out
+ *              with ldy = tp_degree*N_out writes the gathered (AllGather)
+ *              output [T, tp_degree*N_out] directly.
+ * Accumulation is fp32; outputs are rounded to nearest-even bf16.
+ * Alignment (TP_ERR_ALIGNMENT): K % 8 == 0, N_out % 8 == 0, ldy % 8 == 0 and
+ * every pointer 16-byte aligned.  tp_degree <= TP_MAX_DEGREE.
+ * T == 0 or N_r == 0 enqueues nothing and returns TP_OK.
+ */
+TP_API tp_status tp_linear_colwise(const void* x, const void* const* w_shards, const void* const* bias_shards, tp_act act,
+                            int tp_degree, int64_t T, int64_t K, int64_t N_r, void* const* y_shards, int64_t ldy,
+                            tp_stream_t stream);
+
+/*
+ * tp_linear_rowwise -- every rank's rowwise projection and the sum of the
+ * partials in one launch:
+ *     P_r = X_r . W_r^T ,  Z = sum_r P_r (+ bias, once)
+ *
+ * "Tensor parallelism" page, §Colwise and rowwise: each rank computes a
+ * partial sum from its slice of the input features, and one AllReduce at the
+ * block boundary (after the colwise -> rowwise pair) rebuilds the result.
+ * The partials are summed in rank order, in fp32.
+ *
+ * x_shards: host array of tp_degree device pointers, each bf16 [T, K_r]
+ *           (rank r's slice of the input features, e.g. the colwise output).
+ * w_shards: host array of tp_degree device pointers, each bf16 [N, K_r].
+ * bias:     NULL or device bf16 [N]; added once, after the sum.
+ * mode:
+ *   TP_REDUCE_ACCUM: for each output tile, rank 0's, then rank 1's, ...
+ *     products accumulate into one fp32 tensor-memory accumulator; out is
+ *     bf16 [T, N].  No workspace (ws_bytes may be 0).
+ *   TP_REDUCE_WORKSPACE: each rank's fp32 partial tile goes to `workspace`;
+ *     the last rank to finish a tile (atomic per-tile counter, no spinning)
+ *     sums the tp_degree partials in rank order and writes bf16 [T, N] to out.
+ *     Needs ws_bytes >= tp_rowwise_workspace_bytes(...).  The counters are
+ *     cleared on `stream` by the call itself.
+ *   TP_REDUCE_NONE: out is fp32 [tp_degree][T][N], rank r's partial (the bias,
+ *     if any, is added to rank 0's partial only); join with tp_combine.
+ * Alignment (TP_ERR_ALIGNMENT): K_r % 8 == 0, N % 8 == 0, pointers 16-byte
+ * aligned.  tp_degree <= TP_MAX_DEGREE.  T == 0 or N == 0 enqueues nothing.
+ * Calls that share a workspace must not overlap on the GPU.
+ */
+TP_API tp_status tp_linear_rowwise(const void* const* x_shards, const void* const* w_shards, const void* bias, int tp_degree,
+                            int64_t T, int64_t K_r, int64_t N, tp_reduce_mode mode, void* workspace, size_t ws_bytes,
+                            void* out, tp_stream_t stream);
+
+/* Bytes of device workspace tp_linear_rowwise needs for `mode` (0 unless TP_REDUCE_WORKSPACE). */
+TP_API size_t tp_rowwise_workspace_bytes(int tp_degree, int64_t T, int64_t N, tp_reduce_mode mode);
+
+/* ------------------------------------------------------------------------ */
+/* Join                                                                      */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * tp_combine -- join per-rank results in device memory (the page's opening
+ * paragraph: "an AllReduce or AllGather at the layer boundary").
+ *   TP_GATHER: partials[r] is bf16 [T, N_each]; out is bf16 [T, tp_degree*N_each]
+ *              with columns [r*N_each, (r+1)*N_each) taken from rank r.  Bit-exact.
+ *   TP_REDUCE: partials[r] is fp32 [T, N_each]; out is bf16 [T, N_each] =
+ *              round_nearest_even(sum_r partials[r]), summed in rank order in fp32.
+ * partials: host array of tp_degree device pointers.  out: device buffer.
+ * Any alignment is accepted (16-byte aligned rows take the vector path).
+ */
+TP_API tp_status tp_combine(tp_combine_mode mode, const void* const* partials, int tp_degree, int64_t T, int64_t N_each,
+                     void* out, tp_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Diagnostics                                                               */
+/* ------------------------------------------------------------------------ */
+
+/* Message for the calling thread's last failed call ("" if none).  Valid until the thread's next call. */
+TP_API const char* tp_last_error(void);
+
+/* Name of a status code ("TP_OK", "TP_ERR_ALIGNMENT", ...). */
+TP_API const char* tp_status_name(tp_status status);
+
+/*
+ * tp_device_status -- synchronise `stream`, then report whether any kernel of
+ * this library on the current device gave up on an internal wait (every wait
+ * is bounded; a kernel that gives up records it and exits cleanly).  Returns
+ * TP_ERR_TIMEOUT and clears the record if so, TP_ERR_CUDA if the stream
+ * reported an error, TP_OK otherwise.
+ */
+TP_API tp_status tp_device_status(tp_stream_t stream);
+
+/* Library ABI version (major * 100 + minor). */
+TP_API int tp_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TP_H_ */

@@ -1,0 +1,264 @@
+"""GB300-native tensor-parallel sharded projections: a thin binding over libtp.so.
+
+Every function here has the name of the C entry point it calls (see
+``include/tp.h``) and does argument marshalling only: it checks dtypes,
+allocates outputs with PyTorch when the caller passes none, and hands raw
+pointers and the current CUDA stream to the library.  All computation runs in
+the library's CUDA kernels; there is no other path.  If ``libtp.so`` has not
+been built, importing this package raises ImportError.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Sequence
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libtp.so")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(
+        f"{LIB_PATH} is missing: build it with `python -m tensor_sharded_linear_tp_gb300.build` "
+        "(the CUDA library is the only implementation)")
+
+lib = ctypes.CDLL(LIB_PATH)
+
+_i64 = ctypes.c_int64
+_vp = ctypes.c_void_p
+_status = ctypes.c_int
+
+# Status codes and enums, mirrored from include/tp.h.
+TP_OK = 0
+STATUS_NAMES = ["TP_OK", "TP_ERR_INVALID_ARG", "TP_ERR_HEADS_NOT_DIVISIBLE", "TP_ERR_SPLIT_NOT_DIVISIBLE",
+                "TP_ERR_SPLIT_SUM", "TP_ERR_NOT_WHOLE_HEADS", "TP_ERR_ALIGNMENT", "TP_ERR_NOT_PINNED",
+                "TP_ERR_WORKSPACE", "TP_ERR_CUDA", "TP_ERR_TIMEOUT", "TP_ERR_UNSUPPORTED"]
+STYLES = {"colwise": 0, "rowwise": 1}
+ACTS = {"none": 0, "gelu_tanh": 1, "swiglu": 2}
+REDUCE_MODES = {"none": 0, "workspace": 1, "accum": 2}
+COMBINE_MODES = {"gather": 0, "reduce": 1}
+MAX_DEGREE = 16
+MAX_SPLITS = 16
+
+_SIGS = {
+    "tp_validate": (_status, [_i64, _i64, ctypes.c_int, ctypes.c_int, _i64, _i64, ctypes.POINTER(_i64), ctypes.c_int]),
+    "tp_shard_shape": (_status, [_i64, _i64, ctypes.c_int, ctypes.c_int, ctypes.POINTER(_i64), ctypes.c_int,
+                                 ctypes.POINTER(_i64), ctypes.POINTER(_i64)]),
+    "tp_plan_shard": (_status, [_vp, _i64, _i64, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.POINTER(_i64),
+                                ctypes.c_int, _i64, _i64, _vp, _vp]),
+    "tp_linear_colwise": (_status, [_vp, ctypes.POINTER(_vp), ctypes.POINTER(_vp), ctypes.c_int, ctypes.c_int, _i64,
+                                    _i64, _i64, ctypes.POINTER(_vp), _i64, _vp]),
+    "tp_linear_rowwise": (_status, [ctypes.POINTER(_vp), ctypes.POINTER(_vp), _vp, ctypes.c_int, _i64, _i64, _i64,
+                                    ctypes.c_int, _vp, ctypes.c_size_t, _vp, _vp]),
+    "tp_rowwise_workspace_bytes": (ctypes.c_size_t, [ctypes.c_int, _i64, _i64, ctypes.c_int]),
+    "tp_combine": (_status, [ctypes.c_int, ctypes.POINTER(_vp), ctypes.c_int, _i64, _i64, _vp, _vp]),
+    "tp_last_error": (ctypes.c_char_p, []),
+    "tp_status_name": (ctypes.c_char_p, [ctypes.c_int]),
+    "tp_device_status": (_status, [_vp]),
+    "tp_abi_version": (ctypes.c_int, []),
+}
+for _name, (_res, _args) in _SIGS.items():
+    _f = getattr(lib, _name)
+    _f.restype = _res
+    _f.argtypes = _args
+
+EXPORTED = tuple(_SIGS)
+
+
+class TPError(RuntimeError):
+    """A libtp call returned a status other than TP_OK."""
+
+    def __init__(self, status: int, message: str):
+        self.status = status
+        self.name = STATUS_NAMES[status] if 0 <= status < len(STATUS_NAMES) else f"status {status}"
+        super().__init__(message or self.name)
+
+
+def _check(status: int) -> None:
+    if status != TP_OK:
+        raise TPError(status, lib.tp_last_error().decode())
+
+
+def _splits(fused_splits):
+    if not fused_splits:
+        return None, 0
+    arr = (_i64 * len(fused_splits))(*[int(s) for s in fused_splits])
+    return arr, len(fused_splits)
+
+
+def _ptrs(tensors):
+    return (_vp * len(tensors))(*[_ptr(t) for t in tensors])
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        if not torch.cuda.is_available():
+            return None
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _need_bf16(name, t):
+    if t.dtype != torch.bfloat16:
+        raise TypeError(f"{name} must be bfloat16, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+# ---------------------------------------------------------------------------
+# Plan
+# ---------------------------------------------------------------------------
+
+def tp_validate(rows: int, cols: int, style: str, tp_degree: int, num_heads: int = 0, head_dim: int = 0,
+                fused_splits: Sequence[int] | None = None) -> None:
+    """Raise TPError unless the plan is valid (tp_degree divides the heads, blocks divide, whole heads)."""
+    arr, n = _splits(fused_splits)
+    _check(lib.tp_validate(rows, cols, STYLES[style], tp_degree, num_heads, head_dim, arr, n))
+
+
+def tp_shard_shape(rows: int, cols: int, style: str, tp_degree: int,
+                   fused_splits: Sequence[int] | None = None) -> tuple[int, int]:
+    arr, n = _splits(fused_splits)
+    r, c = _i64(), _i64()
+    _check(lib.tp_shard_shape(rows, cols, STYLES[style], tp_degree, arr, n, ctypes.byref(r), ctypes.byref(c)))
+    return r.value, c.value
+
+
+# ---------------------------------------------------------------------------
+# Shard extraction
+# ---------------------------------------------------------------------------
+
+def tp_plan_shard(weight: torch.Tensor, style: str, tp_degree: int, rank: int,
+                  fused_splits: Sequence[int] | None = None, num_heads: int = 0, head_dim: int = 0,
+                  out: torch.Tensor | None = None, device=None, stream=None) -> torch.Tensor:
+    """Rank ``rank``'s dense shard of a bf16 weight, on the GPU.
+
+    ``weight`` is a bf16 [rows, cols] tensor in page-locked host memory
+    (shard-on-read: only the slice crosses to the device) or on the GPU.
+    """
+    _need_bf16("weight", weight)
+    rows, cols = weight.shape
+    arr, n = _splits(fused_splits)
+    if out is None:
+        shape = tp_shard_shape(rows, cols, style, tp_degree, fused_splits)
+        dev = device if device is not None else (weight.device if weight.is_cuda else torch.device("cuda"))
+        out = torch.empty(shape, dtype=torch.bfloat16, device=dev)
+    _check(lib.tp_plan_shard(_ptr(weight), rows, cols, STYLES[style], tp_degree, rank, arr, n, num_heads, head_dim,
+                             _ptr(out), _stream(stream)))
+    return out
+
+
+# ---------------------------------------------------------------------------
+# Projections
+# ---------------------------------------------------------------------------
+
+def tp_linear_colwise(x: torch.Tensor, w_shards: Sequence[torch.Tensor], act: str = "none",
+                      bias_shards: Sequence[torch.Tensor | None] | None = None,
+                      y_shards: Sequence[torch.Tensor] | None = None, ldy: int = 0, stream=None):
+    """Y_r = act(X W_r^T + b_r) for every rank r, one launch.  Returns the list of Y_r."""
+    _need_bf16("x", x)
+    p = len(w_shards)
+    T, K = x.shape
+    N_r = w_shards[0].shape[0]
+    for w in w_shards:
+        _need_bf16("w_shards[i]", w)
+    n_out = N_r // 2 if act == "swiglu" else N_r
+    if y_shards is None:
+        y_shards = [torch.empty((T, n_out), dtype=torch.bfloat16, device=x.device) for _ in range(p)]
+    bias_arr = _ptrs(bias_shards) if bias_shards is not None else None
+    _check(lib.tp_linear_colwise(_ptr(x), _ptrs(w_shards), bias_arr, ACTS[act], p, T, K, N_r, _ptrs(y_shards), ldy,
+                                 _stream(stream)))
+    return y_shards
+
+
+def tp_rowwise_workspace_bytes(tp_degree: int, T: int, N: int, mode: str = "workspace") -> int:
+    return int(lib.tp_rowwise_workspace_bytes(tp_degree, T, N, REDUCE_MODES[mode]))
+
+
+def tp_linear_rowwise(x_shards: Sequence[torch.Tensor], w_shards: Sequence[torch.Tensor],
+                      bias: torch.Tensor | None = None, mode: str = "accum", workspace: torch.Tensor | None = None,
+                      out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Z = sum_r X_r W_r^T (+ bias once), one launch.
+
+    mode "accum" / "workspace" return bf16 [T, N]; "none" returns the fp32
+    partials [tp_degree, T, N] (join them with ``tp_combine("reduce", ...)``).
+    """
+    p = len(w_shards)
+    T, K_r = x_shards[0].shape
+    N = w_shards[0].shape[0]
+    for t in list(x_shards) + list(w_shards):
+        _need_bf16("shard", t)
+    dev = x_shards[0].device
+    if out is None:
+        if mode == "none":
+            out = torch.empty((p, T, N), dtype=torch.float32, device=dev)
+        else:
+            out = torch.empty((T, N), dtype=torch.bfloat16, device=dev)
+    need = tp_rowwise_workspace_bytes(p, T, N, mode)
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(lib.tp_linear_rowwise(_ptrs(x_shards), _ptrs(w_shards), _ptr(bias), p, T, K_r, N, REDUCE_MODES[mode],
+                                 _ptr(workspace), ws_bytes, _ptr(out), _stream(stream)))
+    return out
+
+
+# ---------------------------------------------------------------------------
+# Join
+# ---------------------------------------------------------------------------
+
+def tp_combine(mode: str, partials: Sequence[torch.Tensor], out: torch.Tensor | None = None,
+               stream=None) -> torch.Tensor:
+    """Gather bf16 [T, N_each] slices into [T, p*N_each], or reduce fp32 partials into bf16 [T, N_each]."""
+    p = len(partials)
+    T, N_each = partials[0].shape
+    if out is None:
+        cols = N_each * p if mode == "gather" else N_each
+        out = torch.empty((T, cols), dtype=torch.bfloat16, device=partials[0].device)
+    _check(lib.tp_combine(COMBINE_MODES[mode], _ptrs(partials), p, T, N_each, _ptr(out), _stream(stream)))
+    return out
+
+
+# ---------------------------------------------------------------------------
+# Diagnostics
+# ---------------------------------------------------------------------------
+
+def tp_last_error() -> str:
+    return lib.tp_last_error().decode()
+
+
+def tp_status_name(status: int) -> str:
+    return lib.tp_status_name(status).decode()
+
+
+def tp_device_status(stream=None) -> None:
+    """Synchronise the stream; raise TPError if a kernel gave up on a bounded wait."""
+    _check(lib.tp_device_status(_stream(stream)))
+
+
+def tp_abi_version() -> int:
+    return int(lib.tp_abi_version())
+
+
+def bf16_from_bits(bits, device=None) -> torch.Tensor:
+    """A bf16 tensor holding the given uint16 bit patterns (numpy array), optionally moved to `device`."""
+    import numpy as np
+    t = torch.from_numpy(np.ascontiguousarray(bits, dtype=np.uint16).view(np.int16)).view(torch.bfloat16)
+    return t.to(device) if device is not None else t
+
+
+def bits_from_bf16(t: torch.Tensor):
+    """uint16 numpy bit patterns of a bf16 tensor (copied to the host)."""
+    import numpy as np
+    return t.detach().contiguous().cpu().view(torch.int16).numpy().view(np.uint16)

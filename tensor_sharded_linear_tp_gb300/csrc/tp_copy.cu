@@ -1,0 +1,306 @@
+// Shard extraction (tp_plan_shard) and the in-memory joins (tp_combine).
+//
+// Both extraction styles and the gather are the same memory operation: a list
+// of up to 16 strided 2-D copies ("segments"), each `rows` rows of `row_bytes`
+// bytes, between two row strides.  One launch moves every segment:
+//   * colwise (packed): one segment per packed block -- the rank's part of a
+//     block is (s_b / p) consecutive rows, i.e. one contiguous run;
+//   * rowwise (packed): one segment per block -- a column window of every row;
+//   * gather: one segment per rank -- rank r's [T, N_each] into columns
+//     [r*N_each, (r+1)*N_each) of the joined output.
+// Rows are cut into pieces of at most 4 KiB; a warp copies one piece with
+// 16-byte vector loads and stores, 4 independent loads in flight per lane.
+// Grid: a multiple of the SM count, grid-stride over pieces.  HBM-bound: the
+// algorithmic traffic is exactly 2 x the bytes copied.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "tp_internal.h"
+
+namespace tp {
+namespace {
+
+constexpr int kMaxSegs = 16;
+constexpr int64_t kPieceBytes = 4096;
+constexpr int kCopyThreads = 256;
+
+struct CopySeg {
+  const uint8_t* src;
+  uint8_t* dst;
+  int64_t rows;
+  int64_t row_bytes;
+  int64_t src_stride;  // bytes between consecutive rows of the source
+  int64_t dst_stride;  // bytes between consecutive rows of the destination
+  int64_t pieces;      // pieces per row
+  int64_t unit_begin;  // first work unit (row x piece) of this segment
+};
+
+struct CopyParams {
+  CopySeg seg[kMaxSegs];
+  int nseg;
+  int64_t total_units;
+};
+
+__device__ __forceinline__ uint4 load16(const uint4* p, bool host_src) {
+  uint4 v;
+  if (host_src) {
+    // Mapped page-locked host memory: plain coherent load over the CPU-GPU link.
+    asm volatile("ld.global.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+  } else {
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+  }
+  return v;
+}
+
+// 16-byte path: every pointer, stride and row length is a multiple of 16 bytes.
+template <bool kHostSrc>
+__global__ void __launch_bounds__(kCopyThreads) copy_segments_v16(const __grid_constant__ CopyParams p) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+  for (int64_t u = warp; u < p.total_units; u += nwarps) {
+    int s = 0;
+    while (s + 1 < p.nseg && u >= p.seg[s + 1].unit_begin) ++s;
+    const CopySeg& g = p.seg[s];
+    const int64_t lu = u - g.unit_begin;
+    const int64_t row = lu / g.pieces;
+    const int64_t piece = lu - row * g.pieces;
+    const int64_t off = piece * kPieceBytes;
+    const int64_t nbytes = min(kPieceBytes, g.row_bytes - off);
+    const uint4* src = reinterpret_cast<const uint4*>(g.src + row * g.src_stride + off);
+    uint4* dst = reinterpret_cast<uint4*>(g.dst + row * g.dst_stride + off);
+    const int n = static_cast<int>(nbytes >> 4);
+    for (int i = lane; i < n; i += 128) {
+      uint4 v0, v1, v2, v3;
+      const bool h1 = i + 32 < n, h2 = i + 64 < n, h3 = i + 96 < n;
+      v0 = load16(src + i, kHostSrc);
+      if (h1) v1 = load16(src + i + 32, kHostSrc);
+      if (h2) v2 = load16(src + i + 64, kHostSrc);
+      if (h3) v3 = load16(src + i + 96, kHostSrc);
+      dst[i] = v0;
+      if (h1) dst[i + 32] = v1;
+      if (h2) dst[i + 64] = v2;
+      if (h3) dst[i + 96] = v3;
+    }
+  }
+}
+
+// 2-byte path for shapes whose rows are not 16-byte multiples (same work split).
+__global__ void __launch_bounds__(kCopyThreads) copy_segments_b16(const __grid_constant__ CopyParams p) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+  for (int64_t u = warp; u < p.total_units; u += nwarps) {
+    int s = 0;
+    while (s + 1 < p.nseg && u >= p.seg[s + 1].unit_begin) ++s;
+    const CopySeg& g = p.seg[s];
+    const int64_t lu = u - g.unit_begin;
+    const int64_t row = lu / g.pieces;
+    const int64_t piece = lu - row * g.pieces;
+    const int64_t off = piece * kPieceBytes;
+    const int64_t nbytes = min(kPieceBytes, g.row_bytes - off);
+    const uint16_t* src = reinterpret_cast<const uint16_t*>(g.src + row * g.src_stride + off);
+    uint16_t* dst = reinterpret_cast<uint16_t*>(g.dst + row * g.dst_stride + off);
+    const int n = static_cast<int>(nbytes >> 1);
+    for (int i = lane; i < n; i += 32) dst[i] = src[i];
+  }
+}
+
+struct SegBuilder {
+  CopyParams p{};
+  bool vec_ok = true;
+  void add(const void* src, void* dst, int64_t rows, int64_t row_bytes, int64_t src_stride, int64_t dst_stride) {
+    if (rows <= 0 || row_bytes <= 0) return;
+    CopySeg& g = p.seg[p.nseg++];
+    g.src = static_cast<const uint8_t*>(src);
+    g.dst = static_cast<uint8_t*>(dst);
+    g.rows = rows;
+    g.row_bytes = row_bytes;
+    g.src_stride = src_stride;
+    g.dst_stride = dst_stride;
+    g.pieces = (row_bytes + kPieceBytes - 1) / kPieceBytes;
+    g.unit_begin = p.total_units;
+    p.total_units += rows * g.pieces;
+    if (!aligned16(src) || !aligned16(dst) || (row_bytes & 15) || (rows > 1 && ((src_stride & 15) || (dst_stride & 15))))
+      vec_ok = false;
+  }
+};
+
+tp_status launch_copy(SegBuilder& b, bool host_src, cudaStream_t stream) {
+  if (b.p.total_units == 0) return TP_OK;
+  const int sms = sm_count();
+  if (sms <= 0) return fail(TP_ERR_CUDA, "cannot query the SM count of the current device");
+  const int64_t warps_needed = b.p.total_units;
+  const int64_t blocks_needed = (warps_needed * 32 + kCopyThreads - 1) / kCopyThreads;
+  // Up to 8 resident blocks of 256 threads per SM; grid is a multiple of the SM count when large.
+  int64_t grid = blocks_needed;
+  const int64_t cap = static_cast<int64_t>(sms) * 8;
+  if (grid > cap) grid = cap;
+  if (b.vec_ok) {
+    if (host_src)
+      copy_segments_v16<true><<<static_cast<unsigned>(grid), kCopyThreads, 0, stream>>>(b.p);
+    else
+      copy_segments_v16<false><<<static_cast<unsigned>(grid), kCopyThreads, 0, stream>>>(b.p);
+  } else {
+    copy_segments_b16<<<static_cast<unsigned>(grid), kCopyThreads, 0, stream>>>(b.p);
+  }
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "copy kernel launch");
+  return TP_OK;
+}
+
+// ---------------------------------------------------------------------------
+// Reduce: out[i] = bf16_rne(sum_r partials[r][i]), fp32 sum in rank order.
+// ---------------------------------------------------------------------------
+
+struct ReduceParams {
+  const float* part[TP_MAX_DEGREE];
+  __nv_bfloat16* out;
+  int64_t n;  // elements
+  int p;
+};
+
+__global__ void __launch_bounds__(256) reduce_partials_v8(const __grid_constant__ ReduceParams p) {
+  const int64_t groups = p.n >> 3;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t g = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; g < groups; g += stride) {
+    float acc[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc[j] = 0.f;
+    for (int r = 0; r < p.p; ++r) {
+      const float4* src = reinterpret_cast<const float4*>(p.part[r]) + 2 * g;
+      float4 a = __ldcs(src);
+      float4 b = __ldcs(src + 1);
+      acc[0] += a.x; acc[1] += a.y; acc[2] += a.z; acc[3] += a.w;
+      acc[4] += b.x; acc[5] += b.y; acc[6] += b.z; acc[7] += b.w;
+    }
+    __align__(16) __nv_bfloat162 o[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) o[j] = __floats2bfloat162_rn(acc[2 * j], acc[2 * j + 1]);
+    reinterpret_cast<uint4*>(p.out)[g] = *reinterpret_cast<const uint4*>(o);
+  }
+}
+
+__global__ void __launch_bounds__(256) reduce_partials_scalar(const __grid_constant__ ReduceParams p, int64_t begin) {
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = begin + static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < p.n; i += stride) {
+    float acc = 0.f;
+    for (int r = 0; r < p.p; ++r) acc += p.part[r][i];
+    p.out[i] = __float2bfloat16_rn(acc);
+  }
+}
+
+}  // namespace
+}  // namespace tp
+
+extern "C" {
+
+tp_status tp_plan_shard(const void* weight, int64_t rows, int64_t cols, tp_style style, int tp_degree, int rank,
+                        const int64_t* fused_splits, int n_splits, int64_t num_heads, int64_t head_dim, void* dev_out,
+                        tp_stream_t stream) {
+  using namespace tp;
+  clear_error();
+  if (rank < 0) return fail(TP_ERR_INVALID_ARG, "rank %d is negative", rank);
+  int64_t sizes[TP_MAX_SPLITS];
+  int n = 0;
+  tp_status st = validate_plan(rows, cols, style, tp_degree, rank, num_heads, head_dim, fused_splits, n_splits, sizes, &n);
+  if (st != TP_OK) return st;
+  const int64_t shard_elems = rows * cols / tp_degree;
+  if (shard_elems == 0) return TP_OK;
+  if (weight == nullptr || dev_out == nullptr) return fail(TP_ERR_INVALID_ARG, "weight or dev_out is NULL");
+
+  // Where does the source live?  Page-locked host memory is read through its
+  // device mapping; pageable host memory is refused rather than staged.
+  cudaPointerAttributes attr{};
+  cudaError_t e = cudaPointerGetAttributes(&attr, weight);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaPointerGetAttributes(weight)");
+  const void* src = weight;
+  bool host_src = false;
+  if (attr.type == cudaMemoryTypeHost) {
+    if (attr.devicePointer == nullptr) return fail(TP_ERR_NOT_PINNED, "page-locked weight has no device mapping");
+    src = attr.devicePointer;
+    host_src = true;
+  } else if (attr.type == cudaMemoryTypeUnregistered) {
+    return fail(TP_ERR_NOT_PINNED, "weight is pageable host memory; page-lock it (cudaHostAlloc/cudaHostRegister)");
+  }
+  cudaPointerAttributes oattr{};
+  e = cudaPointerGetAttributes(&oattr, dev_out);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaPointerGetAttributes(dev_out)");
+  if (oattr.type != cudaMemoryTypeDevice && oattr.type != cudaMemoryTypeManaged)
+    return fail(TP_ERR_INVALID_ARG, "dev_out is not device memory");
+
+  SegBuilder b;
+  const int64_t esz = 2;  // bf16
+  const uint8_t* s8 = static_cast<const uint8_t*>(src);
+  uint8_t* d8 = static_cast<uint8_t*>(dev_out);
+  int64_t offset = 0;      // block offset along the sharded dimension
+  int64_t out_offset = 0;  // where this block's part starts in the shard
+  for (int bi = 0; bi < n; ++bi) {
+    const int64_t part = sizes[bi] / tp_degree;
+    const int64_t lo = offset + static_cast<int64_t>(rank) * part;
+    if (style == TP_COLWISE) {
+      // Rows [lo, lo+part) of W -> rows [out_offset, out_offset+part) of the shard.
+      b.add(s8 + lo * cols * esz, d8 + out_offset * cols * esz, part, cols * esz, cols * esz, cols * esz);
+    } else {
+      // Columns [lo, lo+part) of every row -> columns [out_offset, ...) of the shard.
+      const int64_t shard_cols = cols / tp_degree;
+      b.add(s8 + lo * esz, d8 + out_offset * esz, rows, part * esz, cols * esz, shard_cols * esz);
+    }
+    offset += sizes[bi];
+    out_offset += part;
+  }
+  return launch_copy(b, host_src, reinterpret_cast<cudaStream_t>(stream));
+}
+
+tp_status tp_combine(tp_combine_mode mode, const void* const* partials, int tp_degree, int64_t T, int64_t N_each,
+                     void* out, tp_stream_t stream) {
+  using namespace tp;
+  clear_error();
+  if (mode != TP_GATHER && mode != TP_REDUCE) return fail(TP_ERR_INVALID_ARG, "unknown combine mode %d", (int)mode);
+  if (tp_degree < 1 || tp_degree > TP_MAX_DEGREE)
+    return fail(tp_degree < 1 ? TP_ERR_INVALID_ARG : TP_ERR_UNSUPPORTED, "tp_degree=%d outside [1, %d]", tp_degree,
+                TP_MAX_DEGREE);
+  if (T < 0 || N_each < 0) return fail(TP_ERR_INVALID_ARG, "negative size");
+  if (T == 0 || N_each == 0) return TP_OK;
+  if (partials == nullptr || out == nullptr) return fail(TP_ERR_INVALID_ARG, "partials or out is NULL");
+  for (int r = 0; r < tp_degree; ++r)
+    if (partials[r] == nullptr) return fail(TP_ERR_INVALID_ARG, "partials[%d] is NULL", r);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (mode == TP_GATHER) {
+    SegBuilder b;
+    const int64_t row_bytes = N_each * 2;
+    for (int r = 0; r < tp_degree; ++r)
+      b.add(partials[r], static_cast<uint8_t*>(out) + r * row_bytes, T, row_bytes, row_bytes, row_bytes * tp_degree);
+    return launch_copy(b, false, s);
+  }
+  ReduceParams p{};
+  for (int r = 0; r < tp_degree; ++r) p.part[r] = static_cast<const float*>(partials[r]);
+  p.out = static_cast<__nv_bfloat16*>(out);
+  p.n = T * N_each;
+  p.p = tp_degree;
+  const int sms = sm_count();
+  if (sms <= 0) return fail(TP_ERR_CUDA, "cannot query the SM count of the current device");
+  bool vec = aligned16(out);
+  for (int r = 0; r < tp_degree; ++r) vec = vec && aligned16(partials[r]);
+  int64_t begin = 0;
+  if (vec && p.n >= 8) {
+    const int64_t groups = p.n >> 3;
+    int64_t grid = (groups + 255) / 256;
+    if (grid > static_cast<int64_t>(sms) * 8) grid = static_cast<int64_t>(sms) * 8;
+    reduce_partials_v8<<<static_cast<unsigned>(grid), 256, 0, s>>>(p);
+    begin = groups << 3;
+  }
+  if (begin < p.n) {
+    int64_t rem = p.n - begin;
+    int64_t grid = (rem + 255) / 256;
+    if (grid > static_cast<int64_t>(sms) * 8) grid = static_cast<int64_t>(sms) * 8;
+    reduce_partials_scalar<<<static_cast<unsigned>(grid), 256, 0, s>>>(p, begin);
+  }
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "reduce kernel launch");
+  return TP_OK;
+}
+
+}  // extern "C"

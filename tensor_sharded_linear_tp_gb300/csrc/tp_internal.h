@@ -1,0 +1,39 @@
+// Host-side helpers shared by the library's translation units (not part of the ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cstdarg>
+#include <cstdint>
+
+#include "tp.h"
+
+namespace tp {
+
+// Record a message for tp_last_error() and return `st`.
+tp_status fail(tp_status st, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
+
+// Clear the calling thread's last error.
+void clear_error();
+
+// Convert a CUDA error into TP_ERR_CUDA with a message naming `what`.
+tp_status cuda_fail(cudaError_t err, const char* what);
+
+// Number of SMs of the current device (cached per device).
+int sm_count();
+
+// Device address of the library's kernel status word on the current device
+// (bit 0: a kernel gave up on a bounded wait).  Looked up once per device.
+unsigned int* status_word();
+
+// Plan validation shared by every entry point.  On TP_OK, `sizes` holds the
+// n_sizes absolute block sizes along the sharded dimension.
+tp_status validate_plan(int64_t rows, int64_t cols, tp_style style, int tp_degree, int rank, int64_t num_heads,
+                        int64_t head_dim, const int64_t* splits, int n_splits, int64_t* sizes, int* n_sizes);
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace tp
+
+// Bit 0 of the status word: a bounded wait gave up.
+#define TP_DEVSTATUS_TIMEOUT 1u

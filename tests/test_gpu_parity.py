@@ -1,0 +1,330 @@
+"""Parity of the CUDA path (through the C-ABI) with the CPU oracle.
+
+Extraction and gathers are compared bit for bit; products of integer-valued
+inputs are exact in fp32 and are compared bit for bit too; everything else is
+held to the tolerance in ``tolerance.py``.  Small shapes span several 128 x 256
+tiles with ragged tails; the full-size workloads are checked on a seeded
+sample of token rows, which the oracle computes exactly.
+"""
+import numpy as np
+import pytest
+import torch
+
+import tp_inputs
+from oracle import tp_oracle as O
+from tolerance import assert_close
+
+pytestmark = pytest.mark.gpu
+
+tp = pytest.importorskip("tensor_sharded_linear_tp_gb300")
+
+DEV = "cuda"
+
+
+def dev(bits):
+    return tp.bf16_from_bits(bits, DEV)
+
+
+def pinned(bits):
+    t = tp.bf16_from_bits(bits)
+    p = torch.empty(t.shape, dtype=torch.bfloat16, pin_memory=True)
+    p.copy_(t)
+    return p
+
+
+def host_bits(t):
+    torch.cuda.synchronize()
+    return tp.bits_from_bf16(t)
+
+
+def f64(t):
+    torch.cuda.synchronize()
+    return O.bf16_to_f64(tp.bits_from_bf16(t))
+
+
+@pytest.fixture(autouse=True)
+def _device_status_clean():
+    yield
+    tp.tp_device_status()   # raises if any kernel gave up on a bounded wait
+
+
+# ----------------------------------------------------------------------------- extraction
+
+EXTRACT_CASES = [
+    # (rows, cols, style, tp, splits, heads, head_dim)
+    (96, 64, "colwise", 2, None, 0, 0),
+    (18, 24, "colwise", 2, [2, 2, 2, 6, 6], 0, 0),          # [1,1,1,3,3] fused QKV+gate+up
+    (48, 40, "colwise", 4, [24, 24], 0, 0),                 # gate/up [1,1]
+    (3 * 96, 64, "colwise", 3, [96, 96, 96], 12, 8),        # QKV, whole heads
+    (40, 96, "rowwise", 4, None, 0, 0),
+    (24, 96, "rowwise", 2, [32, 64], 0, 0),                 # packed rowwise [inner, mlp_hidden]
+    (33, 48, "rowwise", 3, None, 0, 0),                     # 32-byte windows of odd row counts
+    (10, 20, "rowwise", 2, None, 0, 0),                     # 20-byte rows: 2-byte path
+    (14, 6, "colwise", 2, None, 0, 0),                      # 12-byte rows: 2-byte path
+    (0, 16, "colwise", 2, None, 0, 0),                      # empty
+]
+
+
+@pytest.mark.parametrize("case", EXTRACT_CASES, ids=lambda c: f"{c[2]}-{c[0]}x{c[1]}-tp{c[3]}-{c[4]}")
+@pytest.mark.parametrize("source", ["device", "pinned_host"])
+def test_extract_bit_exact(case, source):
+    rows, cols, style, p, splits, h, d = case
+    w = tp_inputs.random_bits(100, rows * 1000 + cols, (rows, cols))   # any 16-bit pattern, NaN payloads too
+    src = dev(w) if source == "device" else pinned(w)
+    for r in range(p):
+        out = tp.tp_plan_shard(src, style, p, r, splits, h, d, device=DEV)
+        exp = O.shard(w, style, p, r, splits, num_heads=h, head_dim=d)
+        got = host_bits(out)
+        assert got.shape == exp.shape and np.array_equal(got, exp), (case, r)
+
+
+def test_extract_pageable_host_refused():
+    w = tp.bf16_from_bits(tp_inputs.random_bits(101, 0, (16, 16)))   # ordinary (pageable) CPU tensor
+    with pytest.raises(tp.TPError) as e:
+        tp.tp_plan_shard(w, "colwise", 2, 0, device=DEV)
+    assert e.value.name == "TP_ERR_NOT_PINNED"
+
+
+@pytest.mark.parametrize("which", ["attn_qkv", "attn_out", "mlp_gate_up", "mlp_down"])
+@pytest.mark.parametrize("source", ["device", "pinned_host"])
+def test_extract_full_size_bit_exact(which, source):
+    if which == "attn_qkv":
+        shape, style, splits, h, d = (9216, 3072), "colwise", [3072] * 3, 24, 128
+    elif which == "attn_out":
+        shape, style, splits, h, d = (3072, 3072), "rowwise", None, 24, 128
+    elif which == "mlp_gate_up":
+        shape, style, splits, h, d = (36864, 6144), "colwise", [18432, 18432], 48, 0
+    else:
+        shape, style, splits, h, d = (6144, 18432), "rowwise", None, 48, 0
+    w = tp_inputs.random_bits(102, len(which), shape)
+    src = dev(w) if source == "device" else pinned(w)
+    for r in range(4):
+        out = tp.tp_plan_shard(src, style, 4, r, splits, h, d, device=DEV)
+        assert np.array_equal(host_bits(out), O.shard(w, style, 4, r, splits, num_heads=h, head_dim=d)), r
+
+
+# ----------------------------------------------------------------------------- combine
+
+def test_gather_bit_exact():
+    for p, T, n in ((4, 37, 24), (3, 5, 3), (2, 300, 512)):
+        parts = [tp_inputs.random_bits(103, 10 * p + r, (T, n)) for r in range(p)]
+        got = host_bits(tp.tp_combine("gather", [dev(b) for b in parts]))
+        assert np.array_equal(got, O.combine_gather(parts))
+
+
+def test_reduce_integer_exact_and_normal_within_tolerance():
+    p, T, n = 4, 129, 200
+    rng = np.random.default_rng(104)
+    ints = [rng.integers(-300, 300, size=(T, n)).astype(np.float32) for _ in range(p)]
+    got = host_bits(tp.tp_combine("reduce", [torch.from_numpy(a).to(DEV) for a in ints]))
+    assert np.array_equal(got, O.f64_to_bf16(O.combine_reduce(ints)))
+    normals = [rng.standard_normal((T, n)).astype(np.float32) for _ in range(p)]
+    out = tp.tp_combine("reduce", [torch.from_numpy(a).to(DEV) for a in normals])
+    assert_close(f64(out), O.combine_reduce(normals), "reduce")
+    # Unaligned length: scalar tail path.
+    odd = [rng.integers(-5, 5, size=(3, 7)).astype(np.float32) for _ in range(3)]
+    got = host_bits(tp.tp_combine("reduce", [torch.from_numpy(a).to(DEV) for a in odd]))
+    assert np.array_equal(got, O.f64_to_bf16(O.combine_reduce(odd)))
+
+
+# ----------------------------------------------------------------------------- colwise GEMM
+
+COLWISE_SHAPES = [
+    # (T, K, N_r, p): several tiles with ragged tails in M, N and K.
+    (300, 200, 520, 2),
+    (64, 256, 512, 2),
+    (129, 64, 264, 3),
+    (1, 8, 8, 1),
+    (517, 1032, 1040, 4),
+]
+
+
+@pytest.mark.parametrize("shape", COLWISE_SHAPES, ids=str)
+def test_colwise_integer_bit_exact(shape):
+    T, K, N_r, p = shape
+    x = tp_inputs.int_bf16(110, 0, (T, K))
+    w = tp_inputs.int_bf16(110, 1, (N_r * p, K))
+    shards = [O.shard(w, "colwise", p, r) for r in range(p)]
+    ys = tp.tp_linear_colwise(dev(x), [dev(s) for s in shards], "none")
+    ref = O.colwise_forward(x, shards, "none")
+    for r in range(p):
+        assert np.array_equal(host_bits(ys[r]), O.f64_to_bf16(ref[r])), r
+
+
+@pytest.mark.parametrize("act", ["none", "gelu_tanh", "swiglu"])
+@pytest.mark.parametrize("shape", COLWISE_SHAPES[:3] + [(1000, 512, 1024, 4)], ids=str)
+def test_colwise_normal_within_tolerance(shape, act):
+    T, K, N_r, p = shape
+    if act == "swiglu":
+        N_r = ((N_r + 15) // 16) * 16   # gate and up halves of whole 8-column groups
+    x = tp_inputs.activation_bf16(111, 0, (T, K))
+    w = tp_inputs.weight_bf16(111, 1, (N_r * p, K))
+    splits = [N_r * p // 2] * 2 if act == "swiglu" else None
+    shards = [O.shard(w, "colwise", p, r, splits) for r in range(p)]
+    ys = tp.tp_linear_colwise(dev(x), [dev(s) for s in shards], act)
+    ref = O.colwise_forward(x, shards, act)
+    for r in range(p):
+        assert_close(f64(ys[r]), ref[r], f"{act} rank {r}")
+
+
+def test_colwise_bias_and_gathered_output():
+    T, K, N_r, p = 200, 128, 136, 3
+    x = tp_inputs.activation_bf16(112, 0, (T, K))
+    w = tp_inputs.weight_bf16(112, 1, (N_r * p, K))
+    b = tp_inputs.weight_bf16(112, 2, (N_r * p,))
+    shards = [O.shard(w, "colwise", p, r) for r in range(p)]
+    bsh = [np.ascontiguousarray(b[r * N_r:(r + 1) * N_r]) for r in range(p)]
+    # Write every rank's slice straight into the joined [T, p*N_r] output (the AllGather fused away).
+    y = torch.empty((T, p * N_r), dtype=torch.bfloat16, device=DEV)
+    tp.tp_linear_colwise(dev(x), [dev(s) for s in shards], "gelu_tanh", bias_shards=[dev(v) for v in bsh],
+                         y_shards=[y[:, r * N_r:] for r in range(p)], ldy=p * N_r)
+    ref = O.combine_gather(O.colwise_forward(x, shards, "gelu_tanh", bsh))
+    assert_close(f64(y), ref, "colwise bias gathered")
+    # And the unsharded layer equals it (tp_degree=1 is the plain layer).
+    y1 = tp.tp_linear_colwise(dev(x), [dev(w)], "gelu_tanh", bias_shards=[dev(b)])[0]
+    assert_close(f64(y1), ref, "tp=1 plain layer")
+
+
+def test_colwise_swiglu_bias():
+    T, K, F, p = 130, 64, 96, 2
+    x = tp_inputs.activation_bf16(113, 0, (T, K))
+    w = tp_inputs.weight_bf16(113, 1, (2 * F, K))
+    b = tp_inputs.weight_bf16(113, 2, (2 * F,))
+    shards = [O.shard(w, "colwise", p, r, [F, F]) for r in range(p)]
+    bsh = [O.shard(b[:, None], "colwise", p, r, [F, F])[:, 0].copy() for r in range(p)]
+    ys = tp.tp_linear_colwise(dev(x), [dev(s) for s in shards], "swiglu", bias_shards=[dev(v) for v in bsh])
+    ref = O.colwise_forward(x, shards, "swiglu", bsh)
+    for r in range(p):
+        assert_close(f64(ys[r]), ref[r], f"swiglu bias rank {r}")
+
+
+# ----------------------------------------------------------------------------- rowwise GEMM
+
+ROWWISE_SHAPES = [
+    # (T, K_r, N, p)
+    (300, 200, 520, 2),
+    (64, 512, 256, 2),
+    (129, 72, 264, 3),
+    (517, 1032, 1040, 4),
+    (33, 16, 8, 8),
+]
+MODES = ["accum", "workspace", "none"]
+
+
+def _rowwise_gpu(xs, ws, mode, bias=None):
+    out = tp.tp_linear_rowwise([dev(a) for a in xs], [dev(a) for a in ws], bias=None if bias is None else dev(bias),
+                               mode=mode)
+    if mode == "none":
+        return tp.tp_combine("reduce", list(out))
+    return out
+
+
+@pytest.mark.parametrize("mode", MODES)
+@pytest.mark.parametrize("shape", ROWWISE_SHAPES, ids=str)
+def test_rowwise_integer_bit_exact(shape, mode):
+    T, K_r, N, p = shape
+    x = tp_inputs.int_bf16(120, 0, (T, K_r * p))
+    w = tp_inputs.int_bf16(120, 1, (N, K_r * p))
+    xs = [O.shard(x, "rowwise", p, r) for r in range(p)]
+    ws = [O.shard(w, "rowwise", p, r) for r in range(p)]
+    z = _rowwise_gpu(xs, ws, mode)
+    assert np.array_equal(host_bits(z), O.f64_to_bf16(O.rowwise_forward(xs, ws)))
+
+
+@pytest.mark.parametrize("mode", MODES)
+@pytest.mark.parametrize("shape", ROWWISE_SHAPES[:4], ids=str)
+def test_rowwise_normal_within_tolerance(shape, mode):
+    T, K_r, N, p = shape
+    x = tp_inputs.activation_bf16(121, 0, (T, K_r * p))
+    w = tp_inputs.weight_bf16(121, 1, (N, K_r * p))
+    b = tp_inputs.weight_bf16(121, 2, (N,))
+    xs = [O.shard(x, "rowwise", p, r) for r in range(p)]
+    ws = [O.shard(w, "rowwise", p, r) for r in range(p)]
+    z = _rowwise_gpu(xs, ws, mode, bias=b)
+    assert_close(f64(z), O.rowwise_forward(xs, ws, b), mode)
+
+
+def test_rowwise_workspace_reused_across_calls():
+    # The tile counters reset themselves; a second call on the same workspace gives the same answer.
+    T, K_r, N, p = 260, 64, 264, 4
+    x = tp_inputs.int_bf16(122, 0, (T, K_r * p))
+    w = tp_inputs.int_bf16(122, 1, (N, K_r * p))
+    xs = [dev(O.shard(x, "rowwise", p, r)) for r in range(p)]
+    ws = [dev(O.shard(w, "rowwise", p, r)) for r in range(p)]
+    space = torch.empty(tp.tp_rowwise_workspace_bytes(p, T, N), dtype=torch.uint8, device=DEV)
+    exp = O.f64_to_bf16(O.rowwise_forward([O.shard(x, "rowwise", p, r) for r in range(p)],
+                                          [O.shard(w, "rowwise", p, r) for r in range(p)]))
+    for _ in range(3):
+        z = tp.tp_linear_rowwise(xs, ws, mode="workspace", workspace=space)
+        assert np.array_equal(host_bits(z), exp)
+
+
+# ----------------------------------------------------------------------------- workloads
+
+def _shard_all(w, style, p, splits=None, h=0, d=0):
+    return [O.shard(w, style, p, r, splits, num_heads=h, head_dim=d) for r in range(p)]
+
+
+def _plan_all(w_dev, rows, cols, style, p, splits=None, h=0, d=0):
+    return [tp.tp_plan_shard(w_dev, style, p, r, splits, h, d, device=DEV) for r in range(p)]
+
+
+def test_tiny_mlp_block():
+    """Tiny MLP, tp_degree 2: colwise up-projection + GELU(tanh), rowwise down-projection, summed."""
+    cfg = tp_inputs.WORKLOADS["tiny_mlp_tp2"]
+    p, H, F = cfg["tp"], cfg["hidden"], cfg["ffn"]
+    w_up, w_down, x = tp_inputs.tiny_mlp_inputs()
+    up = _plan_all(dev(w_up), F, H, "colwise", p, h=cfg["heads"])
+    down = _plan_all(dev(w_down), H, F, "rowwise", p, h=cfg["heads"])
+    for r in range(p):   # extraction is bit-exact
+        assert np.array_equal(host_bits(up[r]), O.shard(w_up, "colwise", p, r))
+        assert np.array_equal(host_bits(down[r]), O.shard(w_down, "rowwise", p, r))
+    h_ref, z_ref = O.mlp_forward(x, _shard_all(w_up, "colwise", p), _shard_all(w_down, "rowwise", p), "gelu_tanh")
+    for mode in MODES:
+        hs = tp.tp_linear_colwise(dev(x), up, "gelu_tanh")
+        z = tp.tp_linear_rowwise(hs, down, mode=mode)
+        if mode == "none":
+            z = tp.tp_combine("reduce", list(z))
+        assert_close(f64(z), z_ref, f"tiny mlp {mode}")
+        for r in range(p):
+            assert_close(f64(hs[r]), O.bf16_to_f64(h_ref[r]), "hidden")
+
+
+@pytest.mark.slow
+def test_attention_projections_full_size():
+    """Fused QKV colwise (6 whole heads per rank) + out-projection rowwise, tp 4, at full size, sampled rows."""
+    cfg = tp_inputs.WORKLOADS["attn_proj_tp4"]
+    p, T, H, h, d = cfg["tp"], cfg["tokens"], cfg["hidden"], cfg["heads"], cfg["head_dim"]
+    w_qkv, w_out, x, a = tp_inputs.attn_proj_inputs()
+    qkv = _plan_all(dev(w_qkv), 3 * H, H, "colwise", p, [H] * 3, h, d)
+    wo = _plan_all(dev(w_out), H, H, "rowwise", p, None, h, d)
+    a_sh = [dev(O.shard(a, "rowwise", p, r)) for r in range(p)]
+    ys = tp.tp_linear_colwise(dev(x), qkv, "none")
+    rows = tp_inputs.sample_rows(cfg["seed"], T, 256)
+    qkv_ref = O.colwise_forward(x[rows], _shard_all(w_qkv, "colwise", p, [H] * 3, h, d), "none")
+    for r in range(p):
+        assert_close(f64(ys[r])[rows], qkv_ref[r], f"qkv rank {r}")
+    z_ref = O.rowwise_forward([O.shard(a[rows], "rowwise", p, r) for r in range(p)], _shard_all(w_out, "rowwise", p))
+    for mode in MODES:
+        z = tp.tp_linear_rowwise(a_sh, wo, mode=mode)
+        if mode == "none":
+            z = tp.tp_combine("reduce", list(z))
+        assert_close(f64(z)[rows], z_ref, f"out-proj {mode}")
+
+
+@pytest.mark.slow
+def test_swiglu_mlp_full_size():
+    """Fused gate/up colwise with SwiGLU + down rowwise, tp 4, full size, sampled rows."""
+    cfg = tp_inputs.WORKLOADS["swiglu_mlp_tp4"]
+    p, T, H, F = cfg["tp"], cfg["tokens"], cfg["hidden"], cfg["ffn"]
+    w_gu, w_down, x = tp_inputs.swiglu_mlp_inputs()
+    gu = _plan_all(dev(w_gu), 2 * F, H, "colwise", p, [F, F], cfg["heads"], 0)
+    dn = _plan_all(dev(w_down), H, F, "rowwise", p, None, cfg["heads"], 0)
+    hs = tp.tp_linear_colwise(dev(x), gu, "swiglu")
+    z = tp.tp_linear_rowwise(hs, dn, mode="accum")
+    rows = tp_inputs.sample_rows(cfg["seed"], T, 128)
+    h_ref, z_ref = O.mlp_forward(x[rows], _shard_all(w_gu, "colwise", p, [F, F]), _shard_all(w_down, "rowwise", p),
+                                 "swiglu")
+    for r in range(p):
+        assert_close(f64(hs[r])[rows], O.bf16_to_f64(h_ref[r]), f"h rank {r}")
+    assert_close(f64(z)[rows], z_ref, "swiglu mlp out")
