@@ -7,7 +7,8 @@ tp_degree 4, all four ranks on this GPU):
 
   1. shard extraction of the fused QKV weight [9216, 3072] (colwise, whole
      heads of Q, K and V per rank) and of the out-projection [3072, 3072]
-     (rowwise) from device-resident full weights -- 8 tp_plan_shard calls;
+     (rowwise) from device-resident full weights -- one tp_plan_shard_ranks
+     launch per weight, covering all four ranks;
   2. the colwise QKV projection of every rank, one launch;
   3. the AllGather of the four QKV slices into [4096, 9216] (tp_combine);
   4. the rowwise out-projection of every rank with the partial sums joined on
@@ -242,8 +243,9 @@ class AttnProjWorkload:
         self.flops = self.flops_qkv + self.flops_out
         self.extract_bytes = 2.0 * 2 * (3 * H * H + H * H)   # read + write of every shard
         self.gather_bytes = 2.0 * 2 * T * 3 * H
-        self.launches_per_step = 2 * p + 3 + (1 if reduce_mode == "workspace" else 0) + \
-            (1 if reduce_mode == "none" else 0)
+        # 2 extraction launches (every rank of each weight), colwise, gather, rowwise (+ the counter
+        # clear of the workspace mode, or the separate reduce of the unfused mode).
+        self.launches_per_step = 5 + (1 if reduce_mode in ("workspace", "none") else 0)
         # Pinned host copies for the end-to-end measurement.
         self.pin = None
 
@@ -252,12 +254,10 @@ class AttnProjWorkload:
         tp, p, H = self.tp, self.p, self.H
         if marks:
             marks[0].record(stream)
-        for r in range(p):
-            tp.tp_plan_shard(self.w_qkv, "colwise", p, r, [H] * 3, self.heads, self.hd, out=self.qkv_sh[r],
-                             stream=stream)
-        for r in range(p):
-            tp.tp_plan_shard(self.w_out, "rowwise", p, r, None, self.heads, self.hd, out=self.out_sh[r],
-                             stream=stream)
+        tp.tp_plan_shard_ranks(self.w_qkv, "colwise", p, 0, p, [H] * 3, self.heads, self.hd, outs=self.qkv_sh,
+                               stream=stream)
+        tp.tp_plan_shard_ranks(self.w_out, "rowwise", p, 0, p, None, self.heads, self.hd, outs=self.out_sh,
+                               stream=stream)
         if marks:
             marks[1].record(stream)
         tp.tp_linear_colwise(self.x, self.qkv_sh, "none", y_shards=self.y_sh, stream=stream)
@@ -301,11 +301,11 @@ class AttnProjWorkload:
             self.x_in.copy_(self.pin["x"], non_blocking=True)
             for dst, src in zip(self.a_in, self.pin["a_sh"]):
                 dst.copy_(src, non_blocking=True)
-        for r in range(p):   # shard-on-read: only each rank's slice leaves host memory
-            tp.tp_plan_shard(self.pin["w_qkv"], "colwise", p, r, [H] * 3, self.heads, self.hd, out=self.qkv_sh[r],
-                             stream=stream)
-            tp.tp_plan_shard(self.pin["w_out"], "rowwise", p, r, None, self.heads, self.hd, out=self.out_sh[r],
-                             stream=stream)
+        # Shard-on-read: every rank's slice goes from host memory straight into its device buffer.
+        tp.tp_plan_shard_ranks(self.pin["w_qkv"], "colwise", p, 0, p, [H] * 3, self.heads, self.hd,
+                               outs=self.qkv_sh, stream=stream)
+        tp.tp_plan_shard_ranks(self.pin["w_out"], "rowwise", p, 0, p, None, self.heads, self.hd, outs=self.out_sh,
+                               stream=stream)
         tp.tp_linear_colwise(self.x_in, self.qkv_sh, "none", y_shards=self.y_sh, stream=stream)
         tp.tp_combine("gather", self.y_sh, out=self.y, stream=stream)
         self._rowwise(self.a_in, stream)
@@ -460,8 +460,9 @@ def run_ours(args):
             "config": {"workload": WORKLOAD, "tokens": wl.T, "hidden": wl.H, "heads": wl.heads, "head_dim": wl.hd,
                        "tp_degree": wl.p, "parallelism": f"tp{wl.p} simulated on each GPU; replicas across GPUs",
                        "rowwise_reduce": args.reduce_mode, "l2": "flushed between steps (256 MiB write)",
-                       "step": "8x tp_plan_shard (device) + tp_linear_colwise + tp_combine(gather) + "
-                               "tp_linear_rowwise"},
+                       "step": "2x tp_plan_shard_ranks (device, 4 ranks each) + tp_linear_colwise + "
+                               "tp_combine(gather) + tp_linear_rowwise", "sms": torch.cuda.get_device_properties(
+                                   device).multi_processor_count},
             "roofline": roofline, "kernels": kernels, "extract_gbs": kernels["extract"]["GB/s"],
             "extract_frac_hbm": kernels["extract"]["frac_hbm"], "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": wl.launches_per_step * args.steps, "clocks": clocks,

@@ -155,6 +155,18 @@ TP_API tp_status tp_plan_shard(const void* weight, int64_t rows, int64_t cols, t
                         const int64_t* fused_splits, int n_splits, int64_t num_heads, int64_t head_dim,
                         void* dev_out, tp_stream_t stream);
 
+/*
+ * tp_plan_shard_ranks -- tp_plan_shard for ranks [rank_begin, rank_begin +
+ * rank_count) in one launch: dev_outs is a host array of rank_count device
+ * buffers, dev_outs[i] receiving rank (rank_begin + i)'s shard.  Same slice
+ * definition, checks, sources and errors as tp_plan_shard; the range must lie
+ * in [0, tp_degree).  rank_count == 0 validates the plan and copies nothing.
+ * This is how one process that plays every rank loads all their shards.
+ */
+TP_API tp_status tp_plan_shard_ranks(const void* weight, int64_t rows, int64_t cols, tp_style style, int tp_degree,
+                                     int rank_begin, int rank_count, const int64_t* fused_splits, int n_splits,
+                                     int64_t num_heads, int64_t head_dim, void* const* dev_outs, tp_stream_t stream);
+
 /* ------------------------------------------------------------------------ */
 /* Sharded projections                                                       */
 /* ------------------------------------------------------------------------ */

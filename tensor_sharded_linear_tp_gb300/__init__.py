@@ -20,7 +20,7 @@ LIB_PATH = os.path.join(_HERE, "libtp.so")
 
 if not os.path.exists(LIB_PATH):
     raise ImportError(
-        f"{LIB_PATH} is missing: build it with `python -m tensor_sharded_linear_tp_gb300.build` "
+        f"{LIB_PATH} is missing: build it with `python tensor_sharded_linear_tp_gb300/build.py` "
         "(the CUDA library is the only implementation)")
 
 lib = ctypes.CDLL(LIB_PATH)
@@ -47,6 +47,8 @@ _SIGS = {
                                  ctypes.POINTER(_i64), ctypes.POINTER(_i64)]),
     "tp_plan_shard": (_status, [_vp, _i64, _i64, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.POINTER(_i64),
                                 ctypes.c_int, _i64, _i64, _vp, _vp]),
+    "tp_plan_shard_ranks": (_status, [_vp, _i64, _i64, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                      ctypes.POINTER(_i64), ctypes.c_int, _i64, _i64, ctypes.POINTER(_vp), _vp]),
     "tp_linear_colwise": (_status, [_vp, ctypes.POINTER(_vp), ctypes.POINTER(_vp), ctypes.c_int, ctypes.c_int, _i64,
                                     _i64, _i64, ctypes.POINTER(_vp), _i64, _vp]),
     "tp_linear_rowwise": (_status, [ctypes.POINTER(_vp), ctypes.POINTER(_vp), _vp, ctypes.c_int, _i64, _i64, _i64,
@@ -157,6 +159,25 @@ def tp_plan_shard(weight: torch.Tensor, style: str, tp_degree: int, rank: int,
     _check(lib.tp_plan_shard(_ptr(weight), rows, cols, STYLES[style], tp_degree, rank, arr, n, num_heads, head_dim,
                              _ptr(out), _stream(stream)))
     return out
+
+
+def tp_plan_shard_ranks(weight: torch.Tensor, style: str, tp_degree: int, rank_begin: int = 0,
+                        rank_count: int | None = None, fused_splits: Sequence[int] | None = None, num_heads: int = 0,
+                        head_dim: int = 0, outs: Sequence[torch.Tensor] | None = None, device=None,
+                        stream=None) -> list[torch.Tensor]:
+    """Shards of ranks [rank_begin, rank_begin + rank_count) in one launch (default: every rank)."""
+    _need_bf16("weight", weight)
+    rows, cols = weight.shape
+    if rank_count is None:
+        rank_count = tp_degree - rank_begin
+    arr, n = _splits(fused_splits)
+    if outs is None:
+        shape = tp_shard_shape(rows, cols, style, tp_degree, fused_splits)
+        dev = device if device is not None else (weight.device if weight.is_cuda else torch.device("cuda"))
+        outs = [torch.empty(shape, dtype=torch.bfloat16, device=dev) for _ in range(rank_count)]
+    _check(lib.tp_plan_shard_ranks(_ptr(weight), rows, cols, STYLES[style], tp_degree, rank_begin, rank_count, arr, n,
+                                   num_heads, head_dim, _ptrs(outs) if outs else None, _stream(stream)))
+    return list(outs)
 
 
 # ---------------------------------------------------------------------------

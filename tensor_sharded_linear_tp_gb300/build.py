@@ -1,9 +1,10 @@
 """Build libtp.so (the C-ABI CUDA library) in-tree for sm_103a.
 
 Each translation unit is compiled by its own nvcc process, in parallel, then
-linked into one shared library next to this file.  Usage::
+linked into one shared library next to this file.  Usage (run it as a
+script: importing the package needs the library it builds)::
 
-    python -m tensor_sharded_linear_tp_gb300.build [--force] [--verbose]
+    python tensor_sharded_linear_tp_gb300/build.py [--force] [--verbose]
 """
 from __future__ import annotations
 

@@ -1,17 +1,19 @@
 // Shard extraction (tp_plan_shard) and the in-memory joins (tp_combine).
 //
 // Both extraction styles and the gather are the same memory operation: a list
-// of up to 16 strided 2-D copies ("segments"), each `rows` rows of `row_bytes`
+// of up to 64 strided 2-D copies ("segments"), each `rows` rows of `row_bytes`
 // bytes, between two row strides.  One launch moves every segment:
 //   * colwise (packed): one segment per packed block -- the rank's part of a
 //     block is (s_b / p) consecutive rows, i.e. one contiguous run;
 //   * rowwise (packed): one segment per block -- a column window of every row;
 //   * gather: one segment per rank -- rank r's [T, N_each] into columns
 //     [r*N_each, (r+1)*N_each) of the joined output.
-// Rows are cut into pieces of at most 4 KiB; a warp copies one piece with
-// 16-byte vector loads and stores, 4 independent loads in flight per lane.
-// Grid: a multiple of the SM count, grid-stride over pieces.  HBM-bound: the
-// algorithmic traffic is exactly 2 x the bytes copied.
+// A segment whose rows are back to back in both source and destination is
+// copied as one long row.  Rows are cut into pieces of at most 4 KiB; a warp
+// copies one piece with 16-byte vector loads and stores, all of the piece's
+// loads (up to 8 per lane) issued before its stores.  Grid: up to 8 blocks of
+// 256 threads per SM, grid-stride over pieces.  HBM-bound: the algorithmic
+// traffic is exactly 2 x the bytes copied.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -20,7 +22,7 @@
 namespace tp {
 namespace {
 
-constexpr int kMaxSegs = 16;
+constexpr int kMaxSegs = 64;
 constexpr int64_t kPieceBytes = 4096;
 constexpr int kCopyThreads = 256;
 
@@ -71,19 +73,14 @@ __global__ void __launch_bounds__(kCopyThreads) copy_segments_v16(const __grid_c
     const int64_t nbytes = min(kPieceBytes, g.row_bytes - off);
     const uint4* src = reinterpret_cast<const uint4*>(g.src + row * g.src_stride + off);
     uint4* dst = reinterpret_cast<uint4*>(g.dst + row * g.dst_stride + off);
-    const int n = static_cast<int>(nbytes >> 4);
-    for (int i = lane; i < n; i += 128) {
-      uint4 v0, v1, v2, v3;
-      const bool h1 = i + 32 < n, h2 = i + 64 < n, h3 = i + 96 < n;
-      v0 = load16(src + i, kHostSrc);
-      if (h1) v1 = load16(src + i + 32, kHostSrc);
-      if (h2) v2 = load16(src + i + 64, kHostSrc);
-      if (h3) v3 = load16(src + i + 96, kHostSrc);
-      dst[i] = v0;
-      if (h1) dst[i + 32] = v1;
-      if (h2) dst[i + 64] = v2;
-      if (h3) dst[i + 96] = v3;
-    }
+    const int n = static_cast<int>(nbytes >> 4);  // <= 256 chunks: 8 per lane
+    uint4 v[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      if (lane + 32 * j < n) v[j] = load16(src + lane + 32 * j, kHostSrc);
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      if (lane + 32 * j < n) dst[lane + 32 * j] = v[j];
   }
 }
 
@@ -111,8 +108,14 @@ __global__ void __launch_bounds__(kCopyThreads) copy_segments_b16(const __grid_c
 struct SegBuilder {
   CopyParams p{};
   bool vec_ok = true;
+  bool full() const { return p.nseg == kMaxSegs; }
   void add(const void* src, void* dst, int64_t rows, int64_t row_bytes, int64_t src_stride, int64_t dst_stride) {
     if (rows <= 0 || row_bytes <= 0) return;
+    if (rows > 1 && src_stride == row_bytes && dst_stride == row_bytes) {
+      // Back-to-back rows on both sides: one long row.
+      row_bytes *= rows;
+      rows = 1;
+    }
     CopySeg& g = p.seg[p.nseg++];
     g.src = static_cast<const uint8_t*>(src);
     g.dst = static_cast<uint8_t*>(dst);
@@ -125,6 +128,10 @@ struct SegBuilder {
     p.total_units += rows * g.pieces;
     if (!aligned16(src) || !aligned16(dst) || (row_bytes & 15) || (rows > 1 && ((src_stride & 15) || (dst_stride & 15))))
       vec_ok = false;
+  }
+  void reset() {
+    p = CopyParams{};
+    vec_ok = true;
   }
 };
 
@@ -197,19 +204,26 @@ __global__ void __launch_bounds__(256) reduce_partials_scalar(const __grid_const
 
 extern "C" {
 
-tp_status tp_plan_shard(const void* weight, int64_t rows, int64_t cols, tp_style style, int tp_degree, int rank,
-                        const int64_t* fused_splits, int n_splits, int64_t num_heads, int64_t head_dim, void* dev_out,
-                        tp_stream_t stream) {
+tp_status tp_plan_shard_ranks(const void* weight, int64_t rows, int64_t cols, tp_style style, int tp_degree,
+                              int rank_begin, int rank_count, const int64_t* fused_splits, int n_splits,
+                              int64_t num_heads, int64_t head_dim, void* const* dev_outs, tp_stream_t stream) {
   using namespace tp;
   clear_error();
-  if (rank < 0) return fail(TP_ERR_INVALID_ARG, "rank %d is negative", rank);
+  if (rank_count < 0) return fail(TP_ERR_INVALID_ARG, "rank_count %d is negative", rank_count);
+  if (rank_begin < 0) return fail(TP_ERR_INVALID_ARG, "rank %d is negative", rank_begin);
   int64_t sizes[TP_MAX_SPLITS];
   int n = 0;
-  tp_status st = validate_plan(rows, cols, style, tp_degree, rank, num_heads, head_dim, fused_splits, n_splits, sizes, &n);
+  // Validate the whole plan (and the first and last rank) before touching any memory.
+  tp_status st = validate_plan(rows, cols, style, tp_degree, rank_count > 0 ? rank_begin : -1, num_heads, head_dim,
+                               fused_splits, n_splits, sizes, &n);
   if (st != TP_OK) return st;
+  if (rank_count > 0 && rank_begin + rank_count > tp_degree)
+    return fail(TP_ERR_INVALID_ARG, "ranks [%d, %d) outside [0, %d)", rank_begin, rank_begin + rank_count, tp_degree);
   const int64_t shard_elems = rows * cols / tp_degree;
-  if (shard_elems == 0) return TP_OK;
-  if (weight == nullptr || dev_out == nullptr) return fail(TP_ERR_INVALID_ARG, "weight or dev_out is NULL");
+  if (shard_elems == 0 || rank_count == 0) return TP_OK;
+  if (weight == nullptr || dev_outs == nullptr) return fail(TP_ERR_INVALID_ARG, "weight or dev_outs is NULL");
+  for (int i = 0; i < rank_count; ++i)
+    if (dev_outs[i] == nullptr) return fail(TP_ERR_INVALID_ARG, "dev_outs[%d] is NULL", i);
 
   // Where does the source live?  Page-locked host memory is read through its
   // device mapping; pageable host memory is refused rather than staged.
@@ -225,33 +239,72 @@ tp_status tp_plan_shard(const void* weight, int64_t rows, int64_t cols, tp_style
   } else if (attr.type == cudaMemoryTypeUnregistered) {
     return fail(TP_ERR_NOT_PINNED, "weight is pageable host memory; page-lock it (cudaHostAlloc/cudaHostRegister)");
   }
-  cudaPointerAttributes oattr{};
-  e = cudaPointerGetAttributes(&oattr, dev_out);
-  if (e != cudaSuccess) return cuda_fail(e, "cudaPointerGetAttributes(dev_out)");
-  if (oattr.type != cudaMemoryTypeDevice && oattr.type != cudaMemoryTypeManaged)
-    return fail(TP_ERR_INVALID_ARG, "dev_out is not device memory");
+  for (int i = 0; i < rank_count; ++i) {
+    cudaPointerAttributes oattr{};
+    e = cudaPointerGetAttributes(&oattr, dev_outs[i]);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaPointerGetAttributes(dev_out)");
+    if (oattr.type != cudaMemoryTypeDevice && oattr.type != cudaMemoryTypeManaged)
+      return fail(TP_ERR_INVALID_ARG, "dev_outs[%d] is not device memory", i);
+  }
 
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   SegBuilder b;
   const int64_t esz = 2;  // bf16
   const uint8_t* s8 = static_cast<const uint8_t*>(src);
-  uint8_t* d8 = static_cast<uint8_t*>(dev_out);
-  int64_t offset = 0;      // block offset along the sharded dimension
-  int64_t out_offset = 0;  // where this block's part starts in the shard
-  for (int bi = 0; bi < n; ++bi) {
-    const int64_t part = sizes[bi] / tp_degree;
-    const int64_t lo = offset + static_cast<int64_t>(rank) * part;
-    if (style == TP_COLWISE) {
-      // Rows [lo, lo+part) of W -> rows [out_offset, out_offset+part) of the shard.
-      b.add(s8 + lo * cols * esz, d8 + out_offset * cols * esz, part, cols * esz, cols * esz, cols * esz);
-    } else {
-      // Columns [lo, lo+part) of every row -> columns [out_offset, ...) of the shard.
-      const int64_t shard_cols = cols / tp_degree;
-      b.add(s8 + lo * esz, d8 + out_offset * esz, rows, part * esz, cols * esz, shard_cols * esz);
+  for (int i = 0; i < rank_count; ++i) {
+    const int rank = rank_begin + i;
+    uint8_t* d8 = static_cast<uint8_t*>(dev_outs[i]);
+    int64_t offset = 0;      // block offset along the sharded dimension
+    int64_t out_offset = 0;  // where this block's part starts in the shard
+    for (int bi = 0; bi < n; ++bi) {
+      const int64_t part = sizes[bi] / tp_degree;
+      const int64_t lo = offset + static_cast<int64_t>(rank) * part;
+      if (b.full()) {
+        st = launch_copy(b, host_src, s);
+        if (st != TP_OK) return st;
+        b.reset();
+      }
+      if (style == TP_COLWISE) {
+        // Rows [lo, lo+part) of W -> rows [out_offset, out_offset+part) of the shard.
+        b.add(s8 + lo * cols * esz, d8 + out_offset * cols * esz, part, cols * esz, cols * esz, cols * esz);
+      } else {
+        // Columns [lo, lo+part) of every row -> columns [out_offset, ...) of the shard.
+        const int64_t shard_cols = cols / tp_degree;
+        b.add(s8 + lo * esz, d8 + out_offset * esz, rows, part * esz, cols * esz, shard_cols * esz);
+      }
+      offset += sizes[bi];
+      out_offset += part;
     }
-    offset += sizes[bi];
-    out_offset += part;
   }
-  return launch_copy(b, host_src, reinterpret_cast<cudaStream_t>(stream));
+  return launch_copy(b, host_src, s);
+}
+
+tp_status tp_plan_shard(const void* weight, int64_t rows, int64_t cols, tp_style style, int tp_degree, int rank,
+                        const int64_t* fused_splits, int n_splits, int64_t num_heads, int64_t head_dim, void* dev_out,
+                        tp_stream_t stream) {
+  using namespace tp;
+  if (rank < 0 || rank >= tp_degree) {
+    clear_error();
+    // Report plan errors first (they do not depend on the rank), then the rank itself.
+    int64_t sizes[TP_MAX_SPLITS];
+    int n = 0;
+    tp_status st = validate_plan(rows, cols, style, tp_degree, -1, num_heads, head_dim, fused_splits, n_splits,
+                                 sizes, &n);
+    if (st != TP_OK) return st;
+    return fail(TP_ERR_INVALID_ARG, "rank %d outside [0, %d)", rank, tp_degree);
+  }
+  void* outs[1] = {dev_out};
+  if (dev_out == nullptr && rows * cols != 0) {
+    clear_error();
+    int64_t sizes[TP_MAX_SPLITS];
+    int n = 0;
+    tp_status st = validate_plan(rows, cols, style, tp_degree, rank, num_heads, head_dim, fused_splits, n_splits,
+                                 sizes, &n);
+    if (st != TP_OK) return st;
+    return fail(TP_ERR_INVALID_ARG, "dev_out is NULL");
+  }
+  return tp_plan_shard_ranks(weight, rows, cols, style, tp_degree, rank, 1, fused_splits, n_splits, num_heads,
+                             head_dim, outs, stream);
 }
 
 tp_status tp_combine(tp_combine_mode mode, const void* const* partials, int tp_degree, int64_t T, int64_t N_each,

@@ -18,7 +18,7 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 HEADER = os.path.join(ROOT, "include", "tp.h")
 
 tp = pytest.importorskip("tensor_sharded_linear_tp_gb300",
-                         reason="libtp.so not built (python -m tensor_sharded_linear_tp_gb300.build)")
+                         reason="libtp.so not built (python tensor_sharded_linear_tp_gb300/build.py)")
 
 REASON_TO_STATUS = {"OK": "TP_OK", O.INVALID_ARG: "TP_ERR_INVALID_ARG",
                     O.HEADS_NOT_DIVISIBLE: "TP_ERR_HEADS_NOT_DIVISIBLE",

@@ -78,6 +78,24 @@ def test_extract_bit_exact(case, source):
         assert got.shape == exp.shape and np.array_equal(got, exp), (case, r)
 
 
+@pytest.mark.parametrize("source", ["device", "pinned_host"])
+def test_extract_all_ranks_one_launch(source):
+    # 3 packed blocks x 8 ranks = 24 segments in one launch; 16 blocks x 8 ranks spills past 64 segments.
+    for rows, cols, style, p, splits in ((3 * 64, 48, "colwise", 8, [64, 64, 64]), (128, 24, "colwise", 8, [8] * 16),
+                                         (16, 64, "rowwise", 8, [32, 32])):
+        w = tp_inputs.random_bits(105, rows + cols, (rows, cols))
+        src = dev(w) if source == "device" else pinned(w)
+        outs = tp.tp_plan_shard_ranks(src, style, p, fused_splits=splits, device=DEV)
+        for r in range(p):
+            assert np.array_equal(host_bits(outs[r]), O.shard(w, style, p, r, splits)), (rows, r)
+        mid = tp.tp_plan_shard_ranks(src, style, p, 2, 3, fused_splits=splits, device=DEV)
+        for i in range(3):
+            assert np.array_equal(host_bits(mid[i]), O.shard(w, style, p, 2 + i, splits))
+    with pytest.raises(tp.TPError) as e:
+        tp.tp_plan_shard_ranks(dev(w), "rowwise", 8, 6, 3, fused_splits=[32, 32], device=DEV)
+    assert e.value.name == "TP_ERR_INVALID_ARG"
+
+
 def test_extract_pageable_host_refused():
     w = tp.bf16_from_bits(tp_inputs.random_bits(101, 0, (16, 16)))   # ordinary (pageable) CPU tensor
     with pytest.raises(tp.TPError) as e:
