@@ -238,6 +238,42 @@ TP_API tp_status tp_linear_rowwise(const void* const* x_shards, const void* cons
 /* Bytes of device workspace tp_linear_rowwise needs for `mode` (0 unless TP_REDUCE_WORKSPACE). */
 TP_API size_t tp_rowwise_workspace_bytes(int tp_degree, int64_t T, int64_t N, tp_reduce_mode mode);
 
+/* Size of the library's built-in scratch array used by tp_linear_rowwise_noalloc (64 MiB per GPU). */
+#define TP_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
+
+/*
+ * tp_linear_rowwise_noalloc -- tp_linear_rowwise in TP_REDUCE_WORKSPACE mode,
+ * for callers that cannot allocate device memory.  The pages have no
+ * counterpart of this call; it exists for the host program, not the method.
+ *
+ * Who needs it: code that runs where allocating is not allowed or not
+ * possible -- for instance a plug-in called by a framework that owns all
+ * device memory and hands out none, or a process whose memory was claimed up
+ * front by a pool so that a new cudaMalloc would fail (cudaMalloc can also
+ * stall the whole device, which latency-bound callers must avoid).  Such a
+ * caller still passes its inputs and output; the fp32 partials and tile
+ * counters live in one fixed array compiled into this library
+ * (TP_NOALLOC_SCRATCH_BYTES of device memory, held by every GPU that loads the
+ * library until the process exits).
+ *
+ * Arguments, layout, result and numerics are those of tp_linear_rowwise with
+ * mode TP_REDUCE_WORKSPACE: x_shards/w_shards are host arrays of tp_degree
+ * device pointers (bf16 [T, K_r] and [N, K_r]), bias is NULL or bf16 [N]
+ * (added once), out is bf16 [T, N].
+ * Limits: the call is refused with TP_ERR_WORKSPACE, before any device work,
+ * when tp_rowwise_workspace_bytes(tp_degree, T, N, TP_REDUCE_WORKSPACE)
+ * exceeds TP_NOALLOC_SCRATCH_BYTES (roughly tp_degree * T * N <= 16M).
+ * The first call on a device looks up the array's device address (once per
+ * device, with that device current); make that first call before any stream
+ * capture.  No allocation happens in this call or the ones it makes.
+ * Every call uses the same array and it keeps the last call's contents; the
+ * call clears the tile counters itself.  Calls whose kernels overlap on the
+ * GPU (other streams, other threads) race on the array: serialise them.
+ */
+TP_API tp_status tp_linear_rowwise_noalloc(const void* const* x_shards, const void* const* w_shards, const void* bias,
+                                           int tp_degree, int64_t T, int64_t K_r, int64_t N, void* out,
+                                           tp_stream_t stream);
+
 /* ------------------------------------------------------------------------ */
 /* Join                                                                      */
 /* ------------------------------------------------------------------------ */

@@ -53,6 +53,8 @@ _SIGS = {
                                     _i64, _i64, ctypes.POINTER(_vp), _i64, _vp]),
     "tp_linear_rowwise": (_status, [ctypes.POINTER(_vp), ctypes.POINTER(_vp), _vp, ctypes.c_int, _i64, _i64, _i64,
                                     ctypes.c_int, _vp, ctypes.c_size_t, _vp, _vp]),
+    "tp_linear_rowwise_noalloc": (_status, [ctypes.POINTER(_vp), ctypes.POINTER(_vp), _vp, ctypes.c_int, _i64, _i64,
+                                            _i64, _vp, _vp]),
     "tp_rowwise_workspace_bytes": (ctypes.c_size_t, [ctypes.c_int, _i64, _i64, ctypes.c_int]),
     "tp_combine": (_status, [ctypes.c_int, ctypes.POINTER(_vp), ctypes.c_int, _i64, _i64, _vp, _vp]),
     "tp_last_error": (ctypes.c_char_p, []),
@@ -232,6 +234,31 @@ def tp_linear_rowwise(x_shards: Sequence[torch.Tensor], w_shards: Sequence[torch
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     _check(lib.tp_linear_rowwise(_ptrs(x_shards), _ptrs(w_shards), _ptr(bias), p, T, K_r, N, REDUCE_MODES[mode],
                                  _ptr(workspace), ws_bytes, _ptr(out), _stream(stream)))
+    return out
+
+
+NOALLOC_SCRATCH_BYTES = 64 << 20
+
+
+def tp_linear_rowwise_noalloc(x_shards: Sequence[torch.Tensor], w_shards: Sequence[torch.Tensor],
+                              bias: torch.Tensor | None = None, out: torch.Tensor | None = None,
+                              stream=None) -> torch.Tensor:
+    """Rowwise projection with the summed partials, using the library's built-in scratch.
+
+    For callers that may not allocate device memory: the fp32 partials live in
+    a fixed 64 MiB array inside libtp.so instead of a caller workspace.  Only
+    ``out`` (bf16 [T, N]) is allocated here, and only when none is passed.
+    Calls that overlap on the GPU share that array and must be serialised.
+    """
+    p = len(w_shards)
+    T, K_r = x_shards[0].shape
+    N = w_shards[0].shape[0]
+    for t in list(x_shards) + list(w_shards):
+        _need_bf16("shard", t)
+    if out is None:
+        out = torch.empty((T, N), dtype=torch.bfloat16, device=x_shards[0].device)
+    _check(lib.tp_linear_rowwise_noalloc(_ptrs(x_shards), _ptrs(w_shards), _ptr(bias), p, T, K_r, N, _ptr(out),
+                                         _stream(stream)))
     return out
 
 

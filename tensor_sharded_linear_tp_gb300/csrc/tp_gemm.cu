@@ -673,3 +673,62 @@ tp_status tp_linear_rowwise(const void* const* x_shards, const void* const* w_sh
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Rowwise workspace mode for callers that cannot allocate: the scratch is a
+// fixed array compiled into the library.  Host code must not pass the
+// array's name to a kernel (on the host it is only a stand-in symbol); its
+// device address is looked up once per device and cached.
+// ---------------------------------------------------------------------------
+
+namespace tp {
+namespace {
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[TP_NOALLOC_SCRATCH_BYTES];
+
+std::mutex g_noalloc_mutex;
+void* g_noalloc_ptr[64] = {nullptr};
+
+tp_status noalloc_scratch(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= 64) return fail(TP_ERR_UNSUPPORTED, "device index %d above 63", dev);
+  std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+  if (g_noalloc_ptr[dev] == nullptr) {
+    void* ptr = nullptr;
+    e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(built-in scratch)");
+    g_noalloc_ptr[dev] = ptr;
+  }
+  *out = g_noalloc_ptr[dev];
+  return TP_OK;
+}
+
+}  // namespace
+}  // namespace tp
+
+extern "C" tp_status tp_linear_rowwise_noalloc(const void* const* x_shards, const void* const* w_shards,
+                                               const void* bias, int tp_degree, int64_t T, int64_t K_r, int64_t N,
+                                               void* out, tp_stream_t stream) {
+  using namespace tp;
+  clear_error();
+  if (tp_degree < 1 || tp_degree > TP_MAX_DEGREE || T < 0 || N < 0 || K_r < 0)
+    // Argument errors are reported by the shared entry point, before any device work.
+    return tp_linear_rowwise(x_shards, w_shards, bias, tp_degree, T, K_r, N, TP_REDUCE_WORKSPACE, nullptr, 0, out,
+                             stream);
+  const size_t need = tp_rowwise_workspace_bytes(tp_degree, T, N, TP_REDUCE_WORKSPACE);
+  if (need > TP_NOALLOC_SCRATCH_BYTES)
+    return fail(TP_ERR_WORKSPACE,
+                "tp_degree=%d, T=%lld, N=%lld needs %zu bytes of scratch; the built-in array holds %zu "
+                "(TP_NOALLOC_SCRATCH_BYTES): pass a workspace to tp_linear_rowwise instead",
+                tp_degree, (long long)T, (long long)N, need, (size_t)TP_NOALLOC_SCRATCH_BYTES);
+  if (need == 0)  // empty problem: nothing to launch, nothing to look up
+    return tp_linear_rowwise(x_shards, w_shards, bias, tp_degree, T, K_r, N, TP_REDUCE_WORKSPACE, nullptr, 0, out,
+                             stream);
+  void* scratch = nullptr;
+  tp_status st = noalloc_scratch(&scratch);
+  if (st != TP_OK) return st;
+  return tp_linear_rowwise(x_shards, w_shards, bias, tp_degree, T, K_r, N, TP_REDUCE_WORKSPACE, scratch,
+                           TP_NOALLOC_SCRATCH_BYTES, out, stream);
+}
