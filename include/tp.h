@@ -74,7 +74,7 @@ typedef enum { TP_GATHER = 0, TP_REDUCE = 1 } tp_combine_mode;
 typedef enum { TP_ACT_NONE = 0, TP_ACT_GELU_TANH = 1, TP_ACT_SWIGLU = 2 } tp_act;
 typedef enum {
   TP_REDUCE_NONE = 0,      /* write every rank's fp32 partial; join later with tp_combine(TP_REDUCE) */
-  TP_REDUCE_WORKSPACE = 1, /* fp32 partials to a workspace; the last rank to finish a tile sums them */
+  TP_REDUCE_WORKSPACE = 1, /* fp32 partials to a workspace, summed in the GEMM epilogue by the ranks */
   TP_REDUCE_ACCUM = 2      /* each tile's ranks accumulate in turn into one fp32 on-chip accumulator */
 } tp_reduce_mode;
 
@@ -220,11 +220,13 @@ TP_API tp_status tp_linear_colwise(const void* x, const void* const* w_shards, c
  *   TP_REDUCE_ACCUM: for each output tile, rank 0's, then rank 1's, ...
  *     products accumulate into one fp32 tensor-memory accumulator; out is
  *     bf16 [T, N].  No workspace (ws_bytes may be 0).
- *   TP_REDUCE_WORKSPACE: each rank's fp32 partial tile goes to `workspace`;
- *     the last rank to finish a tile (atomic per-tile counter, no spinning)
- *     sums the tp_degree partials in rank order and writes bf16 [T, N] to out.
- *     Needs ws_bytes >= tp_rowwise_workspace_bytes(...).  The counters are
- *     cleared on `stream` by the call itself.
+ *   TP_REDUCE_WORKSPACE: each rank's fp32 partial tile goes to `workspace`
+ *     and is counted on a per-tile atomic counter; when all tp_degree partials
+ *     of a tile are in (a bounded wait; the launch is cooperative so the ranks'
+ *     CTAs are resident together), each rank sums its 1/tp_degree share of the
+ *     tile's rows in rank order and writes bf16 [T, N] to out.  Needs
+ *     ws_bytes >= tp_rowwise_workspace_bytes(...).  The counters are cleared on
+ *     `stream` by the call itself.
  *   TP_REDUCE_NONE: out is fp32 [tp_degree][T][N], rank r's partial (the bias,
  *     if any, is added to rank 0's partial only); join with tp_combine.
  * Alignment (TP_ERR_ALIGNMENT): K_r % 8 == 0, N % 8 == 0, pointers 16-byte

@@ -10,17 +10,27 @@
 //                same fp32 TMEM accumulator -- the partial sums are joined on
 //                chip, in rank order, and written once as bf16.
 //     WORKSPACE  work item = (rank, m-tile, n-tile) with the rank varying
-//                fastest; each rank writes its fp32 partial tile, then an
-//                atomic per-tile counter elects the last rank to finish, which
-//                sums the partials in rank order and writes bf16 (no spin).
+//                fastest; each rank writes its fp32 partial tile to the
+//                workspace and counts it on an atomic per-tile counter; once
+//                all tp_degree partials are in (bounded wait), each rank sums
+//                its 1/tp_degree share of the tile's rows in rank order and
+//                writes bf16.
 //     NONE       work item = (rank, m-tile, n-tile); fp32 partials out.
 //
-// CTA layout (192 threads, one CTA per SM, grid = min(#tiles, #SMs)):
-//   warp 0      TMA producer: A (128 x 64) and B (256 x 64) bf16 boxes with
-//               128-byte swizzle into a 4-stage shared-memory ring.
-//   warp 1      MMA issuer: one thread issues tcgen05.mma (M=128, N=256,
-//               K=16) into one of two TMEM accumulators (2 x 256 columns),
-//               so the epilogue of tile i overlaps the main loop of tile i+1.
+// Two tile shapes share one kernel template:
+//   single CTA  128 x 256 output tile per CTA, grid = min(#tiles, #SMs),
+//               4-stage ring of A (128 x 64) + B (256 x 64) bf16 boxes;
+//   CTA pair    256 x 256 output tile per cluster of two CTAs (used when the
+//               output has more than 128 rows): each CTA stages its 128 rows
+//               of A and 128 rows of B (6-stage ring, 32 KB per stage), and
+//               the even CTA issues cta_group::2 MMAs (M=256) that read both
+//               CTAs' shared memory -- half the B traffic per SM of the
+//               single-CTA tile, which is shared-memory-bandwidth bound.
+// CTA layout (192 threads, one CTA per SM):
+//   warp 0      TMA producer, 128-byte swizzled boxes into the ring.
+//   warp 1      MMA issuer: one thread issues tcgen05.mma (K=16 steps) into
+//               one of two TMEM accumulators (2 x 256 columns), so the
+//               epilogue of tile i overlaps the main loop of tile i+1.
 //   warps 2..5  epilogue: tcgen05.ld 32 columns at a time, bias, activation
 //               (GELU-tanh or SwiGLU) in fp32, round to bf16, store.
 //
@@ -40,27 +50,36 @@
 namespace tp {
 namespace {
 
-constexpr int BM = 128;
-constexpr int BN = 256;
-constexpr int BK = 64;
-constexpr int STAGES = 4;
+constexpr int BM = 128;        // accumulator rows per CTA (TMEM lanes)
+constexpr int BN = 256;        // accumulator columns per tile
+constexpr int BK = 64;         // K per stage: one 128-byte swizzle row of bf16
 constexpr int GROUP_M = 16;
 constexpr int kThreads = 192;
-constexpr int kTmemCols = 512;
-constexpr uint32_t A_BYTES = BM * BK * 2;
-constexpr uint32_t B_BYTES = BN * BK * 2;
-constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int kTmemCols = 512; // two accumulators of BN columns
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
 enum Epi : int { EPI_BF16 = 0, EPI_GELU = 1, EPI_SWIGLU = 2, EPI_F32 = 3, EPI_WS_REDUCE = 4 };
 
+// Tile shape of the single-CTA (kPair = false) and CTA-pair (kPair = true) kernels.
+template <bool kPair>
+struct Cfg {
+  static constexpr int TILE_M = kPair ? 2 * BM : BM;   // output rows per work tile
+  static constexpr int B_ROWS = kPair ? BN / 2 : BN;   // B rows each CTA stages
+  static constexpr int STAGES = kPair ? 6 : 4;
+  static constexpr uint32_t A_BYTES = BM * BK * 2;
+  static constexpr uint32_t B_BYTES = B_ROWS * BK * 2;
+  static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
+};
+
 struct GemmParams {
   CUtensorMap map_a[TP_MAX_DEGREE];
   CUtensorMap map_b[TP_MAX_DEGREE];
+  CUtensorMap map_out[TP_MAX_DEGREE];        // per output group: 64 x 32 bf16 or 32 x 32 fp32 store boxes
+  CUtensorMap map_out_tail[TP_MAX_DEGREE];   // per output group: 32 x 32 bf16 boxes (odd multiples of 32)
   void* out[TP_MAX_DEGREE];                  // per output group
   const __nv_bfloat16* bias[TP_MAX_DEGREE];  // per output group, nullable
   float* ws;                                 // WS_REDUCE: fp32 partials [n_groups][M][N]
-  int* counters;                             // WS_REDUCE: [m_tiles * n_tiles]
+  int* counters;                             // WS_REDUCE: one per 128 x 256 output block
   __nv_bfloat16* reduce_out;                 // WS_REDUCE: bf16 [M][ldo]
   const __nv_bfloat16* reduce_bias;          // WS_REDUCE: nullable [N]
   unsigned int* status;
@@ -70,14 +89,16 @@ struct GemmParams {
   int n_ksegs;        // K segments per tile (ranks) -- >1 only for ACCUM
   int kblocks;        // 64-wide K blocks per segment
   int m_tiles, n_tiles;
+  int bn;             // accumulator columns per tile: a multiple of 32, <= 256 (256 for SwiGLU)
+  int n_counters;     // WS_REDUCE: counters per 128-row block (one per n-tile)
   int b_up_row;       // SwiGLU: first row of the up block inside W_r
   int rank_fastest;   // tile order with the rank varying fastest
   int a_shared;       // one A map for every rank (colwise)
 };
 
 struct alignas(8) SmemCtrl {
-  uint64_t full[STAGES];
-  uint64_t empty[STAGES];
+  uint64_t full[8];
+  uint64_t empty[8];
   uint64_t tfull[2];
   uint64_t tempty[2];
   uint64_t drain;
@@ -86,14 +107,26 @@ struct alignas(8) SmemCtrl {
   int is_last;
 };
 
-constexpr size_t kSmemBytes = 1024 /*alignment slack*/ + STAGES * STAGE_BYTES + sizeof(SmemCtrl);
+// Epilogue staging: every epilogue warp owns two 4 KB buffers (a 32 x 32 fp32 or bf16 chunk each),
+// written with swizzled 16-byte stores and sent to global memory by TMA stores.
+constexpr uint32_t kStageBuf = 4096;
+constexpr uint32_t kStagingBytes = 4 /*warps*/ * 2 * kStageBuf;
+
+template <bool kPair>
+constexpr size_t smem_bytes() {
+  return 1024 /*alignment slack*/ + Cfg<kPair>::STAGES * Cfg<kPair>::STAGE_BYTES + kStagingBytes + sizeof(SmemCtrl);
+}
 
 __device__ __forceinline__ void decode_tile(const GemmParams& p, int t, int& g, int& mb, int& nb) {
   const int tiles_mn = p.m_tiles * p.n_tiles;
   int mn;
   if (p.rank_fastest) {
-    g = t % p.n_groups;
+    // The ranks of one (m, n) tile are consecutive work items, so they run at the
+    // same time on different CTAs and their partials meet in L2.  The rank is
+    // rotated by the tile index so that a persistent CTA does not get the same
+    // rank on every tile (with #CTAs a multiple of tp_degree it would).
     mn = t / p.n_groups;
+    g = (t + mn) % p.n_groups;
   } else {
     g = t / tiles_mn;
     mn = t - g * tiles_mn;
@@ -111,12 +144,16 @@ __device__ __forceinline__ void decode_tile(const GemmParams& p, int t, int& g, 
 
 // Bounded wait: true when the phase completed; false when this CTA is aborting
 // (another role gave up) or the wait itself ran out of time.
+template <bool kClusterScope = false>
 __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                              unsigned int* status, bool ignore_abort) {
-  if (ptx::mbar_try_wait(bar, parity)) return true;
+  auto probe = [&]() {
+    return kClusterScope ? ptx::mbar_try_wait_cluster(bar, parity) : ptx::mbar_try_wait(bar, parity);
+  };
+  if (probe()) return true;
   const uint64_t t0 = ptx::globaltimer_ns();
   for (uint32_t i = 1;; ++i) {
-    if (ptx::mbar_try_wait(bar, parity)) return true;
+    if (probe()) return true;
     if ((i & 63u) == 0) {
       if (!ignore_abort && *abort_flag) return false;
       if (ptx::globaltimer_ns() - t0 > kWaitLimitNs) {
@@ -128,6 +165,23 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, vola
   }
 }
 
+// Bounded wait until *ctr >= target (a tile counter other CTAs increment); false on abort or timeout.
+__device__ __noinline__ bool wait_counter(const int* ctr, int target, volatile int* abort_flag, unsigned int* status) {
+  const uint64_t t0 = ptx::globaltimer_ns();
+  for (;;) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(ctr) : "memory");
+    if (v >= target) return true;
+    if (*abort_flag) return false;
+    if (ptx::globaltimer_ns() - t0 > kWaitLimitNs) {
+      *abort_flag = 1;
+      atomicOr(status, TP_DEVSTATUS_TIMEOUT);
+      return false;
+    }
+    __nanosleep(100);
+  }
+}
+
 __device__ __forceinline__ float gelu_tanh_f(float x) {
   const float k0 = 0.7978845608028654f;  // sqrt(2/pi)
   const float k1 = 0.044715f;
@@ -135,53 +189,310 @@ __device__ __forceinline__ float gelu_tanh_f(float x) {
 }
 __device__ __forceinline__ float silu_f(float x) { return x / (1.0f + __expf(-x)); }
 
-// Store 32 consecutive fp32 values as bf16 (64 bytes), masked at 8-column granularity.
-__device__ __forceinline__ void store_bf16x32(__nv_bfloat16* dst, const float (&f)[32], int valid_cols) {
-  uint32_t packed[16];
+// Epilogue output path.  A warp drains its 32 rows (one row per lane) in chunks:
+// 64 bf16 columns or 32 fp32 columns (128-byte rows, 4 KB per chunk), plus a
+// 32-column bf16 chunk for a tile width that is an odd multiple of 32.  A chunk is
+// written to one of the warp's two shared-memory buffers with 16-byte stores in
+// the tensor map's swizzled order -- 128-byte swizzle: 16-byte piece j of row r
+// sits in slot j ^ (r & 7); 64-byte swizzle (32 bf16 columns): slot j ^ ((r >> 1) & 3)
+// -- so the 32 lanes hit all banks, and then sent to global memory by one TMA store
+// (rows and columns outside the output are clipped).  A buffer is reused only after
+// its previous store has finished reading it.
+__device__ __forceinline__ uint32_t stage_buffer(uint32_t wbuf, int nchunk, int lane) {
+  const uint32_t buf = wbuf + static_cast<uint32_t>(nchunk & 1) * kStageBuf;
+  if (nchunk >= 2) {
+    if (lane == 0) ptx::bulk_wait_read_1();
+    __syncwarp();
+  }
+  return buf;
+}
+
+__device__ __forceinline__ void stage_issue(const CUtensorMap* map, uint32_t buf, int& nchunk, int lane, int x,
+                                            int y) {
+  ptx::fence_proxy_async_smem();  // make the generic-proxy writes visible to the TMA engine
+  __syncwarp();
+  if (lane == 0) {
+    ptx::tma_store_2d(map, buf, x, y);
+    ptx::bulk_commit();
+  }
+  ++nchunk;
+}
+
+__device__ __forceinline__ void pack_bf16x32(const float (&f)[32], uint32_t (&packed)[16]) {
 #pragma unroll
   for (int j = 0; j < 16; ++j) {
     __nv_bfloat162 h = __floats2bfloat162_rn(f[2 * j], f[2 * j + 1]);
     packed[j] = *reinterpret_cast<uint32_t*>(&h);
   }
-  uint4* d = reinterpret_cast<uint4*>(dst);
-#pragma unroll
-  for (int q = 0; q < 4; ++q)
-    if (8 * q < valid_cols) d[q] = make_uint4(packed[4 * q], packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]);
 }
 
-__device__ __forceinline__ void store_f32x32(float* dst, const uint32_t (&v)[32], float b0, const float* bvec,
-                                             int valid_cols) {
-  float4* d = reinterpret_cast<float4*>(dst);
+// fp32: 32 columns.
+__device__ __forceinline__ void stage_store_f32(const CUtensorMap* map, uint32_t wbuf, int& nchunk, int lane,
+                                                const float (&f)[32], int x, int y) {
+  const uint32_t buf = stage_buffer(wbuf, nchunk, lane);
+  const uint32_t row = buf + static_cast<uint32_t>(lane) * 128;
 #pragma unroll
-  for (int q = 0; q < 8; ++q) {
-    if (4 * q < valid_cols) {
-      float4 o;
-      o.x = __uint_as_float(v[4 * q + 0]) + (bvec ? bvec[4 * q + 0] : b0);
-      o.y = __uint_as_float(v[4 * q + 1]) + (bvec ? bvec[4 * q + 1] : b0);
-      o.z = __uint_as_float(v[4 * q + 2]) + (bvec ? bvec[4 * q + 2] : b0);
-      o.w = __uint_as_float(v[4 * q + 3]) + (bvec ? bvec[4 * q + 3] : b0);
-      d[q] = o;
+  for (int j = 0; j < 8; ++j)
+    ptx::st_shared_v4(row + (static_cast<uint32_t>(j ^ (lane & 7)) << 4), __float_as_uint(f[4 * j]),
+                      __float_as_uint(f[4 * j + 1]), __float_as_uint(f[4 * j + 2]), __float_as_uint(f[4 * j + 3]));
+  stage_issue(map, buf, nchunk, lane, x, y);
+}
+
+// bf16: 64 columns given as two halves of 32.
+__device__ __forceinline__ void stage_store_bf16x64(const CUtensorMap* map, uint32_t wbuf, int& nchunk, int lane,
+                                                    const float (&lo)[32], const float (&hi)[32], int x, int y) {
+  const uint32_t buf = stage_buffer(wbuf, nchunk, lane);
+  const uint32_t row = buf + static_cast<uint32_t>(lane) * 128;
+  uint32_t packed[16];
+  pack_bf16x32(lo, packed);
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+    ptx::st_shared_v4(row + (static_cast<uint32_t>(j ^ (lane & 7)) << 4), packed[4 * j], packed[4 * j + 1],
+                      packed[4 * j + 2], packed[4 * j + 3]);
+  pack_bf16x32(hi, packed);
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+    ptx::st_shared_v4(row + (static_cast<uint32_t>((4 + j) ^ (lane & 7)) << 4), packed[4 * j], packed[4 * j + 1],
+                      packed[4 * j + 2], packed[4 * j + 3]);
+  stage_issue(map, buf, nchunk, lane, x, y);
+}
+
+// bf16: 32 columns (the last chunk of a tile whose width is an odd multiple of 32).
+__device__ __forceinline__ void stage_store_bf16x32(const CUtensorMap* map, uint32_t wbuf, int& nchunk, int lane,
+                                                    const float (&f)[32], int x, int y) {
+  const uint32_t buf = stage_buffer(wbuf, nchunk, lane);
+  const uint32_t row = buf + static_cast<uint32_t>(lane) * 64;
+  uint32_t packed[16];
+  pack_bf16x32(f, packed);
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+    ptx::st_shared_v4(row + (static_cast<uint32_t>(j ^ ((lane >> 1) & 3)) << 4), packed[4 * j], packed[4 * j + 1],
+                      packed[4 * j + 2], packed[4 * j + 3]);
+  stage_issue(map, buf, nchunk, lane, x, y);
+}
+
+// One accumulator tile: 128 rows (this CTA's TMEM lanes) x p.bn columns; this warp drains
+// its 32 rows [row0, row0 + 32), one row per lane, 32 columns at a time.
+// `release` is called once, right after the last TMEM read, to hand the accumulator back to
+// the MMA warp.  Out-of-range rows and columns are clipped by the TMA stores.
+template <int kEpi, typename Release>
+__device__ __forceinline__ void epilogue_tile(const GemmParams& p, SmemCtrl* ctl, uint32_t taddr, uint32_t wbuf,
+                                              int& nchunk, int g, int row0, int mb128, int nb, int lane, int epi_tid,
+                                              Release release) {
+  const CUtensorMap* omap = &p.map_out[g];
+  if constexpr (kEpi == EPI_SWIGLU) {
+    const __nv_bfloat16* bias = p.bias[g];
+    auto swiglu32 = [&](const uint32_t (&gv)[32], const uint32_t (&uv)[32], int col0, float (&f)[32]) {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const int col = col0 + j;
+        float gg = __uint_as_float(gv[j]);
+        float uu = __uint_as_float(uv[j]);
+        if (bias != nullptr && col < p.N) {
+          gg += __bfloat162float(bias[col]);
+          uu += __bfloat162float(bias[p.b_up_row + col]);
+        }
+        f[j] = silu_f(gg) * uu;
+      }
+    };
+#pragma unroll 1
+    for (int c = 0; c < BN / 2; c += 64) {
+      const int col0 = nb * (BN / 2) + c;
+      float lo[32], hi[32];
+      {
+        uint32_t gv[32], uv[32];
+        ptx::tmem_ld_32x32b_x32(taddr + c, gv);
+        ptx::tmem_ld_32x32b_x32(taddr + BN / 2 + c, uv);
+        ptx::tmem_ld_wait();
+        swiglu32(gv, uv, col0, lo);
+      }
+      {
+        uint32_t gv[32], uv[32];
+        ptx::tmem_ld_32x32b_x32(taddr + c + 32, gv);
+        ptx::tmem_ld_32x32b_x32(taddr + BN / 2 + c + 32, uv);
+        ptx::tmem_ld_wait();
+        if (c + 64 >= BN / 2) release();
+        swiglu32(gv, uv, col0 + 32, hi);
+      }
+      if (col0 < p.N) stage_store_bf16x64(omap, wbuf, nchunk, lane, lo, hi, col0, row0);
+    }
+  } else if constexpr (kEpi == EPI_BF16 || kEpi == EPI_GELU) {
+    const __nv_bfloat16* bias = p.bias[g];
+    auto act32 = [&](const uint32_t (&v)[32], int col0, float (&f)[32]) {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        float x = __uint_as_float(v[j]);
+        if (bias != nullptr && col0 + j < p.N) x += __bfloat162float(bias[col0 + j]);
+        f[j] = (kEpi == EPI_GELU) ? gelu_tanh_f(x) : x;
+      }
+    };
+#pragma unroll 1
+    for (int c = 0; c < p.bn; c += 64) {
+      const int col0 = nb * p.bn + c;
+      const bool pair64 = c + 64 <= p.bn;
+      float lo[32], hi[32];
+      {
+        uint32_t v[32];
+        ptx::tmem_ld_32x32b_x32(taddr + c, v);
+        ptx::tmem_ld_wait();
+        if (!pair64) release();
+        act32(v, col0, lo);
+      }
+      if (pair64) {
+        uint32_t v[32];
+        ptx::tmem_ld_32x32b_x32(taddr + c + 32, v);
+        ptx::tmem_ld_wait();
+        if (c + 64 >= p.bn) release();
+        act32(v, col0 + 32, hi);
+        if (col0 < p.N) stage_store_bf16x64(omap, wbuf, nchunk, lane, lo, hi, col0, row0);
+      } else if (col0 < p.N) {
+        stage_store_bf16x32(&p.map_out_tail[g], wbuf, nchunk, lane, lo, col0, row0);
+      }
+    }
+  } else {
+    // fp32 partial tile: to the caller's buffer (EPI_F32) or this rank's workspace plane (EPI_WS_REDUCE).
+    const __nv_bfloat16* bias = (kEpi == EPI_F32) ? p.bias[g] : nullptr;
+#pragma unroll 1
+    for (int c = 0; c < p.bn; c += 32) {
+      uint32_t v[32];
+      ptx::tmem_ld_32x32b_x32(taddr + c, v);
+      ptx::tmem_ld_wait();
+      if (c + 32 >= p.bn) release();
+      const int col0 = nb * p.bn + c;
+      if (col0 < p.N) {
+        float f[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          f[j] = __uint_as_float(v[j]);
+          if (bias != nullptr && col0 + j < p.N) f[j] += __bfloat162float(bias[col0 + j]);
+        }
+        stage_store_f32(omap, wbuf, nchunk, lane, f, col0, row0);
+      }
+    }
+    if constexpr (kEpi == EPI_WS_REDUCE) {
+      // Publish this rank's partial of the 128-row block, count it, wait until every
+      // rank's partial is in, then sum this rank's 1/tp_degree share of the block's rows
+      // (all partials, in rank order).  Every CTA of the tile sums an equal share, so no
+      // CTA is left with all the sums; the launch is cooperative, so the CTAs that wait
+      // on each other are resident together, and the wait is bounded.
+      if (mb128 * BM < p.M) {
+        if (lane == 0) {
+          ptx::bulk_wait_all();             // this warp's partial stores are complete ...
+          ptx::fence_proxy_async_global();  // ... and ordered before what follows
+        }
+        __syncwarp();
+        __threadfence();
+        ptx::named_bar_sync(1, 128);
+        int* ctr = &p.counters[mb128 * p.n_counters + nb];
+        if (epi_tid == 0) {
+          atomicAdd(ctr, 1);
+          const bool ready = wait_counter(ctr, p.n_groups, reinterpret_cast<volatile int*>(&ctl->abort), p.status);
+          *reinterpret_cast<volatile int*>(&ctl->is_last) = ready ? 1 : 0;
+        }
+        ptx::named_bar_sync(1, 128);
+        if (*reinterpret_cast<volatile int*>(&ctl->is_last) != 0) {
+          __threadfence();
+          const int block0 = mb128 * BM;
+          const int rows = min(BM, p.M - block0);
+          const int lo = block0 + g * rows / p.n_groups;
+          const int hi = block0 + (g + 1) * rows / p.n_groups;
+          const int col = nb * p.bn + lane * 8;
+          const bool col_ok = lane * 8 < p.bn && col < p.N;
+          const int64_t plane = static_cast<int64_t>(p.M) * p.N;
+          const int warp_e = epi_tid >> 5;
+#pragma unroll 1
+          for (int row = lo + warp_e; row < hi; row += 8) {
+            // Two rows per pass (row and row + 4), every rank's loads in flight before the adds.
+            const bool ok1 = row + 4 < hi;
+            float a8[2][8];
+#pragma unroll
+            for (int u = 0; u < 2; ++u)
+#pragma unroll
+              for (int j = 0; j < 8; ++j) a8[u][j] = 0.f;
+            if (col_ok) {
+              const float* src0 = p.ws + static_cast<int64_t>(row) * p.N + col;
+              const float* src1 = src0 + 4 * static_cast<int64_t>(p.N);
+#pragma unroll 1
+              for (int r0 = 0; r0 < p.n_groups; r0 += 4) {
+                float4 v[4][2][2];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                  if (r0 + u < p.n_groups) {
+                    const float4* s0 = reinterpret_cast<const float4*>(src0 + (r0 + u) * plane);
+                    v[u][0][0] = __ldcg(s0);
+                    v[u][0][1] = __ldcg(s0 + 1);
+                    if (ok1) {
+                      const float4* s1 = reinterpret_cast<const float4*>(src1 + (r0 + u) * plane);
+                      v[u][1][0] = __ldcg(s1);
+                      v[u][1][1] = __ldcg(s1 + 1);
+                    }
+                  }
+                }
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                  if (r0 + u < p.n_groups) {
+#pragma unroll
+                    for (int w = 0; w < 2; ++w) {
+                      if (w == 1 && !ok1) continue;
+                      a8[w][0] += v[u][w][0].x; a8[w][1] += v[u][w][0].y;
+                      a8[w][2] += v[u][w][0].z; a8[w][3] += v[u][w][0].w;
+                      a8[w][4] += v[u][w][1].x; a8[w][5] += v[u][w][1].y;
+                      a8[w][6] += v[u][w][1].z; a8[w][7] += v[u][w][1].w;
+                    }
+                  }
+                }
+              }
+#pragma unroll
+              for (int w = 0; w < 2; ++w) {
+                if (w == 1 && !ok1) continue;
+                if (p.reduce_bias != nullptr) {
+#pragma unroll
+                  for (int j = 0; j < 8; ++j) a8[w][j] += __bfloat162float(p.reduce_bias[col + j]);
+                }
+                uint32_t pk[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                  __nv_bfloat162 h = __floats2bfloat162_rn(a8[w][2 * j], a8[w][2 * j + 1]);
+                  pk[j] = *reinterpret_cast<uint32_t*>(&h);
+                }
+                *reinterpret_cast<uint4*>(p.reduce_out + static_cast<int64_t>(row + 4 * w) * p.ldo + col) =
+                    make_uint4(pk[0], pk[1], pk[2], pk[3]);
+              }
+            }
+          }
+        }
+      }
     }
   }
 }
 
-template <int kEpi>
+// kPair = false: one CTA per 128 x 256 tile.  kPair = true: a cluster of two
+// CTAs per 256 x 256 tile -- each CTA stages its own 128 rows of A and half of
+// B, the even CTA issues cta_group::2 MMAs that read both CTAs' shared memory
+// and write both CTAs' tensor memory, and each CTA's epilogue drains its own
+// 128 rows.
+template <int kEpi, bool kPair>
 __global__ void __launch_bounds__(kThreads, 1) tp_gemm_kernel(const __grid_constant__ GemmParams p) {
+  using C = Cfg<kPair>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  SmemCtrl* ctl = reinterpret_cast<SmemCtrl*>(base + STAGES * STAGE_BYTES);
+  uint8_t* staging = base + C::STAGES * C::STAGE_BYTES;
+  SmemCtrl* ctl = reinterpret_cast<SmemCtrl*>(staging + kStagingBytes);
   volatile int* abort_flag = &ctl->abort;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const uint32_t cta = kPair ? ptx::cluster_ctarank() : 0u;  // 0 = leader of the pair
+  const int unit = kPair ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+  const int nunits = kPair ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < STAGES; ++s) {
+    for (int s = 0; s < C::STAGES; ++s) {
       ptx::mbar_init(ptx::smem_addr(&ctl->full[s]), 1);
       ptx::mbar_init(ptx::smem_addr(&ctl->empty[s]), 1);
     }
     for (int a = 0; a < 2; ++a) {
       ptx::mbar_init(ptx::smem_addr(&ctl->tfull[a]), 1);
-      ptx::mbar_init(ptx::smem_addr(&ctl->tempty[a]), 128);
+      ptx::mbar_init(ptx::smem_addr(&ctl->tempty[a]), kPair ? 256 : 128);
     }
     ptx::mbar_init(ptx::smem_addr(&ctl->drain), 1);
     ctl->abort = 0;
@@ -190,11 +501,16 @@ __global__ void __launch_bounds__(kThreads, 1) tp_gemm_kernel(const __grid_const
     ptx::fence_proxy_async_smem();
   }
   if (warp == 0) {
-    ptx::tmem_alloc(ptx::smem_addr(&ctl->tmem_base), kTmemCols);
-    ptx::tmem_relinquish();
+    if constexpr (kPair) {
+      ptx::tmem_alloc_pair(ptx::smem_addr(&ctl->tmem_base), kTmemCols);
+      ptx::tmem_relinquish_pair();
+    } else {
+      ptx::tmem_alloc(ptx::smem_addr(&ctl->tmem_base), kTmemCols);
+      ptx::tmem_relinquish();
+    }
   }
   ptx::tc_fence_before();
-  __syncthreads();
+  if constexpr (kPair) ptx::cluster_sync(); else __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = ctl->tmem_base;
 
@@ -203,244 +519,167 @@ __global__ void __launch_bounds__(kThreads, 1) tp_gemm_kernel(const __grid_const
   if (warp == 0) {
     if (lane == 0) {
       // ------------------------------------------------------------ producer
+      // Pull every tensor map this launch uses into the TMA descriptor cache up
+      // front, so switching ranks inside a tile does not stall on a descriptor fetch.
+      const int nmaps = (p.n_ksegs > 1) ? p.n_ksegs : p.n_groups;
+      for (int r = 0; r < nmaps; ++r) {
+        ptx::prefetch_tensormap(&p.map_b[r]);
+        if (!p.a_shared || r == 0) ptx::prefetch_tensormap(&p.map_a[r]);
+      }
       uint32_t it = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+      for (int t = unit; t < total && ok; t += nunits) {
         int g, mb, nb;
         decode_tile(p, t, g, mb, nb);
+        const int a_row = mb * C::TILE_M + static_cast<int>(cta) * BM;
         for (int seg = 0; seg < p.n_ksegs && ok; ++seg) {
           const int r = (p.n_ksegs > 1) ? seg : g;
           const CUtensorMap* ma = &p.map_a[p.a_shared ? 0 : r];
           const CUtensorMap* mbm = &p.map_b[r];
           for (int kb = 0; kb < p.kblocks; ++kb) {
-            const uint32_t s = it % STAGES;
-            const uint32_t ph = (it / STAGES) & 1u;
+            const uint32_t s = it % C::STAGES;
+            const uint32_t ph = (it / C::STAGES) & 1u;
             if (!wait_bounded(ptx::smem_addr(&ctl->empty[s]), ph ^ 1u, abort_flag, p.status, false)) {
               ok = false;
               break;
             }
             const uint32_t full = ptx::smem_addr(&ctl->full[s]);
-            const uint32_t sa = ptx::smem_addr(base + s * STAGE_BYTES);
-            const uint32_t sb = sa + A_BYTES;
-            ptx::mbar_arrive_expect_tx(full, STAGE_BYTES);
-            ptx::tma_load_2d(sa, ma, full, kb * BK, mb * BM);
-            if (kEpi == EPI_SWIGLU) {
-              ptx::tma_load_2d(sb, mbm, full, kb * BK, nb * (BN / 2));
-              ptx::tma_load_2d(sb + B_BYTES / 2, mbm, full, kb * BK, p.b_up_row + nb * (BN / 2));
+            const uint32_t sa = ptx::smem_addr(base + s * C::STAGE_BYTES);
+            const uint32_t sb = sa + C::A_BYTES;
+            if constexpr (kPair) {
+              // Both CTAs' copies complete on the leader's barrier; the leader expects all of them.
+              const uint32_t full_leader = ptx::mapa_shared(full, 0);
+              if (cta == 0) ptx::mbar_arrive_expect_tx(full, 2 * C::A_BYTES + static_cast<uint32_t>(p.bn) * (BK * 2));
+              ptx::tma_load_2d_pair(sa, ma, full_leader, kb * BK, a_row);
+              int b_row;
+              if (kEpi == EPI_SWIGLU)
+                b_row = (cta == 0 ? 0 : p.b_up_row) + nb * (BN / 2);  // leader: gate rows, peer: up rows
+              else
+                b_row = nb * p.bn + static_cast<int>(cta) * (p.bn / 2);
+              ptx::tma_load_2d_pair(sb, mbm, full_leader, kb * BK, b_row);
             } else {
-              ptx::tma_load_2d(sb, mbm, full, kb * BK, nb * BN);
+              ptx::mbar_arrive_expect_tx(full, C::A_BYTES + static_cast<uint32_t>(p.bn) * (BK * 2));
+              ptx::tma_load_2d(sa, ma, full, kb * BK, a_row);
+              if (kEpi == EPI_SWIGLU) {
+                ptx::tma_load_2d(sb, mbm, full, kb * BK, nb * (BN / 2));
+                ptx::tma_load_2d(sb + C::B_BYTES / 2, mbm, full, kb * BK, p.b_up_row + nb * (BN / 2));
+              } else {
+                ptx::tma_load_2d(sb, mbm, full, kb * BK, nb * p.bn);
+              }
             }
             ++it;
           }
         }
       }
-      // Let every copy this thread issued land before the CTA can exit.
-      const uint32_t first = it > STAGES ? it - STAGES : 0;
-      for (uint32_t j = first; j < it; ++j)
-        wait_bounded(ptx::smem_addr(&ctl->full[j % STAGES]), (j / STAGES) & 1u, abort_flag, p.status, true);
+      // Let every copy this thread issued land before the CTA can exit.  In a
+      // pair, the leader's full barriers count both CTAs' copies.
+      if (!kPair || cta == 0) {
+        const uint32_t first = it > C::STAGES ? it - C::STAGES : 0;
+        for (uint32_t j = first; j < it; ++j)
+          wait_bounded(ptx::smem_addr(&ctl->full[j % C::STAGES]), (j / C::STAGES) & 1u, abort_flag, p.status, true);
+      } else if (*abort_flag) {
+        // The peer cannot observe its own copies; give any in flight time to land (abort path only).
+        const uint64_t t0 = ptx::globaltimer_ns();
+        while (ptx::globaltimer_ns() - t0 < 100000ull) {
+        }
+      }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
-      // ------------------------------------------------------------ MMA issuer
-      constexpr uint32_t idesc = ptx::idesc_bf16_f32(BM, BN);
+    if (lane == 0 && cta == 0) {
+      // ------------------------------------------------------------ MMA issuer (leader CTA)
+      const uint32_t idesc = ptx::idesc_bf16_f32(C::TILE_M, p.bn);
       uint32_t it = 0, tcount = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++tcount) {
+      for (int t = unit; t < total && ok; t += nunits, ++tcount) {
         const uint32_t acc = tcount & 1u;
         const uint32_t aph = (tcount >> 1) & 1u;
-        if (!wait_bounded(ptx::smem_addr(&ctl->tempty[acc]), aph ^ 1u, abort_flag, p.status, false)) break;
+        if (!wait_bounded<kPair>(ptx::smem_addr(&ctl->tempty[acc]), aph ^ 1u, abort_flag, p.status, false)) break;
         ptx::tc_fence_after();
-        const uint32_t d_tmem = tmem + acc * BN;
+        const uint32_t d_tmem = tmem + acc * static_cast<uint32_t>(p.bn);
         uint32_t accumulate = 0;
         for (int seg = 0; seg < p.n_ksegs && ok; ++seg) {
           for (int kb = 0; kb < p.kblocks; ++kb) {
-            const uint32_t s = it % STAGES;
-            const uint32_t ph = (it / STAGES) & 1u;
+            const uint32_t s = it % C::STAGES;
+            const uint32_t ph = (it / C::STAGES) & 1u;
             if (!wait_bounded(ptx::smem_addr(&ctl->full[s]), ph, abort_flag, p.status, false)) {
               ok = false;
               break;
             }
             ptx::tc_fence_after();
-            const uint32_t sa = ptx::smem_addr(base + s * STAGE_BYTES);
+            const uint32_t sa = ptx::smem_addr(base + s * C::STAGE_BYTES);
             const uint64_t adesc = ptx::sw128_kmajor_desc(sa);
-            const uint64_t bdesc = ptx::sw128_kmajor_desc(sa + A_BYTES);
+            const uint64_t bdesc = ptx::sw128_kmajor_desc(sa + C::A_BYTES);
 #pragma unroll
             for (int k = 0; k < BK / 16; ++k) {
               // +32 bytes along K inside the 128-byte swizzled row = +2 in the >>4 address field.
-              ptx::umma_bf16(d_tmem, adesc + 2u * k, bdesc + 2u * k, idesc, accumulate);
+              if constexpr (kPair)
+                ptx::umma_bf16_pair(d_tmem, adesc + 2u * k, bdesc + 2u * k, idesc, accumulate);
+              else
+                ptx::umma_bf16(d_tmem, adesc + 2u * k, bdesc + 2u * k, idesc, accumulate);
               accumulate = 1;
             }
-            ptx::umma_commit(ptx::smem_addr(&ctl->empty[s]));
+            if constexpr (kPair)
+              ptx::umma_commit_pair(ptx::smem_addr(&ctl->empty[s]), 0x3);
+            else
+              ptx::umma_commit(ptx::smem_addr(&ctl->empty[s]));
             ++it;
           }
         }
         if (!ok) break;
-        ptx::umma_commit(ptx::smem_addr(&ctl->tfull[acc]));
+        if constexpr (kPair)
+          ptx::umma_commit_pair(ptx::smem_addr(&ctl->tfull[acc]), 0x3);
+        else
+          ptx::umma_commit(ptx::smem_addr(&ctl->tfull[acc]));
       }
-      // Wait for every MMA this thread issued before TMEM and shared memory go away.
-      ptx::umma_commit(ptx::smem_addr(&ctl->drain));
+      // Wait for every MMA issued before TMEM and shared memory go away (in both CTAs of a pair).
+      if constexpr (kPair)
+        ptx::umma_commit_pair(ptx::smem_addr(&ctl->drain), 0x3);
+      else
+        ptx::umma_commit(ptx::smem_addr(&ctl->drain));
+      wait_bounded(ptx::smem_addr(&ctl->drain), 0, abort_flag, p.status, true);
+    } else if (kPair && lane == 0) {
+      // The peer CTA: its shared memory feeds the leader's MMAs until the final drain arrives.
       wait_bounded(ptx::smem_addr(&ctl->drain), 0, abort_flag, p.status, true);
     }
   } else {
     // ---------------------------------------------------------------- epilogue
     const int q = warp & 3;  // TMEM lane quarter this warp may read
     const int epi_tid = threadIdx.x - 64;
+    const uint32_t wbuf = ptx::smem_addr(staging) + static_cast<uint32_t>(warp - 2) * 2 * kStageBuf;
+    int nchunk = 0;
     uint32_t tcount = 0;
-    for (int t = blockIdx.x; t < total; t += gridDim.x, ++tcount) {
+    for (int t = unit; t < total; t += nunits, ++tcount) {
       int g, mb, nb;
       decode_tile(p, t, g, mb, nb);
       const uint32_t acc = tcount & 1u;
       const uint32_t aph = (tcount >> 1) & 1u;
       if (!wait_bounded(ptx::smem_addr(&ctl->tfull[acc]), aph, abort_flag, p.status, false)) break;
       ptx::tc_fence_after();
-      const int row = mb * BM + q * 32 + lane;
-      const bool row_ok = row < p.M;
-      const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + acc * BN;
+      const int mb128 = mb * (C::TILE_M / BM) + static_cast<int>(cta);
+      const int row0 = mb128 * BM + q * 32;
+      const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + acc * static_cast<uint32_t>(p.bn);
       const uint32_t tempty = ptx::smem_addr(&ctl->tempty[acc]);
-
-      if constexpr (kEpi == EPI_SWIGLU) {
-        __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out[g]);
-        const __nv_bfloat16* bias = p.bias[g];
-#pragma unroll 1
-        for (int c = 0; c < BN / 2; c += 32) {
-          uint32_t gv[32], uv[32];
-          ptx::tmem_ld_32x32b_x32(taddr + c, gv);
-          ptx::tmem_ld_32x32b_x32(taddr + BN / 2 + c, uv);
-          ptx::tmem_ld_wait();
-          if (c + 32 >= BN / 2) {
-            ptx::tc_fence_before();
-            ptx::mbar_arrive(tempty);
-          }
-          const int col0 = nb * (BN / 2) + c;
-          if (row_ok && col0 < p.N) {
-            float f[32];
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              const int col = col0 + j;
-              float gg = __uint_as_float(gv[j]);
-              float uu = __uint_as_float(uv[j]);
-              if (bias != nullptr && col < p.N) {
-                gg += __bfloat162float(bias[col]);
-                uu += __bfloat162float(bias[p.b_up_row + col]);
-              }
-              f[j] = silu_f(gg) * uu;
-            }
-            store_bf16x32(out + static_cast<int64_t>(row) * p.ldo + col0, f, p.N - col0);
-          }
-        }
-      } else if constexpr (kEpi == EPI_BF16 || kEpi == EPI_GELU) {
-        __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out[g]);
-        const __nv_bfloat16* bias = p.bias[g];
-#pragma unroll 1
-        for (int c = 0; c < BN; c += 32) {
-          uint32_t v[32];
-          ptx::tmem_ld_32x32b_x32(taddr + c, v);
-          ptx::tmem_ld_wait();
-          if (c + 32 >= BN) {
-            ptx::tc_fence_before();
-            ptx::mbar_arrive(tempty);
-          }
-          const int col0 = nb * BN + c;
-          if (row_ok && col0 < p.N) {
-            float f[32];
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              float x = __uint_as_float(v[j]);
-              if (bias != nullptr && col0 + j < p.N) x += __bfloat162float(bias[col0 + j]);
-              f[j] = (kEpi == EPI_GELU) ? gelu_tanh_f(x) : x;
-            }
-            store_bf16x32(out + static_cast<int64_t>(row) * p.ldo + col0, f, p.N - col0);
-          }
-        }
-      } else {
-        // fp32 partial tile: to the caller's buffer (EPI_F32) or the workspace (EPI_WS_REDUCE).
-        float* out;
-        int64_t ld;
-        const __nv_bfloat16* bias;
-        if constexpr (kEpi == EPI_F32) {
-          out = static_cast<float*>(p.out[g]);
-          ld = p.ldo;
-          bias = p.bias[g];
-        } else {
-          out = p.ws + static_cast<int64_t>(g) * p.M * p.N;
-          ld = p.N;
-          bias = nullptr;
-        }
-#pragma unroll 1
-        for (int c = 0; c < BN; c += 32) {
-          uint32_t v[32];
-          ptx::tmem_ld_32x32b_x32(taddr + c, v);
-          ptx::tmem_ld_wait();
-          if (c + 32 >= BN) {
-            ptx::tc_fence_before();
-            ptx::mbar_arrive(tempty);
-          }
-          const int col0 = nb * BN + c;
-          if (row_ok && col0 < p.N) {
-            float bv[32];
-            if (bias != nullptr) {
-#pragma unroll
-              for (int j = 0; j < 32; ++j) bv[j] = (col0 + j < p.N) ? __bfloat162float(bias[col0 + j]) : 0.f;
-            }
-            store_f32x32(out + static_cast<int64_t>(row) * ld + col0, v, 0.f, bias ? bv : nullptr, p.N - col0);
-          }
-        }
-        if constexpr (kEpi == EPI_WS_REDUCE) {
-          // Publish this rank's partial tile, count it, and let the last rank to arrive sum all of them.
-          __threadfence();
-          ptx::named_bar_sync(1, 128);
-          if (epi_tid == 0) {
-            const int old = atomicAdd(&p.counters[mb * p.n_tiles + nb], 1);
-            *reinterpret_cast<volatile int*>(&ctl->is_last) = (old == p.n_groups - 1);
-          }
-          ptx::named_bar_sync(1, 128);
-          const bool last = *reinterpret_cast<volatile int*>(&ctl->is_last) != 0;
-          if (last) {
-            __threadfence();
-            if (row_ok) {
-              const int64_t plane = static_cast<int64_t>(p.M) * p.N;
-#pragma unroll 1
-              for (int c = 0; c < BN; c += 8) {
-                const int col = nb * BN + c;
-                if (col >= p.N) break;
-                float a8[8];
-#pragma unroll
-                for (int j = 0; j < 8; ++j) a8[j] = 0.f;
-                const float* src = p.ws + static_cast<int64_t>(row) * p.N + col;
-                for (int r = 0; r < p.n_groups; ++r) {
-                  const float4* s4 = reinterpret_cast<const float4*>(src + r * plane);
-                  const float4 x0 = __ldcg(s4);
-                  const float4 x1 = __ldcg(s4 + 1);
-                  a8[0] += x0.x; a8[1] += x0.y; a8[2] += x0.z; a8[3] += x0.w;
-                  a8[4] += x1.x; a8[5] += x1.y; a8[6] += x1.z; a8[7] += x1.w;
-                }
-                if (p.reduce_bias != nullptr) {
-#pragma unroll
-                  for (int j = 0; j < 8; ++j) a8[j] += __bfloat162float(p.reduce_bias[col + j]);
-                }
-                uint32_t pk[4];
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                  __nv_bfloat162 h = __floats2bfloat162_rn(a8[2 * j], a8[2 * j + 1]);
-                  pk[j] = *reinterpret_cast<uint32_t*>(&h);
-                }
-                *reinterpret_cast<uint4*>(p.reduce_out + static_cast<int64_t>(row) * p.ldo + col) =
-                    make_uint4(pk[0], pk[1], pk[2], pk[3]);
-              }
-            }
-            if (epi_tid == 0) p.counters[mb * p.n_tiles + nb] = 0;  // ready for the next call
-          }
-        }
-      }
+      auto release = [&]() {
+        ptx::tc_fence_before();
+        if constexpr (kPair)
+          ptx::mbar_arrive_cluster(ptx::mapa_shared(tempty, 0));  // the leader's MMA warp owns the accumulator
+        else
+          ptx::mbar_arrive(tempty);
+      };
+      epilogue_tile<kEpi>(p, ctl, taddr, wbuf, nchunk, g, row0, mb128, nb, lane, epi_tid, release);
     }
+    if (lane == 0) ptx::bulk_wait_all();  // every output store of this warp has landed
   }
 
   __syncwarp();
   ptx::tc_fence_before();
-  __syncthreads();
+  if constexpr (kPair) ptx::cluster_sync(); else __syncthreads();
   if (warp == 0) {
     ptx::tc_fence_after();
-    ptx::tmem_dealloc(tmem, kTmemCols);
+    if constexpr (kPair)
+      ptx::tmem_dealloc_pair(tmem, kTmemCols);
+    else
+      ptx::tmem_dealloc(tmem, kTmemCols);
   }
 }
 
@@ -477,27 +716,159 @@ tp_status make_map(CUtensorMap* m, const void* ptr, int64_t inner, int64_t outer
   return TP_OK;
 }
 
+// Largest number of CTA pairs that can be resident at once (cached per device and epilogue).
 template <int kEpi>
-tp_status launch_gemm(const GemmParams& p, cudaStream_t stream) {
-  const int sms = sm_count();
-  if (sms <= 0) return fail(TP_ERR_CUDA, "cannot query the SM count of the current device");
-  static std::once_flag attr_once[64];
+int max_active_pairs(int sms) {
+  static int cached[64] = {0};
+  static std::mutex mu;
   int dev = 0;
   cudaGetDevice(&dev);
-  cudaError_t attr_err = cudaSuccess;
-  std::call_once(attr_once[dev & 63], [&] {
-    attr_err = cudaFuncSetAttribute(tp_gemm_kernel<kEpi>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    static_cast<int>(kSmemBytes));
+  std::lock_guard<std::mutex> lock(mu);
+  if (cached[dev & 63] == 0) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(2 * (sms / 2), 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem_bytes<true>();
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, tp_gemm_kernel<kEpi, true>, &cfg) != cudaSuccess || n <= 0) {
+      cudaGetLastError();
+      n = sms / 2;
+    }
+    cached[dev & 63] = n;
+  }
+  return cached[dev & 63];
+}
+
+template <int kEpi, bool kPair>
+tp_status set_smem_attr() {
+  static std::once_flag once[64];
+  int dev = 0;
+  cudaGetDevice(&dev);
+  cudaError_t err = cudaSuccess;
+  std::call_once(once[dev & 63], [&] {
+    err = cudaFuncSetAttribute(tp_gemm_kernel<kEpi, kPair>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(smem_bytes<kPair>()));
   });
-  if (attr_err != cudaSuccess) return cuda_fail(attr_err, "cudaFuncSetAttribute(max dynamic shared memory)");
+  if (err != cudaSuccess) return cuda_fail(err, "cudaFuncSetAttribute(max dynamic shared memory)");
+  return TP_OK;
+}
+
+// Launch the single-CTA kernel (pair == false: 128-row tiles) or the CTA-pair kernel
+// (pair == true: 256-row tiles, clusters of two CTAs).  p.m_tiles must match.
+// Output map: a row-major [rows, cols] matrix (bf16 or fp32) with row stride `ld` elements,
+// written in boxes of 32 rows from the epilogue's swizzled staging buffers: 64 bf16 or
+// 32 fp32 columns (128-byte rows, 128-byte swizzle), or, for `narrow` bf16 maps, 32
+// columns (64-byte rows, 64-byte swizzle).
+tp_status make_out_map(CUtensorMap* m, void* ptr, bool f32, int64_t cols, int64_t rows, int64_t ld,
+                       bool narrow = false) {
+  auto enc = encoder();
+  if (enc == nullptr) return fail(TP_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  const int esz = f32 ? 4 : 2;
+  const bool sw64 = !f32 && narrow;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * esz};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>((f32 || narrow) ? 32 : 64), 32};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, ptr, dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   sw64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(TP_ERR_CUDA, "cuTensorMapEncodeTiled (output) failed (CUresult %d)", static_cast<int>(r));
+  return TP_OK;
+}
+
+template <int kEpi>
+tp_status launch_gemm(const GemmParams& p, bool pair, cudaStream_t stream) {
+  const int sms = sm_count();
+  if (sms <= 0) return fail(TP_ERR_CUDA, "cannot query the SM count of the current device");
   const int64_t total = static_cast<int64_t>(p.n_groups) * p.m_tiles * p.n_tiles;
   if (total <= 0) return TP_OK;
   if (total > 0x7FFFFFFF) return fail(TP_ERR_UNSUPPORTED, "too many tiles (%lld)", (long long)total);
-  const int grid = static_cast<int>(total < sms ? total : sms);
-  tp_gemm_kernel<kEpi><<<grid, kThreads, kSmemBytes, stream>>>(p);
-  cudaError_t e = cudaGetLastError();
+  // The workspace mode's CTAs wait on each other (bounded), so that launch is
+  // cooperative: it is refused rather than started if they cannot all be resident.
+  const bool coop = (kEpi == EPI_WS_REDUCE);
+  cudaLaunchConfig_t cfg{};
+  cudaLaunchAttribute attr[2];
+  int nattr = 0;
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.stream = stream;
+  if (coop) {
+    attr[nattr].id = cudaLaunchAttributeCooperative;
+    attr[nattr].val.cooperative = 1;
+    ++nattr;
+  }
+  cudaError_t e;
+  if (!pair) {
+    tp_status st = set_smem_attr<kEpi, false>();
+    if (st != TP_OK) return st;
+    cfg.gridDim = dim3(static_cast<unsigned>(total < sms ? total : sms), 1, 1);
+    cfg.dynamicSmemBytes = smem_bytes<false>();
+    cfg.attrs = attr;
+    cfg.numAttrs = nattr;
+    e = cudaLaunchKernelEx(&cfg, tp_gemm_kernel<kEpi, false>, p);
+    if (e != cudaSuccess) return cuda_fail(e, "GEMM launch");
+  } else {
+    tp_status st = set_smem_attr<kEpi, true>();
+    if (st != TP_OK) return st;
+    const int pairs_max = max_active_pairs<kEpi>(sms);
+    const int pairs = static_cast<int>(total < pairs_max ? total : pairs_max);
+    if (coop && pairs < p.n_groups)  // each rank of a tile needs its own resident CTA pair
+      return fail(TP_ERR_UNSUPPORTED, "%d resident CTA pairs cannot hold %d ranks", pairs, p.n_groups);
+    cfg.gridDim = dim3(2 * pairs, 1, 1);
+    cfg.dynamicSmemBytes = smem_bytes<true>();
+    attr[nattr].id = cudaLaunchAttributeClusterDimension;
+    attr[nattr].val.clusterDim.x = 2;
+    attr[nattr].val.clusterDim.y = 1;
+    attr[nattr].val.clusterDim.z = 1;
+    ++nattr;
+    cfg.attrs = attr;
+    cfg.numAttrs = nattr;
+    e = cudaLaunchKernelEx(&cfg, tp_gemm_kernel<kEpi, true>, p);
+    if (e != cudaSuccess) return cuda_fail(e, "GEMM (CTA pair) launch");
+  }
+  e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "GEMM kernel launch");
   return TP_OK;
+}
+
+// CTA pairs (256-row tiles) pay off once there is more than one 128-row block of output rows.
+inline bool use_pair(int64_t T) { return T > BM; }
+
+// Work units (CTAs, or CTA pairs) that run at the same time.
+int resident_units(bool pair) {
+  const int sms = sm_count();
+  if (!pair) return sms;
+  if (set_smem_attr<EPI_BF16, true>() != TP_OK) return sms / 2;
+  return max_active_pairs<EPI_BF16>(sms);
+}
+
+// Accumulator width of a launch without SwiGLU: among the widths the epilogue
+// supports (multiples of 32 up to 256), the one whose tiles finish in the
+// fewest waves x width -- e.g. N = 3072 on 76 pairs with 16 m-tiles takes 3
+// waves of 224-wide tiles instead of 2.5 (so 3) waves of 256-wide ones.
+// Ties go to the widest tile.
+int choose_bn(int64_t n_out, int64_t groups_x_mtiles, int units) {
+  static const int kWidths[] = {256, 224, 192, 160, 128};
+  int best = 256;
+  int64_t best_cost = -1;
+  for (int bn : kWidths) {
+    const int64_t tiles = groups_x_mtiles * ((n_out + bn - 1) / bn);
+    const int64_t waves = (tiles + units - 1) / units;
+    const int64_t cost = waves * bn;
+    if (best_cost < 0 || cost < best_cost) {
+      best = bn;
+      best_cost = cost;
+    }
+  }
+  return best;
 }
 
 inline int ceil_div(int64_t a, int64_t b) { return static_cast<int>((a + b - 1) / b); }
@@ -549,15 +920,21 @@ tp_status tp_linear_colwise(const void* x, const void* const* w_shards, const vo
   unsigned int* status = status_word();
   if (status == nullptr) return fail(TP_ERR_CUDA, "cannot locate the kernel status word");
 
+  const bool pair = use_pair(T);
   GemmParams p{};
   st = make_map(&p.map_a[0], x, K, T, K, BM);
   if (st != TP_OK) return st;
-  const int box_b = (act == TP_ACT_SWIGLU) ? BN / 2 : BN;
+  const int64_t m_tiles = (T + (pair ? 2 * BM : BM) - 1) / (pair ? 2 * BM : BM);
+  const int bn = (act == TP_ACT_SWIGLU) ? BN : choose_bn(n_out, tp_degree * m_tiles, resident_units(pair));
+  const int box_b = (act == TP_ACT_SWIGLU) ? BN / 2 : (pair ? bn / 2 : bn);
   for (int r = 0; r < tp_degree; ++r) {
     st = make_map(&p.map_b[r], w_shards[r], K, N_r, K, box_b);
     if (st != TP_OK) return st;
     p.out[r] = y_shards[r];
     p.bias[r] = bias_shards ? static_cast<const __nv_bfloat16*>(bias_shards[r]) : nullptr;
+    st = make_out_map(&p.map_out[r], y_shards[r], false, n_out, T, ldy);
+    if (st == TP_OK) st = make_out_map(&p.map_out_tail[r], y_shards[r], false, n_out, T, ldy, true);
+    if (st != TP_OK) return st;
   }
   p.status = status;
   p.ldo = ldy;
@@ -566,16 +943,17 @@ tp_status tp_linear_colwise(const void* x, const void* const* w_shards, const vo
   p.n_groups = tp_degree;
   p.n_ksegs = 1;
   p.kblocks = ceil_div(K, BK);
-  p.m_tiles = ceil_div(T, BM);
-  p.n_tiles = ceil_div(n_out, (act == TP_ACT_SWIGLU) ? BN / 2 : BN);
+  p.m_tiles = ceil_div(T, pair ? 2 * BM : BM);
+  p.n_tiles = ceil_div(n_out, (act == TP_ACT_SWIGLU) ? BN / 2 : bn);
+  p.bn = bn;
   p.b_up_row = static_cast<int>(N_r / 2);
   p.rank_fastest = 0;
   p.a_shared = 1;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   switch (act) {
-    case TP_ACT_GELU_TANH: return launch_gemm<EPI_GELU>(p, s);
-    case TP_ACT_SWIGLU: return launch_gemm<EPI_SWIGLU>(p, s);
-    default: return launch_gemm<EPI_BF16>(p, s);
+    case TP_ACT_GELU_TANH: return launch_gemm<EPI_GELU>(p, pair, s);
+    case TP_ACT_SWIGLU: return launch_gemm<EPI_SWIGLU>(p, pair, s);
+    default: return launch_gemm<EPI_BF16>(p, pair, s);
   }
 }
 
@@ -583,7 +961,8 @@ size_t tp_rowwise_workspace_bytes(int tp_degree, int64_t T, int64_t N, tp_reduce
   if (mode != TP_REDUCE_WORKSPACE || tp_degree < 1 || T <= 0 || N <= 0) return 0;
   const size_t partials = static_cast<size_t>(tp_degree) * static_cast<size_t>(T) * static_cast<size_t>(N) * 4;
   const size_t aligned = (partials + 255) & ~static_cast<size_t>(255);
-  const size_t tiles = static_cast<size_t>((T + tp::BM - 1) / tp::BM) * static_cast<size_t>((N + tp::BN - 1) / tp::BN);
+  // One counter per 128-row block and n-tile, sized for the narrowest tile (128 columns).
+  const size_t tiles = static_cast<size_t>((T + tp::BM - 1) / tp::BM) * static_cast<size_t>((N + 127) / 128);
   return aligned + tiles * sizeof(int);
 }
 
@@ -622,44 +1001,59 @@ tp_status tp_linear_rowwise(const void* const* x_shards, const void* const* w_sh
   unsigned int* status = status_word();
   if (status == nullptr) return fail(TP_ERR_CUDA, "cannot locate the kernel status word");
 
+  const bool pair = use_pair(T);
+  const int64_t m_tiles = (T + (pair ? 2 * BM : BM) - 1) / (pair ? 2 * BM : BM);
+  const int groups = (mode == TP_REDUCE_ACCUM) ? 1 : tp_degree;
+  const int bn = choose_bn(N, groups * m_tiles, resident_units(pair));
   GemmParams p{};
   for (int r = 0; r < tp_degree; ++r) {
     st = make_map(&p.map_a[r], x_shards[r], K_r, T, K_r, BM);
     if (st != TP_OK) return st;
-    st = make_map(&p.map_b[r], w_shards[r], K_r, N, K_r, BN);
+    st = make_map(&p.map_b[r], w_shards[r], K_r, N, K_r, pair ? bn / 2 : bn);
     if (st != TP_OK) return st;
   }
   p.status = status;
   p.M = static_cast<int>(T);
   p.N = static_cast<int>(N);
   p.kblocks = ceil_div(K_r, BK);
-  p.m_tiles = ceil_div(T, BM);
-  p.n_tiles = ceil_div(N, BN);
+  p.m_tiles = ceil_div(T, pair ? 2 * BM : BM);
+  p.n_tiles = ceil_div(N, bn);
+  p.bn = bn;
+  p.n_counters = ceil_div(N, 128);
   p.a_shared = 0;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (mode == TP_REDUCE_ACCUM) {
+    st = make_out_map(&p.map_out[0], out, false, N, T, N);
+    if (st == TP_OK) st = make_out_map(&p.map_out_tail[0], out, false, N, T, N, true);
+    if (st != TP_OK) return st;
     p.out[0] = out;
     p.bias[0] = static_cast<const __nv_bfloat16*>(bias);
     p.ldo = N;
     p.n_groups = 1;
     p.n_ksegs = tp_degree;
     p.rank_fastest = 0;
-    return launch_gemm<EPI_BF16>(p, s);
+    return launch_gemm<EPI_BF16>(p, pair, s);
   }
   if (mode == TP_REDUCE_NONE) {
     for (int r = 0; r < tp_degree; ++r) {
       p.out[r] = static_cast<float*>(out) + static_cast<int64_t>(r) * T * N;
       p.bias[r] = (r == 0) ? static_cast<const __nv_bfloat16*>(bias) : nullptr;
+      st = make_out_map(&p.map_out[r], p.out[r], true, N, T, N);
+      if (st != TP_OK) return st;
     }
     p.ldo = N;
     p.n_groups = tp_degree;
     p.n_ksegs = 1;
     p.rank_fastest = 0;
-    return launch_gemm<EPI_F32>(p, s);
+    return launch_gemm<EPI_F32>(p, pair, s);
   }
   // TP_REDUCE_WORKSPACE
   const size_t partial_bytes = (static_cast<size_t>(tp_degree) * T * N * 4 + 255) & ~static_cast<size_t>(255);
   p.ws = static_cast<float*>(workspace);
+  for (int r = 0; r < tp_degree; ++r) {
+    st = make_out_map(&p.map_out[r], p.ws + static_cast<int64_t>(r) * T * N, true, N, T, N);
+    if (st != TP_OK) return st;
+  }
   p.counters = reinterpret_cast<int*>(static_cast<uint8_t*>(workspace) + partial_bytes);
   p.reduce_out = static_cast<__nv_bfloat16*>(out);
   p.reduce_bias = static_cast<const __nv_bfloat16*>(bias);
@@ -669,7 +1063,7 @@ tp_status tp_linear_rowwise(const void* const* x_shards, const void* const* w_sh
   p.rank_fastest = 1;
   cudaError_t e = cudaMemsetAsync(p.counters, 0, need - partial_bytes, s);
   if (e != cudaSuccess) return cuda_fail(e, "clearing the tile counters");
-  return launch_gemm<EPI_WS_REDUCE>(p, s);
+  return launch_gemm<EPI_WS_REDUCE>(p, pair, s);
 }
 
 }  // extern "C"

@@ -110,10 +110,10 @@ def test_last_error_message():
 
 
 def test_workspace_bytes():
-    # p partials of T x N fp32 (rounded up to 256 B) plus one int counter per 128 x 256 output tile.
+    # p partials of T x N fp32 (rounded up to 256 B) plus one int counter per 128 x 128 output block.
     p, T, N = 4, 4096, 3072
     part = p * T * N * 4
-    assert tp.tp_rowwise_workspace_bytes(p, T, N, "workspace") == ((part + 255) // 256) * 256 + 32 * 12 * 4
+    assert tp.tp_rowwise_workspace_bytes(p, T, N, "workspace") == ((part + 255) // 256) * 256 + 32 * 24 * 4
     assert tp.tp_rowwise_workspace_bytes(p, T, N, "accum") == 0
     assert tp.tp_rowwise_workspace_bytes(p, T, N, "none") == 0
     assert tp.tp_rowwise_workspace_bytes(p, 0, N, "workspace") == 0

@@ -216,6 +216,31 @@ def test_colwise_swiglu_bias():
         assert_close(f64(ys[r]), ref[r], f"swiglu bias rank {r}")
 
 
+# Shapes whose wave-count heuristic picks each accumulator width (160, 192, 224, 256 columns) on
+# 76 resident CTA pairs; K is small to keep them quick, values integer so the check is exact.
+WIDTH_SHAPES = [(257, 64, 1600, 3), (257, 64, 1472, 4), (257, 64, 2368, 3), (257, 64, 2048, 4)]
+
+
+@pytest.mark.parametrize("shape", WIDTH_SHAPES, ids=str)
+def test_tile_widths_integer_bit_exact(shape):
+    T, K, N, p = shape
+    x = tp_inputs.int_bf16(114, 0, (T, K * p))
+    w = tp_inputs.int_bf16(114, 1, (N * p, K))
+    shards = [O.shard(w, "colwise", p, r) for r in range(p)]
+    xk = x[:, :K]
+    ys = tp.tp_linear_colwise(dev(xk), [dev(s) for s in shards], "none")
+    ref = O.colwise_forward(xk, shards, "none")
+    for r in range(p):
+        assert np.array_equal(host_bits(ys[r]), O.f64_to_bf16(ref[r])), ("colwise", r)
+    # The same widths through the rowwise workspace and unfused modes (one output group per rank).
+    wr = tp_inputs.int_bf16(114, 2, (N, K * p))
+    xs = [O.shard(x, "rowwise", p, r) for r in range(p)]
+    wsh = [O.shard(wr, "rowwise", p, r) for r in range(p)]
+    exp = O.f64_to_bf16(O.rowwise_forward(xs, wsh))
+    for mode in ("workspace", "none"):
+        assert np.array_equal(host_bits(_rowwise_gpu(xs, wsh, mode)), exp), mode
+
+
 # ----------------------------------------------------------------------------- rowwise GEMM
 
 ROWWISE_SHAPES = [
