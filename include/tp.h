@@ -277,6 +277,36 @@ TP_API tp_status tp_linear_rowwise_noalloc(const void* const* x_shards, const vo
                                            tp_stream_t stream);
 
 /* ------------------------------------------------------------------------ */
+/* Attention over a rank's local heads                                       */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * tp_attention_heads -- attention of one rank over its local heads:
+ *     O_h = softmax(Q_h K_h^T / sqrt(head_dim)) V_h     for h < n_heads
+ *
+ * "Tensor parallelism" page, §Colwise and rowwise: the colwise Q, K and V
+ * projections give each rank a subset of heads (tp_degree divides the head
+ * count), so the rank attends over them alone and its output feeds its
+ * rowwise out-projection directly.  No mask, no positional embedding; head h
+ * occupies columns [h*head_dim, (h+1)*head_dim) of each of Q, K and V.
+ *
+ * qkv:  device bf16 [T, 3*n_heads*head_dim] with row stride ld_qkv elements
+ *       (0 = dense): Q, then K, then V -- the rank's colwise QKV output.
+ * out:  device bf16 [T, n_heads*head_dim] with row stride ldo (0 = dense).
+ * workspace: device buffer of tp_attention_workspace_bytes(T, n_heads,
+ *       head_dim) bytes (fp32 scores for up to 16 heads at a time and V^T).
+ * Scores and softmax are fp32; the probabilities are rounded to bf16 for the
+ * P.V product (fp32 accumulation); O is rounded to bf16.
+ * Alignment (TP_ERR_ALIGNMENT): T, head_dim, ld_qkv, ldo multiples of 8, pointers
+ * 16-byte aligned.  T == 0 enqueues nothing.  TP_ERR_WORKSPACE if too small.
+ */
+TP_API tp_status tp_attention_heads(const void* qkv, int64_t ld_qkv, int64_t T, int n_heads, int head_dim,
+                                    void* workspace, size_t ws_bytes, void* out, int64_t ldo, tp_stream_t stream);
+
+/* Bytes of device workspace tp_attention_heads needs. */
+TP_API size_t tp_attention_workspace_bytes(int64_t T, int n_heads, int head_dim);
+
+/* ------------------------------------------------------------------------ */
 /* Join                                                                      */
 /* ------------------------------------------------------------------------ */
 

@@ -337,7 +337,8 @@ def combine_reduce(parts: Sequence[np.ndarray]) -> np.ndarray:
 # Attention over a rank's local heads
 # ---------------------------------------------------------------------------
 
-def attention_core(q: np.ndarray, k: np.ndarray, v: np.ndarray, n_heads: int, head_dim: int) -> np.ndarray:
+def attention_core(q: np.ndarray, k: np.ndarray, v: np.ndarray, n_heads: int, head_dim: int,
+                   store_p_bf16: bool = False) -> np.ndarray:
     """softmax(Q_h K_h^T / sqrt(d)) V_h for each of the rank's local heads, float64.
 
     "Tensor parallelism" page, §Colwise and rowwise: colwise Q, K and V give
@@ -347,6 +348,10 @@ def attention_core(q: np.ndarray, k: np.ndarray, v: np.ndarray, n_heads: int, he
     §What to leave out), scale 1/sqrt(head_dim), max-subtracted softmax, head j
     occupying columns [j*d, (j+1)*d) of each of Q, K, V.  ``q`` may hold only
     some query rows; ``k`` and ``v`` hold every token.
+
+    ``store_p_bf16``: round the probabilities to bf16 before the product with
+    V, for a path that stores them in bf16 (the bf16-storage reading: every
+    tensor a path materialises is bf16).  Off, the result is exact.
     """
     q = np.asarray(q, dtype=np.float64)
     k = np.asarray(k, dtype=np.float64)
@@ -359,6 +364,8 @@ def attention_core(q: np.ndarray, k: np.ndarray, v: np.ndarray, n_heads: int, he
         s = s - s.max(axis=1, keepdims=True)
         e = np.exp(s)
         pr = e / e.sum(axis=1, keepdims=True)
+        if store_p_bf16:
+            pr = bf16_to_f64(f64_to_bf16(pr))
         out[:, cols] = pr @ v[:, cols]
     return out
 
@@ -387,12 +394,13 @@ def mlp_forward(x_bits, w_in_shards, w_out_shards, act: str):
 
 
 def attention_block_forward(x_bits, wqkv_shards, wout_shards, n_local_heads: int, head_dim: int,
-                            q_rows: np.ndarray | None = None):
+                            q_rows: np.ndarray | None = None, store_p_bf16: bool = True):
     """QKV colwise -> per-rank attention -> out-projection rowwise + sum.
 
     Returns (qkv_bits per rank, o_bits per rank, Z float64).  With ``q_rows``
     only those token rows are computed for the query side (K and V always use
-    every token), which is exact for those rows.
+    every token), which is exact for those rows.  The attention probabilities
+    are stored in bf16 like every other tensor of the path (``store_p_bf16``).
     """
     width = n_local_heads * head_dim
     qkv = [f64_to_bf16(y) for y in colwise_forward(x_bits, wqkv_shards, "none")]
@@ -402,13 +410,14 @@ def attention_block_forward(x_bits, wqkv_shards, wout_shards, n_local_heads: int
         if q_rows is not None:
             qb = qb[q_rows]
         o.append(f64_to_bf16(attention_core(bf16_to_f64(qb), bf16_to_f64(kb), bf16_to_f64(vb),
-                                            n_local_heads, head_dim)))
+                                            n_local_heads, head_dim, store_p_bf16=store_p_bf16)))
     z = rowwise_forward(o, wout_shards)
     return qkv, o, z
 
 
 def transformer_block_forward(x_bits, wqkv_shards, wout_shards, wgu_shards, wdown_shards,
-                              n_local_heads: int, head_dim: int, q_rows: np.ndarray | None = None):
+                              n_local_heads: int, head_dim: int, q_rows: np.ndarray | None = None,
+                              store_p_bf16: bool = True):
     """Attention + SwiGLU MLP block, both halves sharded colwise -> rowwise.
 
     x -> QKV (colwise) -> attention over local heads -> out-projection
@@ -418,7 +427,7 @@ def transformer_block_forward(x_bits, wqkv_shards, wout_shards, wgu_shards, wdow
     intermediates and the unrounded final output ``z``.
     """
     qkv, o, z1 = attention_block_forward(x_bits, wqkv_shards, wout_shards, n_local_heads, head_dim,
-                                         q_rows=q_rows)
+                                         q_rows=q_rows, store_p_bf16=store_p_bf16)
     z1_bits = f64_to_bf16(z1)
     h, z2 = mlp_forward(z1_bits, wgu_shards, wdown_shards, "swiglu")
     return dict(qkv=qkv, o=o, z1=z1, z1_bits=z1_bits, h=h, z=z2)

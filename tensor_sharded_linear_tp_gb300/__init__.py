@@ -56,6 +56,9 @@ _SIGS = {
     "tp_linear_rowwise_noalloc": (_status, [ctypes.POINTER(_vp), ctypes.POINTER(_vp), _vp, ctypes.c_int, _i64, _i64,
                                             _i64, _vp, _vp]),
     "tp_rowwise_workspace_bytes": (ctypes.c_size_t, [ctypes.c_int, _i64, _i64, ctypes.c_int]),
+    "tp_attention_heads": (_status, [_vp, _i64, _i64, ctypes.c_int, ctypes.c_int, _vp, ctypes.c_size_t, _vp, _i64,
+                                     _vp]),
+    "tp_attention_workspace_bytes": (ctypes.c_size_t, [_i64, ctypes.c_int, ctypes.c_int]),
     "tp_combine": (_status, [ctypes.c_int, ctypes.POINTER(_vp), ctypes.c_int, _i64, _i64, _vp, _vp]),
     "tp_last_error": (ctypes.c_char_p, []),
     "tp_status_name": (ctypes.c_char_p, [ctypes.c_int]),
@@ -155,6 +158,7 @@ def tp_plan_shard(weight: torch.Tensor, style: str, tp_degree: int, rank: int,
     rows, cols = weight.shape
     arr, n = _splits(fused_splits)
     if out is None:
+        tp_validate(rows, cols, style, tp_degree, num_heads, head_dim, fused_splits)  # before allocating
         shape = tp_shard_shape(rows, cols, style, tp_degree, fused_splits)
         dev = device if device is not None else (weight.device if weight.is_cuda else torch.device("cuda"))
         out = torch.empty(shape, dtype=torch.bfloat16, device=dev)
@@ -174,6 +178,7 @@ def tp_plan_shard_ranks(weight: torch.Tensor, style: str, tp_degree: int, rank_b
         rank_count = tp_degree - rank_begin
     arr, n = _splits(fused_splits)
     if outs is None:
+        tp_validate(rows, cols, style, tp_degree, num_heads, head_dim, fused_splits)  # before allocating
         shape = tp_shard_shape(rows, cols, style, tp_degree, fused_splits)
         dev = device if device is not None else (weight.device if weight.is_cuda else torch.device("cuda"))
         outs = [torch.empty(shape, dtype=torch.bfloat16, device=dev) for _ in range(rank_count)]
@@ -259,6 +264,31 @@ def tp_linear_rowwise_noalloc(x_shards: Sequence[torch.Tensor], w_shards: Sequen
         out = torch.empty((T, N), dtype=torch.bfloat16, device=x_shards[0].device)
     _check(lib.tp_linear_rowwise_noalloc(_ptrs(x_shards), _ptrs(w_shards), _ptr(bias), p, T, K_r, N, _ptr(out),
                                          _stream(stream)))
+    return out
+
+
+# ---------------------------------------------------------------------------
+# Attention over a rank's local heads
+# ---------------------------------------------------------------------------
+
+def tp_attention_workspace_bytes(T: int, n_heads: int, head_dim: int) -> int:
+    return int(lib.tp_attention_workspace_bytes(T, n_heads, head_dim))
+
+
+def tp_attention_heads(qkv: torch.Tensor, n_heads: int, head_dim: int, out: torch.Tensor | None = None,
+                       workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """softmax(Q_h K_h^T / sqrt(d)) V_h for each local head of a rank's QKV output [T, 3*n_heads*d]."""
+    _need_bf16("qkv", qkv)
+    T = qkv.shape[0]
+    width = n_heads * head_dim
+    if out is None:
+        out = torch.empty((T, width), dtype=torch.bfloat16, device=qkv.device)
+    need = tp_attention_workspace_bytes(T, n_heads, head_dim)
+    if workspace is None and need:
+        workspace = torch.empty(need, dtype=torch.uint8, device=qkv.device)
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(lib.tp_attention_heads(_ptr(qkv), qkv.stride(0), T, n_heads, head_dim, _ptr(workspace), ws_bytes,
+                                  _ptr(out), out.stride(0), _stream(stream)))
     return out
 
 

@@ -1,0 +1,188 @@
+// Attention over one rank's local heads (tp_attention_heads).
+//
+// diffusers "Tensor parallelism" page, §Colwise and rowwise: the colwise Q, K
+// and V projections give each rank a subset of heads, so attention needs no
+// communication -- each rank attends over its own heads and its output feeds
+// the rowwise out-projection directly.  For local head h (columns
+// [h*d, (h+1)*d) of each of Q, K, V in the rank's QKV output):
+//     O_h = softmax(Q_h K_h^T / sqrt(d)) V_h        (no mask)
+//
+// Steps, per batch of up to 16 heads:
+//   1. S_h = Q_h . K_h^T   -- batched tcgen05 GEMM, fp32 scores [T, T];
+//   2. P_h = softmax(S_h / sqrt(d)) row by row, fp32 math, written as bf16
+//      over the first half of each score row (one warp per row);
+//   3. O_h = P_h . V_h     -- batched tcgen05 GEMM with B = V_h^T (V is
+//      transposed once per call), bf16 written straight into the rank's
+//      attention output columns [h*d, (h+1)*d).
+// The score matrices are memory traffic (about 10 bytes per score); a fused
+// kernel that keeps S and P on chip is the next step for this path.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+
+#include "tp_internal.h"
+
+namespace tp {
+namespace {
+
+constexpr int kHeadBatch = TP_MAX_DEGREE;
+
+// Vt[j][t] = V[t][j] for j < width: V is [T, width] with row stride ld_v elements.
+__global__ void __launch_bounds__(256) transpose_bf16(const __nv_bfloat16* __restrict__ v, int64_t ld_v,
+                                                      __nv_bfloat16* __restrict__ vt, int64_t T, int64_t width) {
+  __shared__ __nv_bfloat16 tile[32][34];
+  const int64_t t0 = static_cast<int64_t>(blockIdx.x) * 32;
+  const int64_t j0 = static_cast<int64_t>(blockIdx.y) * 32;
+  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;  // 32 x 8 threads
+#pragma unroll
+  for (int k = 0; k < 32; k += 8) {
+    const int64_t t = t0 + ty + k, j = j0 + tx;
+    if (t < T && j < width) tile[ty + k][tx] = v[t * ld_v + j];
+  }
+  __syncthreads();
+#pragma unroll
+  for (int k = 0; k < 32; k += 8) {
+    const int64_t j = j0 + ty + k, t = t0 + tx;
+    if (j < width && t < T) vt[j * T + t] = tile[tx][ty + k];
+  }
+}
+
+// Row softmax of fp32 scores scaled by `scale`, written as bf16 over the first
+// half of the same row (row i of P starts at byte 4*T*i).  One warp per row;
+// pass 1 keeps a running (max, sum of exponentials) per lane and merges them
+// across the warp, pass 2 writes exp(scale*(s - max)) / sum.  A warp reads a
+// 256-element piece (all lanes) before any lane writes the 512 bytes of P that
+// overlay its first half, so no score is overwritten before it is read.
+__global__ void __launch_bounds__(256) softmax_rows_inplace(float* s, int64_t rows, int T, float scale_log2e) {
+  const int lane = threadIdx.x & 31;
+  const int64_t row = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+  if (row >= rows) return;
+  float* srow = s + row * T;
+  float m = -INFINITY, l = 0.f;
+  for (int i = lane * 4; i < T; i += 128) {
+    const float4 v = *reinterpret_cast<const float4*>(srow + i);
+    const float x[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float mn = fmaxf(m, x[k]);
+      l = l * exp2f((m - mn) * scale_log2e) + exp2f((x[k] - mn) * scale_log2e);
+      m = mn;
+    }
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    const float mo = __shfl_xor_sync(0xffffffffu, m, off);
+    const float lo = __shfl_xor_sync(0xffffffffu, l, off);
+    const float mn = fmaxf(m, mo);
+    l = (m == -INFINITY ? 0.f : l * exp2f((m - mn) * scale_log2e)) +
+        (mo == -INFINITY ? 0.f : lo * exp2f((mo - mn) * scale_log2e));
+    m = mn;
+  }
+  const float inv = 1.0f / l;
+  __nv_bfloat16* prow = reinterpret_cast<__nv_bfloat16*>(srow);
+  for (int base = 0; base < T; base += 256) {
+    const int i = base + lane * 8;
+    float x[8];
+    if (i < T) {
+      const float4 a = *reinterpret_cast<const float4*>(srow + i);
+      const float4 b = *reinterpret_cast<const float4*>(srow + i + 4);
+      x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w; x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+    }
+    __syncwarp();  // every lane's reads of this piece happen before any lane's writes
+    if (i < T) {
+      uint32_t pk[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        __nv_bfloat162 h = __floats2bfloat162_rn(exp2f((x[2 * k] - m) * scale_log2e) * inv,
+                                                 exp2f((x[2 * k + 1] - m) * scale_log2e) * inv);
+        pk[k] = *reinterpret_cast<uint32_t*>(&h);
+      }
+      *reinterpret_cast<uint4*>(prow + i) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+    }
+    __syncwarp();
+  }
+}
+
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+}  // namespace
+}  // namespace tp
+
+extern "C" {
+
+size_t tp_attention_workspace_bytes(int64_t T, int n_heads, int head_dim) {
+  if (T <= 0 || n_heads <= 0 || head_dim <= 0) return 0;
+  const size_t hb = static_cast<size_t>(n_heads < tp::kHeadBatch ? n_heads : tp::kHeadBatch);
+  return tp::align256(hb * static_cast<size_t>(T) * static_cast<size_t>(T) * 4) +
+         tp::align256(static_cast<size_t>(n_heads) * static_cast<size_t>(head_dim) * static_cast<size_t>(T) * 2);
+}
+
+tp_status tp_attention_heads(const void* qkv, int64_t ld_qkv, int64_t T, int n_heads, int head_dim, void* workspace,
+                             size_t ws_bytes, void* out, int64_t ldo, tp_stream_t stream) {
+  using namespace tp;
+  clear_error();
+  if (T < 0 || n_heads < 1 || head_dim < 1) return fail(TP_ERR_INVALID_ARG, "T >= 0, n_heads >= 1, head_dim >= 1");
+  const int64_t width = static_cast<int64_t>(n_heads) * head_dim;
+  if (ld_qkv == 0) ld_qkv = 3 * width;
+  if (ldo == 0) ldo = width;
+  if (ld_qkv < 3 * width || ldo < width) return fail(TP_ERR_INVALID_ARG, "ld_qkv or ldo smaller than the rows");
+  if (T == 0) return TP_OK;
+  if (qkv == nullptr || out == nullptr) return fail(TP_ERR_INVALID_ARG, "qkv or out is NULL");
+  if ((T % 8) || (head_dim % 8) || (ld_qkv % 8) || (ldo % 8))
+    return fail(TP_ERR_ALIGNMENT, "T, head_dim, ld_qkv and ldo must be multiples of 8");
+  if (T > 0x7FFFFFFF / 2) return fail(TP_ERR_UNSUPPORTED, "T=%lld too large", (long long)T);
+  if (!aligned16(qkv) || !aligned16(out) || (workspace && !aligned16(workspace)))
+    return fail(TP_ERR_ALIGNMENT, "qkv, out or workspace is not 16-byte aligned");
+  const size_t need = tp_attention_workspace_bytes(T, n_heads, head_dim);
+  if (workspace == nullptr || ws_bytes < need)
+    return fail(TP_ERR_WORKSPACE, "workspace of %zu bytes given, %zu needed", workspace ? ws_bytes : 0, need);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const size_t hb = static_cast<size_t>(n_heads < kHeadBatch ? n_heads : kHeadBatch);
+  float* scores = static_cast<float*>(workspace);
+  __nv_bfloat16* vt = reinterpret_cast<__nv_bfloat16*>(static_cast<uint8_t*>(workspace) +
+                                                       align256(hb * static_cast<size_t>(T) * T * 4));
+  const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(qkv);
+  const __nv_bfloat16* k = q + width;
+  const __nv_bfloat16* v = q + 2 * width;
+  __nv_bfloat16* o = static_cast<__nv_bfloat16*>(out);
+
+  // V^T once for all heads: [width, T].
+  dim3 tgrid(static_cast<unsigned>((T + 31) / 32), static_cast<unsigned>((width + 31) / 32));
+  transpose_bf16<<<tgrid, 256, 0, s>>>(v, ld_qkv, vt, T, width);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "transpose launch");
+
+  const float scale_log2e = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(head_dim)));
+  for (int h0 = 0; h0 < n_heads; h0 += kHeadBatch) {
+    const int nb = (n_heads - h0) < kHeadBatch ? (n_heads - h0) : kHeadBatch;
+    const void* a[kHeadBatch];
+    const void* b[kHeadBatch];
+    void* c[kHeadBatch];
+    // 1. Scores: S_j = Q_h . K_h^T (fp32).
+    for (int j = 0; j < nb; ++j) {
+      a[j] = q + static_cast<int64_t>(h0 + j) * head_dim;
+      b[j] = k + static_cast<int64_t>(h0 + j) * head_dim;
+      c[j] = scores + static_cast<int64_t>(j) * T * T;
+    }
+    tp_status st = gemm_batched(nb, a, ld_qkv, b, ld_qkv, c, T, true, T, T, head_dim, s);
+    if (st != TP_OK) return st;
+    // 2. Softmax rows in place: P (bf16, row stride 2T elements) over S.
+    const int64_t rows = static_cast<int64_t>(nb) * T;
+    softmax_rows_inplace<<<static_cast<unsigned>((rows + 7) / 8), 256, 0, s>>>(scores, rows, static_cast<int>(T),
+                                                                                scale_log2e);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "softmax launch");
+    // 3. O_h = P_h . V_h, B = V_h^T [head_dim, T].
+    for (int j = 0; j < nb; ++j) {
+      a[j] = scores + static_cast<int64_t>(j) * T * T;  // bf16 view: row stride 2T elements
+      b[j] = vt + static_cast<int64_t>(h0 + j) * head_dim * T;
+      c[j] = o + static_cast<int64_t>(h0 + j) * head_dim;
+    }
+    st = gemm_batched(nb, a, 2 * T, b, T, c, ldo, false, T, head_dim, T, s);
+    if (st != TP_OK) return st;
+  }
+  return TP_OK;
+}
+
+}  // extern "C"

@@ -1126,3 +1126,51 @@ extern "C" tp_status tp_linear_rowwise_noalloc(const void* const* x_shards, cons
   return tp_linear_rowwise(x_shards, w_shards, bias, tp_degree, T, K_r, N, TP_REDUCE_WORKSPACE, scratch,
                            TP_NOALLOC_SCRATCH_BYTES, out, stream);
 }
+
+// ---------------------------------------------------------------------------
+// Batched GEMM for the attention core (library-internal): group i computes
+// out_i = A_i . B_i^T with A_i [M, K] (row stride lda), B_i [N, K] (row stride
+// ldb), out_i [M, N] (row stride ldo, bf16 or fp32), K-major bf16 operands.
+// ---------------------------------------------------------------------------
+
+namespace tp {
+
+tp_status gemm_batched(int groups, const void* const* a, int64_t lda, const void* const* b, int64_t ldb,
+                       void* const* out, int64_t ldo, bool out_f32, int64_t M, int64_t N, int64_t K,
+                       cudaStream_t stream) {
+  if (groups < 1 || groups > TP_MAX_DEGREE) return fail(TP_ERR_INVALID_ARG, "batched GEMM of %d groups", groups);
+  if (M == 0 || N == 0) return TP_OK;
+  if (K <= 0 || (K % 8) || (N % 8) || (lda % 8) || (ldb % 8) || (ldo % 8))
+    return fail(TP_ERR_ALIGNMENT, "batched GEMM needs K, N and leading dimensions that are multiples of 8");
+  unsigned int* status = status_word();
+  if (status == nullptr) return fail(TP_ERR_CUDA, "cannot locate the kernel status word");
+  const bool pair = use_pair(M);
+  const int64_t m_tiles = (M + (pair ? 2 * BM : BM) - 1) / (pair ? 2 * BM : BM);
+  const int bn = choose_bn(N, groups * m_tiles, resident_units(pair));
+  GemmParams p{};
+  for (int g = 0; g < groups; ++g) {
+    if (!aligned16(a[g]) || !aligned16(b[g]) || !aligned16(out[g]))
+      return fail(TP_ERR_ALIGNMENT, "batched GEMM operand of group %d is not 16-byte aligned", g);
+    tp_status st = make_map(&p.map_a[g], a[g], K, M, lda, BM);
+    if (st == TP_OK) st = make_map(&p.map_b[g], b[g], K, N, ldb, pair ? bn / 2 : bn);
+    if (st == TP_OK) st = make_out_map(&p.map_out[g], out[g], out_f32, N, M, ldo);
+    if (st == TP_OK && !out_f32) st = make_out_map(&p.map_out_tail[g], out[g], false, N, M, ldo, true);
+    if (st != TP_OK) return st;
+    p.out[g] = out[g];
+  }
+  p.status = status;
+  p.ldo = ldo;
+  p.M = static_cast<int>(M);
+  p.N = static_cast<int>(N);
+  p.n_groups = groups;
+  p.n_ksegs = 1;
+  p.kblocks = ceil_div(K, BK);
+  p.m_tiles = static_cast<int>(m_tiles);
+  p.n_tiles = ceil_div(N, bn);
+  p.bn = bn;
+  p.a_shared = 0;
+  p.rank_fastest = 0;
+  return out_f32 ? launch_gemm<EPI_F32>(p, pair, stream) : launch_gemm<EPI_BF16>(p, pair, stream);
+}
+
+}  // namespace tp

@@ -37,3 +37,10 @@ inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 
 
 // Bit 0 of the status word: a bounded wait gave up.
 #define TP_DEVSTATUS_TIMEOUT 1u
+
+namespace tp {
+// Library-internal batched GEMM (tp_gemm.cu): out_g = A_g . B_g^T for up to TP_MAX_DEGREE groups.
+tp_status gemm_batched(int groups, const void* const* a, int64_t lda, const void* const* b, int64_t ldb,
+                       void* const* out, int64_t ldo, bool out_f32, int64_t M, int64_t N, int64_t K,
+                       cudaStream_t stream);
+}  // namespace tp

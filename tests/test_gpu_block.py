@@ -1,0 +1,206 @@
+"""Attention over a rank's local heads, and the full attention + SwiGLU MLP block, against the oracle.
+
+The block is: x -> fused QKV (colwise, whole heads per rank) -> attention over
+each rank's heads -> out-projection (rowwise, partials summed) -> fused
+gate/up (colwise, SwiGLU) -> down-projection (rowwise, summed).  tp_degree is
+swept over the divisors of the head count the workload names; 5 and 7 must be
+refused before any weight is touched.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import tp_inputs
+from oracle import tp_oracle as O
+from tolerance import assert_close
+
+pytestmark = pytest.mark.gpu
+
+tp = pytest.importorskip("tensor_sharded_linear_tp_gb300")
+
+DEV = "cuda"
+
+
+def dev(bits):
+    return tp.bf16_from_bits(bits, DEV)
+
+
+def f64(t):
+    torch.cuda.synchronize()
+    return O.bf16_to_f64(tp.bits_from_bf16(t))
+
+
+@pytest.fixture(autouse=True)
+def _device_status_clean():
+    yield
+    tp.tp_device_status()
+
+
+# ----------------------------------------------------------------------------- attention core
+
+@pytest.mark.parametrize("T,heads,d", [(304, 3, 64), (520, 5, 128), (256, 18, 32), (8, 1, 8)])
+def test_attention_heads_within_tolerance(T, heads, d):
+    qkv = tp_inputs.activation_bf16(150, heads * 1000 + T, (T, 3 * heads * d))
+    out = tp.tp_attention_heads(dev(qkv), heads, d)
+    qf = O.bf16_to_f64(qkv)
+    H = heads * d
+    ref = O.attention_core(qf[:, :H], qf[:, H:2 * H], qf[:, 2 * H:], heads, d)
+    assert_close(f64(out), ref, f"attention T={T} heads={heads} d={d}")
+
+
+def test_attention_one_dominant_key_returns_its_value():
+    # Query t is 400*e_t and key u is e_u (head_dim 64): its own key scores 400/8 = 50
+    # above the others, so the softmax puts all but e^-50 of its weight there and O ~= V.
+    T, d = 64, 64
+    q = np.zeros((T, d))
+    k = np.zeros((T, d))
+    for t in range(T):
+        q[t, t] = 400.0
+        k[t, t] = 1.0
+    v = O.bf16_to_f64(tp_inputs.activation_bf16(151, 0, (T, d)))
+    qkv = O.f64_to_bf16(np.concatenate([q, k, v], axis=1))
+    out = f64(tp.tp_attention_heads(dev(qkv), 1, d))
+    ref = O.attention_core(q, k, v, 1, d)
+    assert np.max(np.abs(ref - v)) < 1e-12
+    assert_close(out, ref, "one-hot attention")
+
+
+def test_attention_writes_into_strided_output():
+    # The rank's attention output can land in a wider buffer (row stride ldo).
+    T, heads, d = 136, 2, 64
+    qkv = tp_inputs.activation_bf16(152, 0, (T, 3 * heads * d))
+    wide = torch.zeros((T, 3 * heads * d), dtype=torch.bfloat16, device=DEV)
+    tp.tp_attention_heads(dev(qkv), heads, d, out=wide[:, :heads * d])
+    qf = O.bf16_to_f64(qkv)
+    H = heads * d
+    ref = O.attention_core(qf[:, :H], qf[:, H:2 * H], qf[:, 2 * H:], heads, d)
+    got = f64(wide)
+    assert_close(got[:, :H], ref, "strided attention output")
+    assert np.all(got[:, H:] == 0)
+
+
+# ----------------------------------------------------------------------------- full block
+
+def gpu_block(x_bits, wqkv, wout, wgu, wdown, p, heads, d, F, mode="accum"):
+    """The block through the library: every rank's shards extracted from device copies of the weights."""
+    H = heads * d
+    x = dev(x_bits)
+    qkv_sh = tp.tp_plan_shard_ranks(dev(wqkv), "colwise", p, 0, p, [H] * 3, heads, d, device=DEV)
+    out_sh = tp.tp_plan_shard_ranks(dev(wout), "rowwise", p, 0, p, None, heads, d, device=DEV)
+    gu_sh = tp.tp_plan_shard_ranks(dev(wgu), "colwise", p, 0, p, [F, F], heads, 0, device=DEV)
+    dn_sh = tp.tp_plan_shard_ranks(dev(wdown), "rowwise", p, 0, p, None, heads, 0, device=DEV)
+    ys = tp.tp_linear_colwise(x, qkv_sh, "none")
+    hl = heads // p
+    os_ = [tp.tp_attention_heads(y, hl, d) for y in ys]
+    z1 = tp.tp_linear_rowwise(os_, out_sh, mode=mode)
+    if mode == "none":
+        z1 = tp.tp_combine("reduce", list(z1))
+    hs = tp.tp_linear_colwise(z1, gu_sh, "swiglu")
+    z2 = tp.tp_linear_rowwise(hs, dn_sh, mode=mode)
+    if mode == "none":
+        z2 = tp.tp_combine("reduce", list(z2))
+    return dict(qkv=ys, o=os_, z1=z1, h=hs, z=z2)
+
+
+def oracle_block(x_bits, wqkv, wout, wgu, wdown, p, heads, d, F, q_rows=None):
+    H = heads * d
+    return O.transformer_block_forward(
+        x_bits if q_rows is None else x_bits,
+        [O.shard(wqkv, "colwise", p, r, [H] * 3, num_heads=heads, head_dim=d) for r in range(p)],
+        [O.shard(wout, "rowwise", p, r, num_heads=heads, head_dim=d) for r in range(p)],
+        [O.shard(wgu, "colwise", p, r, [F, F]) for r in range(p)],
+        [O.shard(wdown, "rowwise", p, r) for r in range(p)],
+        n_local_heads=heads // p, head_dim=d, q_rows=q_rows)
+
+
+SMALL = dict(T=256, heads=48, d=16, F=1536)   # the sweep's 48 heads, at a size the oracle runs in full
+
+
+def gpu_mlp(z1_bits, wgu, wdown, p, F, heads, mode="accum"):
+    """The MLP block alone through the library, from a given input."""
+    gu_sh = tp.tp_plan_shard_ranks(dev(wgu), "colwise", p, 0, p, [F, F], heads, 0, device=DEV)
+    dn_sh = tp.tp_plan_shard_ranks(dev(wdown), "rowwise", p, 0, p, None, heads, 0, device=DEV)
+    hs = tp.tp_linear_colwise(dev(z1_bits), gu_sh, "swiglu")
+    z = tp.tp_linear_rowwise(hs, dn_sh, mode=mode)
+    return tp.tp_combine("reduce", list(z)) if mode == "none" else z
+
+
+def check_block_against_oracle(got, ref, x_rows, wgu, wdown, p, F, heads, what, mode="accum"):
+    # Block 1 (QKV -> attention -> out-projection) from the same input x.
+    assert_close(f64(got["z1"])[x_rows], ref["z1"], f"attention block, {what}")
+    # Block 2 (gate/up + SwiGLU -> down) from the oracle's own stored block-1 output.
+    z_mlp = f64(gpu_mlp(ref["z1_bits"], wgu, wdown, p, F, heads, mode))
+    assert_close(z_mlp, ref["z"], f"MLP block, {what}")
+    # The two blocks chained: both blocks' errors, so twice the bar.
+    assert_close(f64(got["z"])[x_rows], ref["z"], f"attention + MLP chain, {what}", blocks=2)
+
+
+@pytest.mark.parametrize("p", [1, 2, 3, 4, 6, 8])
+def test_block_small_matches_oracle(p):
+    T, heads, d, F = SMALL["T"], SMALL["heads"], SMALL["d"], SMALL["F"]
+    H = heads * d
+    wqkv, wout, wgu, wdown, x = tp_inputs.block_inputs(3, tokens=T, hidden=H, ffn=F)
+    got = gpu_block(x, wqkv, wout, wgu, wdown, p, heads, d, F)
+    ref = oracle_block(x, wqkv, wout, wgu, wdown, p, heads, d, F)
+    check_block_against_oracle(got, ref, np.arange(T), wgu, wdown, p, F, heads, f"tp={p}")
+
+
+def test_block_small_every_tp_degree_is_bit_identical_to_tp1():
+    # With the on-chip rank-ordered sum and K slices on 64-element boundaries, every output
+    # element is accumulated over the same products in the same order for every tp_degree:
+    # the sharded block reproduces the plain one exactly.
+    T, heads, d, F = SMALL["T"], SMALL["heads"], SMALL["d"], SMALL["F"]
+    H = heads * d
+    wqkv, wout, wgu, wdown, x = tp_inputs.block_inputs(3, tokens=T, hidden=H, ffn=F)
+    base = tp.bits_from_bf16(gpu_block(x, wqkv, wout, wgu, wdown, 1, heads, d, F)["z"])
+    for p in (2, 3, 4, 6, 8):
+        got = tp.bits_from_bf16(gpu_block(x, wqkv, wout, wgu, wdown, p, heads, d, F)["z"])
+        assert np.array_equal(got, base), p
+
+
+@pytest.mark.parametrize("p", [5, 7])
+def test_block_rejects_tp_not_dividing_heads(p):
+    T, heads, d, F = SMALL["T"], SMALL["heads"], SMALL["d"], SMALL["F"]
+    H = heads * d
+    wqkv = tp_inputs.weight_bf16(3, 0, (3 * H, H))
+    for style, rows, cols, splits, hd in (("colwise", 3 * H, H, [H] * 3, d), ("rowwise", H, H, None, d)):
+        with pytest.raises(tp.TPError) as e:
+            tp.tp_validate(rows, cols, style, p, heads, hd, splits)
+        assert e.value.name == "TP_ERR_HEADS_NOT_DIVISIBLE"
+    with pytest.raises(tp.TPError) as e:
+        tp.tp_plan_shard_ranks(dev(wqkv), "colwise", p, 0, p, [H] * 3, heads, d, device=DEV)
+    assert e.value.name == "TP_ERR_HEADS_NOT_DIVISIBLE"
+
+
+@pytest.mark.parametrize("mode", ["workspace", "none"])
+def test_block_small_other_join_modes(mode):
+    T, heads, d, F = SMALL["T"], SMALL["heads"], SMALL["d"], SMALL["F"]
+    H = heads * d
+    wqkv, wout, wgu, wdown, x = tp_inputs.block_inputs(3, tokens=T, hidden=H, ffn=F)
+    got = gpu_block(x, wqkv, wout, wgu, wdown, 4, heads, d, F, mode=mode)
+    ref = oracle_block(x, wqkv, wout, wgu, wdown, 4, heads, d, F)
+    check_block_against_oracle(got, ref, np.arange(T), wgu, wdown, 4, F, heads, mode, mode=mode)
+
+
+@pytest.mark.slow
+def test_block_sweep_full_size():
+    """hidden 6144, 48 heads x 128, ffn 18432, tokens 4608: every tp_degree against tp_degree 1 and the oracle."""
+    cfg = tp_inputs.WORKLOADS["block_sweep"]
+    T, H, F, heads, d = cfg["tokens"], cfg["hidden"], cfg["ffn"], cfg["heads"], cfg["head_dim"]
+    wqkv, wout, wgu, wdown, x = tp_inputs.block_inputs(cfg["seed"], tokens=T, hidden=H, ffn=F)
+    rows = tp_inputs.sample_rows(cfg["seed"], T, 48)
+    ref = oracle_block(x, wqkv, wout, wgu, wdown, 1, heads, d, F, q_rows=rows)
+    base = None
+    for p in cfg["tp_list"]:
+        got = gpu_block(x, wqkv, wout, wgu, wdown, p, heads, d, F)
+        z = tp.bits_from_bf16(got["z"])
+        if base is None:
+            base = z
+            check_block_against_oracle(got, ref, rows, wgu, wdown, p, F, heads, "tp=1 full size")
+        else:
+            # The sum / concatenation invariant against tp_degree 1, bit for bit.
+            assert np.array_equal(z, base), f"tp={p} differs from tp=1"
+        del got
+        torch.cuda.empty_cache()
