@@ -18,6 +18,9 @@ tp_degree 4, all four ranks on this GPU):
 second of device time: extraction and gather count as time, not as work.
 Inputs are resident in HBM when the timed region starts; L2 is flushed
 between steps (a 256 MiB write), so every step reads its operands from HBM.
+Each phase of the step is captured once as a CUDA graph and the timed steps
+replay them, with CUDA events between the phases (``--eager`` launches every
+call from Python instead; the eager per-phase times are reported either way).
 
 ``e2e`` is the same metric through the same public calls with host buffers:
 the weights are extracted shard-on-read from page-locked host memory, the
@@ -249,24 +252,31 @@ class AttnProjWorkload:
         # Pinned host copies for the end-to-end measurement.
         self.pin = None
 
-    def step(self, stream, marks=None):
-        """Enqueue one step on `stream`; `marks` (list of 5 events) bracket the four phases."""
+    # The four phases of a step, each enqueued on `stream`.
+    def phase_extract(self, stream):
         tp, p, H = self.tp, self.p, self.H
-        if marks:
-            marks[0].record(stream)
         tp.tp_plan_shard_ranks(self.w_qkv, "colwise", p, 0, p, [H] * 3, self.heads, self.hd, outs=self.qkv_sh,
                                stream=stream)
         tp.tp_plan_shard_ranks(self.w_out, "rowwise", p, 0, p, None, self.heads, self.hd, outs=self.out_sh,
                                stream=stream)
-        if marks:
-            marks[1].record(stream)
-        tp.tp_linear_colwise(self.x, self.qkv_sh, "none", y_shards=self.y_sh, stream=stream)
-        if marks:
-            marks[2].record(stream)
-        tp.tp_combine("gather", self.y_sh, out=self.y, stream=stream)
-        if marks:
-            marks[3].record(stream)
+
+    def phase_colwise(self, stream):
+        self.tp.tp_linear_colwise(self.x, self.qkv_sh, "none", y_shards=self.y_sh, stream=stream)
+
+    def phase_gather(self, stream):
+        self.tp.tp_combine("gather", self.y_sh, out=self.y, stream=stream)
+
+    def phase_rowwise(self, stream):
         self._rowwise(self.a_sh, stream)
+
+    PHASES = ("phase_extract", "phase_colwise", "phase_gather", "phase_rowwise")
+
+    def step(self, stream, marks=None):
+        """Enqueue one step on `stream`; `marks` (list of 5 events) bracket the four phases."""
+        for i, name in enumerate(self.PHASES):
+            if marks:
+                marks[i].record(stream)
+            getattr(self, name)(stream)
         if marks:
             marks[4].record(stream)
 
@@ -343,14 +353,24 @@ def calibrate_rows(host, T, p, H, heads, hd, target_s):
 
 
 def cpu_baseline(host, T, p, H, heads, hd, flops_full, target_s=12.0):
+    """The oracle on a bounded sample: whole steps repeated, or a row sample of one, for ~target_s."""
     rows_n = calibrate_rows(host, T, p, H, heads, hd, target_s)
     rows = tp_inputs.sample_rows(12, T, rows_n)
+    reps = 1
     dt = time_oracle(host, rows, p, H, heads, hd)
-    flops = flops_full * rows_n / T
+    if rows_n == T and dt < target_s:
+        # The whole step is quicker than the target: repeat it.
+        reps = max(1, int(round(target_s / max(dt, 1e-3))))
+        t0 = time.perf_counter()
+        for _ in range(reps):
+            oracle_sample_step(host, rows, p, H, heads, hd)
+        dt = time.perf_counter() - t0
+    flops = flops_full * rows_n / T * reps
+    what = f"{reps} repetitions of the whole step" if rows_n == T else f"{rows_n} of {T} token rows of one step"
     return {"value": flops / dt / 1e12, "unit": UNIT, "cores": int(os.environ["OPENBLAS_NUM_THREADS"]),
             "kind": "oracle",
-            "sample": f"{rows_n} of {T} token rows of the full step (all shards extracted, float64 numpy), "
-                      f"{dt:.1f} s; TFLOP/s = that sample's GEMM FLOPs / its time"}
+            "sample": f"{what} (all shards extracted, float64 numpy oracle), {dt:.1f} s; TFLOP/s = the "
+                      f"sample's GEMM FLOPs / its time"}
 
 
 # ----------------------------------------------------------------------------- arms
@@ -377,6 +397,38 @@ def run_ours(args):
     stream.synchronize()
     tp.tp_device_status(stream)
 
+    # Eager launches: host enqueue cost per step, and a per-phase cross-check.
+    n_eager = min(args.steps, 50)
+    eager_marks = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(n_eager)]
+    torch.cuda.synchronize()
+    host_s = 0.0
+    for k in range(n_eager):
+        with torch.cuda.stream(stream):
+            flush.zero_()
+        t0 = time.perf_counter()
+        wl.step(stream, eager_marks[k])
+        host_s += time.perf_counter() - t0
+    torch.cuda.synchronize()
+    eager_phase = np.array([[m[i].elapsed_time(m[i + 1]) for i in range(4)] for m in eager_marks])
+    host_enqueue_ms = host_s / n_eager * 1e3
+
+    # The timed region replays each phase as a captured CUDA graph (the launches a
+    # serving loop would replay), with events between the phases: the GPU runs the
+    # step back to back instead of waiting on Python.
+    graphs = []
+    if not args.eager:
+        for name in wl.PHASES:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                getattr(wl, name)(stream)
+            graphs.append(g)
+        with torch.cuda.stream(stream):
+            for _ in range(args.warmup):
+                for g in graphs:
+                    g.replay()
+        stream.synchronize()
+        tp.tp_device_status(stream)
+
     marks = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
     sampler = ClockSampler(local_rank)
     sampler.start()
@@ -387,7 +439,13 @@ def run_ours(args):
     for k in range(args.steps):
         with torch.cuda.stream(stream):
             flush.zero_()          # L2 flush between steps, outside the step's events
-        wl.step(stream, marks[k])
+            if graphs:
+                for i, g in enumerate(graphs):
+                    marks[k][i].record(stream)
+                    g.replay()
+                marks[k][4].record(stream)
+            else:
+                wl.step(stream, marks[k])
     torch.cuda.synchronize()
     barrier(dist, device)
     t_wall = time.perf_counter() - t_wall0
@@ -435,7 +493,7 @@ def run_ours(args):
         wl.step_e2e(stream)
     stream.synchronize()
     e2e_ms = []
-    for _ in range(args.steps):
+    for _ in range(min(args.steps, 100)):
         s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         s.record(stream)
         wl.step_e2e(stream)
@@ -466,7 +524,10 @@ def run_ours(args):
             "roofline": roofline, "kernels": kernels, "extract_gbs": kernels["extract"]["GB/s"],
             "extract_frac_hbm": kernels["extract"]["frac_hbm"], "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": wl.launches_per_step * args.steps, "clocks": clocks,
-            "bracket_s": t_wall, "peaks": peaks,
+            "bracket_s": t_wall, "peaks": peaks, "launch": "eager" if args.eager else "cuda_graph_per_phase",
+            "eager_ms_per_step": float(eager_phase.sum(axis=1).mean()),
+            "eager_phase_ms": [round(float(v), 5) for v in eager_phase.mean(axis=0)],
+            "host_enqueue_ms_per_step": host_enqueue_ms,
         }
         print(json.dumps(line))
     if dist is not None:
@@ -484,7 +545,7 @@ def run_reference(args):
     host = dict(w_qkv=w_qkv, w_out=w_out, x=x, a=a)
     flops_full = 2.0 * T * H * 3 * H + 2.0 * T * H * H
     # Each step a bounded sample so that warmup + steps stay within a few minutes.
-    per_step_s = max(0.5, min(6.0, 150.0 / max(1, args.steps + args.warmup)))
+    per_step_s = max(0.05, min(6.0, 150.0 / max(1, args.steps + args.warmup)))
     rows_n = calibrate_rows(host, T, p, H, heads, hd, per_step_s)
     for w in range(args.warmup):
         time_oracle(host, tp_inputs.sample_rows(20 + w, T, rows_n), p, H, heads, hd)
@@ -508,11 +569,12 @@ def run_reference(args):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--reduce-mode", choices=["accum", "workspace", "none"], default="accum")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing leg")
+    ap.add_argument("--eager", action="store_true", help="launch the timed steps eagerly instead of as graphs")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)   # at least three untimed warm-up steps, whatever was asked
     if args.impl == "reference":

@@ -42,7 +42,9 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <cstring>
 #include <mutex>
+#include <unordered_map>
 
 #include "tp_internal.h"
 #include "tp_ptx.cuh"
@@ -700,20 +702,68 @@ PFN_cuTensorMapEncodeTiled_v12000 encoder() {
   return fn;
 }
 
-// 2-D bf16 map over a row-major [outer, inner] matrix with row stride `ld` elements,
-// box = 64 (inner) x box_outer rows, 128-byte swizzle, out-of-range reads as zero.
-tp_status make_map(CUtensorMap* m, const void* ptr, int64_t inner, int64_t outer, int64_t ld, int box_outer) {
+// Encoded tensor maps are cached: a call that reuses the buffers of an earlier
+// call (the usual case in a model's forward pass) skips the driver encode.  The
+// key is every argument of the encode, so a cached map is exactly what the
+// encode would return now, even if the memory was freed and reallocated at the
+// same address.  The cache is cleared when it reaches kMapCacheMax entries.
+struct MapKey {
+  uint64_t ptr, inner, outer, stride;
+  uint32_t box_inner, box_outer, dtype, swizzle;
+  bool operator==(const MapKey& o) const { return std::memcmp(this, &o, sizeof(MapKey)) == 0; }
+};
+struct MapKeyHash {
+  size_t operator()(const MapKey& k) const {
+    uint64_t h = 1469598103934665603ull;
+    const unsigned char* b = reinterpret_cast<const unsigned char*>(&k);
+    for (size_t i = 0; i < sizeof(MapKey); ++i) h = (h ^ b[i]) * 1099511628211ull;
+    return static_cast<size_t>(h);
+  }
+};
+constexpr size_t kMapCacheMax = 4096;
+std::mutex g_map_mutex;
+std::unordered_map<MapKey, CUtensorMap, MapKeyHash> g_map_cache;
+
+tp_status encode_2d(CUtensorMap* m, const void* ptr, CUtensorMapDataType dtype, int esz, int64_t inner, int64_t outer,
+                    int64_t ld, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swizzle,
+                    CUtensorMapL2promotion promo) {
+  MapKey key{};
+  key.ptr = reinterpret_cast<uint64_t>(ptr);
+  key.inner = static_cast<uint64_t>(inner);
+  key.outer = static_cast<uint64_t>(outer);
+  key.stride = static_cast<uint64_t>(ld) * esz;
+  key.box_inner = box_inner;
+  key.box_outer = box_outer;
+  key.dtype = static_cast<uint32_t>(dtype) | (static_cast<uint32_t>(promo) << 16);
+  key.swizzle = static_cast<uint32_t>(swizzle);
+  {
+    std::lock_guard<std::mutex> lock(g_map_mutex);
+    auto it = g_map_cache.find(key);
+    if (it != g_map_cache.end()) {
+      *m = it->second;
+      return TP_OK;
+    }
+  }
   auto enc = encoder();
   if (enc == nullptr) return fail(TP_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(outer)};
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2};
-  cuuint32_t box[2] = {static_cast<cuuint32_t>(BK), static_cast<cuuint32_t>(box_outer)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * esz};
+  cuuint32_t box[2] = {box_inner, box_outer};
   cuuint32_t estr[2] = {1, 1};
-  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  CUresult r = enc(m, dtype, 2, const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   swizzle, promo, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(TP_ERR_CUDA, "cuTensorMapEncodeTiled failed (CUresult %d)", static_cast<int>(r));
+  std::lock_guard<std::mutex> lock(g_map_mutex);
+  if (g_map_cache.size() >= kMapCacheMax) g_map_cache.clear();
+  g_map_cache.emplace(key, *m);
   return TP_OK;
+}
+
+// 2-D bf16 operand map over a row-major [outer, inner] matrix with row stride `ld`
+// elements: box = 64 (inner) x box_outer rows, 128-byte swizzle, out-of-range reads as zero.
+tp_status make_map(CUtensorMap* m, const void* ptr, int64_t inner, int64_t outer, int64_t ld, int box_outer) {
+  return encode_2d(m, ptr, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, inner, outer, ld, BK,
+                   static_cast<uint32_t>(box_outer), CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
 }
 
 // Largest number of CTA pairs that can be resident at once (cached per device and epilogue).
@@ -768,21 +818,10 @@ tp_status set_smem_attr() {
 // columns (64-byte rows, 64-byte swizzle).
 tp_status make_out_map(CUtensorMap* m, void* ptr, bool f32, int64_t cols, int64_t rows, int64_t ld,
                        bool narrow = false) {
-  auto enc = encoder();
-  if (enc == nullptr) return fail(TP_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
-  const int esz = f32 ? 4 : 2;
   const bool sw64 = !f32 && narrow;
-  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * esz};
-  cuuint32_t box[2] = {static_cast<cuuint32_t>((f32 || narrow) ? 32 : 64), 32};
-  cuuint32_t estr[2] = {1, 1};
-  CUresult r = enc(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, ptr, dims, strides,
-                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                   sw64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS)
-    return fail(TP_ERR_CUDA, "cuTensorMapEncodeTiled (output) failed (CUresult %d)", static_cast<int>(r));
-  return TP_OK;
+  return encode_2d(m, ptr, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, f32 ? 4 : 2,
+                   cols, rows, ld, (f32 || narrow) ? 32u : 64u, 32u,
+                   sw64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE);
 }
 
 template <int kEpi>
