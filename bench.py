@@ -323,6 +323,128 @@ class AttnProjWorkload:
             self.pin["z"].copy_(self.z, non_blocking=True)
 
 
+class StackWorkload:
+    """Eight SwiGLU MLP blocks (hidden 6144, ffn 18432, tp 4) from a page-locked host state dict."""
+
+    def __init__(self, tp, torch, device):
+        cfg = tp_inputs.WORKLOADS["stack8_swiglu_tp4"]
+        self.tp, self.torch, self.device = tp, torch, device
+        self.p, self.nb, self.T, self.H, self.F = cfg["tp"], cfg["blocks"], cfg["tokens"], cfg["hidden"], cfg["ffn"]
+        self.heads = cfg["heads"]
+        seed = cfg["seed"]
+        pin = lambda b: torch.empty(b.shape, dtype=torch.bfloat16, pin_memory=True).copy_(  # noqa: E731
+            tp.bf16_from_bits(b))
+        self.host = [(pin(tp_inputs.stack_weight(seed, b, "gate_up", self.H, self.F)),
+                      pin(tp_inputs.stack_weight(seed, b, "down", self.H, self.F))) for b in range(self.nb)]
+        x = tp_inputs.stack_input(seed, self.nb, self.T, self.H)
+        self.x_pin = pin(x)
+        self.x = tp.bf16_from_bits(x, device)
+        self.z_pin = torch.empty((self.T, self.H), dtype=torch.bfloat16, pin_memory=True)
+        p, H, F = self.p, self.H, self.F
+        e = lambda *sh: torch.empty(sh, dtype=torch.bfloat16, device=device)  # noqa: E731
+        self.shards = [([e(2 * F // p, H) for _ in range(p)], [e(H, F // p) for _ in range(p)])
+                       for _ in range(self.nb)]
+        self.h = [e(self.T, F // p) for _ in range(p)]
+        self.z = [e(self.T, H), e(self.T, H)]
+        self.shard_bytes = self.nb * (2 * F * H + H * F) * 2
+        self.flops = self.nb * (2.0 * self.T * H * 2 * F + 2.0 * self.T * F * H)
+        self.launches_per_step = 2 * self.nb
+
+    def load(self, stream):
+        tp, p, F = self.tp, self.p, self.F
+        for (gu, dn), (gu_sh, dn_sh) in zip(self.host, self.shards):
+            tp.tp_plan_shard_ranks(gu, "colwise", p, 0, p, [F, F], self.heads, 0, outs=gu_sh, stream=stream)
+            tp.tp_plan_shard_ranks(dn, "rowwise", p, 0, p, None, self.heads, 0, outs=dn_sh, stream=stream)
+
+    def forward(self, stream, x=None):
+        tp = self.tp
+        z = self.x if x is None else x
+        for b, (gu_sh, dn_sh) in enumerate(self.shards):
+            tp.tp_linear_colwise(z, gu_sh, "swiglu", y_shards=self.h, stream=stream)
+            out = self.z[b % 2]
+            tp.tp_linear_rowwise(self.h, dn_sh, mode="accum", out=out, stream=stream)
+            z = out
+        return z
+
+
+def run_stack(args):
+    """Shard-on-read load of the 8-block state dict, then the forward pass, on one GPU."""
+    import torch
+    from __graft_entry__ import build
+    build()
+    import tensor_sharded_linear_tp_gb300 as tp
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    wl = StackWorkload(tp, torch, device)
+    stream = torch.cuda.Stream(device)
+    ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+    peaks = load_peaks()
+
+    def timed(fn, reps):
+        out = []
+        for _ in range(reps):
+            a, b = ev(), ev()
+            a.record(stream)
+            fn()
+            b.record(stream)
+            b.synchronize()
+            out.append(a.elapsed_time(b))
+        return float(np.mean(out))
+
+    # Shard-on-read load over the CPU-GPU link, against a plain page-locked copy of equal size.
+    wl.load(stream)
+    stream.synchronize()
+    load_ms = timed(lambda: wl.load(stream), 3)
+    probe_n = 1 << 30
+    src = torch.empty(probe_n, dtype=torch.uint8, pin_memory=True)
+    dst = torch.empty(probe_n, dtype=torch.uint8, device=device)
+    with torch.cuda.stream(stream):
+        dst.copy_(src, non_blocking=True)
+    copy_ms = timed(lambda: dst.copy_(src, non_blocking=True), 3)
+    del dst
+    load_gbs = wl.shard_bytes / (load_ms * 1e-3) / 1e9
+    link_gbs = probe_n / (copy_ms * 1e-3) / 1e9
+
+    for _ in range(args.warmup):
+        wl.forward(stream)
+    stream.synchronize()
+    sampler = ClockSampler(0)
+    sampler.start()
+    time.sleep(0.3)
+    fwd_ms = timed(lambda: wl.forward(stream), max(1, min(args.steps, 50)))
+    clocks = sampler.stop()
+    tp.tp_device_status(stream)
+
+    def e2e_step():
+        wl.load(stream)
+        with torch.cuda.stream(stream):
+            xin = wl.x_pin.to(device, non_blocking=True)
+        z = wl.forward(stream, xin)
+        with torch.cuda.stream(stream):
+            wl.z_pin.copy_(z, non_blocking=True)
+
+    e2e_ms = timed(e2e_step, 3)
+    value = wl.flops / (fwd_ms * 1e-3) / 1e12
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1, "steps": max(1, min(args.steps, 50)),
+        "warmup": args.warmup, "ms_per_step": fwd_ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,0.02) weights, N(0,1) activations)",
+        "config": {"workload": "stack8_swiglu_tp4", "blocks": wl.nb, "tokens": wl.T, "hidden": wl.H, "ffn": wl.F,
+                   "tp_degree": wl.p, "l2": "weights 5.44 GB, larger than L2",
+                   "step": "8 x (tp_linear_colwise SwiGLU + tp_linear_rowwise accum)"},
+        "roofline": {"bound": "tensor", "achieved": value, "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
+                     "frac": value / peaks["bf16_tflops_sustained"], "kernel": "tp_gemm_kernel (16 launches)",
+                     "peak_source": peaks["source"] + " sustained", "traffic": None},
+        "shard_load": {"bytes": wl.shard_bytes, "ms": load_ms, "GB/s": load_gbs,
+                       "link_copy_GB/s": link_gbs, "frac_of_link_copy": load_gbs / link_gbs,
+                       "frac_hbm": load_gbs / peaks["hbm_gbs"]},
+        "e2e": {"value": wl.flops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT, "ms_per_step": e2e_ms,
+                "h2d_bytes_per_step": wl.shard_bytes + wl.T * wl.H * 2, "d2h_bytes_per_step": wl.T * wl.H * 2},
+        "gpu_launches": wl.launches_per_step * max(1, min(args.steps, 50)), "clocks": clocks, "peaks": peaks,
+    }
+    print(json.dumps(line))
+
+
 # ----------------------------------------------------------------------------- CPU oracle timing
 
 def oracle_sample_step(host, rows, p, H, heads, hd):
@@ -575,10 +697,14 @@ def main(argv=None):
     ap.add_argument("--reduce-mode", choices=["accum", "workspace", "none"], default="accum")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing leg")
     ap.add_argument("--eager", action="store_true", help="launch the timed steps eagerly instead of as graphs")
+    ap.add_argument("--workload", choices=[WORKLOAD, "stack8_swiglu_tp4"], default=WORKLOAD,
+                    help="the attention projections (default) or the 8-block stack loaded shard-on-read")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)   # at least three untimed warm-up steps, whatever was asked
     if args.impl == "reference":
         run_reference(args)
+    elif args.workload == "stack8_swiglu_tp4":
+        run_stack(args)
     else:
         run_ours(args)
 
