@@ -252,6 +252,22 @@ class AttnProjWorkload:
         # Pinned host copies for the end-to-end measurement.
         self.pin = None
 
+    def config(self):
+        return {"workload": WORKLOAD, "tokens": self.T, "hidden": self.H, "heads": self.heads, "head_dim": self.hd,
+                "tp_degree": self.p, "rowwise_reduce": self.mode,
+                "step": "2x tp_plan_shard_ranks (device, 4 ranks each) + tp_linear_colwise + tp_combine(gather) + "
+                        "tp_linear_rowwise"}
+
+    def phases(self):
+        """(label, enqueue function, roofline kind, algorithmic work per step: FLOPs or bytes)."""
+        return [("extract", self.phase_extract, "hbm", self.extract_bytes),
+                ("colwise_qkv", self.phase_colwise, "tensor", self.flops_qkv),
+                ("gather", self.phase_gather, "hbm", self.gather_bytes),
+                ("rowwise_out", self.phase_rowwise, "tensor", self.flops_out)]
+
+    def oracle_step(self, rows):
+        return oracle_sample_step(self.host, rows, self.p, self.H, self.heads, self.hd)
+
     # The four phases of a step, each enqueued on `stream`.
     def phase_extract(self, stream):
         tp, p, H = self.tp, self.p, self.H
@@ -268,17 +284,6 @@ class AttnProjWorkload:
 
     def phase_rowwise(self, stream):
         self._rowwise(self.a_sh, stream)
-
-    PHASES = ("phase_extract", "phase_colwise", "phase_gather", "phase_rowwise")
-
-    def step(self, stream, marks=None):
-        """Enqueue one step on `stream`; `marks` (list of 5 events) bracket the four phases."""
-        for i, name in enumerate(self.PHASES):
-            if marks:
-                marks[i].record(stream)
-            getattr(self, name)(stream)
-        if marks:
-            marks[4].record(stream)
 
     def _rowwise(self, a_sh, stream):
         tp = self.tp
@@ -321,6 +326,165 @@ class AttnProjWorkload:
         self._rowwise(self.a_in, stream)
         with torch.cuda.stream(stream):
             self.pin["z"].copy_(self.z, non_blocking=True)
+
+
+def run_step(wl, stream, marks=None):
+    """Enqueue one step of `wl` on `stream`; `marks` (one more event than phases) bracket the phases."""
+    for i, (_, fn, _, _) in enumerate(wl.phases()):
+        if marks:
+            marks[i].record(stream)
+        fn(stream)
+    if marks:
+        marks[-1].record(stream)
+
+
+class MlpWorkload:
+    """One MLP block: colwise in-projection with its activation, rowwise out-projection summed on chip.
+
+    tiny_mlp_tp2: hidden 256, ffn 1024, 64 tokens, GELU(tanh), tp 2.
+    swiglu_mlp_tp4: hidden 6144, ffn 18432 (fused gate/up [36864, 6144]), 4608 tokens, SwiGLU, tp 4.
+    """
+
+    def __init__(self, tp, torch, device, name):
+        cfg = tp_inputs.WORKLOADS[name]
+        self.name, self.tp, self.torch, self.device = name, tp, torch, device
+        self.p, self.T, self.H, self.F = cfg["tp"], cfg["tokens"], cfg["hidden"], cfg["ffn"]
+        self.heads, self.act = cfg["heads"], cfg["act"]
+        p, T, H, F = self.p, self.T, self.H, self.F
+        if self.act == "swiglu":
+            w_in, w_out, x = tp_inputs.swiglu_mlp_inputs(cfg["seed"], T, H, F)
+            self.splits, n_in = [F, F], 2 * F
+        else:
+            w_in, w_out, x = tp_inputs.tiny_mlp_inputs(cfg["seed"], T, H, F)
+            self.splits, n_in = None, F
+        self.host = dict(w_in=w_in, w_out=w_out, x=x)
+        bf = lambda b: tp.bf16_from_bits(b, device)  # noqa: E731
+        self.w_in, self.w_out, self.x = bf(w_in), bf(w_out), bf(x)
+        e = lambda *sh: torch.empty(sh, dtype=torch.bfloat16, device=device)  # noqa: E731
+        self.in_sh = [e(n_in // p, H) for _ in range(p)]
+        self.out_sh = [e(H, F // p) for _ in range(p)]
+        self.h_sh = [e(T, F // p) for _ in range(p)]
+        self.z = e(T, H)
+        self.flops_in = 2.0 * T * H * n_in
+        self.flops_out = 2.0 * T * F * H
+        self.flops = self.flops_in + self.flops_out
+        self.extract_bytes = 2.0 * 2 * (n_in * H + H * F)
+        self.launches_per_step = 4
+
+    def config(self):
+        return {"workload": self.name, "tokens": self.T, "hidden": self.H, "ffn": self.F, "act": self.act,
+                "tp_degree": self.p, "rowwise_reduce": "accum",
+                "step": "2x tp_plan_shard_ranks (device) + tp_linear_colwise (act) + tp_linear_rowwise"}
+
+    def phase_extract(self, stream):
+        tp, p = self.tp, self.p
+        tp.tp_plan_shard_ranks(self.w_in, "colwise", p, 0, p, self.splits, self.heads, 0, outs=self.in_sh,
+                               stream=stream)
+        tp.tp_plan_shard_ranks(self.w_out, "rowwise", p, 0, p, None, self.heads, 0, outs=self.out_sh, stream=stream)
+
+    def phase_colwise(self, stream):
+        self.tp.tp_linear_colwise(self.x, self.in_sh, self.act, y_shards=self.h_sh, stream=stream)
+
+    def phase_rowwise(self, stream):
+        self.tp.tp_linear_rowwise(self.h_sh, self.out_sh, mode="accum", out=self.z, stream=stream)
+
+    def phases(self):
+        return [("extract", self.phase_extract, "hbm", self.extract_bytes),
+                ("colwise_" + self.act, self.phase_colwise, "tensor", self.flops_in),
+                ("rowwise_down", self.phase_rowwise, "tensor", self.flops_out)]
+
+    def oracle_step(self, rows):
+        from oracle import tp_oracle as O
+        p, h = self.p, self.host
+        w_in = [O.shard(h["w_in"], "colwise", p, r, self.splits) for r in range(p)]
+        w_out = [O.shard(h["w_out"], "rowwise", p, r) for r in range(p)]
+        return O.mlp_forward(h["x"][rows], w_in, w_out, self.act)[1]
+
+
+class BlockWorkload:
+    """The full attention + SwiGLU MLP block (hidden 6144, 48 heads x 128, ffn 18432, 4608 tokens) at one tp."""
+
+    def __init__(self, tp, torch, device, p):
+        cfg = tp_inputs.WORKLOADS["block_sweep"]
+        self.tp, self.torch, self.device = tp, torch, device
+        self.p, self.T, self.H, self.F = p, cfg["tokens"], cfg["hidden"], cfg["ffn"]
+        self.heads, self.hd = cfg["heads"], cfg["head_dim"]
+        tp.tp_validate(3 * self.H, self.H, "colwise", p, self.heads, self.hd, [self.H] * 3)  # 5 and 7 raise here
+        T, H, F, hl = self.T, self.H, self.F, self.heads // p
+        wqkv, wout, wgu, wdown, x = tp_inputs.block_inputs(cfg["seed"], T, H, F)
+        self.host = dict(wqkv=wqkv, wout=wout, wgu=wgu, wdown=wdown, x=x)
+        bf = lambda b: tp.bf16_from_bits(b, device)  # noqa: E731
+        self.w = {k: bf(v) for k, v in self.host.items() if k != "x"}
+        self.x = bf(x)
+        e = lambda *sh: torch.empty(sh, dtype=torch.bfloat16, device=device)  # noqa: E731
+        self.qkv_sh = [e(3 * H // p, H) for _ in range(p)]
+        self.out_sh = [e(H, H // p) for _ in range(p)]
+        self.gu_sh = [e(2 * F // p, H) for _ in range(p)]
+        self.dn_sh = [e(H, F // p) for _ in range(p)]
+        self.y_sh = [e(T, 3 * H // p) for _ in range(p)]
+        self.o_sh = [e(T, H // p) for _ in range(p)]
+        self.z1 = e(T, H)
+        self.h_sh = [e(T, F // p) for _ in range(p)]
+        self.z = e(T, H)
+        self.attn_ws = torch.empty(tp.tp_attention_workspace_bytes(T, hl, self.hd), dtype=torch.uint8,
+                                   device=device)
+        self.fl = dict(qkv=2.0 * T * H * 3 * H, attn=4.0 * T * T * self.hd * self.heads, out=2.0 * T * H * H,
+                       gu=2.0 * T * H * 2 * F, down=2.0 * T * F * H)
+        self.flops = sum(self.fl.values())
+        self.extract_bytes = 2.0 * 2 * (4 * H * H + 3 * H * F)
+        self.launches_per_step = 4 + 1 + p * (1 + 3 * ((hl + 15) // 16)) + 3
+
+    def config(self):
+        return {"workload": "block_sweep", "tokens": self.T, "hidden": self.H, "ffn": self.F, "heads": self.heads,
+                "head_dim": self.hd, "tp_degree": self.p, "rowwise_reduce": "accum",
+                "flops": "projections + attention core (4*T^2*head_dim per head)",
+                "step": "4x tp_plan_shard_ranks + QKV colwise + tp_attention_heads per rank + out rowwise + "
+                        "gate/up colwise SwiGLU + down rowwise"}
+
+    def phase_extract(self, stream):
+        tp, p, H, F = self.tp, self.p, self.H, self.F
+        tp.tp_plan_shard_ranks(self.w["wqkv"], "colwise", p, 0, p, [H] * 3, self.heads, self.hd, outs=self.qkv_sh,
+                               stream=stream)
+        tp.tp_plan_shard_ranks(self.w["wout"], "rowwise", p, 0, p, None, self.heads, self.hd, outs=self.out_sh,
+                               stream=stream)
+        tp.tp_plan_shard_ranks(self.w["wgu"], "colwise", p, 0, p, [F, F], self.heads, 0, outs=self.gu_sh,
+                               stream=stream)
+        tp.tp_plan_shard_ranks(self.w["wdown"], "rowwise", p, 0, p, None, self.heads, 0, outs=self.dn_sh,
+                               stream=stream)
+
+    def phase_qkv(self, stream):
+        self.tp.tp_linear_colwise(self.x, self.qkv_sh, "none", y_shards=self.y_sh, stream=stream)
+
+    def phase_attention(self, stream):
+        for y, o in zip(self.y_sh, self.o_sh):
+            self.tp.tp_attention_heads(y, self.heads // self.p, self.hd, out=o, workspace=self.attn_ws, stream=stream)
+
+    def phase_out(self, stream):
+        self.tp.tp_linear_rowwise(self.o_sh, self.out_sh, mode="accum", out=self.z1, stream=stream)
+
+    def phase_gate_up(self, stream):
+        self.tp.tp_linear_colwise(self.z1, self.gu_sh, "swiglu", y_shards=self.h_sh, stream=stream)
+
+    def phase_down(self, stream):
+        self.tp.tp_linear_rowwise(self.h_sh, self.dn_sh, mode="accum", out=self.z, stream=stream)
+
+    def phases(self):
+        return [("extract", self.phase_extract, "hbm", self.extract_bytes),
+                ("colwise_qkv", self.phase_qkv, "tensor", self.fl["qkv"]),
+                ("attention", self.phase_attention, "tensor", self.fl["attn"]),
+                ("rowwise_out", self.phase_out, "tensor", self.fl["out"]),
+                ("colwise_swiglu", self.phase_gate_up, "tensor", self.fl["gu"]),
+                ("rowwise_down", self.phase_down, "tensor", self.fl["down"])]
+
+    def oracle_step(self, rows):
+        from oracle import tp_oracle as O
+        p, h, H, F = self.p, self.host, self.H, self.F
+        return O.transformer_block_forward(
+            h["x"], [O.shard(h["wqkv"], "colwise", p, r, [H] * 3) for r in range(p)],
+            [O.shard(h["wout"], "rowwise", p, r) for r in range(p)],
+            [O.shard(h["wgu"], "colwise", p, r, [F, F]) for r in range(p)],
+            [O.shard(h["wdown"], "rowwise", p, r) for r in range(p)],
+            n_local_heads=self.heads // p, head_dim=self.hd, q_rows=rows)["z"]
 
 
 class StackWorkload:
@@ -400,7 +564,11 @@ def run_stack(args):
     dst = torch.empty(probe_n, dtype=torch.uint8, device=device)
     with torch.cuda.stream(stream):
         dst.copy_(src, non_blocking=True)
-    copy_ms = timed(lambda: dst.copy_(src, non_blocking=True), 3)
+    def link_copy():
+        with torch.cuda.stream(stream):
+            dst.copy_(src, non_blocking=True)
+
+    copy_ms = timed(link_copy, 3)
     del dst
     load_gbs = wl.shard_bytes / (load_ms * 1e-3) / 1e9
     link_gbs = probe_n / (copy_ms * 1e-3) / 1e9
@@ -497,6 +665,40 @@ def cpu_baseline(host, T, p, H, heads, hd, flops_full, target_s=12.0):
 
 # ----------------------------------------------------------------------------- arms
 
+def make_workload(args, tp, torch, device):
+    if args.workload == WORKLOAD:
+        return AttnProjWorkload(tp, torch, device, args.reduce_mode)
+    if args.workload in ("tiny_mlp_tp2", "swiglu_mlp_tp4"):
+        return MlpWorkload(tp, torch, device, args.workload)
+    if args.workload == "block_sweep":
+        return BlockWorkload(tp, torch, device, args.tp)
+    raise ValueError(args.workload)
+
+
+def generic_cpu_baseline(wl, target_s=12.0):
+    """The oracle on a bounded sample of the workload's token rows, scaled to TFLOP/s."""
+    T = wl.T
+    n = 16
+    t0 = time.perf_counter()
+    wl.oracle_step(tp_inputs.sample_rows(11, T, n))
+    dt = time.perf_counter() - t0
+    while dt < target_s / 4 and n < T:
+        n = min(T, n * 4)
+        t0 = time.perf_counter()
+        wl.oracle_step(tp_inputs.sample_rows(11, T, n))
+        dt = time.perf_counter() - t0
+    reps = max(1, int(round(target_s / max(dt, 1e-3)))) if n == T else 1
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        wl.oracle_step(tp_inputs.sample_rows(12, T, n))
+    dt = time.perf_counter() - t0
+    flops = wl.flops * n / T * reps
+    what = f"{reps} repetitions of the whole step" if n == T else f"{n} of {T} token rows of one step"
+    return {"value": flops / dt / 1e12, "unit": UNIT, "cores": int(os.environ["OPENBLAS_NUM_THREADS"]),
+            "kind": "oracle", "sample": f"{what} (float64 numpy oracle), {dt:.1f} s; TFLOP/s = the sample's "
+                                        f"FLOPs (the step's FLOPs scaled by rows) / its time"}
+
+
 def run_ours(args):
     import torch
     rank, world, local_rank = dist_env()
@@ -509,29 +711,31 @@ def run_ours(args):
     barrier(dist, device)
     import tensor_sharded_linear_tp_gb300 as tp
 
-    wl = AttnProjWorkload(tp, torch, device, args.reduce_mode)
+    wl = make_workload(args, tp, torch, device)
+    phases = wl.phases()
+    nph = len(phases)
     stream = torch.cuda.Stream(device)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
     peaks = load_peaks()
 
     for _ in range(args.warmup):
-        wl.step(stream)
+        run_step(wl, stream)
     stream.synchronize()
     tp.tp_device_status(stream)
 
     # Eager launches: host enqueue cost per step, and a per-phase cross-check.
     n_eager = min(args.steps, 50)
-    eager_marks = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(n_eager)]
+    eager_marks = [[torch.cuda.Event(enable_timing=True) for _ in range(nph + 1)] for _ in range(n_eager)]
     torch.cuda.synchronize()
     host_s = 0.0
     for k in range(n_eager):
         with torch.cuda.stream(stream):
             flush.zero_()
         t0 = time.perf_counter()
-        wl.step(stream, eager_marks[k])
+        run_step(wl, stream, eager_marks[k])
         host_s += time.perf_counter() - t0
     torch.cuda.synchronize()
-    eager_phase = np.array([[m[i].elapsed_time(m[i + 1]) for i in range(4)] for m in eager_marks])
+    eager_phase = np.array([[m[i].elapsed_time(m[i + 1]) for i in range(nph)] for m in eager_marks])
     host_enqueue_ms = host_s / n_eager * 1e3
 
     # The timed region replays each phase as a captured CUDA graph (the launches a
@@ -539,10 +743,10 @@ def run_ours(args):
     # step back to back instead of waiting on Python.
     graphs = []
     if not args.eager:
-        for name in wl.PHASES:
+        for _, fn, _, _ in phases:
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=stream):
-                getattr(wl, name)(stream)
+                fn(stream)
             graphs.append(g)
         with torch.cuda.stream(stream):
             for _ in range(args.warmup):
@@ -551,7 +755,7 @@ def run_ours(args):
         stream.synchronize()
         tp.tp_device_status(stream)
 
-    marks = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    marks = [[torch.cuda.Event(enable_timing=True) for _ in range(nph + 1)] for _ in range(args.steps)]
     sampler = ClockSampler(local_rank)
     sampler.start()
     time.sleep(0.3)
@@ -565,35 +769,31 @@ def run_ours(args):
                 for i, g in enumerate(graphs):
                     marks[k][i].record(stream)
                     g.replay()
-                marks[k][4].record(stream)
+                marks[k][nph].record(stream)
             else:
-                wl.step(stream, marks[k])
+                run_step(wl, stream, marks[k])
     torch.cuda.synchronize()
     barrier(dist, device)
     t_wall = time.perf_counter() - t_wall0
     clocks = sampler.stop()
     tp.tp_device_status(stream)
 
-    phase = np.array([[m[i].elapsed_time(m[i + 1]) for i in range(4)] for m in marks])  # ms
-    step_ms = phase.sum(axis=1)
-    mean_step_ms = float(step_ms.mean())
+    phase = np.array([[m[i].elapsed_time(m[i + 1]) for i in range(nph)] for m in marks])  # ms
+    mean_step_ms = float(phase.sum(axis=1).mean())
     slowest_ms = max_over_ranks(dist, mean_step_ms, device)
     total_flops = sum_over_ranks(dist, wl.flops, device)
     value = total_flops / (slowest_ms * 1e-3) / 1e12
 
-    ph = phase.mean(axis=0)   # extract, colwise, gather, rowwise (ms)
-    kernels = {
-        "extract": {"ms": ph[0], "GB/s": wl.extract_bytes / (ph[0] * 1e-3) / 1e9},
-        "colwise_qkv": {"ms": ph[1], "TFLOP/s": wl.flops_qkv / (ph[1] * 1e-3) / 1e12},
-        "gather": {"ms": ph[2], "GB/s": wl.gather_bytes / (ph[2] * 1e-3) / 1e9},
-        "rowwise_out": {"ms": ph[3], "TFLOP/s": wl.flops_out / (ph[3] * 1e-3) / 1e12},
-    }
-    for k, v in kernels.items():
-        if "GB/s" in v:
-            v["frac_hbm"] = v["GB/s"] / peaks["hbm_gbs"]
+    ph = phase.mean(axis=0)
+    kernels = {}
+    for (label, _, kind, work), ms in zip(phases, ph):
+        if kind == "tensor":
+            v = work / (ms * 1e-3) / 1e12
+            kernels[label] = {"ms": round(float(ms), 5), "TFLOP/s": v, "frac_tensor": v / peaks["bf16_tflops"]}
         else:
-            v["frac_tensor"] = v["TFLOP/s"] / peaks["bf16_tflops"]
-        v["ms"] = round(v["ms"], 5)
+            v = work / (ms * 1e-3) / 1e9
+            kernels[label] = {"ms": round(float(ms), 5), "GB/s": v, "frac_hbm": v / peaks["hbm_gbs"]}
+    tensor_phases = [k for k in kernels if "TFLOP/s" in kernels[k]]
     dominant = max(kernels, key=lambda k: kernels[k]["ms"])
     if "TFLOP/s" in kernels[dominant]:
         achieved = kernels[dominant]["TFLOP/s"]
@@ -601,50 +801,55 @@ def run_ours(args):
                     "frac": achieved / peaks["bf16_tflops"],
                     "frac_of_sustained": achieved / peaks["bf16_tflops_sustained"],
                     "kernel": dominant, "peak_source": peaks["source"] + " burst",
-                    "traffic": recorded_traffic("tp_gemm_kernel<0>" if dominant == "colwise_qkv" else dominant,
-                                                "gemm")}
+                    "traffic": recorded_traffic(f"{args.workload}:{dominant}", "gemm")}
     else:
         achieved = kernels[dominant]["GB/s"]
         roofline = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                     "frac": achieved / peaks["hbm_gbs"], "kernel": dominant, "peak_source": peaks["source"],
-                    "traffic": None}
+                    "traffic": recorded_traffic(f"{args.workload}:{dominant}", "copy")}
 
-    # End to end through the same public calls with host buffers.
-    wl.setup_e2e()
-    for _ in range(max(1, args.warmup)):
-        wl.step_e2e(stream)
-    stream.synchronize()
-    e2e_ms = []
-    for _ in range(min(args.steps, 100)):
-        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        s.record(stream)
-        wl.step_e2e(stream)
-        e.record(stream)
-        e.synchronize()
-        e2e_ms.append(s.elapsed_time(e))
-    tp.tp_device_status(stream)
-    e2e_slowest = max_over_ranks(dist, float(np.mean(e2e_ms)), device)
-    e2e = {"value": total_flops / (e2e_slowest * 1e-3) / 1e12, "unit": UNIT,
-           "h2d_bytes_per_step": int(wl.h2d_bytes), "d2h_bytes_per_step": int(wl.d2h_bytes),
-           "ms_per_step": e2e_slowest}
+    # End to end through the same public calls with host buffers (the attention projections).
+    e2e = None
+    if hasattr(wl, "setup_e2e"):
+        wl.setup_e2e()
+        for _ in range(max(1, args.warmup)):
+            wl.step_e2e(stream)
+        stream.synchronize()
+        e2e_ms = []
+        for _ in range(min(args.steps, 100)):
+            s_, e_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s_.record(stream)
+            wl.step_e2e(stream)
+            e_.record(stream)
+            e_.synchronize()
+            e2e_ms.append(s_.elapsed_time(e_))
+        tp.tp_device_status(stream)
+        e2e_slowest = max_over_ranks(dist, float(np.mean(e2e_ms)), device)
+        e2e = {"value": total_flops / (e2e_slowest * 1e-3) / 1e12, "unit": UNIT,
+               "h2d_bytes_per_step": int(wl.h2d_bytes), "d2h_bytes_per_step": int(wl.d2h_bytes),
+               "ms_per_step": e2e_slowest}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(wl.host, wl.T, wl.p, wl.H, wl.heads, wl.hd, wl.flops)
+        if isinstance(wl, AttnProjWorkload):
+            cpu = cpu_baseline(wl.host, wl.T, wl.p, wl.H, wl.heads, wl.hd, wl.flops)
+        else:
+            cpu = generic_cpu_baseline(wl)
 
     if rank == 0:
+        cfg = wl.config()
+        cfg.update({"parallelism": f"tp{wl.p} simulated on each GPU; replicas across GPUs",
+                    "l2": "flushed between steps (256 MiB write)",
+                    "sms": torch.cuda.get_device_properties(device).multi_processor_count})
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": slowest_ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,0.02) weights, N(0,1) activations)",
-            "config": {"workload": WORKLOAD, "tokens": wl.T, "hidden": wl.H, "heads": wl.heads, "head_dim": wl.hd,
-                       "tp_degree": wl.p, "parallelism": f"tp{wl.p} simulated on each GPU; replicas across GPUs",
-                       "rowwise_reduce": args.reduce_mode, "l2": "flushed between steps (256 MiB write)",
-                       "step": "2x tp_plan_shard_ranks (device, 4 ranks each) + tp_linear_colwise + "
-                               "tp_combine(gather) + tp_linear_rowwise", "sms": torch.cuda.get_device_properties(
-                                   device).multi_processor_count},
-            "roofline": roofline, "kernels": kernels, "extract_gbs": kernels["extract"]["GB/s"],
-            "extract_frac_hbm": kernels["extract"]["frac_hbm"], "cpu_baseline": cpu, "e2e": e2e,
+            "config": cfg, "roofline": roofline, "kernels": kernels,
+            "extract_gbs": kernels["extract"]["GB/s"], "extract_frac_hbm": kernels["extract"]["frac_hbm"],
+            "gemm_tflops": sum(wl_work for (lb, _, kd, wl_work) in phases if kd == "tensor") /
+            (sum(kernels[k]["ms"] for k in tensor_phases) * 1e-3) / 1e12,
+            "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": wl.launches_per_step * args.steps, "clocks": clocks,
             "bracket_s": t_wall, "peaks": peaks, "launch": "eager" if args.eager else "cuda_graph_per_phase",
             "eager_ms_per_step": float(eager_phase.sum(axis=1).mean()),
@@ -697,8 +902,11 @@ def main(argv=None):
     ap.add_argument("--reduce-mode", choices=["accum", "workspace", "none"], default="accum")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing leg")
     ap.add_argument("--eager", action="store_true", help="launch the timed steps eagerly instead of as graphs")
-    ap.add_argument("--workload", choices=[WORKLOAD, "stack8_swiglu_tp4"], default=WORKLOAD,
-                    help="the attention projections (default) or the 8-block stack loaded shard-on-read")
+    ap.add_argument("--workload", default=WORKLOAD,
+                    choices=[WORKLOAD, "tiny_mlp_tp2", "swiglu_mlp_tp4", "block_sweep", "stack8_swiglu_tp4"],
+                    help="the attention projections (default), the tiny or SwiGLU MLP block, the full block "
+                         "(with --tp), or the 8-block stack loaded shard-on-read")
+    ap.add_argument("--tp", type=int, default=4, help="tp_degree of --workload block_sweep")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)   # at least three untimed warm-up steps, whatever was asked
     if args.impl == "reference":
