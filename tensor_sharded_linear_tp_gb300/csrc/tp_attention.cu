@@ -7,7 +7,8 @@
 // [h*d, (h+1)*d) of each of Q, K, V in the rank's QKV output):
 //     O_h = softmax(Q_h K_h^T / sqrt(d)) V_h        (no mask)
 //
-// Steps, per batch of up to 16 heads:
+// head_dim 128 runs the fused kernel of tp_flash.cu (scores and probabilities
+// stay on chip).  Other head sizes take these steps, per batch of up to 16 heads:
 //   1. S_h = Q_h . K_h^T   -- batched tcgen05 GEMM, fp32 scores [T, T];
 //   2. P_h = softmax(S_h / sqrt(d)) row by row, fp32 math, written as bf16
 //      over the first half of each score row (one warp per row);
@@ -113,6 +114,8 @@ extern "C" {
 
 size_t tp_attention_workspace_bytes(int64_t T, int n_heads, int head_dim) {
   if (T <= 0 || n_heads <= 0 || head_dim <= 0) return 0;
+  if (head_dim == 128)  // fused kernel: V^T only
+    return tp::align256(static_cast<size_t>(n_heads) * 128 * static_cast<size_t>(T) * 2);
   const size_t hb = static_cast<size_t>(n_heads < tp::kHeadBatch ? n_heads : tp::kHeadBatch);
   return tp::align256(hb * static_cast<size_t>(T) * static_cast<size_t>(T) * 4) +
          tp::align256(static_cast<size_t>(n_heads) * static_cast<size_t>(head_dim) * static_cast<size_t>(T) * 2);
@@ -139,9 +142,11 @@ tp_status tp_attention_heads(const void* qkv, int64_t ld_qkv, int64_t T, int n_h
     return fail(TP_ERR_WORKSPACE, "workspace of %zu bytes given, %zu needed", workspace ? ws_bytes : 0, need);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const size_t hb = static_cast<size_t>(n_heads < kHeadBatch ? n_heads : kHeadBatch);
+  const bool fused = (head_dim == 128);
   float* scores = static_cast<float*>(workspace);
-  __nv_bfloat16* vt = reinterpret_cast<__nv_bfloat16*>(static_cast<uint8_t*>(workspace) +
-                                                       align256(hb * static_cast<size_t>(T) * T * 4));
+  __nv_bfloat16* vt = fused ? static_cast<__nv_bfloat16*>(workspace)
+                            : reinterpret_cast<__nv_bfloat16*>(static_cast<uint8_t*>(workspace) +
+                                                               align256(hb * static_cast<size_t>(T) * T * 4));
   const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(qkv);
   const __nv_bfloat16* k = q + width;
   const __nv_bfloat16* v = q + 2 * width;
@@ -154,6 +159,7 @@ tp_status tp_attention_heads(const void* qkv, int64_t ld_qkv, int64_t T, int n_h
   if (e != cudaSuccess) return cuda_fail(e, "transpose launch");
 
   const float scale_log2e = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(head_dim)));
+  if (fused) return flash_attention_d128(qkv, ld_qkv, T, n_heads, vt, out, ldo, scale_log2e, s);
   for (int h0 = 0; h0 < n_heads; h0 += kHeadBatch) {
     const int nb = (n_heads - h0) < kHeadBatch ? (n_heads - h0) : kHeadBatch;
     const void* a[kHeadBatch];

@@ -655,7 +655,9 @@ __global__ void __launch_bounds__(kThreads, 1) tp_gemm_kernel(const __grid_const
       decode_tile(p, t, g, mb, nb);
       const uint32_t acc = tcount & 1u;
       const uint32_t aph = (tcount >> 1) & 1u;
-      if (!wait_bounded(ptx::smem_addr(&ctl->tfull[acc]), aph, abort_flag, p.status, false)) break;
+      // Warp-uniform outcome: the epilogue's TMEM loads are warp-collective.
+      if (!__all_sync(0xffffffffu, wait_bounded(ptx::smem_addr(&ctl->tfull[acc]), aph, abort_flag, p.status, false)))
+        break;
       ptx::tc_fence_after();
       const int mb128 = mb * (C::TILE_M / BM) + static_cast<int>(cta);
       const int row0 = mb128 * BM + q * 32;
@@ -1210,6 +1212,18 @@ tp_status gemm_batched(int groups, const void* const* a, int64_t lda, const void
   p.a_shared = 0;
   p.rank_fastest = 0;
   return out_f32 ? launch_gemm<EPI_F32>(p, pair, stream) : launch_gemm<EPI_BF16>(p, pair, stream);
+}
+
+}  // namespace tp
+
+namespace tp {
+
+// bf16 2-D tensor map for other kernels of the library (cached like the GEMM's own).
+tp_status encode_bf16_2d(CUtensorMap* m, const void* ptr, int64_t inner, int64_t outer, int64_t ld, uint32_t box_inner,
+                         uint32_t box_outer, bool swizzle128) {
+  return encode_2d(m, ptr, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, inner, outer, ld, box_inner, box_outer,
+                   swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
 }
 
 }  // namespace tp

@@ -1,6 +1,7 @@
 // Host-side helpers shared by the library's translation units (not part of the ABI).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <cstdarg>
@@ -43,4 +44,13 @@ namespace tp {
 tp_status gemm_batched(int groups, const void* const* a, int64_t lda, const void* const* b, int64_t ldb,
                        void* const* out, int64_t ldo, bool out_f32, int64_t M, int64_t N, int64_t K,
                        cudaStream_t stream);
+}  // namespace tp
+
+namespace tp {
+// bf16 2-D tensor map over a row-major [outer, inner] matrix (row stride ld elements), cached (tp_gemm.cu).
+tp_status encode_bf16_2d(CUtensorMap* m, const void* ptr, int64_t inner, int64_t outer, int64_t ld, uint32_t box_inner,
+                         uint32_t box_outer, bool swizzle128);
+// Fused attention for head_dim 128 (tp_flash.cu); vt is V^T [n_heads*128, T].
+tp_status flash_attention_d128(const void* qkv, int64_t ld_qkv, int64_t T, int n_heads, const void* vt, void* out,
+                               int64_t ldo, float scale_log2e, cudaStream_t stream);
 }  // namespace tp

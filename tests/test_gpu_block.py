@@ -67,6 +67,24 @@ def test_attention_one_dominant_key_returns_its_value():
     assert_close(out, ref, "one-hot attention")
 
 
+@pytest.mark.parametrize("T", [512, 1000])
+def test_attention_running_max_raised_in_some_rows(T):
+    # Key tiles of growing magnitude (x1, x3, x9, ...): a query's scores jump between tiles
+    # when it aligns with the keys (its running max is raised and its output rescaled) and
+    # not when it does not -- rows of the same warp take different paths.
+    heads, d = 2, 128
+    rng = np.random.default_rng(153)
+    q = rng.standard_normal((T, heads * d))
+    k = rng.standard_normal((T, heads * d)) * (3.0 ** (np.arange(T) // 128))[:, None] * 0.5
+    v = rng.standard_normal((T, heads * d))
+    qkv = O.f64_to_bf16(np.concatenate([q, k, v], axis=1))
+    out = f64(tp.tp_attention_heads(dev(qkv), heads, d))
+    qf = O.bf16_to_f64(qkv)
+    H = heads * d
+    ref = O.attention_core(qf[:, :H], qf[:, H:2 * H], qf[:, 2 * H:], heads, d)
+    assert_close(out, ref, f"growing keys T={T}")
+
+
 def test_attention_writes_into_strided_output():
     # The rank's attention output can land in a wider buffer (row stride ldo).
     T, heads, d = 136, 2, 64
