@@ -237,6 +237,30 @@ TP_API tp_status tp_linear_rowwise(const void* const* x_shards, const void* cons
                             int64_t T, int64_t K_r, int64_t N, tp_reduce_mode mode, void* workspace, size_t ws_bytes,
                             void* out, tp_stream_t stream);
 
+/*
+ * tp_linear_rowwise_split_input -- the "rowwise_split_input" style: a rowwise
+ * projection whose input is replicated on every rank, each rank computing its
+ * partial from its own slice of that input.
+ *
+ * "Tensor parallelism" page, §Colwise and rowwise table: "rowwise_split_input"
+ * shards the input features (weight dim 1) and each rank computes a partial
+ * result from its slice of the replicated input and its weights; the sum
+ * gives every rank all output features (for a standalone projection reading a
+ * replicated activation, e.g. an AdaLN modulation projection).
+ *     Z = sum_r X[:, r*K/p : (r+1)*K/p] . W_r^T (+ bias, once)
+ *
+ * x: device bf16 [T, K] with row stride ldx elements (0 = K); rank r reads
+ *    columns [r*K/p, (r+1)*K/p) in place (no copy).
+ * w_shards: host array of tp_degree device pointers, each bf16 [N, K/p] (the
+ *    plain rowwise shards).  bias, mode, workspace, out: as tp_linear_rowwise.
+ * Errors: TP_ERR_SPLIT_NOT_DIVISIBLE if tp_degree does not divide K; the
+ * alignment rules of tp_linear_rowwise with K/p and ldx multiples of 8.
+ */
+TP_API tp_status tp_linear_rowwise_split_input(const void* x, int64_t ldx, const void* const* w_shards,
+                                               const void* bias, int tp_degree, int64_t T, int64_t K, int64_t N,
+                                               tp_reduce_mode mode, void* workspace, size_t ws_bytes, void* out,
+                                               tp_stream_t stream);
+
 /* Bytes of device workspace tp_linear_rowwise needs for `mode` (0 unless TP_REDUCE_WORKSPACE). */
 TP_API size_t tp_rowwise_workspace_bytes(int tp_degree, int64_t T, int64_t N, tp_reduce_mode mode);
 

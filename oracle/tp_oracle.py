@@ -320,6 +320,20 @@ def rowwise_forward(x_shards, w_shards, bias_bits: np.ndarray | None = None) -> 
     return z
 
 
+def rowwise_split_input_forward(x_bits: np.ndarray, w_shards, bias_bits: np.ndarray | None = None) -> np.ndarray:
+    """"rowwise_split_input": the input X is replicated and each rank takes its own slice of it.
+
+    "Tensor parallelism" page, §Colwise and rowwise table: the style shards the
+    weight's input features like "rowwise", but the rank computes its partial
+    from its slice of the replicated input (e.g. an AdaLN modulation projection
+    reading the timestep embedding), and the AllReduce sum gives every rank all
+    output features.  Rank r's slice is columns [r*K/p, (r+1)*K/p) of X.
+    """
+    p = len(w_shards)
+    x_shards = [shard(x_bits, ROWWISE, p, r) for r in range(p)]
+    return rowwise_forward(x_shards, w_shards, bias_bits)
+
+
 def combine_gather(parts: Sequence[np.ndarray]) -> np.ndarray:
     """AllGather of colwise outputs: concatenate rank slices along the feature axis."""
     return np.ascontiguousarray(np.concatenate(list(parts), axis=1))

@@ -53,6 +53,8 @@ _SIGS = {
                                     _i64, _i64, ctypes.POINTER(_vp), _i64, _vp]),
     "tp_linear_rowwise": (_status, [ctypes.POINTER(_vp), ctypes.POINTER(_vp), _vp, ctypes.c_int, _i64, _i64, _i64,
                                     ctypes.c_int, _vp, ctypes.c_size_t, _vp, _vp]),
+    "tp_linear_rowwise_split_input": (_status, [_vp, _i64, ctypes.POINTER(_vp), _vp, ctypes.c_int, _i64, _i64, _i64,
+                                                ctypes.c_int, _vp, ctypes.c_size_t, _vp, _vp]),
     "tp_linear_rowwise_noalloc": (_status, [ctypes.POINTER(_vp), ctypes.POINTER(_vp), _vp, ctypes.c_int, _i64, _i64,
                                             _i64, _vp, _vp]),
     "tp_rowwise_workspace_bytes": (ctypes.c_size_t, [ctypes.c_int, _i64, _i64, ctypes.c_int]),
@@ -121,6 +123,14 @@ def _need_bf16(name, t):
         raise TypeError(f"{name} must be bfloat16, got {t.dtype}")
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
+
+
+def _need_bf16_rows(name, t):
+    """bf16 2-D with contiguous rows (any row stride): the library takes the stride."""
+    if t.dtype != torch.bfloat16:
+        raise TypeError(f"{name} must be bfloat16, got {t.dtype}")
+    if t.dim() != 2 or t.stride(1) != 1 or t.stride(0) < t.shape[1]:
+        raise ValueError(f"{name} must be 2-D with contiguous rows")
 
 
 # ---------------------------------------------------------------------------
@@ -242,6 +252,27 @@ def tp_linear_rowwise(x_shards: Sequence[torch.Tensor], w_shards: Sequence[torch
     return out
 
 
+def tp_linear_rowwise_split_input(x: torch.Tensor, w_shards: Sequence[torch.Tensor], bias: torch.Tensor | None = None,
+                                  mode: str = "accum", workspace: torch.Tensor | None = None,
+                                  out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Z = sum_r X[:, r*K/p:(r+1)*K/p] W_r^T (+ bias once): each rank slices the replicated input itself."""
+    _need_bf16_rows("x", x)
+    p = len(w_shards)
+    T, K = x.shape
+    N = w_shards[0].shape[0]
+    if out is None:
+        shape = (p, T, N) if mode == "none" else (T, N)
+        out = torch.empty(shape, dtype=torch.float32 if mode == "none" else torch.bfloat16, device=x.device)
+    need = tp_rowwise_workspace_bytes(p, T, N, mode)
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=x.device)
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(lib.tp_linear_rowwise_split_input(_ptr(x), x.stride(0), _ptrs(w_shards), _ptr(bias), p, T, K, N,
+                                             REDUCE_MODES[mode], _ptr(workspace), ws_bytes, _ptr(out),
+                                             _stream(stream)))
+    return out
+
+
 NOALLOC_SCRATCH_BYTES = 64 << 20
 
 
@@ -278,7 +309,7 @@ def tp_attention_workspace_bytes(T: int, n_heads: int, head_dim: int) -> int:
 def tp_attention_heads(qkv: torch.Tensor, n_heads: int, head_dim: int, out: torch.Tensor | None = None,
                        workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
     """softmax(Q_h K_h^T / sqrt(d)) V_h for each local head of a rank's QKV output [T, 3*n_heads*d]."""
-    _need_bf16("qkv", qkv)
+    _need_bf16_rows("qkv", qkv)
     T = qkv.shape[0]
     width = n_heads * head_dim
     if out is None:

@@ -1007,11 +1007,55 @@ size_t tp_rowwise_workspace_bytes(int tp_degree, int64_t T, int64_t N, tp_reduce
   return aligned + tiles * sizeof(int);
 }
 
+}  // extern "C"
+
+namespace tp {
+namespace {
+tp_status rowwise_impl(const void* const* x_shards, int64_t ldx, const void* const* w_shards, const void* bias,
+                       int tp_degree, int64_t T, int64_t K_r, int64_t N, tp_reduce_mode mode, void* workspace,
+                       size_t ws_bytes, void* out, tp_stream_t stream);
+}  // namespace
+}  // namespace tp
+
+extern "C" {
+
 tp_status tp_linear_rowwise(const void* const* x_shards, const void* const* w_shards, const void* bias, int tp_degree,
                             int64_t T, int64_t K_r, int64_t N, tp_reduce_mode mode, void* workspace, size_t ws_bytes,
                             void* out, tp_stream_t stream) {
+  tp::clear_error();
+  return tp::rowwise_impl(x_shards, K_r, w_shards, bias, tp_degree, T, K_r, N, mode, workspace, ws_bytes, out,
+                          stream);
+}
+
+tp_status tp_linear_rowwise_split_input(const void* x, int64_t ldx, const void* const* w_shards, const void* bias,
+                                        int tp_degree, int64_t T, int64_t K, int64_t N, tp_reduce_mode mode,
+                                        void* workspace, size_t ws_bytes, void* out, tp_stream_t stream) {
   using namespace tp;
   clear_error();
+  if (tp_degree < 1) return fail(TP_ERR_INVALID_ARG, "tp_degree must be >= 1, got %d", tp_degree);
+  if (tp_degree > TP_MAX_DEGREE)
+    return fail(TP_ERR_UNSUPPORTED, "tp_degree=%d above TP_MAX_DEGREE=%d", tp_degree, TP_MAX_DEGREE);
+  if (K < 0 || T < 0 || N < 0) return fail(TP_ERR_INVALID_ARG, "negative size");
+  if (K % tp_degree != 0)
+    return fail(TP_ERR_SPLIT_NOT_DIVISIBLE, "K=%lld not divisible by tp_degree=%d", (long long)K, tp_degree);
+  if (ldx == 0) ldx = K;
+  if (ldx < K) return fail(TP_ERR_INVALID_ARG, "ldx=%lld smaller than K=%lld", (long long)ldx, (long long)K);
+  if (T == 0 || N == 0) return TP_OK;
+  if (x == nullptr) return fail(TP_ERR_INVALID_ARG, "x is NULL");
+  // Rank r's input is the column window [r*K/p, (r+1)*K/p) of the replicated X: a strided view, no copy.
+  const int64_t K_r = K / tp_degree;
+  const void* xs[TP_MAX_DEGREE];
+  for (int r = 0; r < tp_degree; ++r) xs[r] = static_cast<const uint16_t*>(x) + static_cast<int64_t>(r) * K_r;
+  return rowwise_impl(xs, ldx, w_shards, bias, tp_degree, T, K_r, N, mode, workspace, ws_bytes, out, stream);
+}
+
+}  // extern "C"
+
+namespace tp {
+namespace {
+tp_status rowwise_impl(const void* const* x_shards, int64_t ldx, const void* const* w_shards, const void* bias,
+                       int tp_degree, int64_t T, int64_t K_r, int64_t N, tp_reduce_mode mode, void* workspace,
+                       size_t ws_bytes, void* out, tp_stream_t stream) {
   if (tp_degree < 1) return fail(TP_ERR_INVALID_ARG, "tp_degree must be >= 1, got %d", tp_degree);
   if (tp_degree > TP_MAX_DEGREE)
     return fail(TP_ERR_UNSUPPORTED, "tp_degree=%d above TP_MAX_DEGREE=%d", tp_degree, TP_MAX_DEGREE);
@@ -1023,8 +1067,9 @@ tp_status tp_linear_rowwise(const void* const* x_shards, const void* const* w_sh
   if (K_r == 0) return fail(TP_ERR_INVALID_ARG, "K_r (input features per rank) must be positive");
   if (x_shards == nullptr || w_shards == nullptr || out == nullptr)
     return fail(TP_ERR_INVALID_ARG, "x_shards, w_shards or out is NULL");
-  if ((K_r % 8) != 0 || (N % 8) != 0)
-    return fail(TP_ERR_ALIGNMENT, "K_r (%lld) and N (%lld) must be multiples of 8", (long long)K_r, (long long)N);
+  if ((K_r % 8) != 0 || (N % 8) != 0 || (ldx % 8) != 0)
+    return fail(TP_ERR_ALIGNMENT, "K_r (%lld), N (%lld) and the input row stride (%lld) must be multiples of 8",
+                (long long)K_r, (long long)N, (long long)ldx);
   if (!aligned16(out) || (bias != nullptr && !aligned16(bias)))
     return fail(TP_ERR_ALIGNMENT, "out or bias is not 16-byte aligned");
   for (int r = 0; r < tp_degree; ++r) {
@@ -1048,7 +1093,7 @@ tp_status tp_linear_rowwise(const void* const* x_shards, const void* const* w_sh
   const int bn = choose_bn(N, groups * m_tiles, resident_units(pair));
   GemmParams p{};
   for (int r = 0; r < tp_degree; ++r) {
-    st = make_map(&p.map_a[r], x_shards[r], K_r, T, K_r, BM);
+    st = make_map(&p.map_a[r], x_shards[r], K_r, T, ldx, BM);
     if (st != TP_OK) return st;
     st = make_map(&p.map_b[r], w_shards[r], K_r, N, K_r, pair ? bn / 2 : bn);
     if (st != TP_OK) return st;
@@ -1106,8 +1151,8 @@ tp_status tp_linear_rowwise(const void* const* x_shards, const void* const* w_sh
   if (e != cudaSuccess) return cuda_fail(e, "clearing the tile counters");
   return launch_gemm<EPI_WS_REDUCE>(p, pair, s);
 }
-
-}  // extern "C"
+}  // namespace
+}  // namespace tp
 
 // ---------------------------------------------------------------------------
 // Rowwise workspace mode for callers that cannot allocate: the scratch is a

@@ -323,6 +323,24 @@ def pin_rowwise_sum():
     assert np.allclose(zb, full + O.bf16_to_f64(b)[None, :], rtol=1e-13, atol=1e-15)
 
 
+def pin_rowwise_split_input():
+    # Each rank slicing the replicated input and the sum over ranks is the plain layer,
+    # checked against a brute-force loop and the slice arithmetic by hand on a tiny case.
+    T, K, N = 3, 12, 5
+    x = tp_inputs.int_bf16(44, 0, (T, K))
+    w = tp_inputs.int_bf16(44, 1, (N, K))
+    brute = _brute_linear(O.bf16_to_f64(x), O.bf16_to_f64(w))
+    for p in (1, 2, 3, 4, 6):
+        z = O.rowwise_split_input_forward(x, [O.shard(w, O.ROWWISE, p, r) for r in range(p)])
+        assert np.array_equal(z, brute), p
+    # With tp_degree 3 rank 1 sees input columns 4..7 only: zeroing them changes only its partial.
+    x2 = O.bf16_to_f64(x).copy()
+    x2[:, 4:8] = 0
+    z2 = O.rowwise_split_input_forward(O.f64_to_bf16(x2), [O.shard(w, O.ROWWISE, 3, r) for r in range(3)])
+    part1 = O.bf16_to_f64(x)[:, 4:8] @ O.bf16_to_f64(w)[:, 4:8].T
+    assert np.array_equal(brute - z2, part1)
+
+
 def pin_combine():
     parts = [np.full((3, 2), r, dtype=np.uint16) for r in range(4)]
     g = O.combine_gather(parts)
@@ -462,4 +480,4 @@ def pin_block_tp_invariance():
 
 ALL_PINS = [pin_bf16_rounding, pin_plan_rejections, pin_packed_blocks, pin_shard_golden, pin_shard_reassembly,
             pin_whole_heads, pin_linear_bruteforce, pin_activations, pin_colwise_concat, pin_swiglu_packed,
-            pin_rowwise_sum, pin_combine, pin_attention, pin_attention_p_storage, pin_block_tp_invariance]
+            pin_rowwise_sum, pin_rowwise_split_input, pin_combine, pin_attention, pin_attention_p_storage, pin_block_tp_invariance]

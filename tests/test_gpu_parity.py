@@ -302,6 +302,42 @@ def test_rowwise_workspace_reused_across_calls():
         assert np.array_equal(host_bits(z), exp)
 
 
+# ----------------------------------------------------------------------------- rowwise_split_input
+
+@pytest.mark.parametrize("mode", MODES)
+@pytest.mark.parametrize("shape", [(300, 1600, 520, 4), (2, 3072, 18432, 4), (129, 96, 264, 3)], ids=str)
+def test_rowwise_split_input_integer_bit_exact(shape, mode):
+    # (2, 3072, 18432): an AdaLN-modulation-like projection -- two timestep-embedding rows,
+    # six hidden-size modulation vectors out.
+    T, K, N, p = shape
+    x = tp_inputs.int_bf16(160, 0, (T, K))
+    w = tp_inputs.int_bf16(160, 1, (N, K))
+    ws = [O.shard(w, "rowwise", p, r) for r in range(p)]
+    z = tp.tp_linear_rowwise_split_input(dev(x), [dev(a) for a in ws], mode=mode)
+    if mode == "none":
+        z = tp.tp_combine("reduce", list(z))
+    assert np.array_equal(host_bits(z), O.f64_to_bf16(O.rowwise_split_input_forward(x, ws)))
+
+
+def test_rowwise_split_input_normal_with_bias_and_strided_input():
+    T, K, N, p = 517, 1024, 1040, 4
+    wide = tp_inputs.activation_bf16(161, 0, (T, K + 64))
+    x = np.ascontiguousarray(wide[:, :K])
+    w = tp_inputs.weight_bf16(161, 1, (N, K))
+    b = tp_inputs.weight_bf16(161, 2, (N,))
+    ws = [O.shard(w, "rowwise", p, r) for r in range(p)]
+    xd = dev(wide)[:, :K]       # row stride K + 64: each rank's slice is read in place
+    z = tp.tp_linear_rowwise_split_input(xd, [dev(a) for a in ws], bias=dev(b))
+    assert_close(f64(z), O.rowwise_split_input_forward(x, ws, b), "split input")
+
+
+def test_rowwise_split_input_rejects_indivisible_input():
+    with pytest.raises(tp.TPError) as e:
+        tp.tp_linear_rowwise_split_input(dev(tp_inputs.int_bf16(162, 0, (8, 100))),
+                                         [dev(tp_inputs.int_bf16(162, 1, (16, 33)))] * 3)
+    assert e.value.name == "TP_ERR_SPLIT_NOT_DIVISIBLE"
+
+
 # ----------------------------------------------------------------------------- workloads
 
 def _shard_all(w, style, p, splits=None, h=0, d=0):
