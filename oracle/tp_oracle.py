@@ -445,3 +445,36 @@ def transformer_block_forward(x_bits, wqkv_shards, wout_shards, wgu_shards, wdow
     z1_bits = f64_to_bf16(z1)
     h, z2 = mlp_forward(z1_bits, wgu_shards, wdown_shards, "swiglu")
     return dict(qkv=qkv, o=o, z1=z1, z1_bits=z1_bits, h=h, z=z2)
+
+
+def single_stream_block_forward(x_bits, w_in_shards, w_out_shards, n_local_heads: int, head_dim: int,
+                                q_rows: np.ndarray | None = None, store_p_bf16: bool = True):
+    """Single-stream block: one fused colwise in-projection and one packed rowwise out-projection.
+
+    "Tensor parallelism" page, §Fused projections: [1, 1, 1, 3, 3] packs Q, K,
+    V, gate and up (mlp_ratio 3) into one Linear, sharded block by block
+    (PackedColwiseParallel), and the single-stream to_out stores its input's
+    absolute blocks [inner_dim, mlp_hidden_dim] and is sharded block by block
+    along its input (PackedRowwiseParallel).  Rank r's fused output is
+    [Q_r, K_r, V_r, gate_r, up_r]; attention runs over its local heads, SwiGLU
+    joins gate_r and up_r, and [attention_r, mlp_r] -- exactly the columns of
+    its packed to_out shard -- feeds the rowwise projection; the partials are
+    summed.  Returns (per-rank o bits, per-rank h bits, Z float64).
+    """
+    width = n_local_heads * head_dim
+    rows = x_bits if q_rows is None else x_bits[q_rows]
+    os_, hs, cs = [], [], []
+    for w in w_in_shards:
+        # The rank's five outputs for the token rows asked for, and K, V for every token.
+        y = colwise_forward(rows, [w], "none")[0]
+        kv = y[:, width:3 * width] if q_rows is None else colwise_forward(x_bits, [w[width:3 * width]], "none")[0]
+        qb = f64_to_bf16(y[:, :width])
+        kb, vb = f64_to_bf16(kv[:, :width]), f64_to_bf16(kv[:, width:])
+        o = f64_to_bf16(attention_core(bf16_to_f64(qb), bf16_to_f64(kb), bf16_to_f64(vb), n_local_heads, head_dim,
+                                       store_p_bf16=store_p_bf16))
+        h = f64_to_bf16(apply_act(y[:, 3 * width:], "swiglu"))
+        os_.append(o)
+        hs.append(h)
+        cs.append(np.concatenate([o, h], axis=1))
+    z = rowwise_forward(cs, w_out_shards)
+    return os_, hs, z

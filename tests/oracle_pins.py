@@ -478,6 +478,44 @@ def pin_block_tp_invariance():
                     np.max(np.abs(O.bf16_to_f64(res["qkv"][r]) - O.bf16_to_f64(full[:, cols]))) < 1e-2
 
 
+def pin_single_stream_block():
+    # The fused [1,1,1,3,3] in-projection and the packed [inner, mlp] out-projection:
+    # every tp_degree gives the unsharded block (tp_degree 1), and tp_degree 1 equals an
+    # independent torch float64 computation from the packed weights.
+    T, h, d, ratio = 10, 6, 8, 3
+    H, F = h * d, ratio * h * d
+    w_in, w_out, x = tp_inputs.single_stream_inputs(63, tokens=T, hidden=H, mlp_ratio=ratio)
+    assert O.packed_block_sizes(3 * H + 2 * F, [1, 1, 1, 3, 3]) == [H, H, H, F, F]
+    res = {}
+    for p in (1, 2, 3, 6):
+        win = [O.shard(w_in, O.COLWISE, p, r, [H, H, H, F, F], num_heads=h, head_dim=0) for r in range(p)]
+        wout = [O.shard(w_out, O.ROWWISE, p, r, [H, F]) for r in range(p)]
+        res[p] = O.single_stream_block_forward(x, win, wout, h // p, d, store_p_bf16=False)[2]
+    xt = torch.from_numpy(O.bf16_to_f64(x))
+    y = xt @ torch.from_numpy(O.bf16_to_f64(w_in)).T
+    qkv = torch.from_numpy(O.bf16_to_f64(O.f64_to_bf16(y[:, :3 * H].numpy())))
+    heads = lambda a: a.reshape(T, h, d).permute(1, 0, 2)  # noqa: E731
+    att = torch.nn.functional.scaled_dot_product_attention(heads(qkv[:, :H]), heads(qkv[:, H:2 * H]),
+                                                           heads(qkv[:, 2 * H:]))
+    att = torch.from_numpy(O.bf16_to_f64(O.f64_to_bf16(att.permute(1, 0, 2).reshape(T, H).numpy())))
+    mlp = torch.nn.functional.silu(y[:, 3 * H:3 * H + F]) * y[:, 3 * H + F:]
+    mlp = torch.from_numpy(O.bf16_to_f64(O.f64_to_bf16(mlp.numpy())))
+    z = (torch.cat([att, mlp], dim=1) @ torch.from_numpy(O.bf16_to_f64(w_out)).T).numpy()
+    rms = math.sqrt(float(np.mean(z ** 2)))
+    for p, zp in res.items():
+        assert np.max(np.abs(zp - z)) <= 1e-2 * rms, p
+    # Asking for a subset of token rows (queries) gives those rows of the full result.
+    rows = np.array([1, 4, 9])
+    win = [O.shard(w_in, O.COLWISE, 2, r, [H, H, H, F, F]) for r in range(2)]
+    wout = [O.shard(w_out, O.ROWWISE, 2, r, [H, F]) for r in range(2)]
+    full = O.single_stream_block_forward(x, win, wout, h // 2, d)
+    part = O.single_stream_block_forward(x, win, wout, h // 2, d, q_rows=rows)
+    assert np.array_equal(part[2], full[2][rows])
+    for a, b in zip(part[0] + part[1], full[0] + full[1]):
+        assert np.array_equal(a, b[rows])
+
+
 ALL_PINS = [pin_bf16_rounding, pin_plan_rejections, pin_packed_blocks, pin_shard_golden, pin_shard_reassembly,
             pin_whole_heads, pin_linear_bruteforce, pin_activations, pin_colwise_concat, pin_swiglu_packed,
-            pin_rowwise_sum, pin_rowwise_split_input, pin_combine, pin_attention, pin_attention_p_storage, pin_block_tp_invariance]
+            pin_rowwise_sum, pin_rowwise_split_input, pin_combine, pin_attention, pin_attention_p_storage, pin_block_tp_invariance,
+            pin_single_stream_block]

@@ -104,6 +104,14 @@ def _gather_wrong_axis(parts):
     return np.concatenate(list(parts), axis=0)
 
 
+def _single_stream_concat_swapped(x_bits, w_in_shards, w_out_shards, n_local_heads, head_dim, q_rows=None,
+                                  store_p_bf16=True):
+    # Feeds [mlp, attention] to the packed out-projection instead of [attention, mlp].
+    os_, hs, _ = _orig["single_stream_block_forward"](x_bits, w_in_shards, w_out_shards, n_local_heads, head_dim,
+                                                      q_rows=q_rows, store_p_bf16=store_p_bf16)
+    return os_, hs, O.rowwise_forward([np.concatenate([h, o], axis=1) for o, h in zip(os_, hs)], w_out_shards)
+
+
 MUTATIONS = {
     "shard_ignores_packed_blocks": ("shard", _shard_plain_split),
     "shard_wrong_rank_offset": ("shard", _shard_wrong_rank),
@@ -120,6 +128,7 @@ MUTATIONS = {
     "attention_no_scale": ("attention_core", _attention_no_scale),
     "attention_softmax_wrong_axis": ("attention_core", _attention_wrong_axis),
     "gather_wrong_axis": ("combine_gather", _gather_wrong_axis),
+    "single_stream_concat_swapped": ("single_stream_block_forward", _single_stream_concat_swapped),
 }
 
 

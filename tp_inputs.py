@@ -90,6 +90,10 @@ WORKLOADS = {
     # Full attention + MLP block, tp_degree swept (5 and 7 must be rejected: 48 heads).
     "block_sweep": dict(seed=3, tp_list=(1, 2, 3, 4, 6, 8), tp_rejected=(5, 7), tokens=4608,
                         hidden=6144, ffn=18432, heads=48, head_dim=128, act="swiglu"),
+    # Single-stream block at the block sweep's sizes: one fused in-projection packed
+    # [1,1,1,3,3] (Q, K, V, gate, up at mlp_ratio 3) and a packed rowwise out-projection over
+    # [attention, MLP] inputs ([inner_dim, mlp_hidden_dim] = [6144, 18432]).
+    "single_stream_tp4": dict(seed=5, tp=4, tokens=4608, hidden=6144, heads=48, head_dim=128, mlp_ratio=3),
     # Eight SwiGLU MLP blocks loaded shard-on-read from pinned host memory.
     "stack8_swiglu_tp4": dict(seed=4, tp=4, blocks=8, tokens=4608, hidden=6144, ffn=18432, heads=48,
                               head_dim=128, act="swiglu"),
@@ -153,3 +157,17 @@ def stack_weight(seed: int, block: int, which: str, hidden=6144, ffn=18432) -> n
 
 def stack_input(seed: int, blocks: int, tokens=4608, hidden=6144) -> np.ndarray:
     return activation_bf16(seed, 2 * blocks, (tokens, hidden))
+
+
+def single_stream_inputs(seed=5, tokens=4608, hidden=6144, mlp_ratio=3, kind="normal"):
+    """Tensors of one single-stream block.
+
+    Returns (W_in [3*hidden + 2*ffn, hidden] packed as Q, K, V, gate, up;
+    W_out [hidden, hidden + ffn] whose input packs the attention output then the
+    MLP hidden state; X [tokens, hidden]), with ffn = mlp_ratio * hidden.
+    """
+    ffn = mlp_ratio * hidden
+    shapes = [(3 * hidden + 2 * ffn, hidden), (hidden, hidden + ffn)]
+    if kind == "int":
+        return (*[int_bf16(seed, i, s) for i, s in enumerate(shapes)], int_bf16(seed, 2, (tokens, hidden)))
+    return (*[weight_bf16(seed, i, s) for i, s in enumerate(shapes)], activation_bf16(seed, 2, (tokens, hidden)))
