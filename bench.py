@@ -432,7 +432,7 @@ class BlockWorkload:
                        gu=2.0 * T * H * 2 * F, down=2.0 * T * F * H)
         self.flops = sum(self.fl.values())
         self.extract_bytes = 2.0 * 2 * (4 * H * H + 3 * H * F)
-        self.launches_per_step = 4 + 1 + p * (1 + 3 * ((hl + 15) // 16)) + 3
+        self.launches_per_step = 4 + 1 + p * attention_launches(hl, self.hd) + 3
 
     def config(self):
         return {"workload": "block_sweep", "tokens": self.T, "hidden": self.H, "ffn": self.F, "heads": self.heads,
@@ -484,6 +484,92 @@ class BlockWorkload:
             [O.shard(h["wout"], "rowwise", p, r) for r in range(p)],
             [O.shard(h["wgu"], "colwise", p, r, [F, F]) for r in range(p)],
             [O.shard(h["wdown"], "rowwise", p, r) for r in range(p)],
+            n_local_heads=self.heads // p, head_dim=self.hd, q_rows=rows)["z"]
+
+
+def attention_launches(local_heads, head_dim):
+    """Kernels one tp_attention_heads call launches: V^T plus the fused kernel at head_dim 128,
+    else V^T plus scores / softmax / PV per batch of 16 heads."""
+    return 2 if head_dim == 128 else 1 + 3 * ((local_heads + 15) // 16)
+
+
+class SingleStreamWorkload:
+    """The single-stream block (hidden 6144, 48 heads x 128, mlp_ratio 3, 4608 tokens): one fused
+    [1,1,1,3,3] in-projection (colwise) and the packed [inner, mlp] out-projection (rowwise)."""
+
+    def __init__(self, tp, torch, device, p=None):
+        cfg = tp_inputs.WORKLOADS["single_stream_tp4"]
+        self.tp, self.torch, self.device = tp, torch, device
+        self.p = p = p or cfg["tp"]
+        self.T, self.H, self.heads, self.hd = cfg["tokens"], cfg["hidden"], cfg["heads"], cfg["head_dim"]
+        self.F = F = cfg["mlp_ratio"] * self.H
+        T, H = self.T, self.H
+        self.splits_in, self.splits_out = [H, H, H, F, F], [H, F]
+        tp.tp_validate(3 * H + 2 * F, H, "colwise", p, self.heads, 0, self.splits_in)
+        w_in, w_out, x = tp_inputs.single_stream_inputs(cfg["seed"], T, H, cfg["mlp_ratio"])
+        self.host = dict(w_in=w_in, w_out=w_out, x=x)
+        bf = lambda b: tp.bf16_from_bits(b, device)  # noqa: E731
+        self.w_in, self.w_out, self.x = bf(w_in), bf(w_out), bf(x)
+        e = lambda *sh: torch.empty(sh, dtype=torch.bfloat16, device=device)  # noqa: E731
+        w, f = H // p, F // p
+        self.w, self.f = w, f
+        self.in_sh = [e(3 * w + 2 * f, H) for _ in range(p)]
+        self.out_sh = [e(H, w + f) for _ in range(p)]
+        self.qkv = [e(T, 3 * w) for _ in range(p)]
+        self.cat = [e(T, w + f) for _ in range(p)]      # [attention_r, mlp_r]: rank r's out-projection input
+        self.z = e(T, H)
+        self.attn_ws = torch.empty(tp.tp_attention_workspace_bytes(T, self.heads // p, self.hd),
+                                   dtype=torch.uint8, device=device)
+        self.fl = dict(qkv=2.0 * T * H * 3 * H, gu=2.0 * T * H * 2 * F, attn=4.0 * T * T * H,
+                       out=2.0 * T * (H + F) * H)
+        self.flops = sum(self.fl.values())
+        self.extract_bytes = 2.0 * 2 * ((3 * H + 2 * F) * H + H * (H + F))
+        self.launches_per_step = 2 + 2 + p * attention_launches(self.heads // p, self.hd) + 1
+
+    def config(self):
+        return {"workload": "single_stream_tp4", "tokens": self.T, "hidden": self.H, "mlp_hidden": self.F,
+                "heads": self.heads, "head_dim": self.hd, "tp_degree": self.p, "rowwise_reduce": "accum",
+                "flops": "projections + attention core (4*T^2*head_dim per head)",
+                "step": "2x tp_plan_shard_ranks (packed [1,1,1,3,3] colwise, packed [inner, mlp] rowwise) + "
+                        "colwise Q/K/V rows + colwise SwiGLU gate/up rows into [attention, mlp] + "
+                        "tp_attention_heads per rank into [attention, mlp] + packed rowwise to_out"}
+
+    def phase_extract(self, stream):
+        tp, p = self.tp, self.p
+        tp.tp_plan_shard_ranks(self.w_in, "colwise", p, 0, p, self.splits_in, self.heads, 0, outs=self.in_sh,
+                               stream=stream)
+        tp.tp_plan_shard_ranks(self.w_out, "rowwise", p, 0, p, self.splits_out, self.heads, 0, outs=self.out_sh,
+                               stream=stream)
+
+    def phase_qkv(self, stream):
+        self.tp.tp_linear_colwise(self.x, [s[:3 * self.w] for s in self.in_sh], "none", y_shards=self.qkv,
+                                  stream=stream)
+
+    def phase_gate_up(self, stream):
+        self.tp.tp_linear_colwise(self.x, [s[3 * self.w:] for s in self.in_sh], "swiglu",
+                                  y_shards=[c[:, self.w:] for c in self.cat], ldy=self.w + self.f, stream=stream)
+
+    def phase_attention(self, stream):
+        for y, c in zip(self.qkv, self.cat):
+            self.tp.tp_attention_heads(y, self.heads // self.p, self.hd, out=c[:, :self.w], workspace=self.attn_ws,
+                                       stream=stream)
+
+    def phase_out(self, stream):
+        self.tp.tp_linear_rowwise(self.cat, self.out_sh, mode="accum", out=self.z, stream=stream)
+
+    def phases(self):
+        return [("extract", self.phase_extract, "hbm", self.extract_bytes),
+                ("colwise_qkv", self.phase_qkv, "tensor", self.fl["qkv"]),
+                ("colwise_swiglu", self.phase_gate_up, "tensor", self.fl["gu"]),
+                ("attention", self.phase_attention, "tensor", self.fl["attn"]),
+                ("rowwise_out", self.phase_out, "tensor", self.fl["out"])]
+
+    def oracle_step(self, rows):
+        from oracle import tp_oracle as O
+        p, h = self.p, self.host
+        return O.single_stream_block_forward(
+            h["x"], [O.shard(h["w_in"], "colwise", p, r, self.splits_in) for r in range(p)],
+            [O.shard(h["w_out"], "rowwise", p, r, self.splits_out) for r in range(p)],
             n_local_heads=self.heads // p, head_dim=self.hd, q_rows=rows)["z"]
 
 
@@ -672,6 +758,8 @@ def make_workload(args, tp, torch, device):
         return MlpWorkload(tp, torch, device, args.workload)
     if args.workload == "block_sweep":
         return BlockWorkload(tp, torch, device, args.tp)
+    if args.workload == "single_stream_tp4":
+        return SingleStreamWorkload(tp, torch, device, args.tp)
     raise ValueError(args.workload)
 
 
@@ -903,10 +991,11 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing leg")
     ap.add_argument("--eager", action="store_true", help="launch the timed steps eagerly instead of as graphs")
     ap.add_argument("--workload", default=WORKLOAD,
-                    choices=[WORKLOAD, "tiny_mlp_tp2", "swiglu_mlp_tp4", "block_sweep", "stack8_swiglu_tp4"],
+                    choices=[WORKLOAD, "tiny_mlp_tp2", "swiglu_mlp_tp4", "block_sweep", "single_stream_tp4",
+                             "stack8_swiglu_tp4"],
                     help="the attention projections (default), the tiny or SwiGLU MLP block, the full block "
                          "(with --tp), or the 8-block stack loaded shard-on-read")
-    ap.add_argument("--tp", type=int, default=4, help="tp_degree of --workload block_sweep")
+    ap.add_argument("--tp", type=int, default=4, help="tp_degree of --workload block_sweep / single_stream_tp4")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)   # at least three untimed warm-up steps, whatever was asked
     if args.impl == "reference":

@@ -448,7 +448,8 @@ def transformer_block_forward(x_bits, wqkv_shards, wout_shards, wgu_shards, wdow
 
 
 def single_stream_block_forward(x_bits, w_in_shards, w_out_shards, n_local_heads: int, head_dim: int,
-                                q_rows: np.ndarray | None = None, store_p_bf16: bool = True):
+                                q_rows: np.ndarray | None = None, store_p_bf16: bool = True,
+                                with_abs_v: bool = False):
     """Single-stream block: one fused colwise in-projection and one packed rowwise out-projection.
 
     "Tensor parallelism" page, §Fused projections: [1, 1, 1, 3, 3] packs Q, K,
@@ -459,22 +460,31 @@ def single_stream_block_forward(x_bits, w_in_shards, w_out_shards, n_local_heads
     [Q_r, K_r, V_r, gate_r, up_r]; attention runs over its local heads, SwiGLU
     joins gate_r and up_r, and [attention_r, mlp_r] -- exactly the columns of
     its packed to_out shard -- feeds the rowwise projection; the partials are
-    summed.  Returns (per-rank o bits, per-rank h bits, Z float64).
+    summed.  Returns a dict: per-rank attention output "o" (float64, before its
+    bf16 storage) and "o_bits" (stored), per-rank SwiGLU output "h" and
+    "h_bits" likewise, and the final "z" (float64).  ``with_abs_v`` adds
+    "o_abs_v": the same attention over |V| (exact probabilities), the scale of
+    the error that storing the probabilities in bf16 introduces.
     """
     width = n_local_heads * head_dim
     rows = x_bits if q_rows is None else x_bits[q_rows]
-    os_, hs, cs = [], [], []
+    res = dict(o=[], o_bits=[], h=[], h_bits=[])
+    cs = []
     for w in w_in_shards:
         # The rank's five outputs for the token rows asked for, and K, V for every token.
         y = colwise_forward(rows, [w], "none")[0]
         kv = y[:, width:3 * width] if q_rows is None else colwise_forward(x_bits, [w[width:3 * width]], "none")[0]
         qb = f64_to_bf16(y[:, :width])
         kb, vb = f64_to_bf16(kv[:, :width]), f64_to_bf16(kv[:, width:])
-        o = f64_to_bf16(attention_core(bf16_to_f64(qb), bf16_to_f64(kb), bf16_to_f64(vb), n_local_heads, head_dim,
-                                       store_p_bf16=store_p_bf16))
-        h = f64_to_bf16(apply_act(y[:, 3 * width:], "swiglu"))
-        os_.append(o)
-        hs.append(h)
-        cs.append(np.concatenate([o, h], axis=1))
-    z = rowwise_forward(cs, w_out_shards)
-    return os_, hs, z
+        o = attention_core(bf16_to_f64(qb), bf16_to_f64(kb), bf16_to_f64(vb), n_local_heads, head_dim,
+                           store_p_bf16=store_p_bf16)
+        h = apply_act(y[:, 3 * width:], "swiglu")
+        if with_abs_v:
+            res.setdefault("o_abs_v", []).append(
+                attention_core(bf16_to_f64(qb), bf16_to_f64(kb), np.abs(bf16_to_f64(vb)), n_local_heads, head_dim))
+        ob, hb = f64_to_bf16(o), f64_to_bf16(h)
+        for k, v in (("o", o), ("o_bits", ob), ("h", h), ("h_bits", hb)):
+            res[k].append(v)
+        cs.append(np.concatenate([ob, hb], axis=1))
+    res["z"] = rowwise_forward(cs, w_out_shards)
+    return res

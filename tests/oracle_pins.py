@@ -490,7 +490,7 @@ def pin_single_stream_block():
     for p in (1, 2, 3, 6):
         win = [O.shard(w_in, O.COLWISE, p, r, [H, H, H, F, F], num_heads=h, head_dim=0) for r in range(p)]
         wout = [O.shard(w_out, O.ROWWISE, p, r, [H, F]) for r in range(p)]
-        res[p] = O.single_stream_block_forward(x, win, wout, h // p, d, store_p_bf16=False)[2]
+        res[p] = O.single_stream_block_forward(x, win, wout, h // p, d, store_p_bf16=False)["z"]
     xt = torch.from_numpy(O.bf16_to_f64(x))
     y = xt @ torch.from_numpy(O.bf16_to_f64(w_in)).T
     qkv = torch.from_numpy(O.bf16_to_f64(O.f64_to_bf16(y[:, :3 * H].numpy())))
@@ -510,9 +510,10 @@ def pin_single_stream_block():
     wout = [O.shard(w_out, O.ROWWISE, 2, r, [H, F]) for r in range(2)]
     full = O.single_stream_block_forward(x, win, wout, h // 2, d)
     part = O.single_stream_block_forward(x, win, wout, h // 2, d, q_rows=rows)
-    assert np.array_equal(part[2], full[2][rows])
-    for a, b in zip(part[0] + part[1], full[0] + full[1]):
-        assert np.array_equal(a, b[rows])
+    assert np.array_equal(part["z"], full["z"][rows])
+    for k in ("o", "o_bits", "h", "h_bits"):
+        for a, b in zip(part[k], full[k]):
+            assert np.array_equal(a, b[rows]), k
 
 
 ALL_PINS = [pin_bf16_rounding, pin_plan_rejections, pin_packed_blocks, pin_shard_golden, pin_shard_reassembly,

@@ -107,9 +107,11 @@ def _gather_wrong_axis(parts):
 def _single_stream_concat_swapped(x_bits, w_in_shards, w_out_shards, n_local_heads, head_dim, q_rows=None,
                                   store_p_bf16=True):
     # Feeds [mlp, attention] to the packed out-projection instead of [attention, mlp].
-    os_, hs, _ = _orig["single_stream_block_forward"](x_bits, w_in_shards, w_out_shards, n_local_heads, head_dim,
-                                                      q_rows=q_rows, store_p_bf16=store_p_bf16)
-    return os_, hs, O.rowwise_forward([np.concatenate([h, o], axis=1) for o, h in zip(os_, hs)], w_out_shards)
+    res = _orig["single_stream_block_forward"](x_bits, w_in_shards, w_out_shards, n_local_heads, head_dim,
+                                               q_rows=q_rows, store_p_bf16=store_p_bf16)
+    res["z"] = O.rowwise_forward([np.concatenate([h, o], axis=1) for o, h in zip(res["o_bits"], res["h_bits"])],
+                                 w_out_shards)
+    return res
 
 
 MUTATIONS = {
