@@ -981,6 +981,118 @@ def run_reference(args):
     print(json.dumps(line))
 
 
+def _vm_hwm_bytes():
+    with open("/proc/self/status") as fh:
+        for line in fh:
+            if line.startswith("VmHWM:"):
+                return int(line.split()[1]) * 1024
+    return None
+
+
+def run_st_load(args):
+    """Shard-on-read of single-stream blocks (hidden 6144, mlp_ratio 3, tp 4) from a safetensors file.
+
+    A synthetic checkpoint of 4 blocks (the fused [1,1,1,3,3] in-projection and the packed
+    to_out of each, 3.93 GB of bf16) is written to a temporary directory, read once untimed
+    (the page cache is then warm: this measures the loader, not the disk), then every rank's
+    shard of every tensor is loaded with tp_st_plan_shard_ranks.  Beside it: a plain
+    page-locked host-to-device copy of 1 GiB (the link ceiling) and the peak host memory the
+    loads add (the page's "peak CPU/rank" column).
+    """
+    import shutil
+    import tempfile
+
+    import torch
+    from __graft_entry__ import build
+    build()
+    import tensor_sharded_linear_tp_gb300 as tp
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    cfg = tp_inputs.WORKLOADS["single_stream_tp4"]
+    H, p, heads, seed = cfg["hidden"], cfg["tp"], cfg["heads"], cfg["seed"]
+    F = cfg["mlp_ratio"] * H
+    nb = 4
+    total = nb * ((3 * H + 2 * F) * H + H * (H + F)) * 2
+    tmp = tempfile.mkdtemp(prefix="tp_st_bench_")
+    try:
+        if shutil.disk_usage(tmp).free < total + (2 << 30):
+            print(json.dumps({"metric": "shard-on-read load GB/s from a safetensors file", "value": None,
+                              "unavailable": f"not enough free space in {tmp} for a {total / 1e9:.1f} GB file"}))
+            return
+        path = os.path.join(tmp, "single_stream_blocks.safetensors")
+        tensors = []
+        for b in range(nb):
+            w_in = tp_inputs.weight_bf16(seed, 10 + 2 * b, (3 * H + 2 * F, H))
+            w_out = tp_inputs.weight_bf16(seed, 11 + 2 * b, (H, H + F))
+            tensors += [(f"single_transformer_blocks.{b}.attn.to_qkv_mlp_proj.weight", "BF16", w_in),
+                        (f"single_transformer_blocks.{b}.attn.to_out.weight", "BF16", w_out)]
+        tp_inputs.write_safetensors(path, tensors, metadata={"format": "pt"})
+        del tensors
+        e = lambda *sh: torch.empty(sh, dtype=torch.bfloat16, device=device)  # noqa: E731
+        outs = [([e((3 * H + 2 * F) // p, H) for _ in range(p)], [e(H, (H + F) // p) for _ in range(p)])
+                for _ in range(nb)]
+        stream = torch.cuda.Stream(device)
+        f = tp.SafetensorsFile(path)
+
+        def load():
+            for b, (o_in, o_out) in enumerate(outs):
+                f.shard_ranks(f"single_transformer_blocks.{b}.attn.to_qkv_mlp_proj.weight", "colwise", p,
+                              fused_splits=[H, H, H, F, F], num_heads=heads, outs=o_in, stream=stream)
+                f.shard_ranks(f"single_transformer_blocks.{b}.attn.to_out.weight", "rowwise", p,
+                              fused_splits=[H, F], num_heads=heads, outs=o_out, stream=stream)
+            stream.synchronize()
+
+        with open(path, "rb") as fh:              # warm the page cache
+            while fh.read(64 << 20):
+                pass
+        load()
+        hwm_reset = True
+        try:
+            with open("/proc/self/clear_refs", "w") as fh:
+                fh.write("5")
+        except OSError:
+            hwm_reset = False
+        hwm0 = _vm_hwm_bytes()
+        reps = max(1, min(args.steps, 5))
+        t0 = time.perf_counter()
+        for _ in range(reps):
+            load()
+        load_s = (time.perf_counter() - t0) / reps
+        hwm1 = _vm_hwm_bytes()
+        f.close()
+        tp.tp_device_status(stream)
+
+        probe_n = 1 << 30
+        src = torch.empty(probe_n, dtype=torch.uint8, pin_memory=True)
+        dst = torch.empty(probe_n, dtype=torch.uint8, device=device)
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+        with torch.cuda.stream(stream):
+            dst.copy_(src, non_blocking=True)
+            ev[0].record(stream)
+            for _ in range(3):
+                dst.copy_(src, non_blocking=True)
+            ev[1].record(stream)
+        stream.synchronize()
+        link_gbs = 3 * probe_n / (ev[0].elapsed_time(ev[1]) * 1e-3) / 1e9
+        value = total / load_s / 1e9
+        line = {
+            "metric": "shard-on-read load GB/s from a safetensors file", "value": value, "unit": "GB/s",
+            "n_gpus": 1, "steps": reps, "warmup": 1, "ms_per_step": load_s * 1e3, "higher_is_better": True,
+            "dtype": "bf16", "data": "synthetic (seeded N(0,0.02) weights)",
+            "config": {"workload": "st_load_single_stream", "blocks": nb, "hidden": H, "mlp_hidden": F,
+                       "tp_degree": p, "ranks_loaded": p, "file_bytes": total,
+                       "staging_bytes": 2 * (64 << 20), "page_cache": "warm",
+                       "step": "every rank's shard of every tensor: packed [1,1,1,3,3] colwise in-projection "
+                               "and packed [inner, mlp] rowwise to_out, 4 blocks"},
+            "link_copy_GB/s": link_gbs, "frac_of_link_copy": value / link_gbs,
+            "peak_host_rss_growth_bytes": (hwm1 - hwm0) if (hwm_reset and hwm0 is not None) else None,
+            "gpu_launches": nb * (-(-((H + F) * 2 * H) // (64 << 20))) * reps,
+        }
+        print(json.dumps(line))
+    finally:
+        shutil.rmtree(tmp, ignore_errors=True)
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -992,9 +1104,10 @@ def main(argv=None):
     ap.add_argument("--eager", action="store_true", help="launch the timed steps eagerly instead of as graphs")
     ap.add_argument("--workload", default=WORKLOAD,
                     choices=[WORKLOAD, "tiny_mlp_tp2", "swiglu_mlp_tp4", "block_sweep", "single_stream_tp4",
-                             "stack8_swiglu_tp4"],
+                             "stack8_swiglu_tp4", "st_load_single_stream"],
                     help="the attention projections (default), the tiny or SwiGLU MLP block, the full block "
-                         "(with --tp), or the 8-block stack loaded shard-on-read")
+                         "(with --tp), the single-stream block, the 8-block stack loaded shard-on-read from "
+                         "page-locked memory, or shard-on-read from a safetensors file")
     ap.add_argument("--tp", type=int, default=4, help="tp_degree of --workload block_sweep / single_stream_tp4")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)   # at least three untimed warm-up steps, whatever was asked
@@ -1002,6 +1115,8 @@ def main(argv=None):
         run_reference(args)
     elif args.workload == "stack8_swiglu_tp4":
         run_stack(args)
+    elif args.workload == "st_load_single_stream":
+        run_st_load(args)
     else:
         run_ours(args)
 

@@ -66,7 +66,10 @@ typedef enum {
   TP_ERR_WORKSPACE = 8,           /* workspace missing or smaller than tp_rowwise_workspace_bytes() */
   TP_ERR_CUDA = 9,                /* a CUDA runtime call failed (message in tp_last_error) */
   TP_ERR_TIMEOUT = 10,            /* a kernel gave up waiting on an internal barrier (tp_device_status) */
-  TP_ERR_UNSUPPORTED = 11         /* valid plan outside what this build implements (e.g. tp_degree > 16) */
+  TP_ERR_UNSUPPORTED = 11,        /* valid plan outside what this build implements (e.g. tp_degree > 16) */
+  TP_ERR_IO = 12,                 /* a file could not be opened or read (tp_safetensors.h) */
+  TP_ERR_FORMAT = 13,             /* a file is not a well-formed safetensors file (tp_safetensors.h) */
+  TP_ERR_NOT_FOUND = 14           /* no tensor of that name in the file (tp_safetensors.h) */
 } tp_status;
 
 typedef enum { TP_COLWISE = 0, TP_ROWWISE = 1 } tp_style;

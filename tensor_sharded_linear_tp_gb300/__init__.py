@@ -33,7 +33,8 @@ _status = ctypes.c_int
 TP_OK = 0
 STATUS_NAMES = ["TP_OK", "TP_ERR_INVALID_ARG", "TP_ERR_HEADS_NOT_DIVISIBLE", "TP_ERR_SPLIT_NOT_DIVISIBLE",
                 "TP_ERR_SPLIT_SUM", "TP_ERR_NOT_WHOLE_HEADS", "TP_ERR_ALIGNMENT", "TP_ERR_NOT_PINNED",
-                "TP_ERR_WORKSPACE", "TP_ERR_CUDA", "TP_ERR_TIMEOUT", "TP_ERR_UNSUPPORTED"]
+                "TP_ERR_WORKSPACE", "TP_ERR_CUDA", "TP_ERR_TIMEOUT", "TP_ERR_UNSUPPORTED", "TP_ERR_IO",
+                "TP_ERR_FORMAT", "TP_ERR_NOT_FOUND"]
 STYLES = {"colwise": 0, "rowwise": 1}
 ACTS = {"none": 0, "gelu_tanh": 1, "swiglu": 2}
 REDUCE_MODES = {"none": 0, "workspace": 1, "accum": 2}
@@ -66,6 +67,17 @@ _SIGS = {
     "tp_status_name": (ctypes.c_char_p, [ctypes.c_int]),
     "tp_device_status": (_status, [_vp]),
     "tp_abi_version": (ctypes.c_int, []),
+    # include/tp_safetensors.h
+    "tp_st_dtype_size": (ctypes.c_size_t, [ctypes.c_int]),
+    "tp_st_open": (_status, [ctypes.c_char_p, ctypes.c_size_t, ctypes.POINTER(_vp)]),
+    "tp_st_close": (_status, [_vp]),
+    "tp_st_count": (_i64, [_vp]),
+    "tp_st_info": (_status, [_vp, _i64, ctypes.POINTER(ctypes.c_char_p), ctypes.POINTER(ctypes.c_int),
+                             ctypes.POINTER(ctypes.c_int), ctypes.POINTER(_i64), ctypes.POINTER(ctypes.c_uint64),
+                             ctypes.POINTER(ctypes.c_uint64)]),
+    "tp_st_find": (_i64, [_vp, ctypes.c_char_p]),
+    "tp_st_plan_shard_ranks": (_status, [_vp, ctypes.c_char_p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                         ctypes.POINTER(_i64), ctypes.c_int, _i64, _i64, ctypes.POINTER(_vp), _vp]),
 }
 for _name, (_res, _args) in _SIGS.items():
     _f = getattr(lib, _name)
@@ -371,3 +383,111 @@ def bits_from_bf16(t: torch.Tensor):
     """uint16 numpy bit patterns of a bf16 tensor (copied to the host)."""
     import numpy as np
     return t.detach().contiguous().cpu().view(torch.int16).numpy().view(np.uint16)
+
+
+# ---------------------------------------------------------------------------
+# Shard-on-read from a safetensors file (include/tp_safetensors.h)
+# ---------------------------------------------------------------------------
+
+ST_DTYPES = ["BOOL", "U8", "I8", "F8_E4M3", "F8_E5M2", "I16", "U16", "F16", "BF16", "I32", "U32", "F32", "I64",
+             "U64", "F64"]
+ST_MAX_DIMS = 8
+_ST_TORCH = {"BOOL": "bool", "U8": "uint8", "I8": "int8", "F8_E4M3": "float8_e4m3fn", "F8_E5M2": "float8_e5m2",
+             "I16": "int16", "U16": "uint16", "F16": "float16", "BF16": "bfloat16", "I32": "int32", "U32": "uint32",
+             "F32": "float32", "I64": "int64", "U64": "uint64", "F64": "float64"}
+
+
+def st_torch_dtype(dtype: str) -> torch.dtype:
+    """The torch dtype holding a safetensors dtype's elements."""
+    return getattr(torch, _ST_TORCH[dtype])
+
+
+def tp_st_dtype_size(dtype: str) -> int:
+    return int(lib.tp_st_dtype_size(ST_DTYPES.index(dtype)))
+
+
+def tp_st_open(path: str, staging_bytes: int = 0) -> int:
+    """Open a safetensors file and check its header; returns the handle (close it with tp_st_close)."""
+    h = _vp()
+    _check(lib.tp_st_open(os.fsencode(path), staging_bytes, ctypes.byref(h)))
+    return h.value
+
+
+def tp_st_close(handle: int) -> None:
+    _check(lib.tp_st_close(handle))
+
+
+def tp_st_count(handle: int) -> int:
+    return int(lib.tp_st_count(handle))
+
+
+def tp_st_info(handle: int, index: int) -> dict:
+    name = ctypes.c_char_p()
+    dtype, ndim = ctypes.c_int(), ctypes.c_int()
+    shape = (_i64 * ST_MAX_DIMS)()
+    off, nbytes = ctypes.c_uint64(), ctypes.c_uint64()
+    _check(lib.tp_st_info(handle, index, ctypes.byref(name), ctypes.byref(dtype), ctypes.byref(ndim), shape,
+                          ctypes.byref(off), ctypes.byref(nbytes)))
+    return {"name": name.value.decode("utf-8"), "dtype": ST_DTYPES[dtype.value],
+            "shape": tuple(shape[i] for i in range(ndim.value)), "offset": off.value, "nbytes": nbytes.value}
+
+
+def tp_st_find(handle: int, name: str) -> int:
+    return int(lib.tp_st_find(handle, name.encode("utf-8")))
+
+
+def _st_shard_shape(info: dict, style: str, tp_degree: int) -> tuple:
+    shape = info["shape"]
+    if style == "colwise":
+        if not shape:
+            return ()
+        return (shape[0] // tp_degree, *shape[1:])
+    return (shape[0], shape[1] // tp_degree) if len(shape) == 2 else shape
+
+
+def tp_st_plan_shard_ranks(handle: int, name: str, style: str, tp_degree: int, rank_begin: int = 0,
+                           rank_count: int | None = None, fused_splits: Sequence[int] | None = None,
+                           num_heads: int = 0, head_dim: int = 0, outs: Sequence[torch.Tensor] | None = None,
+                           device=None, stream=None) -> list[torch.Tensor]:
+    """Ranks [rank_begin, rank_begin + rank_count)'s shards of tensor ``name``, read from the file to the GPU."""
+    if rank_count is None:
+        rank_count = tp_degree - rank_begin
+    arr, n = _splits(fused_splits)
+    if outs is None:
+        idx = tp_st_find(handle, name)
+        if idx < 0:
+            raise TPError(STATUS_NAMES.index("TP_ERR_NOT_FOUND"), f"TP_ERR_NOT_FOUND: no tensor {name!r}")
+        info = tp_st_info(handle, idx)
+        # Validate before allocating: a refused plan allocates nothing.
+        _check(lib.tp_st_plan_shard_ranks(handle, name.encode("utf-8"), STYLES[style], tp_degree, rank_begin, 0, arr,
+                                          n, num_heads, head_dim, None, None))
+        dev = device if device is not None else torch.device("cuda")
+        outs = [torch.empty(_st_shard_shape(info, style, tp_degree), dtype=st_torch_dtype(info["dtype"]), device=dev)
+                for _ in range(rank_count)]
+    _check(lib.tp_st_plan_shard_ranks(handle, name.encode("utf-8"), STYLES[style], tp_degree, rank_begin, rank_count,
+                                      arr, n, num_heads, head_dim, _ptrs(outs) if outs else None, _stream(stream)))
+    return list(outs)
+
+
+class SafetensorsFile:
+    """A safetensors file opened for shard-on-read (closes on exit of a ``with`` block)."""
+
+    def __init__(self, path: str, staging_bytes: int = 0):
+        self.handle = tp_st_open(path, staging_bytes)
+
+    def tensors(self) -> list[dict]:
+        return [tp_st_info(self.handle, i) for i in range(tp_st_count(self.handle))]
+
+    def shard_ranks(self, name: str, style: str, tp_degree: int, **kw) -> list[torch.Tensor]:
+        return tp_st_plan_shard_ranks(self.handle, name, style, tp_degree, **kw)
+
+    def close(self) -> None:
+        if self.handle:
+            h, self.handle = self.handle, None
+            tp_st_close(h)
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()

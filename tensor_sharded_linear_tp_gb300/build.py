@@ -21,7 +21,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(HERE, "libtp.so")
-SOURCES = ["tp_host.cu", "tp_copy.cu", "tp_gemm.cu", "tp_attention.cu", "tp_flash.cu"]
+SOURCES = ["tp_host.cu", "tp_copy.cu", "tp_gemm.cu", "tp_attention.cu", "tp_flash.cu", "tp_safetensors.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -159,6 +159,9 @@ const char* tp_status_name(tp_status status) {
     case TP_ERR_WORKSPACE: return "TP_ERR_WORKSPACE";
     case TP_ERR_CUDA: return "TP_ERR_CUDA";
     case TP_ERR_TIMEOUT: return "TP_ERR_TIMEOUT";
+    case TP_ERR_IO: return "TP_ERR_IO";
+    case TP_ERR_FORMAT: return "TP_ERR_FORMAT";
+    case TP_ERR_NOT_FOUND: return "TP_ERR_NOT_FOUND";
     case TP_ERR_UNSUPPORTED: return "TP_ERR_UNSUPPORTED";
   }
   return "TP_ERR_UNKNOWN";
@@ -180,6 +183,6 @@ tp_status tp_device_status(tp_stream_t stream) {
   return TP_OK;
 }
 
-int tp_abi_version(void) { return 100; }
+int tp_abi_version(void) { return 101; }
 
 }  // extern "C"

@@ -516,7 +516,34 @@ def pin_single_stream_block():
             assert np.array_equal(a, b[rows]), k
 
 
+def pin_safetensors_reader():
+    # A file assembled byte by byte from the published layout: header length (little-endian
+    # u64), the JSON header, then data whose offsets count from the first byte after it.
+    import os
+    import struct
+    import tempfile
+    from oracle import st_oracle
+    hdr = (b'{"__metadata__":{"format":"pt"},'
+           b'"w":{"dtype":"BF16","shape":[2,3],"data_offsets":[8,20]},'
+           b'"b":{"dtype":"F32","shape":[2],"data_offsets":[0,8]},'
+           b'"s":{"dtype":"I8","shape":[],"data_offsets":[20,21]}}')
+    data = struct.pack("<2f", 1.5, -2.0) + struct.pack("<6H", 0x3F80, 0xC000, 0x0001, 0x7FC1, 0xFF80, 0x8000) + b"\xfe"
+    blob = struct.pack("<Q", len(hdr)) + hdr + data
+    with tempfile.TemporaryDirectory() as d:
+        path = os.path.join(d, "hand.safetensors")
+        with open(path, "wb") as f:
+            f.write(blob)
+        ts, meta = st_oracle.read_safetensors(path)
+    assert meta == {"format": "pt"}
+    assert sorted(ts) == ["b", "s", "w"]
+    assert ts["w"].dtype == np.uint16 and ts["w"].shape == (2, 3)
+    assert ts["w"].tolist() == [[0x3F80, 0xC000, 0x0001], [0x7FC1, 0xFF80, 0x8000]]
+    assert O.bf16_to_f64(ts["w"][0, :2]).tolist() == [1.0, -2.0]
+    assert ts["b"].tolist() == [1.5, -2.0]
+    assert ts["s"].shape == () and int(ts["s"]) == -2
+
+
 ALL_PINS = [pin_bf16_rounding, pin_plan_rejections, pin_packed_blocks, pin_shard_golden, pin_shard_reassembly,
             pin_whole_heads, pin_linear_bruteforce, pin_activations, pin_colwise_concat, pin_swiglu_packed,
             pin_rowwise_sum, pin_rowwise_split_input, pin_combine, pin_attention, pin_attention_p_storage, pin_block_tp_invariance,
-            pin_single_stream_block]
+            pin_single_stream_block, pin_safetensors_reader]

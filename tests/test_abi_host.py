@@ -1,4 +1,4 @@
-"""The C-ABI library on the host: it loads, exports what include/tp.h declares,
+"""The C-ABI library on the host: it loads, exports what include/*.h declare,
 and its plan validation and argument checks behave as the pages require.
 
 No compute call is made here; every case is rejected (or answered) on the
@@ -16,6 +16,8 @@ from oracle import tp_oracle as O
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 HEADER = os.path.join(ROOT, "include", "tp.h")
+HEADERS = sorted(os.path.join(ROOT, "include", f) for f in os.listdir(os.path.join(ROOT, "include"))
+                 if f.endswith(".h"))
 
 tp = pytest.importorskip("tensor_sharded_linear_tp_gb300",
                          reason="libtp.so not built (python tensor_sharded_linear_tp_gb300/build.py)")
@@ -27,14 +29,15 @@ REASON_TO_STATUS = {"OK": "TP_OK", O.INVALID_ARG: "TP_ERR_INVALID_ARG",
 
 
 def declared_functions():
-    text = open(HEADER).read()
+    text = "".join(open(h).read() for h in HEADERS)
     return sorted(set(re.findall(r"TP_API\s+[\w\s\*]+?\b(tp_\w+)\s*\(", text)))
 
 
 def test_header_declares_the_boundary():
     names = declared_functions()
     for required in ("tp_validate", "tp_shard_shape", "tp_plan_shard", "tp_linear_colwise", "tp_linear_rowwise",
-                     "tp_rowwise_workspace_bytes", "tp_combine", "tp_last_error", "tp_device_status"):
+                     "tp_rowwise_workspace_bytes", "tp_combine", "tp_last_error", "tp_device_status", "tp_st_open",
+                     "tp_st_plan_shard_ranks"):
         assert required in names
 
 

@@ -7,9 +7,11 @@ import numpy as np
 import pytest
 
 import oracle_pins
+from oracle import st_oracle
 from oracle import tp_oracle as O
 
 _orig = {name: getattr(O, name) for name in dir(O) if callable(getattr(O, name))}
+_orig_st = {"read_safetensors": st_oracle.read_safetensors}
 
 
 def _shard_plain_split(w, style, tp_degree, rank, splits=None, **kw):
@@ -114,6 +116,28 @@ def _single_stream_concat_swapped(x_bits, w_in_shards, w_out_shards, n_local_hea
     return res
 
 
+def _read_offsets_from_file_start(path):
+    # Counts data_offsets from the start of the file instead of the end of the header.
+    import json
+    with open(path, "rb") as f:
+        raw = f.read()
+    n = int.from_bytes(raw[:8], "little")
+    header = json.loads(raw[8:8 + n])
+    meta = header.pop("__metadata__", None)
+    out = {}
+    for name, e in header.items():
+        dt = np.dtype(st_oracle.DTYPES[e["dtype"]])
+        b, _ = e["data_offsets"]
+        cnt = int(np.prod(e["shape"], dtype=np.int64)) if e["shape"] else 1
+        out[name] = np.frombuffer(raw, dtype=dt, count=cnt, offset=b).reshape(e["shape"])
+    return out, meta
+
+
+def _read_big_endian(path):
+    ts, meta = _orig_st["read_safetensors"](path)
+    return {k: v.byteswap() for k, v in ts.items()}, meta
+
+
 MUTATIONS = {
     "shard_ignores_packed_blocks": ("shard", _shard_plain_split),
     "shard_wrong_rank_offset": ("shard", _shard_wrong_rank),
@@ -133,6 +157,11 @@ MUTATIONS = {
     "single_stream_concat_swapped": ("single_stream_block_forward", _single_stream_concat_swapped),
 }
 
+ST_MUTATIONS = {
+    "safetensors_offsets_from_file_start": ("read_safetensors", _read_offsets_from_file_start),
+    "safetensors_big_endian": ("read_safetensors", _read_big_endian),
+}
+
 
 @pytest.mark.parametrize("name", sorted(MUTATIONS))
 def test_pins_catch_planted_mistake(name, monkeypatch):
@@ -145,3 +174,11 @@ def test_pins_catch_planted_mistake(name, monkeypatch):
         except Exception as e:  # AssertionError or a shape error: the pin noticed
             caught.append((pin.__name__, type(e).__name__))
     assert caught, f"no pin caught the planted mistake {name}"
+
+
+@pytest.mark.parametrize("name", sorted(ST_MUTATIONS))
+def test_pins_catch_planted_reader_mistake(name, monkeypatch):
+    attr, bad = ST_MUTATIONS[name]
+    monkeypatch.setattr(st_oracle, attr, bad)
+    with pytest.raises(Exception):
+        oracle_pins.pin_safetensors_reader()

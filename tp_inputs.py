@@ -171,3 +171,34 @@ def single_stream_inputs(seed=5, tokens=4608, hidden=6144, mlp_ratio=3, kind="no
     if kind == "int":
         return (*[int_bf16(seed, i, s) for i, s in enumerate(shapes)], int_bf16(seed, 2, (tokens, hidden)))
     return (*[weight_bf16(seed, i, s) for i, s in enumerate(shapes)], activation_bf16(seed, 2, (tokens, hidden)))
+
+
+def write_safetensors(path, tensors, metadata=None, ensure_ascii=True) -> None:
+    """Write ``tensors`` (a list of (name, dtype, array)) as a safetensors file.
+
+    The published layout: an 8-byte little-endian header length N, N bytes of
+    JSON (each tensor's dtype, shape and [begin, end) data offsets counted from
+    the first data byte; an optional "__metadata__" of strings), padded with
+    spaces to a multiple of 8, then the tensors' bytes in list order.  Each
+    array's raw bytes are written as they are (bf16 as its uint16 bit
+    patterns), C order.
+    """
+    import json
+    header = {}
+    if metadata is not None:
+        header["__metadata__"] = dict(metadata)
+    offset = 0
+    blobs = []
+    for name, dtype, arr in tensors:
+        raw = np.ascontiguousarray(arr).tobytes()
+        header[name] = {"dtype": dtype, "shape": [int(d) for d in np.shape(arr)],
+                        "data_offsets": [offset, offset + len(raw)]}
+        blobs.append(raw)
+        offset += len(raw)
+    text = json.dumps(header, ensure_ascii=ensure_ascii, separators=(",", ":")).encode("utf-8")
+    text += b" " * ((-len(text)) % 8)
+    with open(path, "wb") as f:
+        f.write(len(text).to_bytes(8, "little"))
+        f.write(text)
+        for raw in blobs:
+            f.write(raw)
