@@ -216,9 +216,10 @@ def recorded_traffic(kernel: str, kind: str):
 class AttnProjWorkload:
     """Attention projections, tp_degree 4: fused QKV colwise + gather, out-projection rowwise (fused sum)."""
 
-    def __init__(self, tp, torch, device, reduce_mode="accum"):
+    def __init__(self, tp, torch, device, reduce_mode="accum", fused_gather=True):
         cfg = tp_inputs.WORKLOADS[WORKLOAD]
         self.tp, self.torch, self.device = tp, torch, device
+        self.fused_gather = fused_gather
         self.p, self.T, self.H = cfg["tp"], cfg["tokens"], cfg["hidden"]
         self.heads, self.hd = cfg["heads"], cfg["head_dim"]
         self.mode = reduce_mode
@@ -236,6 +237,9 @@ class AttnProjWorkload:
         self.out_sh = [e(H, Kr) for _ in range(p)]
         self.y_sh = [e(T, 3 * H // p) for _ in range(p)]
         self.y = e(T, 3 * H)
+        # The AllGather fused into the colwise store: rank r writes columns [r*3H/p, (r+1)*3H/p)
+        # of the gathered output directly (row stride 3H).
+        self.y_cols = [self.y[:, r * 3 * H // p:(r + 1) * 3 * H // p] for r in range(p)]
         self.z = e(T, H)
         ws = tp.tp_rowwise_workspace_bytes(p, T, H, reduce_mode)
         self.ws = torch.empty(max(ws, 1), dtype=torch.uint8, device=device)
@@ -246,20 +250,27 @@ class AttnProjWorkload:
         self.flops = self.flops_qkv + self.flops_out
         self.extract_bytes = 2.0 * 2 * (3 * H * H + H * H)   # read + write of every shard
         self.gather_bytes = 2.0 * 2 * T * 3 * H
-        # 2 extraction launches (every rank of each weight), colwise, gather, rowwise (+ the counter
-        # clear of the workspace mode, or the separate reduce of the unfused mode).
-        self.launches_per_step = 5 + (1 if reduce_mode in ("workspace", "none") else 0)
+        # 2 extraction launches (every rank of each weight), colwise, gather unless fused, rowwise (+ the
+        # counter clear of the workspace mode, or the separate reduce of the unfused mode).
+        self.launches_per_step = (4 if fused_gather else 5) + (1 if reduce_mode in ("workspace", "none") else 0)
         # Pinned host copies for the end-to-end measurement.
         self.pin = None
 
     def config(self):
         return {"workload": WORKLOAD, "tokens": self.T, "hidden": self.H, "heads": self.heads, "head_dim": self.hd,
                 "tp_degree": self.p, "rowwise_reduce": self.mode,
-                "step": "2x tp_plan_shard_ranks (device, 4 ranks each) + tp_linear_colwise + tp_combine(gather) + "
+                "gather": "fused into the colwise store (ldy)" if self.fused_gather else "tp_combine kernel",
+                "step": "2x tp_plan_shard_ranks (device, 4 ranks each) + tp_linear_colwise writing the gathered "
+                        "QKV [T, 3H] + tp_linear_rowwise" if self.fused_gather else
+                        "2x tp_plan_shard_ranks (device, 4 ranks each) + tp_linear_colwise + tp_combine(gather) + "
                         "tp_linear_rowwise"}
 
     def phases(self):
         """(label, enqueue function, roofline kind, algorithmic work per step: FLOPs or bytes)."""
+        if self.fused_gather:
+            return [("extract", self.phase_extract, "hbm", self.extract_bytes),
+                    ("colwise_qkv", self.phase_colwise, "tensor", self.flops_qkv),
+                    ("rowwise_out", self.phase_rowwise, "tensor", self.flops_out)]
         return [("extract", self.phase_extract, "hbm", self.extract_bytes),
                 ("colwise_qkv", self.phase_colwise, "tensor", self.flops_qkv),
                 ("gather", self.phase_gather, "hbm", self.gather_bytes),
@@ -276,14 +287,31 @@ class AttnProjWorkload:
         tp.tp_plan_shard_ranks(self.w_out, "rowwise", p, 0, p, None, self.heads, self.hd, outs=self.out_sh,
                                stream=stream)
 
-    def phase_colwise(self, stream):
-        self.tp.tp_linear_colwise(self.x, self.qkv_sh, "none", y_shards=self.y_sh, stream=stream)
+    def phase_colwise(self, stream, x=None):
+        x = self.x if x is None else x
+        if self.fused_gather:
+            self.tp.tp_linear_colwise(x, self.qkv_sh, "none", y_shards=self.y_cols, ldy=3 * self.H, stream=stream)
+        else:
+            self.tp.tp_linear_colwise(x, self.qkv_sh, "none", y_shards=self.y_sh, stream=stream)
 
     def phase_gather(self, stream):
         self.tp.tp_combine("gather", self.y_sh, out=self.y, stream=stream)
 
     def phase_rowwise(self, stream):
         self._rowwise(self.a_sh, stream)
+
+    def join_phases(self):
+        """The two joins as separate kernels, timed beside the step: the AllGather of the QKV
+        slices and the AllReduce of fp32 rowwise partials (the unfused forms)."""
+        torch, p, T, H = self.torch, self.p, self.T, self.H
+        if getattr(self, "_join_parts", None) is None:
+            self._join_parts = torch.zeros((p, T, H), dtype=torch.float32, device=self.device)
+            self._join_out = torch.empty((T, H), dtype=torch.bfloat16, device=self.device)
+        parts, out = self._join_parts, self._join_out
+        return [("gather", lambda st: self.tp.tp_combine("gather", self.y_sh, out=self.y, stream=st),
+                 self.gather_bytes),
+                ("reduce", lambda st: self.tp.tp_combine("reduce", list(parts), out=out, stream=st),
+                 4.0 * p * T * H + 2.0 * T * H)]
 
     def _rowwise(self, a_sh, stream):
         tp = self.tp
@@ -305,24 +333,33 @@ class AttnProjWorkload:
             z=torch.empty((self.T, self.H), dtype=torch.bfloat16, pin_memory=True))
         self.x_in = torch.empty_like(self.x)
         self.a_in = [torch.empty_like(t) for t in self.a_sh]
-        # Every rank's slice of both weights (together: both whole weights) plus the activations.
-        self.h2d_bytes = (self.pin["w_qkv"].numel() + self.pin["w_out"].numel()) * 2 \
-            + self.pin["x"].numel() * 2 + sum(t.numel() * 2 for t in self.pin["a_sh"])
+        # The step's inputs are its activations; its result is Z.
+        self.h2d_bytes = self.pin["x"].numel() * 2 + sum(t.numel() * 2 for t in self.pin["a_sh"])
         self.d2h_bytes = self.pin["z"].numel() * 2
+        # Variant: the weights too come from host memory every step (shard-on-read).
+        self.h2d_bytes_weights = (self.pin["w_qkv"].numel() + self.pin["w_out"].numel()) * 2
 
-    def step_e2e(self, stream):
+    def step_e2e(self, stream, weights_from_host=False):
+        """One step through the public calls: activations in from page-locked host memory, Z out.
+
+        The weights stay in device memory (a serving process loads them once) and every rank's
+        shard is extracted from them as in the device-timed step; with weights_from_host, each
+        rank's slice is read from page-locked host memory instead (shard-on-read every step).
+        """
         tp, p, H, torch = self.tp, self.p, self.H, self.torch
         with torch.cuda.stream(stream):
             self.x_in.copy_(self.pin["x"], non_blocking=True)
             for dst, src in zip(self.a_in, self.pin["a_sh"]):
                 dst.copy_(src, non_blocking=True)
-        # Shard-on-read: every rank's slice goes from host memory straight into its device buffer.
-        tp.tp_plan_shard_ranks(self.pin["w_qkv"], "colwise", p, 0, p, [H] * 3, self.heads, self.hd,
-                               outs=self.qkv_sh, stream=stream)
-        tp.tp_plan_shard_ranks(self.pin["w_out"], "rowwise", p, 0, p, None, self.heads, self.hd, outs=self.out_sh,
+        w_qkv = self.pin["w_qkv"] if weights_from_host else self.w_qkv
+        w_out = self.pin["w_out"] if weights_from_host else self.w_out
+        tp.tp_plan_shard_ranks(w_qkv, "colwise", p, 0, p, [H] * 3, self.heads, self.hd, outs=self.qkv_sh,
                                stream=stream)
-        tp.tp_linear_colwise(self.x_in, self.qkv_sh, "none", y_shards=self.y_sh, stream=stream)
-        tp.tp_combine("gather", self.y_sh, out=self.y, stream=stream)
+        tp.tp_plan_shard_ranks(w_out, "rowwise", p, 0, p, None, self.heads, self.hd, outs=self.out_sh,
+                               stream=stream)
+        self.phase_colwise(stream, self.x_in)
+        if not self.fused_gather:
+            tp.tp_combine("gather", self.y_sh, out=self.y, stream=stream)
         self._rowwise(self.a_in, stream)
         with torch.cuda.stream(stream):
             self.pin["z"].copy_(self.z, non_blocking=True)
@@ -753,7 +790,7 @@ def cpu_baseline(host, T, p, H, heads, hd, flops_full, target_s=12.0):
 
 def make_workload(args, tp, torch, device):
     if args.workload == WORKLOAD:
-        return AttnProjWorkload(tp, torch, device, args.reduce_mode)
+        return AttnProjWorkload(tp, torch, device, args.reduce_mode, fused_gather=not args.unfused_gather)
     if args.workload in ("tiny_mlp_tp2", "swiglu_mlp_tp4"):
         return MlpWorkload(tp, torch, device, args.workload)
     if args.workload == "block_sweep":
@@ -896,26 +933,63 @@ def run_ours(args):
                     "frac": achieved / peaks["hbm_gbs"], "kernel": dominant, "peak_source": peaks["source"],
                     "traffic": recorded_traffic(f"{args.workload}:{dominant}", "copy")}
 
-    # End to end through the same public calls with host buffers (the attention projections).
+    # The join kernels on their own (when the step fuses them away), L2 flushed before each.
+    joins = None
+    if hasattr(wl, "join_phases"):
+        joins = {}
+        for label, fn, nbytes in wl.join_phases():
+            fn(stream)
+            ms = []
+            for _ in range(20):
+                s_, e_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                with torch.cuda.stream(stream):
+                    flush.zero_()
+                s_.record(stream)
+                fn(stream)
+                e_.record(stream)
+                e_.synchronize()
+                ms.append(s_.elapsed_time(e_))
+            t = float(np.mean(ms))
+            joins[label] = {"ms": round(t, 5), "GB/s": nbytes / (t * 1e-3) / 1e9,
+                            "frac_hbm": nbytes / (t * 1e-3) / 1e9 / peaks["hbm_gbs"]}
+        tp.tp_device_status(stream)
+
+    # End to end through the same public calls with host buffers (the attention projections):
+    # each step copies its activations in from page-locked host memory and reads Z back, and
+    # is timed alone (no overlap with the next step's copies).
     e2e = None
     if hasattr(wl, "setup_e2e"):
         wl.setup_e2e()
-        for _ in range(max(1, args.warmup)):
-            wl.step_e2e(stream)
-        stream.synchronize()
-        e2e_ms = []
-        for _ in range(min(args.steps, 100)):
-            s_, e_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            s_.record(stream)
-            wl.step_e2e(stream)
-            e_.record(stream)
-            e_.synchronize()
-            e2e_ms.append(s_.elapsed_time(e_))
-        tp.tp_device_status(stream)
-        e2e_slowest = max_over_ranks(dist, float(np.mean(e2e_ms)), device)
-        e2e = {"value": total_flops / (e2e_slowest * 1e-3) / 1e12, "unit": UNIT,
+
+        def time_e2e(**kw):
+            for _ in range(max(1, args.warmup)):
+                wl.step_e2e(stream, **kw)
+            stream.synchronize()
+            ms = []
+            for _ in range(min(args.steps, 100)):
+                s_, e_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                with torch.cuda.stream(stream):
+                    flush.zero_()
+                s_.record(stream)
+                wl.step_e2e(stream, **kw)
+                e_.record(stream)
+                e_.synchronize()
+                ms.append(s_.elapsed_time(e_))
+            tp.tp_device_status(stream)
+            return max_over_ranks(dist, float(np.mean(ms)), device)
+
+        e2e_ms = time_e2e()
+        e2e_w_ms = time_e2e(weights_from_host=True)
+        e2e = {"value": total_flops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
                "h2d_bytes_per_step": int(wl.h2d_bytes), "d2h_bytes_per_step": int(wl.d2h_bytes),
-               "ms_per_step": e2e_slowest}
+               "ms_per_step": e2e_ms,
+               "inputs": "activations X and A_r from page-locked host memory; weights resident in HBM, "
+                         "shards extracted every step",
+               "weights_from_host": {
+                   "value": total_flops / (e2e_w_ms * 1e-3) / 1e12, "ms_per_step": e2e_w_ms,
+                   "h2d_bytes_per_step": int(wl.h2d_bytes + wl.h2d_bytes_weights),
+                   "what": "the same step with every rank's weight slice read from page-locked host "
+                           "memory (shard-on-read) every step"}}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -937,7 +1011,7 @@ def run_ours(args):
             "extract_gbs": kernels["extract"]["GB/s"], "extract_frac_hbm": kernels["extract"]["frac_hbm"],
             "gemm_tflops": sum(wl_work for (lb, _, kd, wl_work) in phases if kd == "tensor") /
             (sum(kernels[k]["ms"] for k in tensor_phases) * 1e-3) / 1e12,
-            "cpu_baseline": cpu, "e2e": e2e,
+            "cpu_baseline": cpu, "e2e": e2e, "join_kernels": joins,
             "gpu_launches": wl.launches_per_step * args.steps, "clocks": clocks,
             "bracket_s": t_wall, "peaks": peaks, "launch": "eager" if args.eager else "cuda_graph_per_phase",
             "eager_ms_per_step": float(eager_phase.sum(axis=1).mean()),
@@ -1102,6 +1176,9 @@ def main(argv=None):
     ap.add_argument("--reduce-mode", choices=["accum", "workspace", "none"], default="accum")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing leg")
     ap.add_argument("--eager", action="store_true", help="launch the timed steps eagerly instead of as graphs")
+    ap.add_argument("--unfused-gather", action="store_true",
+                    help="attention projections: gather the QKV slices with a separate tp_combine kernel instead "
+                         "of writing the gathered layout from the colwise GEMM")
     ap.add_argument("--workload", default=WORKLOAD,
                     choices=[WORKLOAD, "tiny_mlp_tp2", "swiglu_mlp_tp4", "block_sweep", "single_stream_tp4",
                              "stack8_swiglu_tp4", "st_load_single_stream"],
