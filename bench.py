@@ -463,19 +463,19 @@ class BlockWorkload:
         self.z1 = e(T, H)
         self.h_sh = [e(T, F // p) for _ in range(p)]
         self.z = e(T, H)
-        self.attn_ws = torch.empty(tp.tp_attention_workspace_bytes(T, hl, self.hd), dtype=torch.uint8,
+        self.attn_ws = torch.empty(tp.tp_attention_ranks_workspace_bytes(p, T, hl, self.hd), dtype=torch.uint8,
                                    device=device)
         self.fl = dict(qkv=2.0 * T * H * 3 * H, attn=4.0 * T * T * self.hd * self.heads, out=2.0 * T * H * H,
                        gu=2.0 * T * H * 2 * F, down=2.0 * T * F * H)
         self.flops = sum(self.fl.values())
         self.extract_bytes = 2.0 * 2 * (4 * H * H + 3 * H * F)
-        self.launches_per_step = 4 + 1 + p * attention_launches(hl, self.hd) + 3
+        self.launches_per_step = 4 + 1 + attention_launches(p, hl, self.hd) + 3
 
     def config(self):
         return {"workload": "block_sweep", "tokens": self.T, "hidden": self.H, "ffn": self.F, "heads": self.heads,
                 "head_dim": self.hd, "tp_degree": self.p, "rowwise_reduce": "accum",
                 "flops": "projections + attention core (4*T^2*head_dim per head)",
-                "step": "4x tp_plan_shard_ranks + QKV colwise + tp_attention_heads per rank + out rowwise + "
+                "step": "4x tp_plan_shard_ranks + QKV colwise + tp_attention_heads_ranks (every rank) + out rowwise + "
                         "gate/up colwise SwiGLU + down rowwise"}
 
     def phase_extract(self, stream):
@@ -493,8 +493,8 @@ class BlockWorkload:
         self.tp.tp_linear_colwise(self.x, self.qkv_sh, "none", y_shards=self.y_sh, stream=stream)
 
     def phase_attention(self, stream):
-        for y, o in zip(self.y_sh, self.o_sh):
-            self.tp.tp_attention_heads(y, self.heads // self.p, self.hd, out=o, workspace=self.attn_ws, stream=stream)
+        self.tp.tp_attention_heads_ranks(self.y_sh, self.heads // self.p, self.hd, outs=self.o_sh,
+                                         workspace=self.attn_ws, stream=stream)
 
     def phase_out(self, stream):
         self.tp.tp_linear_rowwise(self.o_sh, self.out_sh, mode="accum", out=self.z1, stream=stream)
@@ -524,10 +524,12 @@ class BlockWorkload:
             n_local_heads=self.heads // p, head_dim=self.hd, q_rows=rows)["z"]
 
 
-def attention_launches(local_heads, head_dim):
-    """Kernels one tp_attention_heads call launches: V^T plus the fused kernel at head_dim 128,
-    else V^T plus scores / softmax / PV per batch of 16 heads."""
-    return 2 if head_dim == 128 else 1 + 3 * ((local_heads + 15) // 16)
+def attention_launches(ranks, local_heads, head_dim):
+    """Kernels one tp_attention_heads_ranks call launches: one V^T per rank plus one fused kernel
+    for every rank at head_dim 128, else per rank V^T plus scores / softmax / PV per 16 heads."""
+    if head_dim == 128:
+        return ranks + 1
+    return ranks * (1 + 3 * ((local_heads + 15) // 16))
 
 
 class SingleStreamWorkload:
@@ -555,13 +557,13 @@ class SingleStreamWorkload:
         self.qkv = [e(T, 3 * w) for _ in range(p)]
         self.cat = [e(T, w + f) for _ in range(p)]      # [attention_r, mlp_r]: rank r's out-projection input
         self.z = e(T, H)
-        self.attn_ws = torch.empty(tp.tp_attention_workspace_bytes(T, self.heads // p, self.hd),
+        self.attn_ws = torch.empty(tp.tp_attention_ranks_workspace_bytes(p, T, self.heads // p, self.hd),
                                    dtype=torch.uint8, device=device)
         self.fl = dict(qkv=2.0 * T * H * 3 * H, gu=2.0 * T * H * 2 * F, attn=4.0 * T * T * H,
                        out=2.0 * T * (H + F) * H)
         self.flops = sum(self.fl.values())
         self.extract_bytes = 2.0 * 2 * ((3 * H + 2 * F) * H + H * (H + F))
-        self.launches_per_step = 2 + 2 + p * attention_launches(self.heads // p, self.hd) + 1
+        self.launches_per_step = 2 + 2 + attention_launches(p, self.heads // p, self.hd) + 1
 
     def config(self):
         return {"workload": "single_stream_tp4", "tokens": self.T, "hidden": self.H, "mlp_hidden": self.F,
@@ -569,7 +571,7 @@ class SingleStreamWorkload:
                 "flops": "projections + attention core (4*T^2*head_dim per head)",
                 "step": "2x tp_plan_shard_ranks (packed [1,1,1,3,3] colwise, packed [inner, mlp] rowwise) + "
                         "colwise Q/K/V rows + colwise SwiGLU gate/up rows into [attention, mlp] + "
-                        "tp_attention_heads per rank into [attention, mlp] + packed rowwise to_out"}
+                        "tp_attention_heads_ranks into [attention, mlp] + packed rowwise to_out"}
 
     def phase_extract(self, stream):
         tp, p = self.tp, self.p
@@ -587,9 +589,8 @@ class SingleStreamWorkload:
                                   y_shards=[c[:, self.w:] for c in self.cat], ldy=self.w + self.f, stream=stream)
 
     def phase_attention(self, stream):
-        for y, c in zip(self.qkv, self.cat):
-            self.tp.tp_attention_heads(y, self.heads // self.p, self.hd, out=c[:, :self.w], workspace=self.attn_ws,
-                                       stream=stream)
+        self.tp.tp_attention_heads_ranks(self.qkv, self.heads // self.p, self.hd, outs=[c[:, :self.w] for c in self.cat],
+                                         workspace=self.attn_ws, stream=stream)
 
     def phase_out(self, stream):
         self.tp.tp_linear_rowwise(self.cat, self.out_sh, mode="accum", out=self.z, stream=stream)

@@ -62,6 +62,9 @@ _SIGS = {
     "tp_attention_heads": (_status, [_vp, _i64, _i64, ctypes.c_int, ctypes.c_int, _vp, ctypes.c_size_t, _vp, _i64,
                                      _vp]),
     "tp_attention_workspace_bytes": (ctypes.c_size_t, [_i64, ctypes.c_int, ctypes.c_int]),
+    "tp_attention_heads_ranks": (_status, [ctypes.c_int, ctypes.POINTER(_vp), _i64, _i64, ctypes.c_int, ctypes.c_int,
+                                           _vp, ctypes.c_size_t, ctypes.POINTER(_vp), _i64, _vp]),
+    "tp_attention_ranks_workspace_bytes": (ctypes.c_size_t, [ctypes.c_int, _i64, ctypes.c_int, ctypes.c_int]),
     "tp_combine": (_status, [ctypes.c_int, ctypes.POINTER(_vp), ctypes.c_int, _i64, _i64, _vp, _vp]),
     "tp_last_error": (ctypes.c_char_p, []),
     "tp_status_name": (ctypes.c_char_p, [ctypes.c_int]),
@@ -333,6 +336,34 @@ def tp_attention_heads(qkv: torch.Tensor, n_heads: int, head_dim: int, out: torc
     _check(lib.tp_attention_heads(_ptr(qkv), qkv.stride(0), T, n_heads, head_dim, _ptr(workspace), ws_bytes,
                                   _ptr(out), out.stride(0), _stream(stream)))
     return out
+
+
+def tp_attention_ranks_workspace_bytes(n_ranks: int, T: int, n_heads: int, head_dim: int) -> int:
+    return int(lib.tp_attention_ranks_workspace_bytes(n_ranks, T, n_heads, head_dim))
+
+
+def tp_attention_heads_ranks(qkv: Sequence[torch.Tensor], n_heads: int, head_dim: int,
+                             outs: Sequence[torch.Tensor] | None = None, workspace: torch.Tensor | None = None,
+                             stream=None) -> list[torch.Tensor]:
+    """tp_attention_heads for every rank's QKV output in one call (one launch at head_dim 128)."""
+    n = len(qkv)
+    for t in qkv:
+        _need_bf16_rows("qkv[r]", t)
+    if len({t.stride(0) for t in qkv}) != 1:
+        raise ValueError("every rank's qkv must have the same row stride")
+    T = qkv[0].shape[0]
+    width = n_heads * head_dim
+    if outs is None:
+        outs = [torch.empty((T, width), dtype=torch.bfloat16, device=qkv[0].device) for _ in range(n)]
+    if len({t.stride(0) for t in outs}) != 1:
+        raise ValueError("every rank's output must have the same row stride")
+    need = tp_attention_ranks_workspace_bytes(n, T, n_heads, head_dim)
+    if workspace is None and need:
+        workspace = torch.empty(need, dtype=torch.uint8, device=qkv[0].device)
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(lib.tp_attention_heads_ranks(n, _ptrs(qkv), qkv[0].stride(0), T, n_heads, head_dim, _ptr(workspace),
+                                        ws_bytes, _ptrs(outs), outs[0].stride(0), _stream(stream)))
+    return list(outs)
 
 
 # ---------------------------------------------------------------------------

@@ -1,4 +1,4 @@
-// Attention over one rank's local heads (tp_attention_heads).
+// Attention over the local heads of one rank or several (tp_attention_heads, tp_attention_heads_ranks).
 //
 // diffusers "Tensor parallelism" page, §Colwise and rowwise: the colwise Q, K
 // and V projections give each rank a subset of heads, so attention needs no
@@ -110,56 +110,30 @@ size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 }  // namespace
 }  // namespace tp
 
-extern "C" {
+namespace tp {
+namespace {
 
-size_t tp_attention_workspace_bytes(int64_t T, int n_heads, int head_dim) {
-  if (T <= 0 || n_heads <= 0 || head_dim <= 0) return 0;
-  if (head_dim == 128)  // fused kernel: V^T only
-    return tp::align256(static_cast<size_t>(n_heads) * 128 * static_cast<size_t>(T) * 2);
-  const size_t hb = static_cast<size_t>(n_heads < tp::kHeadBatch ? n_heads : tp::kHeadBatch);
-  return tp::align256(hb * static_cast<size_t>(T) * static_cast<size_t>(T) * 4) +
-         tp::align256(static_cast<size_t>(n_heads) * static_cast<size_t>(head_dim) * static_cast<size_t>(T) * 2);
+size_t fused_vt_bytes(int64_t T, int n_heads) {
+  return align256(static_cast<size_t>(n_heads) * 128 * static_cast<size_t>(T) * 2);
 }
 
-tp_status tp_attention_heads(const void* qkv, int64_t ld_qkv, int64_t T, int n_heads, int head_dim, void* workspace,
-                             size_t ws_bytes, void* out, int64_t ldo, tp_stream_t stream) {
-  using namespace tp;
-  clear_error();
-  if (T < 0 || n_heads < 1 || head_dim < 1) return fail(TP_ERR_INVALID_ARG, "T >= 0, n_heads >= 1, head_dim >= 1");
+// Unfused path for one rank (head sizes other than 128), using the whole workspace.
+tp_status attention_unfused(const void* qkv, int64_t ld_qkv, int64_t T, int n_heads, int head_dim, void* workspace,
+                            void* out, int64_t ldo, float scale_log2e, cudaStream_t s) {
   const int64_t width = static_cast<int64_t>(n_heads) * head_dim;
-  if (ld_qkv == 0) ld_qkv = 3 * width;
-  if (ldo == 0) ldo = width;
-  if (ld_qkv < 3 * width || ldo < width) return fail(TP_ERR_INVALID_ARG, "ld_qkv or ldo smaller than the rows");
-  if (T == 0) return TP_OK;
-  if (qkv == nullptr || out == nullptr) return fail(TP_ERR_INVALID_ARG, "qkv or out is NULL");
-  if ((T % 8) || (head_dim % 8) || (ld_qkv % 8) || (ldo % 8))
-    return fail(TP_ERR_ALIGNMENT, "T, head_dim, ld_qkv and ldo must be multiples of 8");
-  if (T > 0x7FFFFFFF / 2) return fail(TP_ERR_UNSUPPORTED, "T=%lld too large", (long long)T);
-  if (!aligned16(qkv) || !aligned16(out) || (workspace && !aligned16(workspace)))
-    return fail(TP_ERR_ALIGNMENT, "qkv, out or workspace is not 16-byte aligned");
-  const size_t need = tp_attention_workspace_bytes(T, n_heads, head_dim);
-  if (workspace == nullptr || ws_bytes < need)
-    return fail(TP_ERR_WORKSPACE, "workspace of %zu bytes given, %zu needed", workspace ? ws_bytes : 0, need);
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const size_t hb = static_cast<size_t>(n_heads < kHeadBatch ? n_heads : kHeadBatch);
-  const bool fused = (head_dim == 128);
   float* scores = static_cast<float*>(workspace);
-  __nv_bfloat16* vt = fused ? static_cast<__nv_bfloat16*>(workspace)
-                            : reinterpret_cast<__nv_bfloat16*>(static_cast<uint8_t*>(workspace) +
-                                                               align256(hb * static_cast<size_t>(T) * T * 4));
+  __nv_bfloat16* vt = reinterpret_cast<__nv_bfloat16*>(static_cast<uint8_t*>(workspace) +
+                                                       align256(hb * static_cast<size_t>(T) * T * 4));
   const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(qkv);
   const __nv_bfloat16* k = q + width;
   const __nv_bfloat16* v = q + 2 * width;
   __nv_bfloat16* o = static_cast<__nv_bfloat16*>(out);
-
   // V^T once for all heads: [width, T].
   dim3 tgrid(static_cast<unsigned>((T + 31) / 32), static_cast<unsigned>((width + 31) / 32));
   transpose_bf16<<<tgrid, 256, 0, s>>>(v, ld_qkv, vt, T, width);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "transpose launch");
-
-  const float scale_log2e = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(head_dim)));
-  if (fused) return flash_attention_d128(qkv, ld_qkv, T, n_heads, vt, out, ldo, scale_log2e, s);
   for (int h0 = 0; h0 < n_heads; h0 += kHeadBatch) {
     const int nb = (n_heads - h0) < kHeadBatch ? (n_heads - h0) : kHeadBatch;
     const void* a[kHeadBatch];
@@ -189,6 +163,89 @@ tp_status tp_attention_heads(const void* qkv, int64_t ld_qkv, int64_t T, int n_h
     if (st != TP_OK) return st;
   }
   return TP_OK;
+}
+
+tp_status attention_ranks(int n_ranks, const void* const* qkv, int64_t ld_qkv, int64_t T, int n_heads, int head_dim,
+                          void* workspace, size_t ws_bytes, void* const* out, int64_t ldo, cudaStream_t s) {
+  if (n_ranks < 1 || n_ranks > TP_MAX_DEGREE)
+    return fail(n_ranks < 1 ? TP_ERR_INVALID_ARG : TP_ERR_UNSUPPORTED, "n_ranks=%d outside [1, %d]", n_ranks,
+                TP_MAX_DEGREE);
+  if (T < 0 || n_heads < 1 || head_dim < 1) return fail(TP_ERR_INVALID_ARG, "T >= 0, n_heads >= 1, head_dim >= 1");
+  const int64_t width = static_cast<int64_t>(n_heads) * head_dim;
+  if (ld_qkv == 0) ld_qkv = 3 * width;
+  if (ldo == 0) ldo = width;
+  if (ld_qkv < 3 * width || ldo < width) return fail(TP_ERR_INVALID_ARG, "ld_qkv or ldo smaller than the rows");
+  if (T == 0) return TP_OK;
+  if (qkv == nullptr || out == nullptr) return fail(TP_ERR_INVALID_ARG, "qkv or out is NULL");
+  for (int r = 0; r < n_ranks; ++r)
+    if (qkv[r] == nullptr || out[r] == nullptr) return fail(TP_ERR_INVALID_ARG, "qkv[%d] or out[%d] is NULL", r, r);
+  if ((T % 8) || (head_dim % 8) || (ld_qkv % 8) || (ldo % 8))
+    return fail(TP_ERR_ALIGNMENT, "T, head_dim, ld_qkv and ldo must be multiples of 8");
+  if (T > 0x7FFFFFFF / 2) return fail(TP_ERR_UNSUPPORTED, "T=%lld too large", (long long)T);
+  for (int r = 0; r < n_ranks; ++r)
+    if (!aligned16(qkv[r]) || !aligned16(out[r]))
+      return fail(TP_ERR_ALIGNMENT, "qkv[%d] or out[%d] is not 16-byte aligned", r, r);
+  if (workspace && !aligned16(workspace)) return fail(TP_ERR_ALIGNMENT, "workspace is not 16-byte aligned");
+  const size_t need = tp_attention_ranks_workspace_bytes(n_ranks, T, n_heads, head_dim);
+  if (workspace == nullptr || ws_bytes < need)
+    return fail(TP_ERR_WORKSPACE, "workspace of %zu bytes given, %zu needed", workspace ? ws_bytes : 0, need);
+  const float scale_log2e = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(head_dim)));
+  if (head_dim != 128) {
+    // One rank after another through the same workspace (stream order keeps them apart).
+    for (int r = 0; r < n_ranks; ++r) {
+      tp_status st = attention_unfused(qkv[r], ld_qkv, T, n_heads, head_dim, workspace, out[r], ldo, scale_log2e, s);
+      if (st != TP_OK) return st;
+    }
+    return TP_OK;
+  }
+  // Fused: every rank's V^T [width, T] into its own workspace slice, then one launch.
+  const void* vt[TP_MAX_DEGREE];
+  dim3 tgrid(static_cast<unsigned>((T + 31) / 32), static_cast<unsigned>((width + 31) / 32));
+  for (int r = 0; r < n_ranks; ++r) {
+    __nv_bfloat16* slice =
+        reinterpret_cast<__nv_bfloat16*>(static_cast<uint8_t*>(workspace) + r * fused_vt_bytes(T, n_heads));
+    transpose_bf16<<<tgrid, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(qkv[r]) + 2 * width, ld_qkv, slice, T,
+                                         width);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "transpose launch");
+    vt[r] = slice;
+  }
+  return flash_attention_d128(n_ranks, qkv, ld_qkv, T, n_heads, vt, out, ldo, scale_log2e, s);
+}
+
+}  // namespace
+}  // namespace tp
+
+extern "C" {
+
+size_t tp_attention_workspace_bytes(int64_t T, int n_heads, int head_dim) {
+  return tp_attention_ranks_workspace_bytes(1, T, n_heads, head_dim);
+}
+
+size_t tp_attention_ranks_workspace_bytes(int n_ranks, int64_t T, int n_heads, int head_dim) {
+  if (n_ranks <= 0 || T <= 0 || n_heads <= 0 || head_dim <= 0) return 0;
+  if (head_dim == 128)  // fused kernel: every rank's V^T
+    return static_cast<size_t>(n_ranks) * tp::fused_vt_bytes(T, n_heads);
+  const size_t hb = static_cast<size_t>(n_heads < tp::kHeadBatch ? n_heads : tp::kHeadBatch);
+  return tp::align256(hb * static_cast<size_t>(T) * static_cast<size_t>(T) * 4) +
+         tp::align256(static_cast<size_t>(n_heads) * static_cast<size_t>(head_dim) * static_cast<size_t>(T) * 2);
+}
+
+tp_status tp_attention_heads(const void* qkv, int64_t ld_qkv, int64_t T, int n_heads, int head_dim, void* workspace,
+                             size_t ws_bytes, void* out, int64_t ldo, tp_stream_t stream) {
+  tp::clear_error();
+  const void* q[1] = {qkv};
+  void* o[1] = {out};
+  return tp::attention_ranks(1, q, ld_qkv, T, n_heads, head_dim, workspace, ws_bytes, o, ldo,
+                             reinterpret_cast<cudaStream_t>(stream));
+}
+
+tp_status tp_attention_heads_ranks(int n_ranks, const void* const* qkv, int64_t ld_qkv, int64_t T, int n_heads,
+                                   int head_dim, void* workspace, size_t ws_bytes, void* const* out, int64_t ldo,
+                                   tp_stream_t stream) {
+  tp::clear_error();
+  return tp::attention_ranks(n_ranks, qkv, ld_qkv, T, n_heads, head_dim, workspace, ws_bytes, out, ldo,
+                             reinterpret_cast<cudaStream_t>(stream));
 }
 
 }  // extern "C"

@@ -1,29 +1,38 @@
-// Fused attention over a rank's local heads for head_dim 128 (tp_attention_heads).
+// Fused attention over the local heads of one or more ranks, head_dim 128 (tp_attention_heads*).
 //
 // diffusers "Tensor parallelism" page, §Colwise and rowwise: the colwise Q, K
 // and V projections give each rank a subset of heads; each rank attends over
-// its own heads.  This kernel computes, for one 128-query tile of one head,
+// its own heads.  This kernel computes, for 256 queries (two 128-query tiles)
+// of one head of one rank,
 //     O = softmax(Q K^T / sqrt(d)) V
-// without writing scores to memory: scores live in tensor memory, the
-// probabilities in shared memory.
+// without writing scores to memory: scores and probabilities live in tensor
+// memory (TMEM), K and V^T tiles stream through shared memory.
 //
-// CTA (192 threads, one per SM), grid = (query tiles, heads):
-//   warp 0      TMA producer: Q once (128 x 128), then K and V^T tiles of 128
-//               keys through a 2-stage ring (128-byte swizzle).
-//   warp 1      one thread issues tcgen05.mma: S_j = Q K_j^T into one of two
-//               TMEM score buffers (columns [0,128) and [128,256)), and
-//               O += P_j V_j into the TMEM output accumulator (columns [256,384)).
-//               The S MMA of tile j+1 runs while the softmax warps work on j.
-//   warps 2..5  online softmax, one query row per thread: row max of S_j,
-//               P_j = 2^(s*scale*log2e - m) written as bf16 to shared memory
-//               in the MMA's K-major swizzled layout, running sum l.  The
-//               running max m is raised (and O rescaled in TMEM by 2^(m_old -
-//               m_new)) only when a tile's max exceeds it by more than 8 (in
-//               log2 units), so P stays below 2^8; the final O / l uses the
-//               same m, so the result is exact either way.  Then O / l is
-//               rounded to bf16 and written by TMA stores.
+// CTA (320 threads, one per SM), grid = (query-tile pairs, heads, ranks):
+//   warp 0       TMA producer: both Q tiles once, then K and V^T tiles of 128
+//                keys, each through its own 2-stage ring (128-byte swizzle).
+//   warp 1       one thread issues tcgen05.mma.  For tile g (0, 1) and key tile j:
+//                  S_g = Q_g K_j^T        into TMEM columns [128g, 128g+128)
+//                  O_g += P_g V_j         P_g read from TMEM (the first 64 columns
+//                                         of S_g's region, bf16 pairs), O_g in
+//                                         columns [256+128g, 256+128g+128).
+//                Per tile the order is PV_g(j), then S_g(j+1): S_g(j+1) may only
+//                overwrite P_g(j) after PV_g(j) read it, which the tensor core's
+//                in-order execution of one thread's MMAs guarantees.
+//   warps 2..5   softmax of tile 0; warps 6..9 softmax of tile 1 (one query row
+//                per thread).  While one tile's softmax runs, the tensor core
+//                works on the other tile's P.V and next S.  Per key tile: the
+//                row of S into registers, its max; if the max exceeds the
+//                running max m by more than 8 (log2 units), m is raised and O
+//                and l rescale by 2^(m_old - m_new) (the whole warp does the TMEM
+//                read-modify-write when any of its rows needs it); P =
+//                2^(s*scale*log2e - m) rounded to bf16 and stored to TMEM; l +=
+//                sum of the unrounded P.  Finally O / l in bf16, staged in the
+//                tile's (now idle) Q buffer and written by TMA stores.
 // Keys past the end of the sequence are masked (weight 0); queries past it are
-// computed and clipped by the store.  Every wait is bounded (~2 s).
+// computed on zero rows and clipped by the store.  Every wait is bounded (~2 s);
+// a CTA that gives up records it in the library status word, lets its copies
+// and MMAs drain, frees TMEM and exits.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -37,19 +46,23 @@ namespace tp {
 namespace {
 
 constexpr int FD = 128;   // head_dim
-constexpr int FQ = 128;   // queries per CTA
+constexpr int FQ = 128;   // queries per tile; two tiles per CTA
 constexpr int FK = 128;   // keys per tile
-constexpr uint32_t SUB = 16384;             // one 128-row x 64-element bf16 swizzled sub-tile
-constexpr uint32_t OFF_Q = 0;               // Q: 2 sub-tiles (d 0..63, 64..127)
-constexpr uint32_t OFF_KV = 32768;          // stage s: K (2 sub-tiles) then V^T (2 sub-tiles), 64 KB
-constexpr uint32_t OFF_P = 32768 + 2 * 65536;  // P buffer b: 2 sub-tiles (keys 0..63, 64..127), 32 KB each
-constexpr uint32_t SMEM_DATA = OFF_P + 2 * 32768;
+constexpr int KS = 2;     // K ring stages
+constexpr int VS = 2;     // V^T ring stages
+constexpr int kMaxRanks = 16;
+constexpr uint32_t SUB = 16384;                         // 128 rows x 64 bf16, 128-byte swizzled
+constexpr uint32_t OFF_Q = 0;                           // tile g: 2 sub-tiles (d 0..63, 64..127)
+constexpr uint32_t OFF_K = 2 * 2 * SUB;                 // stage s: 2 sub-tiles
+constexpr uint32_t OFF_V = OFF_K + KS * 2 * SUB;        // stage s: 2 sub-tiles (keys 0..63, 64..127)
+constexpr uint32_t SMEM_DATA = OFF_V + VS * 2 * SUB;    // 192 KB
 constexpr uint64_t kFlashWaitLimitNs = 2000000000ull;
+constexpr int kThreads = 320;
 
 struct FlashParams {
-  CUtensorMap map_qk;  // the rank's QKV output [T, 3*H*d], boxes of 64 columns x 128 rows
-  CUtensorMap map_vt;  // V^T [H*d, T], boxes of 64 keys x 128 rows
-  CUtensorMap map_o;   // attention output [T, H*d] (row stride ldo), boxes of 64 columns x 32 rows
+  CUtensorMap map_qk[kMaxRanks];  // rank r's QKV output [T, 3*H*d], boxes of 64 columns x 128 rows
+  CUtensorMap map_vt[kMaxRanks];  // rank r's V^T [H*d, T], boxes of 64 keys x 128 rows
+  CUtensorMap map_o[kMaxRanks];   // rank r's attention output [T, H*d], boxes of 64 columns x 32 rows
   int T;
   int n_heads;
   float scale_log2e;
@@ -58,15 +71,18 @@ struct FlashParams {
 
 struct alignas(8) FlashCtrl {
   uint64_t q_full;
-  uint64_t kv_full[2], kv_empty[2];
-  uint64_t s_full[2], s_free[2];
-  uint64_t p_full[2], p_free[2];
-  uint64_t o_full, drain;
+  uint64_t k_full[KS], k_empty[KS];
+  uint64_t v_full[VS], v_empty[VS];
+  uint64_t s_full[2];   // S_g(j) computed (and every MMA before it, PV_g(j-1) included)
+  uint64_t p_full[2];   // P_g(j) stored in TMEM by the tile's 128 softmax threads
+  uint64_t o_done[2];   // the tile's last P.V completed
+  uint64_t drain;
   uint32_t tmem_base;
   int abort;
 };
 
 constexpr size_t kFlashSmem = 1024 + SMEM_DATA + sizeof(FlashCtrl);
+static_assert(kFlashSmem <= 232448, "flash attention shared memory exceeds the per-CTA limit");
 
 __device__ __forceinline__ bool fwait(uint32_t bar, uint32_t parity, volatile int* abort_flag, unsigned int* status,
                                       bool ignore_abort = false) {
@@ -92,34 +108,45 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
-__global__ void __launch_bounds__(192, 1) tp_flash_kernel(const __grid_constant__ FlashParams p) {
+__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+__global__ void __launch_bounds__(kThreads, 1) tp_flash_kernel(const __grid_constant__ FlashParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   FlashCtrl* ctl = reinterpret_cast<FlashCtrl*>(base + SMEM_DATA);
   volatile int* abort_flag = &ctl->abort;
   const uint32_t sbase = ptx::smem_addr(base);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int qt = blockIdx.x, h = blockIdx.y;
-  const int q0 = qt * FQ;
+  const int h = blockIdx.y, rank = blockIdx.z;
+  const int q0 = blockIdx.x * 2 * FQ;
   const int nkv = (p.T + FK - 1) / FK;
+  const CUtensorMap* map_qk = &p.map_qk[rank];
+  const CUtensorMap* map_vt = &p.map_vt[rank];
 
   if (threadIdx.x == 0) {
     ptx::mbar_init(ptx::smem_addr(&ctl->q_full), 1);
-    for (int i = 0; i < 2; ++i) {
-      ptx::mbar_init(ptx::smem_addr(&ctl->kv_full[i]), 1);
-      ptx::mbar_init(ptx::smem_addr(&ctl->kv_empty[i]), 1);
-      ptx::mbar_init(ptx::smem_addr(&ctl->s_full[i]), 1);
-      ptx::mbar_init(ptx::smem_addr(&ctl->s_free[i]), 128);
-      ptx::mbar_init(ptx::smem_addr(&ctl->p_full[i]), 128);
-      ptx::mbar_init(ptx::smem_addr(&ctl->p_free[i]), 1);
+    for (int i = 0; i < KS; ++i) {
+      ptx::mbar_init(ptx::smem_addr(&ctl->k_full[i]), 1);
+      ptx::mbar_init(ptx::smem_addr(&ctl->k_empty[i]), 1);
     }
-    ptx::mbar_init(ptx::smem_addr(&ctl->o_full), 1);
+    for (int i = 0; i < VS; ++i) {
+      ptx::mbar_init(ptx::smem_addr(&ctl->v_full[i]), 1);
+      ptx::mbar_init(ptx::smem_addr(&ctl->v_empty[i]), 1);
+    }
+    for (int g = 0; g < 2; ++g) {
+      ptx::mbar_init(ptx::smem_addr(&ctl->s_full[g]), 1);
+      ptx::mbar_init(ptx::smem_addr(&ctl->p_full[g]), 128);
+      ptx::mbar_init(ptx::smem_addr(&ctl->o_done[g]), 1);
+    }
     ptx::mbar_init(ptx::smem_addr(&ctl->drain), 1);
     ctl->abort = 0;
     ptx::fence_mbar_init();
     ptx::fence_proxy_async_smem();
   }
-  if (warp == 0) {
+  if (warp == 1) {
     ptx::tmem_alloc(ptx::smem_addr(&ctl->tmem_base), 512);
     ptx::tmem_relinquish();
   }
@@ -131,203 +158,192 @@ __global__ void __launch_bounds__(192, 1) tp_flash_kernel(const __grid_constant_
   if (warp == 0) {
     if (lane == 0) {
       // ---------------------------------------------------------------- producer
+      ptx::prefetch_tensormap(map_qk);
+      ptx::prefetch_tensormap(map_vt);
       const uint32_t qf = ptx::smem_addr(&ctl->q_full);
-      ptx::mbar_arrive_expect_tx(qf, 2 * SUB);
-      ptx::tma_load_2d(sbase + OFF_Q, &p.map_qk, qf, h * FD, q0);
-      ptx::tma_load_2d(sbase + OFF_Q + SUB, &p.map_qk, qf, h * FD + 64, q0);
-      int issued = 0;
+      ptx::mbar_arrive_expect_tx(qf, 4 * SUB);
+      for (int g = 0; g < 2; ++g) {
+        ptx::tma_load_2d(sbase + OFF_Q + g * 2 * SUB, map_qk, qf, h * FD, q0 + g * FQ);
+        ptx::tma_load_2d(sbase + OFF_Q + g * 2 * SUB + SUB, map_qk, qf, h * FD + 64, q0 + g * FQ);
+      }
+      int k_issued = 0, v_issued = 0;
       for (int j = 0; j < nkv; ++j) {
-        const int s = j & 1;
-        const uint32_t ph = (j >> 1) & 1;
-        if (!fwait(ptx::smem_addr(&ctl->kv_empty[s]), ph ^ 1u, abort_flag, p.status)) break;
-        const uint32_t full = ptx::smem_addr(&ctl->kv_full[s]);
-        const uint32_t kv = sbase + OFF_KV + s * 65536;
-        ptx::mbar_arrive_expect_tx(full, 4 * SUB);
+        const int ks = j % KS, vs = j % VS;
+        if (!fwait(ptx::smem_addr(&ctl->k_empty[ks]), ((j / KS) & 1) ^ 1u, abort_flag, p.status)) break;
+        const uint32_t kf = ptx::smem_addr(&ctl->k_full[ks]);
+        const uint32_t kdst = sbase + OFF_K + ks * 2 * SUB;
         const int kx = (p.n_heads + h) * FD;
-        ptx::tma_load_2d(kv, &p.map_qk, full, kx, j * FK);
-        ptx::tma_load_2d(kv + SUB, &p.map_qk, full, kx + 64, j * FK);
-        ptx::tma_load_2d(kv + 2 * SUB, &p.map_vt, full, j * FK, h * FD);
-        ptx::tma_load_2d(kv + 3 * SUB, &p.map_vt, full, j * FK + 64, h * FD);
-        ++issued;
+        ptx::mbar_arrive_expect_tx(kf, 2 * SUB);
+        ptx::tma_load_2d(kdst, map_qk, kf, kx, j * FK);
+        ptx::tma_load_2d(kdst + SUB, map_qk, kf, kx + 64, j * FK);
+        ++k_issued;
+        if (!fwait(ptx::smem_addr(&ctl->v_empty[vs]), ((j / VS) & 1) ^ 1u, abort_flag, p.status)) break;
+        const uint32_t vf = ptx::smem_addr(&ctl->v_full[vs]);
+        const uint32_t vdst = sbase + OFF_V + vs * 2 * SUB;
+        ptx::mbar_arrive_expect_tx(vf, 2 * SUB);
+        ptx::tma_load_2d(vdst, map_vt, vf, j * FK, h * FD);
+        ptx::tma_load_2d(vdst + SUB, map_vt, vf, j * FK + 64, h * FD);
+        ++v_issued;
       }
       // Let every copy land before the CTA can exit.
       fwait(qf, 0, abort_flag, p.status, true);
-      for (int j = (issued > 2 ? issued - 2 : 0); j < issued; ++j)
-        fwait(ptx::smem_addr(&ctl->kv_full[j & 1]), (j >> 1) & 1, abort_flag, p.status, true);
+      for (int j = (k_issued > KS ? k_issued - KS : 0); j < k_issued; ++j)
+        fwait(ptx::smem_addr(&ctl->k_full[j % KS]), (j / KS) & 1, abort_flag, p.status, true);
+      for (int j = (v_issued > VS ? v_issued - VS : 0); j < v_issued; ++j)
+        fwait(ptx::smem_addr(&ctl->v_full[j % VS]), (j / VS) & 1, abort_flag, p.status, true);
     }
   } else if (warp == 1) {
     if (lane == 0) {
       // ---------------------------------------------------------------- MMA issuer
-      constexpr uint32_t idesc = ptx::idesc_bf16_f32(FQ, FK);
-      bool ok = fwait(ptx::smem_addr(&ctl->q_full), 0, abort_flag, p.status);
-      for (int j = 0; ok && j <= nkv; ++j) {
-        if (j < nkv) {
-          const int s = j & 1;
-          const uint32_t ph = (j >> 1) & 1;
-          if (!fwait(ptx::smem_addr(&ctl->kv_full[s]), ph, abort_flag, p.status) ||
-              !fwait(ptx::smem_addr(&ctl->s_free[s]), ph ^ 1u, abort_flag, p.status)) {
-            ok = false;
-            break;
-          }
-          ptx::tc_fence_after();
-          const uint32_t kbase = sbase + OFF_KV + s * 65536;
+      constexpr uint32_t idesc = ptx::idesc_bf16_f32(FQ, FK);   // M 128, N 128 for both products
+      auto issue_s = [&](int g, int j) {
+        const uint32_t kb = sbase + OFF_K + (j % KS) * 2 * SUB;
+        const uint32_t qb = sbase + OFF_Q + g * 2 * SUB;
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            const uint32_t sub = (kk >> 2) * SUB, k4 = 2u * (kk & 3);
-            ptx::umma_bf16(tmem + s * FK, ptx::sw128_kmajor_desc(sbase + OFF_Q + sub) + k4,
-                           ptx::sw128_kmajor_desc(kbase + sub) + k4, idesc, kk > 0 ? 1u : 0u);
-          }
-          ptx::umma_commit(ptx::smem_addr(&ctl->s_full[s]));
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t sub = (kk >> 2) * SUB, k4 = 2u * (kk & 3);
+          ptx::umma_bf16(tmem + g * FK, ptx::sw128_kmajor_desc(qb + sub) + k4, ptx::sw128_kmajor_desc(kb + sub) + k4,
+                         idesc, kk > 0 ? 1u : 0u);
         }
-        if (j >= 1) {
-          const int i = j - 1, b = i & 1;
-          if (!fwait(ptx::smem_addr(&ctl->p_full[b]), (i >> 1) & 1, abort_flag, p.status)) {
-            ok = false;
-            break;
-          }
-          ptx::tc_fence_after();
-          const uint32_t pbase = sbase + OFF_P + b * 32768;
-          const uint32_t vbase = sbase + OFF_KV + b * 65536 + 2 * SUB;
+      };
+      auto issue_pv = [&](int g, int j) {
+        const uint32_t vb = sbase + OFF_V + (j % VS) * 2 * SUB;
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            const uint32_t sub = (kk >> 2) * SUB, k4 = 2u * (kk & 3);
-            ptx::umma_bf16(tmem + 2 * FK, ptx::sw128_kmajor_desc(pbase + sub) + k4,
-                           ptx::sw128_kmajor_desc(vbase + sub) + k4, idesc, (i > 0 || kk > 0) ? 1u : 0u);
-          }
-          ptx::umma_commit(ptx::smem_addr(&ctl->p_free[b]));
-          ptx::umma_commit(ptx::smem_addr(&ctl->kv_empty[b]));
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t sub = (kk >> 2) * SUB, k4 = 2u * (kk & 3);
+          ptx::umma_bf16_ts(tmem + 2 * FK + g * FD, tmem + g * FK + kk * 8, ptx::sw128_kmajor_desc(vb + sub) + k4,
+                            idesc, (j > 0 || kk > 0) ? 1u : 0u);
         }
+      };
+      bool ok = fwait(ptx::smem_addr(&ctl->q_full), 0, abort_flag, p.status) &&
+                fwait(ptx::smem_addr(&ctl->k_full[0]), 0, abort_flag, p.status);
+      if (ok) {
+        ptx::tc_fence_after();
+        for (int g = 0; g < 2; ++g) {
+          issue_s(g, 0);
+          ptx::umma_commit(ptx::smem_addr(&ctl->s_full[g]));
+        }
+        ptx::umma_commit(ptx::smem_addr(&ctl->k_empty[0]));
       }
-      if (ok) ptx::umma_commit(ptx::smem_addr(&ctl->o_full));
+      for (int j = 0; ok && j < nkv; ++j) {
+        if (!fwait(ptx::smem_addr(&ctl->v_full[j % VS]), (j / VS) & 1, abort_flag, p.status)) {
+          ok = false;
+          break;
+        }
+        const bool more = j + 1 < nkv;
+        for (int g = 0; g < 2 && ok; ++g) {
+          if (!fwait(ptx::smem_addr(&ctl->p_full[g]), j & 1, abort_flag, p.status) ||
+              (more && g == 0 &&
+               !fwait(ptx::smem_addr(&ctl->k_full[(j + 1) % KS]), ((j + 1) / KS) & 1, abort_flag, p.status))) {
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after();
+          issue_pv(g, j);
+          if (more) {
+            issue_s(g, j + 1);
+            ptx::umma_commit(ptx::smem_addr(&ctl->s_full[g]));
+          } else {
+            ptx::umma_commit(ptx::smem_addr(&ctl->o_done[g]));
+          }
+        }
+        if (!ok) break;
+        ptx::umma_commit(ptx::smem_addr(&ctl->v_empty[j % VS]));
+        if (more) ptx::umma_commit(ptx::smem_addr(&ctl->k_empty[(j + 1) % KS]));
+      }
       ptx::umma_commit(ptx::smem_addr(&ctl->drain));
       fwait(ptx::smem_addr(&ctl->drain), 0, abort_flag, p.status, true);
     }
   } else {
     // ------------------------------------------------------------------ softmax + epilogue
-    const int q = warp & 3;                 // TMEM lane quarter: query rows [32q, 32q+32)
-    const int row = q * 32 + lane;          // this thread's query row inside the tile
-    const uint32_t trow = tmem + (static_cast<uint32_t>(q * 32) << 16);
+    const int g = (warp - 2) >> 2;            // query tile of this warpgroup
+    const int q = warp & 3;                   // TMEM lane quarter: rows [32q, 32q+32) of the tile
+    const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
+    const uint32_t s_addr = tmem + lane_base + g * FK;        // S_g, then P_g in its first 64 columns
+    const uint32_t o_addr = tmem + lane_base + 2 * FK + g * FD;
     const float k = p.scale_log2e;
     float m = -INFINITY, l = 0.f;
     bool ok = true;
     for (int j = 0; j < nkv && ok; ++j) {
-      const int b = j & 1;
-      const uint32_t ph = (j >> 1) & 1;
       // Every wait's outcome is made warp-uniform: the TMEM loads and stores below are
       // warp-collective and must never run in a partial warp.
-      if (!__all_sync(0xffffffffu, fwait(ptx::smem_addr(&ctl->s_full[b]), ph, abort_flag, p.status))) {
+      if (!__all_sync(0xffffffffu, fwait(ptx::smem_addr(&ctl->s_full[g]), j & 1, abort_flag, p.status))) {
         ok = false;
         break;
       }
       ptx::tc_fence_after();
+      uint32_t sv[FK];
+      ptx::tmem_ld_32x32b_x32(s_addr, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
+      ptx::tmem_ld_32x32b_x32(s_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
+      ptx::tmem_ld_32x32b_x32(s_addr + 64, *reinterpret_cast<uint32_t(*)[32]>(&sv[64]));
+      ptx::tmem_ld_32x32b_x32(s_addr + 96, *reinterpret_cast<uint32_t(*)[32]>(&sv[96]));
+      ptx::tmem_ld_wait();
       const int valid = min(FK, p.T - j * FK);
-      const uint32_t sbuf = trow + b * FK;
-      const bool full = (valid == FK);   // only the last key tile can be partial (warp-uniform)
-      // Pass 1: the tile's row max (scaled, log2 units), four independent chains.
-      float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll 1
-      for (int c = 0; c < FK; c += 32) {
-        uint32_t v[32];
-        ptx::tmem_ld_32x32b_x32(sbuf + c, v);
-        ptx::tmem_ld_wait();
-        if (full) {
+      if (valid < FK) {   // only the last key tile can be partial (warp-uniform)
 #pragma unroll
-          for (int t = 0; t < 32; ++t) mx[t & 3] = fmaxf(mx[t & 3], __uint_as_float(v[t]));
-        } else {
-#pragma unroll
-          for (int t = 0; t < 32; ++t)
-            if (c + t < valid) mx[t & 3] = fmaxf(mx[t & 3], __uint_as_float(v[t]));
-        }
+        for (int t = 0; t < FK; ++t)
+          if (t >= valid) sv[t] = __float_as_uint(-INFINITY);
       }
-      float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * k;
+      float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+      for (int t = 0; t < FK; ++t) mx[t & 3] = fmaxf(mx[t & 3], __uint_as_float(sv[t]));
+      const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * k;
       if (j == 0) {
         m = mt;
       } else {
-        // Raise the running max of the rows whose tile max exceeds it by more than 8:
-        // their O (complete through tile j-1) and l scale by 2^(m - mt).  The decision is
-        // per row but the TMEM read-modify-write is per warp, so the whole warp does it
-        // when any of its rows needs it (alpha = 1 for the others).
+        // O_g is complete through key tile j-1 here: s_full_g(j) arrived after every MMA
+        // issued before S_g(j), PV_g(j-1) included.
         const bool need = mt > m + 8.0f;
         if (__any_sync(0xffffffffu, need)) {
-          if (!__all_sync(0xffffffffu, fwait(ptx::smem_addr(&ctl->p_free[(j - 1) & 1]), ((j - 1) >> 1) & 1,
-                                             abort_flag, p.status))) {
-            ok = false;
-            break;
-          }
-          ptx::tc_fence_after();
           const float alpha = need ? ex2(m - mt) : 1.0f;
           l *= alpha;
           if (need) m = mt;
 #pragma unroll 1
           for (int c = 0; c < FD; c += 32) {
             uint32_t v[32];
-            ptx::tmem_ld_32x32b_x32(trow + 2 * FK + c, v);
+            ptx::tmem_ld_32x32b_x32(o_addr + c, v);
             ptx::tmem_ld_wait();
 #pragma unroll
             for (int t = 0; t < 32; ++t) v[t] = __float_as_uint(__uint_as_float(v[t]) * alpha);
-            ptx::tmem_st_32x32b_x32(trow + 2 * FK + c, v);
+            ptx::tmem_st_32x32b_x32(o_addr + c, v);
           }
-          ptx::tmem_st_wait();
         }
       }
-      // P buffer b is free once the P.V MMA of tile j-2 has completed.
-      if (!__all_sync(0xffffffffu, fwait(ptx::smem_addr(&ctl->p_free[b]), ph ^ 1u, abort_flag, p.status))) {
-        ok = false;
-        break;
-      }
-      // Pass 2: P = 2^(s*k - m) as bf16 into the swizzled K-major P tile; l += sum(P)
-      // (the sum of the unrounded values, four independent chains).
-      const uint32_t pbase = sbase + OFF_P + b * 32768;
+      // P = 2^(s*k - m) as bf16 pairs into the first 64 columns of S_g's region; l += sum(P)
+      // (the unrounded values, four independent chains).  Masked keys give 2^-inf = 0.
       const float negm = -m;
       float ls[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 1
-      for (int c = 0; c < FK; c += 32) {
-        uint32_t v[32];
-        ptx::tmem_ld_32x32b_x32(sbuf + c, v);
-        ptx::tmem_ld_wait();
-        uint32_t pk[16];
 #pragma unroll
-        for (int t = 0; t < 16; ++t) {
-          float p0 = ex2(fmaf(__uint_as_float(v[2 * t]), k, negm));
-          float p1 = ex2(fmaf(__uint_as_float(v[2 * t + 1]), k, negm));
-          if (!full) {
-            p0 = (c + 2 * t < valid) ? p0 : 0.f;
-            p1 = (c + 2 * t + 1 < valid) ? p1 : 0.f;
-          }
+      for (int half = 0; half < 2; ++half) {
+        uint32_t pk[32];
+#pragma unroll
+        for (int t = 0; t < 32; ++t) {
+          const float p0 = ex2(fmaf(__uint_as_float(sv[64 * half + 2 * t]), k, negm));
+          const float p1 = ex2(fmaf(__uint_as_float(sv[64 * half + 2 * t + 1]), k, negm));
           ls[t & 3] += p0 + p1;
-          __nv_bfloat162 hp = __floats2bfloat162_rn(p0, p1);
-          pk[t] = *reinterpret_cast<uint32_t*>(&hp);
+          pk[t] = pack_bf16(p0, p1);
         }
-        const uint32_t sub = pbase + (c >> 6) * SUB + static_cast<uint32_t>(row) * 128;
-        const int chunk0 = (c & 63) >> 3;  // 16-byte piece index of column c within the 64-key row
-#pragma unroll
-        for (int t = 0; t < 4; ++t)
-          ptx::st_shared_v4(sub + (static_cast<uint32_t>((chunk0 + t) ^ (row & 7)) << 4), pk[4 * t], pk[4 * t + 1],
-                            pk[4 * t + 2], pk[4 * t + 3]);
+        ptx::tmem_st_32x32b_x32(s_addr + 32 * half, pk);
       }
+      ptx::tmem_st_wait();
       l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
       ptx::tc_fence_before();
-      ptx::mbar_arrive(ptx::smem_addr(&ctl->s_free[b]));
-      ptx::fence_proxy_async_smem();  // P (generic-proxy writes) becomes visible to the MMA
-      ptx::mbar_arrive(ptx::smem_addr(&ctl->p_full[b]));
+      ptx::mbar_arrive(ptx::smem_addr(&ctl->p_full[g]));
     }
-    if (ok && __all_sync(0xffffffffu, fwait(ptx::smem_addr(&ctl->o_full), 0, abort_flag, p.status))) {
+    if (ok && __all_sync(0xffffffffu, fwait(ptx::smem_addr(&ctl->o_done[g]), 0, abort_flag, p.status))) {
       ptx::tc_fence_after();
-      // Epilogue: O / l in bf16, staged in the (now idle) Q buffer, written by TMA stores.
+      // Epilogue: O / l in bf16, staged in the tile's Q buffer (idle: every S MMA of this tile
+      // completed before o_done), written by TMA stores of 32 rows x 64 columns.
       const float inv = 1.0f / l;
-      const uint32_t stage = sbase + OFF_Q + static_cast<uint32_t>(q) * 8192;
+      const uint32_t stage = sbase + OFF_Q + g * 2 * SUB + static_cast<uint32_t>(q) * 8192;
 #pragma unroll 1
       for (int c = 0; c < FD; c += 32) {
         uint32_t v[32];
-        ptx::tmem_ld_32x32b_x32(trow + 2 * FK + c, v);
+        ptx::tmem_ld_32x32b_x32(o_addr + c, v);
         ptx::tmem_ld_wait();
         uint32_t pk[16];
 #pragma unroll
-        for (int t = 0; t < 16; ++t) {
-          __nv_bfloat162 ho =
-              __floats2bfloat162_rn(__uint_as_float(v[2 * t]) * inv, __uint_as_float(v[2 * t + 1]) * inv);
-          pk[t] = *reinterpret_cast<uint32_t*>(&ho);
-        }
+        for (int t = 0; t < 16; ++t) pk[t] = pack_bf16(__uint_as_float(v[2 * t]) * inv, __uint_as_float(v[2 * t + 1]) * inv);
         const uint32_t dst = stage + (c >> 6) * 4096 + static_cast<uint32_t>(lane) * 128;
         const int chunk0 = (c & 63) >> 3;
 #pragma unroll
@@ -337,9 +353,10 @@ __global__ void __launch_bounds__(192, 1) tp_flash_kernel(const __grid_constant_
       }
       ptx::fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) {
-        ptx::tma_store_2d(&p.map_o, stage, h * FD, q0 + q * 32);
-        ptx::tma_store_2d(&p.map_o, stage + 4096, h * FD + 64, q0 + q * 32);
+      const int row0 = q0 + g * FQ + q * 32;
+      if (lane == 0 && row0 < p.T) {
+        ptx::tma_store_2d(&p.map_o[rank], stage, h * FD, row0);
+        ptx::tma_store_2d(&p.map_o[rank], stage + 4096, h * FD + 64, row0);
         ptx::bulk_commit();
         ptx::bulk_wait_all();
       }
@@ -350,7 +367,7 @@ __global__ void __launch_bounds__(192, 1) tp_flash_kernel(const __grid_constant_
   __syncwarp();
   ptx::tc_fence_before();
   __syncthreads();
-  if (warp == 0) {
+  if (warp == 1) {
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem, 512);
   }
@@ -358,17 +375,23 @@ __global__ void __launch_bounds__(192, 1) tp_flash_kernel(const __grid_constant_
 
 }  // namespace
 
-// Fused attention for head_dim 128 (see the file comment).  vt: V^T [n_heads*128, T].
-tp_status flash_attention_d128(const void* qkv, int64_t ld_qkv, int64_t T, int n_heads, const void* vt, void* out,
-                               int64_t ldo, float scale_log2e, cudaStream_t stream) {
+// Fused attention for head_dim 128 over n_ranks ranks in one launch (see the file comment).
+// vt[r]: rank r's V^T [n_heads*128, T].
+tp_status flash_attention_d128(int n_ranks, const void* const* qkv, int64_t ld_qkv, int64_t T, int n_heads,
+                               const void* const* vt, void* const* out, int64_t ldo, float scale_log2e,
+                               cudaStream_t stream) {
+  if (n_ranks < 1 || n_ranks > kMaxRanks)
+    return fail(TP_ERR_UNSUPPORTED, "fused attention over %d ranks in one launch (at most %d)", n_ranks, kMaxRanks);
   unsigned int* status = status_word();
   if (status == nullptr) return fail(TP_ERR_CUDA, "cannot locate the kernel status word");
   FlashParams prm{};
   const int64_t width = static_cast<int64_t>(n_heads) * FD;
-  tp_status st = encode_bf16_2d(&prm.map_qk, qkv, 3 * width, T, ld_qkv, 64, 128, true);
-  if (st == TP_OK) st = encode_bf16_2d(&prm.map_vt, vt, T, width, T, 64, 128, true);
-  if (st == TP_OK) st = encode_bf16_2d(&prm.map_o, out, width, T, ldo, 64, 32, true);
-  if (st != TP_OK) return st;
+  for (int r = 0; r < n_ranks; ++r) {
+    tp_status st = encode_bf16_2d(&prm.map_qk[r], qkv[r], 3 * width, T, ld_qkv, 64, 128, true);
+    if (st == TP_OK) st = encode_bf16_2d(&prm.map_vt[r], vt[r], T, width, T, 64, 128, true);
+    if (st == TP_OK) st = encode_bf16_2d(&prm.map_o[r], out[r], width, T, ldo, 64, 32, true);
+    if (st != TP_OK) return st;
+  }
   prm.T = static_cast<int>(T);
   prm.n_heads = n_heads;
   prm.scale_log2e = scale_log2e;
@@ -382,8 +405,9 @@ tp_status flash_attention_d128(const void* qkv, int64_t ld_qkv, int64_t T, int n
                                static_cast<int>(kFlashSmem));
   });
   if (err != cudaSuccess) return cuda_fail(err, "cudaFuncSetAttribute(flash attention)");
-  dim3 grid(static_cast<unsigned>((T + FQ - 1) / FQ), static_cast<unsigned>(n_heads));
-  tp_flash_kernel<<<grid, 192, kFlashSmem, stream>>>(prm);
+  dim3 grid(static_cast<unsigned>((T + 2 * FQ - 1) / (2 * FQ)), static_cast<unsigned>(n_heads),
+            static_cast<unsigned>(n_ranks));
+  tp_flash_kernel<<<grid, kThreads, kFlashSmem, stream>>>(prm);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "flash attention launch");
   return TP_OK;

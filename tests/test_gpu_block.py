@@ -40,7 +40,8 @@ def _device_status_clean():
 
 # ----------------------------------------------------------------------------- attention core
 
-@pytest.mark.parametrize("T,heads,d", [(304, 3, 64), (520, 5, 128), (256, 18, 32), (8, 1, 8)])
+@pytest.mark.parametrize("T,heads,d", [(304, 3, 64), (520, 5, 128), (256, 18, 32), (8, 1, 8), (8, 2, 128),
+                                       (136, 3, 128), (1160, 1, 128)])
 def test_attention_heads_within_tolerance(T, heads, d):
     qkv = tp_inputs.activation_bf16(150, heads * 1000 + T, (T, 3 * heads * d))
     out = tp.tp_attention_heads(dev(qkv), heads, d)
@@ -48,6 +49,33 @@ def test_attention_heads_within_tolerance(T, heads, d):
     H = heads * d
     ref = O.attention_core(qf[:, :H], qf[:, H:2 * H], qf[:, 2 * H:], heads, d)
     assert_close(f64(out), ref, f"attention T={T} heads={heads} d={d}")
+
+
+@pytest.mark.parametrize("T,heads,d,n", [(520, 2, 128, 3), (136, 4, 128, 2), (200, 2, 64, 3)])
+def test_attention_of_several_ranks_in_one_call(T, heads, d, n):
+    # Every rank's heads in one call (one launch at head_dim 128): each rank's output equals
+    # the single-rank call bit for bit and the oracle within tolerance.
+    H = heads * d
+    qkvs = [tp_inputs.activation_bf16(160 + r, T, (T, 3 * H)) for r in range(n)]
+    outs = tp.tp_attention_heads_ranks([dev(q) for q in qkvs], heads, d)
+    for r, qkv in enumerate(qkvs):
+        single = tp.tp_attention_heads(dev(qkv), heads, d)
+        assert torch.equal(outs[r].view(torch.int16), single.view(torch.int16)), r
+        qf = O.bf16_to_f64(qkv)
+        ref = O.attention_core(qf[:, :H], qf[:, H:2 * H], qf[:, 2 * H:], heads, d)
+        assert_close(f64(outs[r]), ref, f"rank {r} of {n}, T={T}")
+
+
+def test_attention_ranks_workspace_and_limits():
+    assert tp.tp_attention_ranks_workspace_bytes(4, 4608, 12, 128) == 4 * tp.tp_attention_workspace_bytes(4608, 12, 128)
+    assert tp.tp_attention_ranks_workspace_bytes(4, 300, 2, 64) == tp.tp_attention_workspace_bytes(300, 2, 64)
+    q = torch.zeros((16, 3 * 128), dtype=torch.bfloat16, device=DEV)
+    with pytest.raises(tp.TPError) as e:
+        tp.tp_attention_heads_ranks([q] * 17, 1, 128)
+    assert e.value.name == "TP_ERR_UNSUPPORTED"
+    with pytest.raises(tp.TPError) as e:
+        tp.tp_attention_heads_ranks([q, q], 1, 128, workspace=torch.empty(16, dtype=torch.uint8, device=DEV))
+    assert e.value.name == "TP_ERR_WORKSPACE"
 
 
 def test_attention_one_dominant_key_returns_its_value():
@@ -111,7 +139,7 @@ def gpu_block(x_bits, wqkv, wout, wgu, wdown, p, heads, d, F, mode="accum"):
     dn_sh = tp.tp_plan_shard_ranks(dev(wdown), "rowwise", p, 0, p, None, heads, 0, device=DEV)
     ys = tp.tp_linear_colwise(x, qkv_sh, "none")
     hl = heads // p
-    os_ = [tp.tp_attention_heads(y, hl, d) for y in ys]
+    os_ = tp.tp_attention_heads_ranks(ys, hl, d)
     z1 = tp.tp_linear_rowwise(os_, out_sh, mode=mode)
     if mode == "none":
         z1 = tp.tp_combine("reduce", list(z1))

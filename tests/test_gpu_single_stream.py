@@ -50,8 +50,7 @@ def gpu_single_stream(x_bits, w_in, w_out, p, heads, d, F, mode="accum"):
     cat = [torch.full((T, w + f), float("nan"), dtype=torch.bfloat16, device=DEV) for _ in range(p)]
     qkv = tp.tp_linear_colwise(x, [s[:3 * w] for s in in_sh], "none")
     tp.tp_linear_colwise(x, [s[3 * w:] for s in in_sh], "swiglu", y_shards=[c[:, w:] for c in cat], ldy=w + f)
-    for y, c in zip(qkv, cat):
-        tp.tp_attention_heads(y, heads // p, d, out=c[:, :w])
+    tp.tp_attention_heads_ranks(qkv, heads // p, d, outs=[c[:, :w] for c in cat])
     z = tp.tp_linear_rowwise(cat, out_sh, mode=mode)
     if mode == "none":
         z = tp.tp_combine("reduce", list(z))
