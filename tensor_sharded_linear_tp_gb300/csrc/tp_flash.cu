@@ -288,26 +288,24 @@ __global__ void __launch_bounds__(kThreads, 1) tp_flash_kernel(const __grid_cons
 #pragma unroll
       for (int t = 0; t < FK; ++t) mx[t & 3] = fmaxf(mx[t & 3], __uint_as_float(sv[t]));
       const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * k;
+      // Raise the running max of the rows whose tile max exceeds it by more than 8: their
+      // l and O (complete through key tile j-1: s_full_g(j) arrived after every MMA issued
+      // before S_g(j), PV_g(j-1) included) scale by alpha = 2^(m_old - m_new).  The O
+      // rescale is per warp (TMEM access is warp-collective): the whole warp does it when
+      // any of its rows needs it, with alpha = 1 for the others.  It runs after P is stored,
+      // when the S registers are free.
+      bool rescale = false;
+      float alpha = 1.0f;
       if (j == 0) {
         m = mt;
       } else {
-        // O_g is complete through key tile j-1 here: s_full_g(j) arrived after every MMA
-        // issued before S_g(j), PV_g(j-1) included.
         const bool need = mt > m + 8.0f;
-        if (__any_sync(0xffffffffu, need)) {
-          const float alpha = need ? ex2(m - mt) : 1.0f;
-          l *= alpha;
-          if (need) m = mt;
-#pragma unroll 1
-          for (int c = 0; c < FD; c += 32) {
-            uint32_t v[32];
-            ptx::tmem_ld_32x32b_x32(o_addr + c, v);
-            ptx::tmem_ld_wait();
-#pragma unroll
-            for (int t = 0; t < 32; ++t) v[t] = __float_as_uint(__uint_as_float(v[t]) * alpha);
-            ptx::tmem_st_32x32b_x32(o_addr + c, v);
-          }
+        rescale = __any_sync(0xffffffffu, need);
+        if (need) {
+          alpha = ex2(m - mt);
+          m = mt;
         }
+        l *= alpha;
       }
       // P = 2^(s*k - m) as bf16 pairs into the first 64 columns of S_g's region; l += sum(P)
       // (the unrounded values, four independent chains).  Masked keys give 2^-inf = 0.
@@ -315,7 +313,9 @@ __global__ void __launch_bounds__(kThreads, 1) tp_flash_kernel(const __grid_cons
       float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
-        uint32_t pk[32];
+        // Packed in place: the pair for column t comes from entries 2t, 2t+1 (>= t), so
+        // entry t of this half is already consumed when it is overwritten.
+        uint32_t* pk = &sv[64 * half];
 #pragma unroll
         for (int t = 0; t < 32; ++t) {
           const float p0 = ex2(fmaf(__uint_as_float(sv[64 * half + 2 * t]), k, negm));
@@ -323,7 +323,18 @@ __global__ void __launch_bounds__(kThreads, 1) tp_flash_kernel(const __grid_cons
           ls[t & 3] += p0 + p1;
           pk[t] = pack_bf16(p0, p1);
         }
-        ptx::tmem_st_32x32b_x32(s_addr + 32 * half, pk);
+        ptx::tmem_st_32x32b_x32(s_addr + 32 * half, *reinterpret_cast<uint32_t(*)[32]>(pk));
+      }
+      if (rescale) {
+#pragma unroll 1
+        for (int c = 0; c < FD; c += 32) {
+          uint32_t v[32];
+          ptx::tmem_ld_32x32b_x32(o_addr + c, v);
+          ptx::tmem_ld_wait();
+#pragma unroll
+          for (int t = 0; t < 32; ++t) v[t] = __float_as_uint(__uint_as_float(v[t]) * alpha);
+          ptx::tmem_st_32x32b_x32(o_addr + c, v);
+        }
       }
       ptx::tmem_st_wait();
       l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
