@@ -108,6 +108,33 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
+// Packed pairs of fp32 values for the sm_100 two-wide FMA/ADD instructions (half the
+// instruction count of the scalar forms; the softmax is bound by instruction issue).
+__device__ __forceinline__ uint64_t f2(float a, float b) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ void f2_split(uint64_t v, float& a, float& b) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+// Three-input maximum (one instruction on sm_100 and later).
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
   return *reinterpret_cast<uint32_t*>(&h);
@@ -286,7 +313,8 @@ __global__ void __launch_bounds__(kThreads, 1) tp_flash_kernel(const __grid_cons
       }
       float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-      for (int t = 0; t < FK; ++t) mx[t & 3] = fmaxf(mx[t & 3], __uint_as_float(sv[t]));
+      for (int t = 0; t < FK; t += 2)
+        mx[(t >> 1) & 3] = max3(mx[(t >> 1) & 3], __uint_as_float(sv[t]), __uint_as_float(sv[t + 1]));
       const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * k;
       // Raise the running max of the rows whose tile max exceeds it by more than 8: their
       // l and O (complete through key tile j-1: s_full_g(j) arrived after every MMA issued
@@ -309,8 +337,8 @@ __global__ void __launch_bounds__(kThreads, 1) tp_flash_kernel(const __grid_cons
       }
       // P = 2^(s*k - m) as bf16 pairs into the first 64 columns of S_g's region; l += sum(P)
       // (the unrounded values, four independent chains).  Masked keys give 2^-inf = 0.
-      const float negm = -m;
-      float ls[4] = {0.f, 0.f, 0.f, 0.f};
+      const uint64_t k2 = f2(k, k), nm2 = f2(-m, -m);
+      uint64_t ls[4] = {f2(0.f, 0.f), f2(0.f, 0.f), f2(0.f, 0.f), f2(0.f, 0.f)};
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
         // Packed in place: the pair for column t comes from entries 2t, 2t+1 (>= t), so
@@ -318,9 +346,12 @@ __global__ void __launch_bounds__(kThreads, 1) tp_flash_kernel(const __grid_cons
         uint32_t* pk = &sv[64 * half];
 #pragma unroll
         for (int t = 0; t < 32; ++t) {
-          const float p0 = ex2(fmaf(__uint_as_float(sv[64 * half + 2 * t]), k, negm));
-          const float p1 = ex2(fmaf(__uint_as_float(sv[64 * half + 2 * t + 1]), k, negm));
-          ls[t & 3] += p0 + p1;
+          const uint64_t x2 = fma2(f2(__uint_as_float(sv[64 * half + 2 * t]), __uint_as_float(sv[64 * half + 2 * t + 1])),
+                                   k2, nm2);
+          float x0, x1;
+          f2_split(x2, x0, x1);
+          const float p0 = ex2(x0), p1 = ex2(x1);
+          ls[t & 3] = add2(ls[t & 3], f2(p0, p1));
           pk[t] = pack_bf16(p0, p1);
         }
         ptx::tmem_st_32x32b_x32(s_addr + 32 * half, *reinterpret_cast<uint32_t(*)[32]>(pk));
@@ -337,7 +368,11 @@ __global__ void __launch_bounds__(kThreads, 1) tp_flash_kernel(const __grid_cons
         }
       }
       ptx::tmem_st_wait();
-      l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+      {
+        float a0, a1;
+        f2_split(add2(add2(ls[0], ls[1]), add2(ls[2], ls[3])), a0, a1);
+        l += a0 + a1;
+      }
       ptx::tc_fence_before();
       ptx::mbar_arrive(ptx::smem_addr(&ctl->p_full[g]));
     }
