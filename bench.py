@@ -313,6 +313,25 @@ class AttnProjWorkload:
                 ("reduce", lambda st: self.tp.tp_combine("reduce", list(parts), out=out, stream=st),
                  4.0 * p * T * H + 2.0 * T * H)]
 
+    def reference_points(self):
+        """Library and framework equivalents of the step's kernels, timed beside it (reference
+        points, not targets): cuBLAS (torch.matmul) on the unsharded projections and torch's
+        strided copy for the rowwise extraction."""
+        torch, p, H = self.torch, self.p, self.H
+        if getattr(self, "_ref_bufs", None) is None:
+            a_full = torch.cat(self.a_sh, dim=1)
+            self._ref_bufs = (a_full, torch.empty_like(self.y), torch.empty_like(self.z))
+        a_full, y_ref, z_ref = self._ref_bufs
+        Kr = H // p
+        return [
+            ("cublas_colwise_qkv", lambda st: torch.matmul(self.x, self.w_qkv.t(), out=y_ref), "tensor",
+             self.flops_qkv),
+            ("cublas_rowwise_out", lambda st: torch.matmul(a_full, self.w_out.t(), out=z_ref), "tensor",
+             self.flops_out),
+            ("torch_rowwise_extract", lambda st: [self.out_sh[r].copy_(self.w_out[:, r * Kr:(r + 1) * Kr])
+                                                  for r in range(p)], "hbm", 2.0 * 2 * H * H),
+        ]
+
     def _rowwise(self, a_sh, stream):
         tp = self.tp
         if self.mode == "none":
@@ -941,6 +960,36 @@ def run_ours(args):
                     "frac": achieved / peaks["hbm_gbs"], "kernel": dominant, "peak_source": peaks["source"],
                     "traffic": recorded_traffic(f"{args.workload}:{dominant}", "copy")}
 
+    def time_alone(fn, reps=20):
+        with torch.cuda.stream(stream):
+            fn(stream)
+        ms = []
+        for _ in range(reps):
+            s_, e_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(stream):
+                flush.zero_()
+                s_.record(stream)
+                fn(stream)
+                e_.record(stream)
+            e_.synchronize()
+            ms.append(s_.elapsed_time(e_))
+        return float(np.mean(ms))
+
+    # Reference points (cuBLAS / torch on the same work), L2 flushed before each.
+    refs = None
+    if hasattr(wl, "reference_points"):
+        refs = {}
+        for label, fn, kind, work in wl.reference_points():
+            t = time_alone(fn)
+            if kind == "tensor":
+                v = work / (t * 1e-3) / 1e12
+                refs[label] = {"ms": round(t, 5), "TFLOP/s": v, "frac_tensor": v / peaks["bf16_tflops"]}
+            else:
+                v = work / (t * 1e-3) / 1e9
+                refs[label] = {"ms": round(t, 5), "GB/s": v, "frac_hbm": v / peaks["hbm_gbs"]}
+        wl.phase_extract(stream)   # the shards the reference copy overwrote (same bytes) -- keep them exact
+        stream.synchronize()
+
     # The join kernels on their own (when the step fuses them away), L2 flushed before each.
     joins = None
     if hasattr(wl, "join_phases"):
@@ -1020,7 +1069,7 @@ def run_ours(args):
             "extract_gbs": kernels["extract"]["GB/s"], "extract_frac_hbm": kernels["extract"]["frac_hbm"],
             "gemm_tflops": sum(wl_work for (lb, _, kd, wl_work) in phases if kd == "tensor") /
             (sum(kernels[k]["ms"] for k in tensor_phases) * 1e-3) / 1e12,
-            "cpu_baseline": cpu, "e2e": e2e, "join_kernels": joins,
+            "cpu_baseline": cpu, "e2e": e2e, "join_kernels": joins, "reference_points": refs,
             "gpu_launches": wl.launches_per_step * args.steps, "clocks": clocks,
             "bracket_s": t_wall, "peaks": peaks, "launch": "eager" if args.eager else "cuda_graph_per_phase",
             "eager_ms_per_step": float(eager_phase.sum(axis=1).mean()),
