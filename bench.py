@@ -7,15 +7,17 @@ tp_degree 4, all four ranks on this GPU):
 
   1. shard extraction of the fused QKV weight [9216, 3072] (colwise, whole
      heads of Q, K and V per rank) and of the out-projection [3072, 3072]
-     (rowwise) from device-resident full weights -- one tp_plan_shard_ranks
-     launch per weight, covering all four ranks;
-  2. the colwise QKV projection of every rank, one launch;
-  3. the AllGather of the four QKV slices into [4096, 9216] (tp_combine);
-  4. the rowwise out-projection of every rank with the partial sums joined on
+     (rowwise) from device-resident full weights -- one tp_plan_shard_many
+     launch covering both weights and all four ranks;
+  2. the colwise QKV projection of every rank, one launch, each rank's tiles
+     stored straight into its column block of the gathered [4096, 9216]
+     output (the AllGather fused into the store; ``--unfused-gather`` runs it
+     as a separate tp_combine kernel);
+  3. the rowwise out-projection of every rank with the partial sums joined on
      chip in fp32 (tp_linear_rowwise, TP_REDUCE_ACCUM), one launch.
 
 ``value`` = the step's GEMM FLOPs (2*T*K*N summed over the projections) per
-second of device time: extraction and gather count as time, not as work.
+second of device time: extraction counts as time, not as work.
 Inputs are resident in HBM when the timed region starts; L2 is flushed
 between steps (a 256 MiB write), so every step reads its operands from HBM.
 Each phase of the step is captured once as a CUDA graph and the timed steps
@@ -23,9 +25,9 @@ replay them, with CUDA events between the phases (``--eager`` launches every
 call from Python instead; the eager per-phase times are reported either way).
 
 ``e2e`` is the same metric through the same public calls with host buffers:
-the weights are extracted shard-on-read from page-locked host memory, the
-activations are copied in from page-locked memory and the block output is
-read back, all inside the timed region.
+the step's activations are copied in from page-locked memory and the output
+is read back, inside the timed region (``e2e.weights_from_host`` also reads
+every rank's weight slices from page-locked host memory every step).
 
 ``--impl reference`` times the CPU oracle (float64 numpy) on the same
 workload, each step a bounded sample of token rows.
@@ -250,9 +252,9 @@ class AttnProjWorkload:
         self.flops = self.flops_qkv + self.flops_out
         self.extract_bytes = 2.0 * 2 * (3 * H * H + H * H)   # read + write of every shard
         self.gather_bytes = 2.0 * 2 * T * 3 * H
-        # 2 extraction launches (every rank of each weight), colwise, gather unless fused, rowwise (+ the
+        # 1 extraction launch (every rank of both weights), colwise, gather unless fused, rowwise (+ the
         # counter clear of the workspace mode, or the separate reduce of the unfused mode).
-        self.launches_per_step = (4 if fused_gather else 5) + (1 if reduce_mode in ("workspace", "none") else 0)
+        self.launches_per_step = (3 if fused_gather else 4) + (1 if reduce_mode in ("workspace", "none") else 0)
         # Pinned host copies for the end-to-end measurement.
         self.pin = None
 
@@ -260,9 +262,9 @@ class AttnProjWorkload:
         return {"workload": WORKLOAD, "tokens": self.T, "hidden": self.H, "heads": self.heads, "head_dim": self.hd,
                 "tp_degree": self.p, "rowwise_reduce": self.mode,
                 "gather": "fused into the colwise store (ldy)" if self.fused_gather else "tp_combine kernel",
-                "step": "2x tp_plan_shard_ranks (device, 4 ranks each) + tp_linear_colwise writing the gathered "
-                        "QKV [T, 3H] + tp_linear_rowwise" if self.fused_gather else
-                        "2x tp_plan_shard_ranks (device, 4 ranks each) + tp_linear_colwise + tp_combine(gather) + "
+                "step": "tp_plan_shard_many (both weights, 4 ranks each, from device memory) + tp_linear_colwise "
+                        "writing the gathered QKV [T, 3H] + tp_linear_rowwise" if self.fused_gather else
+                        "tp_plan_shard_many (both weights, 4 ranks each) + tp_linear_colwise + tp_combine(gather) + "
                         "tp_linear_rowwise"}
 
     def phases(self):
@@ -281,11 +283,13 @@ class AttnProjWorkload:
 
     # The four phases of a step, each enqueued on `stream`.
     def phase_extract(self, stream):
+        # Both weights' shards, every rank, in one launch.
         tp, p, H = self.tp, self.p, self.H
-        tp.tp_plan_shard_ranks(self.w_qkv, "colwise", p, 0, p, [H] * 3, self.heads, self.hd, outs=self.qkv_sh,
-                               stream=stream)
-        tp.tp_plan_shard_ranks(self.w_out, "rowwise", p, 0, p, None, self.heads, self.hd, outs=self.out_sh,
-                               stream=stream)
+        tp.tp_plan_shard_many([
+            dict(weight=self.w_qkv, style="colwise", tp_degree=p, fused_splits=[H] * 3, num_heads=self.heads,
+                 head_dim=self.hd, outs=self.qkv_sh),
+            dict(weight=self.w_out, style="rowwise", tp_degree=p, num_heads=self.heads, head_dim=self.hd,
+                 outs=self.out_sh)], stream=stream)
 
     def phase_colwise(self, stream, x=None):
         x = self.x if x is None else x
@@ -378,10 +382,11 @@ class AttnProjWorkload:
                 dst.copy_(src, non_blocking=True)
         w_qkv = self.pin["w_qkv"] if weights_from_host else self.w_qkv
         w_out = self.pin["w_out"] if weights_from_host else self.w_out
-        tp.tp_plan_shard_ranks(w_qkv, "colwise", p, 0, p, [H] * 3, self.heads, self.hd, outs=self.qkv_sh,
-                               stream=stream)
-        tp.tp_plan_shard_ranks(w_out, "rowwise", p, 0, p, None, self.heads, self.hd, outs=self.out_sh,
-                               stream=stream)
+        tp.tp_plan_shard_many([
+            dict(weight=w_qkv, style="colwise", tp_degree=p, fused_splits=[H] * 3, num_heads=self.heads,
+                 head_dim=self.hd, outs=self.qkv_sh),
+            dict(weight=w_out, style="rowwise", tp_degree=p, num_heads=self.heads, head_dim=self.hd,
+                 outs=self.out_sh)], stream=stream)
         self.phase_colwise(stream, self.x_in)
         if not self.fused_gather:
             tp.tp_combine("gather", self.y_sh, out=self.y, stream=stream)
@@ -432,18 +437,20 @@ class MlpWorkload:
         self.flops_out = 2.0 * T * F * H
         self.flops = self.flops_in + self.flops_out
         self.extract_bytes = 2.0 * 2 * (n_in * H + H * F)
-        self.launches_per_step = 4
+        self.launches_per_step = 3
 
     def config(self):
         return {"workload": self.name, "tokens": self.T, "hidden": self.H, "ffn": self.F, "act": self.act,
                 "tp_degree": self.p, "rowwise_reduce": "accum",
-                "step": "2x tp_plan_shard_ranks (device) + tp_linear_colwise (act) + tp_linear_rowwise"}
+                "step": "tp_plan_shard_many (both weights, device) + tp_linear_colwise (act) + tp_linear_rowwise"}
 
     def phase_extract(self, stream):
         tp, p = self.tp, self.p
-        tp.tp_plan_shard_ranks(self.w_in, "colwise", p, 0, p, self.splits, self.heads, 0, outs=self.in_sh,
-                               stream=stream)
-        tp.tp_plan_shard_ranks(self.w_out, "rowwise", p, 0, p, None, self.heads, 0, outs=self.out_sh, stream=stream)
+        tp.tp_plan_shard_many([
+            dict(weight=self.w_in, style="colwise", tp_degree=p, fused_splits=self.splits, num_heads=self.heads,
+                 outs=self.in_sh),
+            dict(weight=self.w_out, style="rowwise", tp_degree=p, num_heads=self.heads, outs=self.out_sh)],
+            stream=stream)
 
     def phase_colwise(self, stream):
         self.tp.tp_linear_colwise(self.x, self.in_sh, self.act, y_shards=self.h_sh, stream=stream)
@@ -495,25 +502,27 @@ class BlockWorkload:
                        gu=2.0 * T * H * 2 * F, down=2.0 * T * F * H)
         self.flops = sum(self.fl.values())
         self.extract_bytes = 2.0 * 2 * (4 * H * H + 3 * H * F)
-        self.launches_per_step = 4 + 1 + attention_launches(p, hl, self.hd) + 3
+        self.launches_per_step = 1 + 1 + attention_launches(p, hl, self.hd) + 3
 
     def config(self):
         return {"workload": "block_sweep", "tokens": self.T, "hidden": self.H, "ffn": self.F, "heads": self.heads,
                 "head_dim": self.hd, "tp_degree": self.p, "rowwise_reduce": "accum",
                 "flops": "projections + attention core (4*T^2*head_dim per head)",
-                "step": "4x tp_plan_shard_ranks + QKV colwise + tp_attention_heads_ranks (every rank) + out rowwise + "
+                "step": "tp_plan_shard_many (4 weights) + QKV colwise + tp_attention_heads_ranks (every rank) + out rowwise + "
                         "gate/up colwise SwiGLU + down rowwise"}
 
     def phase_extract(self, stream):
+        # The block's four weights, every rank, in one launch.
         tp, p, H, F = self.tp, self.p, self.H, self.F
-        tp.tp_plan_shard_ranks(self.w["wqkv"], "colwise", p, 0, p, [H] * 3, self.heads, self.hd, outs=self.qkv_sh,
-                               stream=stream)
-        tp.tp_plan_shard_ranks(self.w["wout"], "rowwise", p, 0, p, None, self.heads, self.hd, outs=self.out_sh,
-                               stream=stream)
-        tp.tp_plan_shard_ranks(self.w["wgu"], "colwise", p, 0, p, [F, F], self.heads, 0, outs=self.gu_sh,
-                               stream=stream)
-        tp.tp_plan_shard_ranks(self.w["wdown"], "rowwise", p, 0, p, None, self.heads, 0, outs=self.dn_sh,
-                               stream=stream)
+        tp.tp_plan_shard_many([
+            dict(weight=self.w["wqkv"], style="colwise", tp_degree=p, fused_splits=[H] * 3, num_heads=self.heads,
+                 head_dim=self.hd, outs=self.qkv_sh),
+            dict(weight=self.w["wout"], style="rowwise", tp_degree=p, num_heads=self.heads, head_dim=self.hd,
+                 outs=self.out_sh),
+            dict(weight=self.w["wgu"], style="colwise", tp_degree=p, fused_splits=[F, F], num_heads=self.heads,
+                 outs=self.gu_sh),
+            dict(weight=self.w["wdown"], style="rowwise", tp_degree=p, num_heads=self.heads, outs=self.dn_sh)],
+            stream=stream)
 
     def phase_qkv(self, stream):
         self.tp.tp_linear_colwise(self.x, self.qkv_sh, "none", y_shards=self.y_sh, stream=stream)
@@ -589,22 +598,24 @@ class SingleStreamWorkload:
                        out=2.0 * T * (H + F) * H)
         self.flops = sum(self.fl.values())
         self.extract_bytes = 2.0 * 2 * ((3 * H + 2 * F) * H + H * (H + F))
-        self.launches_per_step = 2 + 2 + attention_launches(p, self.heads // p, self.hd) + 1
+        self.launches_per_step = 1 + 2 + attention_launches(p, self.heads // p, self.hd) + 1
 
     def config(self):
         return {"workload": "single_stream_tp4", "tokens": self.T, "hidden": self.H, "mlp_hidden": self.F,
                 "heads": self.heads, "head_dim": self.hd, "tp_degree": self.p, "rowwise_reduce": "accum",
                 "flops": "projections + attention core (4*T^2*head_dim per head)",
-                "step": "2x tp_plan_shard_ranks (packed [1,1,1,3,3] colwise, packed [inner, mlp] rowwise) + "
+                "step": "tp_plan_shard_many (packed [1,1,1,3,3] colwise, packed [inner, mlp] rowwise) + "
                         "colwise Q/K/V rows + colwise SwiGLU gate/up rows into [attention, mlp] + "
                         "tp_attention_heads_ranks into [attention, mlp] + packed rowwise to_out"}
 
     def phase_extract(self, stream):
+        # Both packed weights, every rank, in one launch.
         tp, p = self.tp, self.p
-        tp.tp_plan_shard_ranks(self.w_in, "colwise", p, 0, p, self.splits_in, self.heads, 0, outs=self.in_sh,
-                               stream=stream)
-        tp.tp_plan_shard_ranks(self.w_out, "rowwise", p, 0, p, self.splits_out, self.heads, 0, outs=self.out_sh,
-                               stream=stream)
+        tp.tp_plan_shard_many([
+            dict(weight=self.w_in, style="colwise", tp_degree=p, fused_splits=self.splits_in, num_heads=self.heads,
+                 outs=self.in_sh),
+            dict(weight=self.w_out, style="rowwise", tp_degree=p, fused_splits=self.splits_out, num_heads=self.heads,
+                 outs=self.out_sh)], stream=stream)
 
     def phase_qkv(self, stream):
         self.tp.tp_linear_colwise(self.x, [s[:3 * self.w] for s in self.in_sh], "none", y_shards=self.qkv,

@@ -170,6 +170,31 @@ TP_API tp_status tp_plan_shard_ranks(const void* weight, int64_t rows, int64_t c
                                      int rank_begin, int rank_count, const int64_t* fused_splits, int n_splits,
                                      int64_t num_heads, int64_t head_dim, void* const* dev_outs, tp_stream_t stream);
 
+/*
+ * tp_plan_shard_many -- several extractions (e.g. every weight of a block) in
+ * as few launches as possible: every request is a tp_plan_shard_ranks call,
+ * with the same slice definition, checks and errors.  All requests are
+ * checked before anything is copied; a refused request leaves every output
+ * untouched and the error message names the request's index.  Requests from
+ * device memory share one launch and requests from page-locked host memory
+ * another (more launches only beyond 64 copy segments: one per packed block
+ * per rank).  1 <= n_requests <= TP_MAX_SHARD_REQUESTS (0 is a no-op);
+ * `requests` and the arrays it points to are read during the call only.
+ */
+#define TP_MAX_SHARD_REQUESTS 64
+typedef struct {
+  const void* weight;           /* bf16 [rows, cols] row-major: page-locked host or device memory */
+  int64_t rows, cols;
+  tp_style style;
+  int tp_degree;
+  int rank_begin, rank_count;   /* ranks [rank_begin, rank_begin + rank_count) */
+  const int64_t* fused_splits;  /* NULL, or n_splits absolute packed block sizes */
+  int n_splits;
+  int64_t num_heads, head_dim;  /* as in tp_validate (0 skips the check) */
+  void* const* dev_outs;        /* host array of rank_count device buffers */
+} tp_shard_request;
+TP_API tp_status tp_plan_shard_many(const tp_shard_request* requests, int n_requests, tp_stream_t stream);
+
 /* ------------------------------------------------------------------------ */
 /* Sharded projections                                                       */
 /* ------------------------------------------------------------------------ */

@@ -82,6 +82,16 @@ _SIGS = {
     "tp_st_plan_shard_ranks": (_status, [_vp, ctypes.c_char_p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                          ctypes.POINTER(_i64), ctypes.c_int, _i64, _i64, ctypes.POINTER(_vp), _vp]),
 }
+class ShardRequest(ctypes.Structure):
+    """Mirror of tp_shard_request (include/tp.h)."""
+    _fields_ = [("weight", _vp), ("rows", _i64), ("cols", _i64), ("style", ctypes.c_int), ("tp_degree", ctypes.c_int),
+                ("rank_begin", ctypes.c_int), ("rank_count", ctypes.c_int), ("fused_splits", ctypes.POINTER(_i64)),
+                ("n_splits", ctypes.c_int), ("num_heads", _i64), ("head_dim", _i64),
+                ("dev_outs", ctypes.POINTER(_vp))]
+
+
+_SIGS["tp_plan_shard_many"] = (_status, [ctypes.POINTER(ShardRequest), ctypes.c_int, _vp])
+
 for _name, (_res, _args) in _SIGS.items():
     _f = getattr(lib, _name)
     _f.restype = _res
@@ -215,6 +225,41 @@ def tp_plan_shard_ranks(weight: torch.Tensor, style: str, tp_degree: int, rank_b
 # ---------------------------------------------------------------------------
 # Projections
 # ---------------------------------------------------------------------------
+
+def tp_plan_shard_many(requests: Sequence[dict], device=None, stream=None) -> list[list[torch.Tensor]]:
+    """Several tp_plan_shard_ranks extractions in as few launches as possible.
+
+    Each request is a dict with keys weight, style, tp_degree and optionally rank_begin,
+    rank_count, fused_splits, num_heads, head_dim, outs (as for tp_plan_shard_ranks).
+    Every request is checked before anything is copied.  Returns each request's outputs.
+    """
+    keep = []
+    arr = (ShardRequest * max(1, len(requests)))()
+    all_outs = []
+    for i, rq in enumerate(requests):
+        w = rq["weight"]
+        _need_bf16("weight", w)
+        rows, cols = w.shape
+        style, p = rq["style"], rq["tp_degree"]
+        rb = rq.get("rank_begin", 0)
+        rc = rq.get("rank_count")
+        rc = p - rb if rc is None else rc
+        splits = rq.get("fused_splits")
+        heads, hd = rq.get("num_heads", 0), rq.get("head_dim", 0)
+        outs = rq.get("outs")
+        if outs is None:
+            tp_validate(rows, cols, style, p, heads, hd, splits)  # before allocating
+            shape = tp_shard_shape(rows, cols, style, p, splits)
+            dev = device if device is not None else (w.device if w.is_cuda else torch.device("cuda"))
+            outs = [torch.empty(shape, dtype=torch.bfloat16, device=dev) for _ in range(rc)]
+        sp, n = _splits(splits)
+        ptrs = _ptrs(outs) if outs else None
+        keep += [sp, ptrs]
+        arr[i] = ShardRequest(_ptr(w), rows, cols, STYLES[style], p, rb, rc, sp, n, heads, hd, ptrs)
+        all_outs.append(list(outs))
+    _check(lib.tp_plan_shard_many(arr, len(requests), _stream(stream)))
+    return all_outs
+
 
 def tp_linear_colwise(x: torch.Tensor, w_shards: Sequence[torch.Tensor], act: str = "none",
                       bias_shards: Sequence[torch.Tensor | None] | None = None,

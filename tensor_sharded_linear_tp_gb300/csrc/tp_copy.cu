@@ -17,6 +17,8 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <string>
+
 #include "tp_internal.h"
 
 namespace tp {
@@ -202,25 +204,50 @@ __global__ void __launch_bounds__(256) reduce_partials_scalar(const __grid_const
 }  // namespace
 }  // namespace tp
 
-extern "C" {
+namespace tp {
+namespace {
 
-tp_status tp_plan_shard_ranks(const void* weight, int64_t rows, int64_t cols, tp_style style, int tp_degree,
-                              int rank_begin, int rank_count, const int64_t* fused_splits, int n_splits,
-                              int64_t num_heads, int64_t head_dim, void* const* dev_outs, tp_stream_t stream) {
-  using namespace tp;
-  clear_error();
+// One validated extraction: the source (device pointer or the device mapping of
+// page-locked host memory), the plan's block sizes and the ranks' outputs.
+struct ShardJob {
+  const uint8_t* src = nullptr;
+  bool host_src = false;
+  bool empty = true;  // nothing to copy (no ranks, or an empty shard)
+  int64_t rows = 0, cols = 0;
+  tp_style style = TP_COLWISE;
+  int tp_degree = 1, rank_begin = 0, rank_count = 0;
+  int64_t sizes[TP_MAX_SPLITS] = {0};
+  int n = 0;
+  void* const* outs = nullptr;
+};
+
+// The plan checks of tp_plan_shard_ranks, in its order (host only, nothing is touched).
+tp_status prepare_plan(const void* weight, int64_t rows, int64_t cols, tp_style style, int tp_degree, int rank_begin,
+                      int rank_count, const int64_t* fused_splits, int n_splits, int64_t num_heads, int64_t head_dim,
+                      void* const* dev_outs, ShardJob* job) {
   if (rank_count < 0) return fail(TP_ERR_INVALID_ARG, "rank_count %d is negative", rank_count);
   if (rank_begin < 0) return fail(TP_ERR_INVALID_ARG, "rank %d is negative", rank_begin);
-  int64_t sizes[TP_MAX_SPLITS];
-  int n = 0;
   // Validate the whole plan (and the first and last rank) before touching any memory.
   tp_status st = validate_plan(rows, cols, style, tp_degree, rank_count > 0 ? rank_begin : -1, num_heads, head_dim,
-                               fused_splits, n_splits, sizes, &n);
+                               fused_splits, n_splits, job->sizes, &job->n);
   if (st != TP_OK) return st;
   if (rank_count > 0 && rank_begin + rank_count > tp_degree)
     return fail(TP_ERR_INVALID_ARG, "ranks [%d, %d) outside [0, %d)", rank_begin, rank_begin + rank_count, tp_degree);
-  const int64_t shard_elems = rows * cols / tp_degree;
-  if (shard_elems == 0 || rank_count == 0) return TP_OK;
+  job->rows = rows;
+  job->cols = cols;
+  job->style = style;
+  job->tp_degree = tp_degree;
+  job->rank_begin = rank_begin;
+  job->rank_count = rank_count;
+  job->outs = dev_outs;
+  job->empty = (rows * cols / tp_degree == 0 || rank_count == 0);
+  return TP_OK;
+}
+
+// The pointer checks of a job whose plan passed: NULLs, where the source lives, device outputs.
+tp_status prepare_pointers(const void* weight, void* const* dev_outs, ShardJob* job) {
+  if (job->empty) return TP_OK;
+  const int rank_count = job->rank_count;
   if (weight == nullptr || dev_outs == nullptr) return fail(TP_ERR_INVALID_ARG, "weight or dev_outs is NULL");
   for (int i = 0; i < rank_count; ++i)
     if (dev_outs[i] == nullptr) return fail(TP_ERR_INVALID_ARG, "dev_outs[%d] is NULL", i);
@@ -230,12 +257,12 @@ tp_status tp_plan_shard_ranks(const void* weight, int64_t rows, int64_t cols, tp
   cudaPointerAttributes attr{};
   cudaError_t e = cudaPointerGetAttributes(&attr, weight);
   if (e != cudaSuccess) return cuda_fail(e, "cudaPointerGetAttributes(weight)");
-  const void* src = weight;
-  bool host_src = false;
+  job->src = static_cast<const uint8_t*>(weight);
+  job->host_src = false;
   if (attr.type == cudaMemoryTypeHost) {
     if (attr.devicePointer == nullptr) return fail(TP_ERR_NOT_PINNED, "page-locked weight has no device mapping");
-    src = attr.devicePointer;
-    host_src = true;
+    job->src = static_cast<const uint8_t*>(attr.devicePointer);
+    job->host_src = true;
   } else if (attr.type == cudaMemoryTypeUnregistered) {
     return fail(TP_ERR_NOT_PINNED, "weight is pageable host memory; page-lock it (cudaHostAlloc/cudaHostRegister)");
   }
@@ -246,37 +273,104 @@ tp_status tp_plan_shard_ranks(const void* weight, int64_t rows, int64_t cols, tp
     if (oattr.type != cudaMemoryTypeDevice && oattr.type != cudaMemoryTypeManaged)
       return fail(TP_ERR_INVALID_ARG, "dev_outs[%d] is not device memory", i);
   }
+  return TP_OK;
+}
 
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  SegBuilder b;
+// Add a job's segments to `b` (launching it whenever it fills up).
+tp_status append_job(SegBuilder& b, const ShardJob& j, cudaStream_t s) {
+  if (j.empty) return TP_OK;
   const int64_t esz = 2;  // bf16
-  const uint8_t* s8 = static_cast<const uint8_t*>(src);
-  for (int i = 0; i < rank_count; ++i) {
-    const int rank = rank_begin + i;
-    uint8_t* d8 = static_cast<uint8_t*>(dev_outs[i]);
+  for (int i = 0; i < j.rank_count; ++i) {
+    const int rank = j.rank_begin + i;
+    uint8_t* d8 = static_cast<uint8_t*>(j.outs[i]);
     int64_t offset = 0;      // block offset along the sharded dimension
     int64_t out_offset = 0;  // where this block's part starts in the shard
-    for (int bi = 0; bi < n; ++bi) {
-      const int64_t part = sizes[bi] / tp_degree;
+    for (int bi = 0; bi < j.n; ++bi) {
+      const int64_t part = j.sizes[bi] / j.tp_degree;
       const int64_t lo = offset + static_cast<int64_t>(rank) * part;
       if (b.full()) {
-        st = launch_copy(b, host_src, s);
+        tp_status st = launch_copy(b, j.host_src, s);
         if (st != TP_OK) return st;
         b.reset();
       }
-      if (style == TP_COLWISE) {
+      if (j.style == TP_COLWISE) {
         // Rows [lo, lo+part) of W -> rows [out_offset, out_offset+part) of the shard.
-        b.add(s8 + lo * cols * esz, d8 + out_offset * cols * esz, part, cols * esz, cols * esz, cols * esz);
+        b.add(j.src + lo * j.cols * esz, d8 + out_offset * j.cols * esz, part, j.cols * esz, j.cols * esz,
+              j.cols * esz);
       } else {
         // Columns [lo, lo+part) of every row -> columns [out_offset, ...) of the shard.
-        const int64_t shard_cols = cols / tp_degree;
-        b.add(s8 + lo * esz, d8 + out_offset * esz, rows, part * esz, cols * esz, shard_cols * esz);
+        const int64_t shard_cols = j.cols / j.tp_degree;
+        b.add(j.src + lo * esz, d8 + out_offset * esz, j.rows, part * esz, j.cols * esz, shard_cols * esz);
       }
-      offset += sizes[bi];
+      offset += j.sizes[bi];
       out_offset += part;
     }
   }
-  return launch_copy(b, host_src, s);
+  return TP_OK;
+}
+
+}  // namespace
+}  // namespace tp
+
+extern "C" {
+
+tp_status tp_plan_shard_ranks(const void* weight, int64_t rows, int64_t cols, tp_style style, int tp_degree,
+                              int rank_begin, int rank_count, const int64_t* fused_splits, int n_splits,
+                              int64_t num_heads, int64_t head_dim, void* const* dev_outs, tp_stream_t stream) {
+  using namespace tp;
+  clear_error();
+  ShardJob job;
+  tp_status st = prepare_plan(weight, rows, cols, style, tp_degree, rank_begin, rank_count, fused_splits, n_splits,
+                              num_heads, head_dim, dev_outs, &job);
+  if (st == TP_OK) st = prepare_pointers(weight, dev_outs, &job);
+  if (st != TP_OK || job.empty) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  SegBuilder b;
+  st = append_job(b, job, s);
+  if (st != TP_OK) return st;
+  return launch_copy(b, job.host_src, s);
+}
+
+tp_status tp_plan_shard_many(const tp_shard_request* requests, int n_requests, tp_stream_t stream) {
+  using namespace tp;
+  clear_error();
+  if (n_requests < 0 || n_requests > TP_MAX_SHARD_REQUESTS)
+    return fail(n_requests < 0 ? TP_ERR_INVALID_ARG : TP_ERR_UNSUPPORTED, "n_requests=%d outside [0, %d]",
+                n_requests, TP_MAX_SHARD_REQUESTS);
+  if (n_requests > 0 && requests == nullptr) return fail(TP_ERR_INVALID_ARG, "requests is NULL");
+  ShardJob jobs[TP_MAX_SHARD_REQUESTS];
+  // Every request's plan first, then every request's pointers: nothing is copied unless all pass.
+  for (int pass = 0; pass < 2; ++pass) {
+    for (int q = 0; q < n_requests; ++q) {
+      const tp_shard_request& r = requests[q];
+      tp_status st = pass == 0 ? prepare_plan(r.weight, r.rows, r.cols, r.style, r.tp_degree, r.rank_begin,
+                                              r.rank_count, r.fused_splits, r.n_splits, r.num_heads, r.head_dim,
+                                              r.dev_outs, &jobs[q])
+                               : prepare_pointers(r.weight, r.dev_outs, &jobs[q]);
+      if (st != TP_OK) {
+        const std::string msg = tp_last_error();
+        return fail(st, "request %d: %s", q, msg.c_str());
+      }
+    }
+  }
+  // Every check passed: copy, device sources in one launch and host sources in another
+  // (more only past 64 segments).
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  for (int kind = 0; kind < 2; ++kind) {
+    SegBuilder b;
+    bool any = false;
+    for (int q = 0; q < n_requests; ++q) {
+      if (jobs[q].empty || static_cast<int>(jobs[q].host_src) != kind) continue;
+      any = true;
+      tp_status st = append_job(b, jobs[q], s);
+      if (st != TP_OK) return st;
+    }
+    if (any) {
+      tp_status st = launch_copy(b, kind == 1, s);
+      if (st != TP_OK) return st;
+    }
+  }
+  return TP_OK;
 }
 
 tp_status tp_plan_shard(const void* weight, int64_t rows, int64_t cols, tp_style style, int tp_degree, int rank,

@@ -146,6 +146,36 @@ def test_plan_shard_rejects_bad_plans_before_copying():
     assert _plan_shard_raw(0, 8, "colwise", 2, 1, w=0, out=0) == "TP_OK"          # empty shard: nothing to do
 
 
+def _shard_request(rows, cols, style, p, splits=None, heads=0, hd=0, rank_begin=0, rank_count=None, w=FAKE, keep=None):
+    rc = p - rank_begin if rank_count is None else rank_count
+    sp = (ctypes.c_int64 * len(splits))(*splits) if splits else None
+    outs = (ctypes.c_void_p * max(1, rc))(*([FAKE] * max(1, rc)))
+    if keep is not None:
+        keep += [sp, outs]
+    return tp.ShardRequest(w, rows, cols, tp.STYLES[style], p, rank_begin, rc, sp, len(splits) if splits else 0,
+                           heads, hd, outs)
+
+
+def test_plan_shard_many_checks_every_request_first():
+    keep = []
+    good = _shard_request(16, 8, "colwise", 2, keep=keep)
+    bad = _shard_request(18432, 6144, "colwise", 5, [6144] * 3, 48, 128, keep=keep)
+    arr = (tp.ShardRequest * 3)(good, good, bad)
+    st = tp.lib.tp_plan_shard_many(arr, 3, None)
+    assert tp.STATUS_NAMES[st] == "TP_ERR_HEADS_NOT_DIVISIBLE"
+    assert "request 2" in tp.tp_last_error()
+    arr = (tp.ShardRequest * 2)(good, _shard_request(8, 16, "colwise", 2, [2, 4], keep=keep))
+    assert tp.STATUS_NAMES[tp.lib.tp_plan_shard_many(arr, 2, None)] == "TP_ERR_SPLIT_SUM"
+    assert tp.STATUS_NAMES[tp.lib.tp_plan_shard_many(arr, -1, None)] == "TP_ERR_INVALID_ARG"
+    assert tp.STATUS_NAMES[tp.lib.tp_plan_shard_many(arr, 65, None)] == "TP_ERR_UNSUPPORTED"
+    assert tp.STATUS_NAMES[tp.lib.tp_plan_shard_many(None, 2, None)] == "TP_ERR_INVALID_ARG"
+    assert tp.lib.tp_plan_shard_many(None, 0, None) == 0
+    # Requests with nothing to copy pass without touching memory.
+    empty = (tp.ShardRequest * 2)(_shard_request(0, 8, "colwise", 2, w=0, keep=keep),
+                                  _shard_request(16, 8, "colwise", 2, rank_count=0, w=0, keep=keep))
+    assert tp.lib.tp_plan_shard_many(empty, 2, None) == 0
+
+
 def _colwise_raw(p=2, T=64, K=256, N_r=512, act="none", ldy=0, x=FAKE, w=FAKE, y=FAKE):
     ws = (ctypes.c_void_p * max(p, 1))(*([w] * max(p, 1)))
     ys = (ctypes.c_void_p * max(p, 1))(*([y] * max(p, 1)))

@@ -407,3 +407,39 @@ def test_swiglu_mlp_full_size():
     for r in range(p):
         assert_close(f64(hs[r])[rows], O.bf16_to_f64(h_ref[r]), f"h rank {r}")
     assert_close(f64(z)[rows], z_ref, "swiglu mlp out")
+
+
+def test_plan_shard_many_equals_the_single_calls():
+    # The attention projections' two weights and a page-locked SwiGLU weight in one call: the
+    # device sources share one launch, the host source gets its own; every shard is bit-exact.
+    H, heads, d, F, p = 768, 6, 128, 1152, 3
+    w_qkv = tp_inputs.random_bits(90, 0, (3 * H, H))
+    w_out = tp_inputs.random_bits(90, 1, (H, H))
+    w_gu = tp_inputs.random_bits(90, 2, (2 * F, H))
+    gu_pin = torch.empty(w_gu.shape, dtype=torch.bfloat16, pin_memory=True)
+    gu_pin.copy_(tp.bf16_from_bits(w_gu))
+    got = tp.tp_plan_shard_many([
+        dict(weight=tp.bf16_from_bits(w_qkv, DEV), style="colwise", tp_degree=p, fused_splits=[H] * 3,
+             num_heads=heads, head_dim=d),
+        dict(weight=tp.bf16_from_bits(w_out, DEV), style="rowwise", tp_degree=p, num_heads=heads, head_dim=d),
+        dict(weight=gu_pin, style="colwise", tp_degree=p, rank_begin=1, rank_count=2, fused_splits=[F, F]),
+    ], device=DEV)
+    torch.cuda.synchronize()
+    for r in range(p):
+        assert np.array_equal(tp.bits_from_bf16(got[0][r]), O.shard(w_qkv, "colwise", p, r, [H] * 3))
+        assert np.array_equal(tp.bits_from_bf16(got[1][r]), O.shard(w_out, "rowwise", p, r))
+    for i, r in enumerate((1, 2)):
+        assert np.array_equal(tp.bits_from_bf16(got[2][i]), O.shard(w_gu, "colwise", p, r, [F, F]))
+
+
+def test_plan_shard_many_refusal_touches_nothing():
+    H, p = 256, 2
+    w = tp.bf16_from_bits(tp_inputs.random_bits(91, 0, (H, H)), DEV)
+    outs = [torch.full((H // p, H), 7, dtype=torch.int16, device=DEV).view(torch.bfloat16) for _ in range(p)]
+    with pytest.raises(tp.TPError) as e:
+        tp.tp_plan_shard_many([dict(weight=w, style="colwise", tp_degree=p, outs=outs),
+                               dict(weight=w, style="rowwise", tp_degree=3, outs=outs[:1])])
+    assert e.value.name == "TP_ERR_SPLIT_NOT_DIVISIBLE"
+    torch.cuda.synchronize()
+    for t in outs:
+        assert torch.all(t.view(torch.int16) == 7)
