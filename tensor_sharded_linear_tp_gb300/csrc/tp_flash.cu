@@ -140,6 +140,118 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
+// One key tile of one query row's online softmax (the row is this thread's TMEM lane): sv holds
+// the row of S_g = Q K^T for key tile j (in registers).  Masks keys past T, updates the running
+// max m (raising it, and rescaling l and O in TMEM, only when the tile's max exceeds it by more
+// than 8 in log2 units), writes P = 2^(s*k - m) as bf16 pairs over the first 64 columns of the
+// tile's S region and adds the unrounded P to l.  Warp-collective (TMEM access).
+__device__ __forceinline__ void softmax_tile(uint32_t (&sv)[FK], int j, int T, float k, uint32_t s_addr,
+                                             uint32_t o_addr, float& m, float& l) {
+  const int valid = min(FK, T - j * FK);
+  if (valid < FK) {   // only the last key tile can be partial (warp-uniform)
+#pragma unroll
+    for (int t = 0; t < FK; ++t)
+      if (t >= valid) sv[t] = __float_as_uint(-INFINITY);
+  }
+  float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+  for (int t = 0; t < FK; t += 2)
+    mx[(t >> 1) & 3] = max3(mx[(t >> 1) & 3], __uint_as_float(sv[t]), __uint_as_float(sv[t + 1]));
+  const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * k;
+  // Raise the running max of the rows whose tile max exceeds it by more than 8: their
+  // l and O (complete through key tile j-1: s_full_g(j) arrived after every MMA issued
+  // before S_g(j), PV_g(j-1) included) scale by alpha = 2^(m_old - m_new).  The O
+  // rescale is per warp (TMEM access is warp-collective): the whole warp does it when
+  // any of its rows needs it, with alpha = 1 for the others.  It runs after P is stored,
+  // when the S registers are free.
+  bool rescale = false;
+  float alpha = 1.0f;
+  if (j == 0) {
+    m = mt;
+  } else {
+    const bool need = mt > m + 8.0f;
+    rescale = __any_sync(0xffffffffu, need);
+    if (need) {
+      alpha = ex2(m - mt);
+      m = mt;
+    }
+    l *= alpha;
+  }
+  // P = 2^(s*k - m) as bf16 pairs into the first 64 columns of S_g's region; l += sum(P)
+  // (the unrounded values, four independent chains).  Masked keys give 2^-inf = 0.
+  const uint64_t k2 = f2(k, k), nm2 = f2(-m, -m);
+  uint64_t ls[4] = {f2(0.f, 0.f), f2(0.f, 0.f), f2(0.f, 0.f), f2(0.f, 0.f)};
+#pragma unroll
+  for (int half = 0; half < 2; ++half) {
+    // Packed in place: the pair for column t comes from entries 2t, 2t+1 (>= t), so
+    // entry t of this half is already consumed when it is overwritten.
+    uint32_t* pk = &sv[64 * half];
+#pragma unroll
+    for (int t = 0; t < 32; ++t) {
+      const uint64_t x2 = fma2(f2(__uint_as_float(sv[64 * half + 2 * t]), __uint_as_float(sv[64 * half + 2 * t + 1])),
+                               k2, nm2);
+      float x0, x1;
+      f2_split(x2, x0, x1);
+      const float p0 = ex2(x0), p1 = ex2(x1);
+      ls[t & 3] = add2(ls[t & 3], f2(p0, p1));
+      pk[t] = pack_bf16(p0, p1);
+    }
+    ptx::tmem_st_32x32b_x32(s_addr + 32 * half, *reinterpret_cast<uint32_t(*)[32]>(pk));
+  }
+  if (rescale) {
+#pragma unroll 1
+    for (int c = 0; c < FD; c += 32) {
+      uint32_t v[32];
+      ptx::tmem_ld_32x32b_x32(o_addr + c, v);
+      ptx::tmem_ld_wait();
+#pragma unroll
+      for (int t = 0; t < 32; ++t) v[t] = __float_as_uint(__uint_as_float(v[t]) * alpha);
+      ptx::tmem_st_32x32b_x32(o_addr + c, v);
+    }
+  }
+  ptx::tmem_st_wait();
+  {
+    float a0, a1;
+    f2_split(add2(add2(ls[0], ls[1]), add2(ls[2], ls[3])), a0, a1);
+    l += a0 + a1;
+  }
+}
+
+// The tile's output rows of this warp: O / l in bf16, staged in the (idle) Q buffer `qbuf` of
+// the tile and written by two TMA stores of 32 rows x 64 columns (rows past T are skipped or
+// clipped).  Warp-collective.
+__device__ __forceinline__ void write_output(const CUtensorMap& map_o, uint32_t o_addr, float l, uint32_t qbuf,
+                                             int q, int lane, int h, int row0, int T) {
+  // Epilogue: O / l in bf16, staged in the tile's Q buffer (idle: every S MMA of this tile
+  // completed before o_done), written by TMA stores of 32 rows x 64 columns.
+  const float inv = 1.0f / l;
+  const uint32_t stage = qbuf + static_cast<uint32_t>(q) * 8192;
+#pragma unroll 1
+  for (int c = 0; c < FD; c += 32) {
+    uint32_t v[32];
+    ptx::tmem_ld_32x32b_x32(o_addr + c, v);
+    ptx::tmem_ld_wait();
+    uint32_t pk[16];
+#pragma unroll
+    for (int t = 0; t < 16; ++t) pk[t] = pack_bf16(__uint_as_float(v[2 * t]) * inv, __uint_as_float(v[2 * t + 1]) * inv);
+    const uint32_t dst = stage + (c >> 6) * 4096 + static_cast<uint32_t>(lane) * 128;
+    const int chunk0 = (c & 63) >> 3;
+#pragma unroll
+    for (int t = 0; t < 4; ++t)
+      ptx::st_shared_v4(dst + (static_cast<uint32_t>((chunk0 + t) ^ (lane & 7)) << 4), pk[4 * t], pk[4 * t + 1],
+                        pk[4 * t + 2], pk[4 * t + 3]);
+  }
+  ptx::fence_proxy_async_smem();
+  __syncwarp();
+  if (lane == 0 && row0 < T) {
+    ptx::tma_store_2d(&map_o, stage, h * FD, row0);
+    ptx::tma_store_2d(&map_o, stage + 4096, h * FD + 64, row0);
+    ptx::bulk_commit();
+    ptx::bulk_wait_all();
+  }
+  __syncwarp();
+}
+
 __global__ void __launch_bounds__(kThreads, 1) tp_flash_kernel(const __grid_constant__ FlashParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -305,108 +417,13 @@ __global__ void __launch_bounds__(kThreads, 1) tp_flash_kernel(const __grid_cons
       ptx::tmem_ld_32x32b_x32(s_addr + 64, *reinterpret_cast<uint32_t(*)[32]>(&sv[64]));
       ptx::tmem_ld_32x32b_x32(s_addr + 96, *reinterpret_cast<uint32_t(*)[32]>(&sv[96]));
       ptx::tmem_ld_wait();
-      const int valid = min(FK, p.T - j * FK);
-      if (valid < FK) {   // only the last key tile can be partial (warp-uniform)
-#pragma unroll
-        for (int t = 0; t < FK; ++t)
-          if (t >= valid) sv[t] = __float_as_uint(-INFINITY);
-      }
-      float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-      for (int t = 0; t < FK; t += 2)
-        mx[(t >> 1) & 3] = max3(mx[(t >> 1) & 3], __uint_as_float(sv[t]), __uint_as_float(sv[t + 1]));
-      const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * k;
-      // Raise the running max of the rows whose tile max exceeds it by more than 8: their
-      // l and O (complete through key tile j-1: s_full_g(j) arrived after every MMA issued
-      // before S_g(j), PV_g(j-1) included) scale by alpha = 2^(m_old - m_new).  The O
-      // rescale is per warp (TMEM access is warp-collective): the whole warp does it when
-      // any of its rows needs it, with alpha = 1 for the others.  It runs after P is stored,
-      // when the S registers are free.
-      bool rescale = false;
-      float alpha = 1.0f;
-      if (j == 0) {
-        m = mt;
-      } else {
-        const bool need = mt > m + 8.0f;
-        rescale = __any_sync(0xffffffffu, need);
-        if (need) {
-          alpha = ex2(m - mt);
-          m = mt;
-        }
-        l *= alpha;
-      }
-      // P = 2^(s*k - m) as bf16 pairs into the first 64 columns of S_g's region; l += sum(P)
-      // (the unrounded values, four independent chains).  Masked keys give 2^-inf = 0.
-      const uint64_t k2 = f2(k, k), nm2 = f2(-m, -m);
-      uint64_t ls[4] = {f2(0.f, 0.f), f2(0.f, 0.f), f2(0.f, 0.f), f2(0.f, 0.f)};
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        // Packed in place: the pair for column t comes from entries 2t, 2t+1 (>= t), so
-        // entry t of this half is already consumed when it is overwritten.
-        uint32_t* pk = &sv[64 * half];
-#pragma unroll
-        for (int t = 0; t < 32; ++t) {
-          const uint64_t x2 = fma2(f2(__uint_as_float(sv[64 * half + 2 * t]), __uint_as_float(sv[64 * half + 2 * t + 1])),
-                                   k2, nm2);
-          float x0, x1;
-          f2_split(x2, x0, x1);
-          const float p0 = ex2(x0), p1 = ex2(x1);
-          ls[t & 3] = add2(ls[t & 3], f2(p0, p1));
-          pk[t] = pack_bf16(p0, p1);
-        }
-        ptx::tmem_st_32x32b_x32(s_addr + 32 * half, *reinterpret_cast<uint32_t(*)[32]>(pk));
-      }
-      if (rescale) {
-#pragma unroll 1
-        for (int c = 0; c < FD; c += 32) {
-          uint32_t v[32];
-          ptx::tmem_ld_32x32b_x32(o_addr + c, v);
-          ptx::tmem_ld_wait();
-#pragma unroll
-          for (int t = 0; t < 32; ++t) v[t] = __float_as_uint(__uint_as_float(v[t]) * alpha);
-          ptx::tmem_st_32x32b_x32(o_addr + c, v);
-        }
-      }
-      ptx::tmem_st_wait();
-      {
-        float a0, a1;
-        f2_split(add2(add2(ls[0], ls[1]), add2(ls[2], ls[3])), a0, a1);
-        l += a0 + a1;
-      }
+      softmax_tile(sv, j, p.T, k, s_addr, o_addr, m, l);
       ptx::tc_fence_before();
       ptx::mbar_arrive(ptx::smem_addr(&ctl->p_full[g]));
     }
     if (ok && __all_sync(0xffffffffu, fwait(ptx::smem_addr(&ctl->o_done[g]), 0, abort_flag, p.status))) {
       ptx::tc_fence_after();
-      // Epilogue: O / l in bf16, staged in the tile's Q buffer (idle: every S MMA of this tile
-      // completed before o_done), written by TMA stores of 32 rows x 64 columns.
-      const float inv = 1.0f / l;
-      const uint32_t stage = sbase + OFF_Q + g * 2 * SUB + static_cast<uint32_t>(q) * 8192;
-#pragma unroll 1
-      for (int c = 0; c < FD; c += 32) {
-        uint32_t v[32];
-        ptx::tmem_ld_32x32b_x32(o_addr + c, v);
-        ptx::tmem_ld_wait();
-        uint32_t pk[16];
-#pragma unroll
-        for (int t = 0; t < 16; ++t) pk[t] = pack_bf16(__uint_as_float(v[2 * t]) * inv, __uint_as_float(v[2 * t + 1]) * inv);
-        const uint32_t dst = stage + (c >> 6) * 4096 + static_cast<uint32_t>(lane) * 128;
-        const int chunk0 = (c & 63) >> 3;
-#pragma unroll
-        for (int t = 0; t < 4; ++t)
-          ptx::st_shared_v4(dst + (static_cast<uint32_t>((chunk0 + t) ^ (lane & 7)) << 4), pk[4 * t], pk[4 * t + 1],
-                            pk[4 * t + 2], pk[4 * t + 3]);
-      }
-      ptx::fence_proxy_async_smem();
-      __syncwarp();
-      const int row0 = q0 + g * FQ + q * 32;
-      if (lane == 0 && row0 < p.T) {
-        ptx::tma_store_2d(&p.map_o[rank], stage, h * FD, row0);
-        ptx::tma_store_2d(&p.map_o[rank], stage + 4096, h * FD + 64, row0);
-        ptx::bulk_commit();
-        ptx::bulk_wait_all();
-      }
-      __syncwarp();
+      write_output(p.map_o[rank], o_addr, l, sbase + OFF_Q + g * 2 * SUB, q, lane, h, q0 + g * FQ + q * 32, p.T);
     }
   }
 
