@@ -20,9 +20,11 @@ tp_degree 4, all four ranks on this GPU):
 second of device time: extraction counts as time, not as work.
 Inputs are resident in HBM when the timed region starts; L2 is flushed
 between steps (a 256 MiB write), so every step reads its operands from HBM.
-Each phase of the step is captured once as a CUDA graph and the timed steps
-replay them, with CUDA events between the phases (``--eager`` launches every
-call from Python instead; the eager per-phase times are reported either way).
+The step is captured once as a CUDA graph and each timed step replays it between
+two CUDA events (``--eager`` launches every call from Python instead); a second,
+untimed pass replays each phase as its own graph with events between the phases
+for the per-phase breakdown (``kernels``; the eager per-phase times are reported
+too).
 
 ``e2e`` is the same metric through the same public calls with host buffers:
 the step's activations are copied in from page-locked memory and the output
@@ -190,8 +192,9 @@ def source_digest(files) -> str:
 
 
 KERNEL_SOURCES = {
-    "gemm": ["tensor_sharded_linear_tp_gb300/csrc/tp_gemm.cu", "tensor_sharded_linear_tp_gb300/csrc/tp_ptx.cuh"],
-    "copy": ["tensor_sharded_linear_tp_gb300/csrc/tp_copy.cu"],
+    "gemm": ["tensor_sharded_linear_tp_gb300/csrc/tp_gemm.cu", "tensor_sharded_linear_tp_gb300/csrc/tp_ptx.cuh",
+             "tensor_sharded_linear_tp_gb300/csrc/tp_internal.h"],
+    "copy": ["tensor_sharded_linear_tp_gb300/csrc/tp_copy.cu", "tensor_sharded_linear_tp_gb300/csrc/tp_internal.h"],
 }
 
 
@@ -943,24 +946,29 @@ def run_ours(args):
     eager_phase = np.array([[m[i].elapsed_time(m[i + 1]) for i in range(nph)] for m in eager_marks])
     host_enqueue_ms = host_s / n_eager * 1e3
 
-    # The timed region replays each phase as a captured CUDA graph (the launches a
-    # serving loop would replay), with events between the phases: the GPU runs the
-    # step back to back instead of waiting on Python.
-    graphs = []
+    # The timed region replays the whole step as one captured CUDA graph (the launches a
+    # serving loop would replay): the GPU runs the step's kernels back to back instead of
+    # waiting on Python.  The per-phase breakdown comes from a second pass that replays
+    # each phase as its own graph with events between them.
+    graphs, step_graph = [], None
     if not args.eager:
         for _, fn, _, _ in phases:
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=stream):
                 fn(stream)
             graphs.append(g)
+        step_graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(step_graph, stream=stream):
+            run_step(wl, stream)
         with torch.cuda.stream(stream):
             for _ in range(args.warmup):
+                step_graph.replay()
                 for g in graphs:
                     g.replay()
         stream.synchronize()
         tp.tp_device_status(stream)
 
-    marks = [[torch.cuda.Event(enable_timing=True) for _ in range(nph + 1)] for _ in range(args.steps)]
+    bounds = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     sampler = ClockSampler(local_rank)
     sampler.start()
     time.sleep(0.3)
@@ -970,6 +978,26 @@ def run_ours(args):
     for k in range(args.steps):
         with torch.cuda.stream(stream):
             flush.zero_()          # L2 flush between steps, outside the step's events
+            bounds[k][0].record(stream)
+            if step_graph is not None:
+                step_graph.replay()
+            else:
+                run_step(wl, stream)
+            bounds[k][1].record(stream)
+    torch.cuda.synchronize()
+    barrier(dist, device)
+    t_wall = time.perf_counter() - t_wall0
+    clocks = sampler.stop()
+    tp.tp_device_status(stream)
+    step_ms = np.array([a.elapsed_time(b) for a, b in bounds])
+    mean_step_ms = float(step_ms.mean())
+
+    # Per-phase breakdown (not the timed region): each phase alone between events.
+    n_phase_steps = min(args.steps, 200)
+    marks = [[torch.cuda.Event(enable_timing=True) for _ in range(nph + 1)] for _ in range(n_phase_steps)]
+    for k in range(n_phase_steps):
+        with torch.cuda.stream(stream):
+            flush.zero_()
             if graphs:
                 for i, g in enumerate(graphs):
                     marks[k][i].record(stream)
@@ -978,13 +1006,8 @@ def run_ours(args):
             else:
                 run_step(wl, stream, marks[k])
     torch.cuda.synchronize()
-    barrier(dist, device)
-    t_wall = time.perf_counter() - t_wall0
-    clocks = sampler.stop()
     tp.tp_device_status(stream)
-
     phase = np.array([[m[i].elapsed_time(m[i + 1]) for i in range(nph)] for m in marks])  # ms
-    mean_step_ms = float(phase.sum(axis=1).mean())
     slowest_ms = max_over_ranks(dist, mean_step_ms, device)
     total_flops = sum_over_ranks(dist, wl.flops, device)
     value = total_flops / (slowest_ms * 1e-3) / 1e12
@@ -1154,7 +1177,8 @@ def run_ours(args):
             (sum(kernels[k]["ms"] for k in tensor_phases) * 1e-3) / 1e12,
             "cpu_baseline": cpu, "e2e": e2e, "join_kernels": joins, "reference_points": refs,
             "gpu_launches": wl.launches_per_step * args.steps, "clocks": clocks,
-            "bracket_s": t_wall, "peaks": peaks, "launch": "eager" if args.eager else "cuda_graph_per_phase",
+            "bracket_s": t_wall, "peaks": peaks, "launch": "eager" if args.eager else "cuda_graph_per_step",
+            "phase_sum_ms": float(phase.sum(axis=1).mean()),
             "eager_ms_per_step": float(eager_phase.sum(axis=1).mean()),
             "eager_phase_ms": [round(float(v), 5) for v in eager_phase.mean(axis=0)],
             "host_enqueue_ms_per_step": host_enqueue_ms,

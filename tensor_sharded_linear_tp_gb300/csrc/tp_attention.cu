@@ -33,6 +33,8 @@ constexpr int kHeadBatch = TP_MAX_DEGREE;
 __global__ void __launch_bounds__(256) transpose_bf16(const __nv_bfloat16* __restrict__ v, int64_t ld_v,
                                                       __nv_bfloat16* __restrict__ vt, int64_t T, int64_t width) {
   __shared__ __nv_bfloat16 tile[32][34];
+  pdl_launch_dependents();
+  pdl_wait();
   const int64_t t0 = static_cast<int64_t>(blockIdx.x) * 32;
   const int64_t j0 = static_cast<int64_t>(blockIdx.y) * 32;
   const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;  // 32 x 8 threads
@@ -131,8 +133,8 @@ tp_status attention_unfused(const void* qkv, int64_t ld_qkv, int64_t T, int n_he
   __nv_bfloat16* o = static_cast<__nv_bfloat16*>(out);
   // V^T once for all heads: [width, T].
   dim3 tgrid(static_cast<unsigned>((T + 31) / 32), static_cast<unsigned>((width + 31) / 32));
-  transpose_bf16<<<tgrid, 256, 0, s>>>(v, ld_qkv, vt, T, width);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_pdl(transpose_bf16, tgrid, dim3(256), 0, s, v, ld_qkv, vt, T, width);
+  if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "transpose launch");
   for (int h0 = 0; h0 < n_heads; h0 += kHeadBatch) {
     const int nb = (n_heads - h0) < kHeadBatch ? (n_heads - h0) : kHeadBatch;
@@ -204,9 +206,9 @@ tp_status attention_ranks(int n_ranks, const void* const* qkv, int64_t ld_qkv, i
   for (int r = 0; r < n_ranks; ++r) {
     __nv_bfloat16* slice =
         reinterpret_cast<__nv_bfloat16*>(static_cast<uint8_t*>(workspace) + r * fused_vt_bytes(T, n_heads));
-    transpose_bf16<<<tgrid, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(qkv[r]) + 2 * width, ld_qkv, slice, T,
-                                         width);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_pdl(transpose_bf16, tgrid, dim3(256), 0, s,
+                               static_cast<const __nv_bfloat16*>(qkv[r]) + 2 * width, ld_qkv, slice, T, width);
+    if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "transpose launch");
     vt[r] = slice;
   }

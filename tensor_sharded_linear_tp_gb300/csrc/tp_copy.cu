@@ -61,6 +61,8 @@ __device__ __forceinline__ uint4 load16(const uint4* p, bool host_src) {
 // 16-byte path: every pointer, stride and row length is a multiple of 16 bytes.
 template <bool kHostSrc>
 __global__ void __launch_bounds__(kCopyThreads) copy_segments_v16(const __grid_constant__ CopyParams p) {
+  pdl_launch_dependents();
+  pdl_wait();
   const int lane = threadIdx.x & 31;
   const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
@@ -88,6 +90,8 @@ __global__ void __launch_bounds__(kCopyThreads) copy_segments_v16(const __grid_c
 
 // 2-byte path for shapes whose rows are not 16-byte multiples (same work split).
 __global__ void __launch_bounds__(kCopyThreads) copy_segments_b16(const __grid_constant__ CopyParams p) {
+  pdl_launch_dependents();
+  pdl_wait();
   const int lane = threadIdx.x & 31;
   const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
@@ -147,15 +151,13 @@ tp_status launch_copy(SegBuilder& b, bool host_src, cudaStream_t stream) {
   int64_t grid = blocks_needed;
   const int64_t cap = static_cast<int64_t>(sms) * 8;
   if (grid > cap) grid = cap;
-  if (b.vec_ok) {
-    if (host_src)
-      copy_segments_v16<true><<<static_cast<unsigned>(grid), kCopyThreads, 0, stream>>>(b.p);
-    else
-      copy_segments_v16<false><<<static_cast<unsigned>(grid), kCopyThreads, 0, stream>>>(b.p);
-  } else {
-    copy_segments_b16<<<static_cast<unsigned>(grid), kCopyThreads, 0, stream>>>(b.p);
-  }
-  cudaError_t e = cudaGetLastError();
+  const dim3 g(static_cast<unsigned>(grid)), blk(kCopyThreads);
+  cudaError_t e;
+  if (b.vec_ok)
+    e = launch_pdl(host_src ? copy_segments_v16<true> : copy_segments_v16<false>, g, blk, 0, stream, b.p);
+  else
+    e = launch_pdl(copy_segments_b16, g, blk, 0, stream, b.p);
+  if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "copy kernel launch");
   return TP_OK;
 }
@@ -172,6 +174,8 @@ struct ReduceParams {
 };
 
 __global__ void __launch_bounds__(256) reduce_partials_v8(const __grid_constant__ ReduceParams p) {
+  pdl_launch_dependents();
+  pdl_wait();
   const int64_t groups = p.n >> 3;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   for (int64_t g = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; g < groups; g += stride) {
@@ -193,6 +197,8 @@ __global__ void __launch_bounds__(256) reduce_partials_v8(const __grid_constant_
 }
 
 __global__ void __launch_bounds__(256) reduce_partials_scalar(const __grid_constant__ ReduceParams p, int64_t begin) {
+  pdl_launch_dependents();
+  pdl_wait();
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   for (int64_t i = begin + static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < p.n; i += stride) {
     float acc = 0.f;
@@ -436,14 +442,16 @@ tp_status tp_combine(tp_combine_mode mode, const void* const* partials, int tp_d
     const int64_t groups = p.n >> 3;
     int64_t grid = (groups + 255) / 256;
     if (grid > static_cast<int64_t>(sms) * 8) grid = static_cast<int64_t>(sms) * 8;
-    reduce_partials_v8<<<static_cast<unsigned>(grid), 256, 0, s>>>(p);
+    cudaError_t le = launch_pdl(reduce_partials_v8, dim3(static_cast<unsigned>(grid)), dim3(256), 0, s, p);
+    if (le != cudaSuccess) return cuda_fail(le, "reduce kernel launch");
     begin = groups << 3;
   }
   if (begin < p.n) {
     int64_t rem = p.n - begin;
     int64_t grid = (rem + 255) / 256;
     if (grid > static_cast<int64_t>(sms) * 8) grid = static_cast<int64_t>(sms) * 8;
-    reduce_partials_scalar<<<static_cast<unsigned>(grid), 256, 0, s>>>(p, begin);
+    cudaError_t le = launch_pdl(reduce_partials_scalar, dim3(static_cast<unsigned>(grid)), dim3(256), 0, s, p, begin);
+    if (le != cudaSuccess) return cuda_fail(le, "reduce kernel launch");
   }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "reduce kernel launch");

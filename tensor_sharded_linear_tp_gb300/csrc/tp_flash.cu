@@ -264,6 +264,7 @@ __global__ void __launch_bounds__(kThreads, 1) tp_flash_kernel(const __grid_cons
   const int nkv = (p.T + FK - 1) / FK;
   const CUtensorMap* map_qk = &p.map_qk[rank];
   const CUtensorMap* map_vt = &p.map_vt[rank];
+  pdl_launch_dependents();
 
   if (threadIdx.x == 0) {
     ptx::mbar_init(ptx::smem_addr(&ctl->q_full), 1);
@@ -293,6 +294,7 @@ __global__ void __launch_bounds__(kThreads, 1) tp_flash_kernel(const __grid_cons
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = ctl->tmem_base;
+  pdl_wait();  // the previous kernel's writes (Q, K, V^T) are complete and visible from here on
 
   if (warp == 0) {
     if (lane == 0) {
@@ -470,8 +472,8 @@ tp_status flash_attention_d128(int n_ranks, const void* const* qkv, int64_t ld_q
   if (err != cudaSuccess) return cuda_fail(err, "cudaFuncSetAttribute(flash attention)");
   dim3 grid(static_cast<unsigned>((T + 2 * FQ - 1) / (2 * FQ)), static_cast<unsigned>(n_heads),
             static_cast<unsigned>(n_ranks));
-  tp_flash_kernel<<<grid, kThreads, kFlashSmem, stream>>>(prm);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_pdl(tp_flash_kernel, grid, dim3(kThreads), kFlashSmem, stream, prm);
+  if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "flash attention launch");
   return TP_OK;
 }

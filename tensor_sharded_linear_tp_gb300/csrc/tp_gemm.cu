@@ -486,6 +486,7 @@ __global__ void __launch_bounds__(kThreads, 1) tp_gemm_kernel(const __grid_const
   const uint32_t cta = kPair ? ptx::cluster_ctarank() : 0u;  // 0 = leader of the pair
   const int unit = kPair ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
   const int nunits = kPair ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
+  pdl_launch_dependents();
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
@@ -515,6 +516,7 @@ __global__ void __launch_bounds__(kThreads, 1) tp_gemm_kernel(const __grid_const
   if constexpr (kPair) ptx::cluster_sync(); else __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = ctl->tmem_base;
+  pdl_wait();  // the previous kernel's writes (operands, output buffers) are complete from here on
 
   const int total = p.n_groups * p.m_tiles * p.n_tiles;
 
@@ -837,13 +839,19 @@ tp_status launch_gemm(const GemmParams& p, bool pair, cudaStream_t stream) {
   // cooperative: it is refused rather than started if they cannot all be resident.
   const bool coop = (kEpi == EPI_WS_REDUCE);
   cudaLaunchConfig_t cfg{};
-  cudaLaunchAttribute attr[2];
+  cudaLaunchAttribute attr[3];
   int nattr = 0;
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.stream = stream;
   if (coop) {
     attr[nattr].id = cudaLaunchAttributeCooperative;
     attr[nattr].val.cooperative = 1;
+    ++nattr;
+  } else {
+    // Programmatic dependent launch (see launch_pdl): the kernel waits for its predecessor
+    // after its prologue.
+    attr[nattr].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[nattr].val.programmaticStreamSerializationAllowed = 1;
     ++nattr;
   }
   cudaError_t e;

@@ -34,6 +34,35 @@ tp_status validate_plan(int64_t rows, int64_t cols, tp_style style, int tp_degre
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Launch with programmatic dependent launch allowed: the kernel's blocks may be scheduled
+// while the previous kernel in the stream is still finishing.  Every kernel launched this way
+// calls pdl_launch_dependents() (its successor may be scheduled) and pdl_wait() before its
+// first global-memory access (it waits for its predecessor's completion and the visibility of
+// its writes), so the order of the results is that of plain stream order; what overlaps is
+// launch latency and each kernel's prologue (barrier set-up, tensor-memory allocation).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Args&&... args) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+}
+
+#ifdef __CUDACC__
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+#endif
+
 }  // namespace tp
 
 // Bit 0 of the status word: a bounded wait gave up.
