@@ -95,6 +95,7 @@ struct GemmParams {
   int n_counters;     // WS_REDUCE: counters per 128-row block (one per n-tile)
   int b_up_row;       // SwiGLU: first row of the up block inside W_r
   int rank_fastest;   // tile order with the rank varying fastest
+  int group_m;        // m-tiles per raster group (choose_group_m)
   int a_shared;       // one A map for every rank (colwise)
 };
 
@@ -133,12 +134,12 @@ __device__ __forceinline__ void decode_tile(const GemmParams& p, int t, int& g, 
     g = t / tiles_mn;
     mn = t - g * tiles_mn;
   }
-  // Grouped raster: GROUP_M m-tiles sweep the n-tiles together so the CTAs
+  // Grouped raster: group_m m-tiles sweep the n-tiles together so the CTAs
   // running at the same time share A and B tiles through L2.
-  const int span = GROUP_M * p.n_tiles;
+  const int span = p.group_m * p.n_tiles;
   const int sr = mn / span;
-  const int first_m = sr * GROUP_M;
-  const int gm = min(p.m_tiles - first_m, GROUP_M);
+  const int first_m = sr * p.group_m;
+  const int gm = min(p.m_tiles - first_m, p.group_m);
   const int in = mn - sr * span;
   mb = first_m + in % gm;
   nb = in / gm;
@@ -835,6 +836,7 @@ tp_status launch_gemm(const GemmParams& p, bool pair, cudaStream_t stream) {
   const int64_t total = static_cast<int64_t>(p.n_groups) * p.m_tiles * p.n_tiles;
   if (total <= 0) return TP_OK;
   if (total > 0x7FFFFFFF) return fail(TP_ERR_UNSUPPORTED, "too many tiles (%lld)", (long long)total);
+  if (p.group_m < 1) return fail(TP_ERR_INVALID_ARG, "GEMM raster group size not set");
   // The workspace mode's CTAs wait on each other (bounded), so that launch is
   // cooperative: it is refused rather than started if they cannot all be resident.
   const bool coop = (kEpi == EPI_WS_REDUCE);
@@ -899,22 +901,35 @@ int resident_units(bool pair) {
   return max_active_pairs<EPI_BF16>(sms);
 }
 
+// m-tiles per raster group.  When the A rows of every m-tile fit comfortably in L2, one group
+// spans them all: each B panel is then read from DRAM once, by all m-tiles at about the same
+// time, and A stays in L2 for the whole sweep.  Otherwise groups of about GROUP_M m-tiles,
+// sized evenly, so that no small last group re-reads all of B for a few m-tiles (18 m-tiles
+// make groups of 9 and 9, not 16 and 2).
+constexpr int64_t kAResidentBytes = 64ll << 20;
+int choose_group_m(int m_tiles, int64_t a_bytes) {
+  if (a_bytes <= kAResidentBytes) return m_tiles;
+  const int groups = (m_tiles + GROUP_M - 1) / GROUP_M;
+  return (m_tiles + groups - 1) / groups;
+}
+
 // Accumulator width of a launch without SwiGLU: among the widths the epilogue
-// supports (multiples of 32 up to 256), the one whose tiles finish in the
-// fewest waves x width -- e.g. N = 3072 on 76 pairs with 16 m-tiles takes 3
-// waves of 224-wide tiles instead of 2.5 (so 3) waves of 256-wide ones.
-// Ties go to the widest tile.
+// supports (multiples of 32 up to 256), the one whose tiles finish in the fewest
+// waves; ties go to the widest tile.  A k-block takes about the same time at every
+// width up to 256 (the operand ring's load round trip, not the MMA, sets it), so a
+// launch's time follows its wave count, not waves x width: a sweep of the 16 x N 3072
+// out-projection gave 60.6 / 60.1 / 73.2 / 86.1 / 100.2 us at widths 256 / 224 /
+// 192 / 160 / 128, i.e. 3 / 3 / 4 / 5 / 6 waves.
 int choose_bn(int64_t n_out, int64_t groups_x_mtiles, int units) {
   static const int kWidths[] = {256, 224, 192, 160, 128};
   int best = 256;
-  int64_t best_cost = -1;
+  int64_t best_waves = -1;
   for (int bn : kWidths) {
     const int64_t tiles = groups_x_mtiles * ((n_out + bn - 1) / bn);
     const int64_t waves = (tiles + units - 1) / units;
-    const int64_t cost = waves * bn;
-    if (best_cost < 0 || cost < best_cost) {
+    if (best_waves < 0 || waves < best_waves) {
       best = bn;
-      best_cost = cost;
+      best_waves = waves;
     }
   }
   return best;
@@ -993,6 +1008,7 @@ tp_status tp_linear_colwise(const void* x, const void* const* w_shards, const vo
   p.n_ksegs = 1;
   p.kblocks = ceil_div(K, BK);
   p.m_tiles = ceil_div(T, pair ? 2 * BM : BM);
+  p.group_m = choose_group_m(p.m_tiles, T * K * 2);  // A = X, shared by every rank
   p.n_tiles = ceil_div(n_out, (act == TP_ACT_SWIGLU) ? BN / 2 : bn);
   p.bn = bn;
   p.b_up_row = static_cast<int>(N_r / 2);
@@ -1111,6 +1127,8 @@ tp_status rowwise_impl(const void* const* x_shards, int64_t ldx, const void* con
   p.N = static_cast<int>(N);
   p.kblocks = ceil_div(K_r, BK);
   p.m_tiles = ceil_div(T, pair ? 2 * BM : BM);
+  // A of one tile sweep: every rank's X_r when the ranks are k-segments of one accumulator.
+  p.group_m = choose_group_m(p.m_tiles, T * K_r * 2 * (mode == TP_REDUCE_ACCUM ? tp_degree : 1));
   p.n_tiles = ceil_div(N, bn);
   p.bn = bn;
   p.n_counters = ceil_div(N, 128);
@@ -1260,6 +1278,7 @@ tp_status gemm_batched(int groups, const void* const* a, int64_t lda, const void
   p.n_ksegs = 1;
   p.kblocks = ceil_div(K, BK);
   p.m_tiles = static_cast<int>(m_tiles);
+  p.group_m = choose_group_m(p.m_tiles, M * K * 2);
   p.n_tiles = ceil_div(N, bn);
   p.bn = bn;
   p.a_shared = 0;
