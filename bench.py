@@ -356,9 +356,13 @@ class AttnProjWorkload:
         self.pin = dict(
             w_qkv=pin(self.host["w_qkv"]), w_out=pin(self.host["w_out"]), x=pin(self.host["x"]),
             a_sh=[pin(np.ascontiguousarray(self.host["a"][:, r * Kr:(r + 1) * Kr])) for r in range(self.p)],
+            a=pin(self.host["a"]),
             z=torch.empty((self.T, self.H), dtype=torch.bfloat16, pin_memory=True))
         self.x_in = torch.empty_like(self.x)
         self.a_in = [torch.empty_like(t) for t in self.a_sh]
+        # The pipelined step keeps every rank's A_r side by side in one [T, H] buffer (rank r's
+        # columns [r*H/p, (r+1)*H/p)), so a block of rows of all ranks is one copy.
+        self.a_in_cat = torch.empty((self.T, self.H), dtype=torch.bfloat16, device=self.device)
         # The step's inputs are its activations; its result is Z.
         self.h2d_bytes = self.pin["x"].numel() * 2 + sum(t.numel() * 2 for t in self.pin["a_sh"])
         self.d2h_bytes = self.pin["z"].numel() * 2
@@ -398,46 +402,56 @@ class AttnProjWorkload:
         with torch.cuda.stream(stream):
             self.pin["z"].copy_(self.z, non_blocking=True)
 
-    def step_e2e_chunked(self, stream, chunks=4):
-        """The e2e step with the tokens in `chunks` row blocks, so that the copies overlap the compute:
-        a copy stream moves chunk i's X and A_r rows in while the compute stream runs the projections
-        of earlier chunks, and a third stream reads chunk i's Z back as soon as it is done.  The
-        same public calls on row blocks of the same buffers (X, A_r, the gathered QKV and Z)."""
+    def step_e2e_chunked(self, stream, a_rows=(4096,), x_rows=(2048, 2048)):
+        """The e2e step pipelined over token row blocks, so that the copies overlap the compute.
+
+        A copy stream moves A in (every rank's A_r side by side, blocks of `a_rows` rows), then X
+        (blocks of `x_rows` rows); the compute stream runs the out-projection of each A block as
+        soon as it has landed (tp_linear_rowwise_split_input: rank r's slice is its columns) and
+        a third stream reads that block of Z back at once, while X is still on the way; then the
+        QKV projection of each X block.  The gathered QKV stays on the device, so once the last,
+        small X block has landed only its projection is left.  The same public calls on row
+        blocks of the same buffers; Z is bit-identical to the device-resident step's."""
         tp, p, H, T, torch = self.tp, self.p, self.H, self.T, self.torch
         if getattr(self, "copy_stream", None) is None:
             self.copy_stream = torch.cuda.Stream(self.device)
         if getattr(self, "d2h_stream", None) is None:
             self.d2h_stream = torch.cuda.Stream(self.device)
         cs, ds = self.copy_stream, self.d2h_stream
-        step = T // chunks
-        bounds = [(i * step, T if i == chunks - 1 else (i + 1) * step) for i in range(chunks)]
+
+        def blocks(rows):
+            assert sum(rows) == T and min(rows) > 0
+            ends = np.cumsum(rows).tolist()
+            return [(e - r, e) for r, e in zip(rows, ends)]
+        ab, xb = blocks(a_rows), blocks(x_rows)
         ev = lambda: torch.cuda.Event()  # noqa: E731
-        ex, ea, ez = [ev() for _ in bounds], [ev() for _ in bounds], [ev() for _ in bounds]
+        ea, ez, ex = [ev() for _ in ab], [ev() for _ in ab], [ev() for _ in xb]
         cs.wait_stream(stream)
         with torch.cuda.stream(cs):
-            for i, (r0, r1) in enumerate(bounds):
+            for i, (r0, r1) in enumerate(ab):
+                self.a_in_cat[r0:r1].copy_(self.pin["a"][r0:r1], non_blocking=True)
+                ea[i].record(cs)
+            for i, (r0, r1) in enumerate(xb):
                 self.x_in[r0:r1].copy_(self.pin["x"][r0:r1], non_blocking=True)
                 ex[i].record(cs)
-                for dst, src in zip(self.a_in, self.pin["a_sh"]):
-                    dst[r0:r1].copy_(src[r0:r1], non_blocking=True)
-                ea[i].record(cs)
         tp.tp_plan_shard_many([
             dict(weight=self.w_qkv, style="colwise", tp_degree=p, fused_splits=[H] * 3, num_heads=self.heads,
                  head_dim=self.hd, outs=self.qkv_sh),
             dict(weight=self.w_out, style="rowwise", tp_degree=p, num_heads=self.heads, head_dim=self.hd,
                  outs=self.out_sh)], stream=stream)
         ds.wait_stream(stream)
-        for i, (r0, r1) in enumerate(bounds):
-            stream.wait_event(ex[i])
-            tp.tp_linear_colwise(self.x_in[r0:r1], self.qkv_sh, "none", y_shards=[y[r0:r1] for y in self.y_cols],
-                                 ldy=3 * H, stream=stream)
+        for i, (r0, r1) in enumerate(ab):
             stream.wait_event(ea[i])
-            tp.tp_linear_rowwise([a[r0:r1] for a in self.a_in], self.out_sh, mode="accum", out=self.z[r0:r1],
-                                 stream=stream)
+            tp.tp_linear_rowwise_split_input(self.a_in_cat[r0:r1], self.out_sh, mode="accum", out=self.z[r0:r1],
+                                             stream=stream)
             ez[i].record(stream)
             ds.wait_event(ez[i])
             with torch.cuda.stream(ds):
                 self.pin["z"][r0:r1].copy_(self.z[r0:r1], non_blocking=True)
+        for i, (r0, r1) in enumerate(xb):
+            stream.wait_event(ex[i])
+            tp.tp_linear_colwise(self.x_in[r0:r1], self.qkv_sh, "none", y_shards=[y[r0:r1] for y in self.y_cols],
+                                 ldy=3 * H, stream=stream)
         stream.wait_stream(ds)
 
 
@@ -1143,8 +1157,10 @@ def run_ours(args):
                "ms_per_step": head_ms,
                "inputs": "activations X and A_r from page-locked host memory; weights resident in HBM, "
                          "shards extracted every step",
-               "pipelining": "tokens in 4 row blocks: copies in, projections and copies out overlap; the "
-                             "step replayed as one CUDA graph" if e2e_chunked_ms is not None else "none",
+               "pipelining": "A (every rank's A_r side by side) copied in first and its out-projection's Z "
+                             "read back while X comes in, in two row blocks, each projected as soon as it "
+                             "has landed; the step replayed as one CUDA graph"
+                             if e2e_chunked_ms is not None else "none",
                "pipelined_output_bit_identical_to_device_step": chunked_matches,
                "unchunked": {"value": total_flops / (e2e_ms * 1e-3) / 1e12, "ms_per_step": e2e_ms,
                              "what": "the same step as one block of rows (copies of A_r overlap the QKV "
