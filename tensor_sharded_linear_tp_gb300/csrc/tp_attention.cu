@@ -29,26 +29,63 @@ namespace {
 
 constexpr int kHeadBatch = TP_MAX_DEGREE;
 
-// Vt[j][t] = V[t][j] for j < width: V is [T, width] with row stride ld_v elements.
-__global__ void __launch_bounds__(256) transpose_bf16(const __nv_bfloat16* __restrict__ v, int64_t ld_v,
-                                                      __nv_bfloat16* __restrict__ vt, int64_t T, int64_t width) {
-  __shared__ __nv_bfloat16 tile[32][34];
+// Vt_r[j][t] = V_r[t][j] for t < T, j < width, for every rank r = blockIdx.z (one launch for
+// all ranks): V_r is [T, width] with row stride ld_v elements, Vt_r dense [width, T].
+struct TransposeRanks {
+  const __nv_bfloat16* v[TP_MAX_DEGREE];
+  __nv_bfloat16* vt[TP_MAX_DEGREE];
+  int64_t ld_v, T, width;
+};
+
+// 64 x 64 tiles through shared memory, two bf16 per 4-byte access on both sides, so a warp
+// reads 128 contiguous bytes of a V row and writes 128 contiguous bytes of a V^T row.
+// T and width are multiples of 8, so a pair never straddles the edge.
+__global__ void __launch_bounds__(256) transpose_ranks_bf16(const __grid_constant__ TransposeRanks p) {
+  __shared__ __align__(4) __nv_bfloat16 tile[64][66];  // [t][j]; 66: 4-byte rows, 2-way reads
   pdl_launch_dependents();
   pdl_wait();
-  const int64_t t0 = static_cast<int64_t>(blockIdx.x) * 32;
-  const int64_t j0 = static_cast<int64_t>(blockIdx.y) * 32;
-  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;  // 32 x 8 threads
+  const __nv_bfloat16* v = p.v[blockIdx.z];
+  __nv_bfloat16* vt = p.vt[blockIdx.z];
+  const int64_t t0 = static_cast<int64_t>(blockIdx.x) * 64;
+  const int64_t j0 = static_cast<int64_t>(blockIdx.y) * 64;
+  const int lane = threadIdx.x & 31, wy = threadIdx.x >> 5;  // 32 lanes x 8 warps
 #pragma unroll
-  for (int k = 0; k < 32; k += 8) {
-    const int64_t t = t0 + ty + k, j = j0 + tx;
-    if (t < T && j < width) tile[ty + k][tx] = v[t * ld_v + j];
+  for (int k = 0; k < 64; k += 8) {
+    const int64_t t = t0 + wy + k, j = j0 + 2 * lane;
+    if (t < p.T && j < p.width)
+      *reinterpret_cast<uint32_t*>(&tile[wy + k][2 * lane]) =
+          *reinterpret_cast<const uint32_t*>(v + t * p.ld_v + j);
   }
   __syncthreads();
 #pragma unroll
-  for (int k = 0; k < 32; k += 8) {
-    const int64_t j = j0 + ty + k, t = t0 + tx;
-    if (j < width && t < T) vt[j * T + t] = tile[tx][ty + k];
+  for (int k = 0; k < 64; k += 8) {
+    const int64_t j = j0 + wy + k, t = t0 + 2 * lane;
+    if (j < p.width && t < p.T) {
+      __nv_bfloat162 pr;
+      pr.x = tile[2 * lane][wy + k];
+      pr.y = tile[2 * lane + 1][wy + k];
+      *reinterpret_cast<__nv_bfloat162*>(vt + j * p.T + t) = pr;
+    }
   }
+}
+
+// Launch the transpose of n_ranks V_r slices (n_ranks <= TP_MAX_DEGREE).
+tp_status transpose_ranks(int n_ranks, const __nv_bfloat16* const* v, int64_t ld_v, __nv_bfloat16* const* vt, int64_t T,
+                          int64_t width, cudaStream_t s) {
+  TransposeRanks prm{};
+  for (int r = 0; r < n_ranks; ++r) {
+    prm.v[r] = v[r];
+    prm.vt[r] = vt[r];
+  }
+  prm.ld_v = ld_v;
+  prm.T = T;
+  prm.width = width;
+  const dim3 grid(static_cast<unsigned>((T + 63) / 64), static_cast<unsigned>((width + 63) / 64),
+                  static_cast<unsigned>(n_ranks));
+  cudaError_t e = launch_pdl(transpose_ranks_bf16, grid, dim3(256), 0, s, prm);
+  if (e == cudaSuccess) e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "transpose launch");
+  return TP_OK;
 }
 
 // Row softmax of fp32 scores scaled by `scale`, written as bf16 over the first
@@ -132,10 +169,8 @@ tp_status attention_unfused(const void* qkv, int64_t ld_qkv, int64_t T, int n_he
   const __nv_bfloat16* v = q + 2 * width;
   __nv_bfloat16* o = static_cast<__nv_bfloat16*>(out);
   // V^T once for all heads: [width, T].
-  dim3 tgrid(static_cast<unsigned>((T + 31) / 32), static_cast<unsigned>((width + 31) / 32));
-  cudaError_t e = launch_pdl(transpose_bf16, tgrid, dim3(256), 0, s, v, ld_qkv, vt, T, width);
-  if (e == cudaSuccess) e = cudaGetLastError();
-  if (e != cudaSuccess) return cuda_fail(e, "transpose launch");
+  tp_status ts = transpose_ranks(1, &v, ld_qkv, &vt, T, width, s);
+  if (ts != TP_OK) return ts;
   for (int h0 = 0; h0 < n_heads; h0 += kHeadBatch) {
     const int nb = (n_heads - h0) < kHeadBatch ? (n_heads - h0) : kHeadBatch;
     const void* a[kHeadBatch];
@@ -153,7 +188,7 @@ tp_status attention_unfused(const void* qkv, int64_t ld_qkv, int64_t T, int n_he
     const int64_t rows = static_cast<int64_t>(nb) * T;
     softmax_rows_inplace<<<static_cast<unsigned>((rows + 7) / 8), 256, 0, s>>>(scores, rows, static_cast<int>(T),
                                                                                 scale_log2e);
-    e = cudaGetLastError();
+    cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "softmax launch");
     // 3. O_h = P_h . V_h, B = V_h^T [head_dim, T].
     for (int j = 0; j < nb; ++j) {
@@ -200,18 +235,18 @@ tp_status attention_ranks(int n_ranks, const void* const* qkv, int64_t ld_qkv, i
     }
     return TP_OK;
   }
-  // Fused: every rank's V^T [width, T] into its own workspace slice, then one launch.
+  // Fused: every rank's V^T [width, T] into its own workspace slice (one launch), then the
+  // attention of every rank (one launch).
   const void* vt[TP_MAX_DEGREE];
-  dim3 tgrid(static_cast<unsigned>((T + 31) / 32), static_cast<unsigned>((width + 31) / 32));
+  const __nv_bfloat16* vsrc[TP_MAX_DEGREE];
+  __nv_bfloat16* vdst[TP_MAX_DEGREE];
   for (int r = 0; r < n_ranks; ++r) {
-    __nv_bfloat16* slice =
-        reinterpret_cast<__nv_bfloat16*>(static_cast<uint8_t*>(workspace) + r * fused_vt_bytes(T, n_heads));
-    cudaError_t e = launch_pdl(transpose_bf16, tgrid, dim3(256), 0, s,
-                               static_cast<const __nv_bfloat16*>(qkv[r]) + 2 * width, ld_qkv, slice, T, width);
-    if (e == cudaSuccess) e = cudaGetLastError();
-    if (e != cudaSuccess) return cuda_fail(e, "transpose launch");
-    vt[r] = slice;
+    vsrc[r] = static_cast<const __nv_bfloat16*>(qkv[r]) + 2 * width;
+    vdst[r] = reinterpret_cast<__nv_bfloat16*>(static_cast<uint8_t*>(workspace) + r * fused_vt_bytes(T, n_heads));
+    vt[r] = vdst[r];
   }
+  tp_status ts = transpose_ranks(n_ranks, vsrc, ld_qkv, vdst, T, width, s);
+  if (ts != TP_OK) return ts;
   return flash_attention_d128(n_ranks, qkv, ld_qkv, T, n_heads, vt, out, ldo, scale_log2e, s);
 }
 
