@@ -346,8 +346,9 @@ TP_API tp_status tp_linear_rowwise_noalloc(const void* const* x_shards, const vo
  *       (0 = dense): Q, then K, then V -- the rank's colwise QKV output.
  * out:  device bf16 [T, n_heads*head_dim] with row stride ldo (0 = dense).
  * workspace: device buffer of tp_attention_workspace_bytes(T, n_heads,
- *       head_dim) bytes (V^T; for head sizes other than 128 also the fp32
- *       scores of up to 16 heads at a time).
+ *       head_dim) bytes, owned by the caller; none (NULL, 0) at head_dim 128,
+ *       where the fused kernel reads Q, K and V in place; for other head
+ *       sizes V^T and the fp32 scores of up to 16 heads at a time.
  * Scores and softmax are fp32; the probabilities are rounded to bf16 for the
  * P.V product (fp32 accumulation); O is rounded to bf16.
  * Alignment (TP_ERR_ALIGNMENT): T, head_dim, ld_qkv, ldo multiples of 8, pointers
@@ -356,7 +357,7 @@ TP_API tp_status tp_linear_rowwise_noalloc(const void* const* x_shards, const vo
 TP_API tp_status tp_attention_heads(const void* qkv, int64_t ld_qkv, int64_t T, int n_heads, int head_dim,
                                     void* workspace, size_t ws_bytes, void* out, int64_t ldo, tp_stream_t stream);
 
-/* Bytes of device workspace tp_attention_heads needs. */
+/* Bytes of device workspace tp_attention_heads needs (0 at head_dim 128). */
 TP_API size_t tp_attention_workspace_bytes(int64_t T, int n_heads, int head_dim);
 
 /*
@@ -364,9 +365,9 @@ TP_API size_t tp_attention_workspace_bytes(int64_t T, int n_heads, int head_dim)
  * call: qkv[r] and out[r] (host arrays of n_ranks device pointers) are rank
  * r's QKV output and attention output, every rank with the same T, n_heads,
  * head_dim, ld_qkv and ldo.  With head_dim 128 one kernel launch covers every
- * rank's heads (after one V transpose per rank), so a small per-rank head
- * count still fills the GPU; other head sizes run the ranks one after
- * another through the same workspace.  Same arithmetic, checks and errors as
+ * rank's heads, so a small per-rank head count still fills the GPU, and no
+ * workspace is needed; other head sizes run the ranks one after another
+ * through the same workspace.  Same arithmetic, checks and errors as
  * tp_attention_heads; 1 <= n_ranks <= TP_MAX_DEGREE (TP_ERR_UNSUPPORTED above).
  * workspace: tp_attention_ranks_workspace_bytes(n_ranks, T, n_heads, head_dim).
  */
@@ -374,7 +375,8 @@ TP_API tp_status tp_attention_heads_ranks(int n_ranks, const void* const* qkv, i
                                           int head_dim, void* workspace, size_t ws_bytes, void* const* out,
                                           int64_t ldo, tp_stream_t stream);
 
-/* Bytes of device workspace tp_attention_heads_ranks needs (0 for an empty or invalid call). */
+/* Bytes of device workspace tp_attention_heads_ranks needs (0 at head_dim 128, and for an empty or
+ * invalid call). */
 TP_API size_t tp_attention_ranks_workspace_bytes(int n_ranks, int64_t T, int n_heads, int head_dim);
 
 /* ------------------------------------------------------------------------ */

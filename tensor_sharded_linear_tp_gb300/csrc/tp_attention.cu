@@ -152,10 +152,6 @@ size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 namespace tp {
 namespace {
 
-size_t fused_vt_bytes(int64_t T, int n_heads) {
-  return align256(static_cast<size_t>(n_heads) * 128 * static_cast<size_t>(T) * 2);
-}
-
 // Unfused path for one rank (head sizes other than 128), using the whole workspace.
 tp_status attention_unfused(const void* qkv, int64_t ld_qkv, int64_t T, int n_heads, int head_dim, void* workspace,
                             void* out, int64_t ldo, float scale_log2e, cudaStream_t s) {
@@ -224,7 +220,7 @@ tp_status attention_ranks(int n_ranks, const void* const* qkv, int64_t ld_qkv, i
       return fail(TP_ERR_ALIGNMENT, "qkv[%d] or out[%d] is not 16-byte aligned", r, r);
   if (workspace && !aligned16(workspace)) return fail(TP_ERR_ALIGNMENT, "workspace is not 16-byte aligned");
   const size_t need = tp_attention_ranks_workspace_bytes(n_ranks, T, n_heads, head_dim);
-  if (workspace == nullptr || ws_bytes < need)
+  if (need > 0 && (workspace == nullptr || ws_bytes < need))
     return fail(TP_ERR_WORKSPACE, "workspace of %zu bytes given, %zu needed", workspace ? ws_bytes : 0, need);
   const float scale_log2e = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(head_dim)));
   if (head_dim != 128) {
@@ -235,19 +231,8 @@ tp_status attention_ranks(int n_ranks, const void* const* qkv, int64_t ld_qkv, i
     }
     return TP_OK;
   }
-  // Fused: every rank's V^T [width, T] into its own workspace slice (one launch), then the
-  // attention of every rank (one launch).
-  const void* vt[TP_MAX_DEGREE];
-  const __nv_bfloat16* vsrc[TP_MAX_DEGREE];
-  __nv_bfloat16* vdst[TP_MAX_DEGREE];
-  for (int r = 0; r < n_ranks; ++r) {
-    vsrc[r] = static_cast<const __nv_bfloat16*>(qkv[r]) + 2 * width;
-    vdst[r] = reinterpret_cast<__nv_bfloat16*>(static_cast<uint8_t*>(workspace) + r * fused_vt_bytes(T, n_heads));
-    vt[r] = vdst[r];
-  }
-  tp_status ts = transpose_ranks(n_ranks, vsrc, ld_qkv, vdst, T, width, s);
-  if (ts != TP_OK) return ts;
-  return flash_attention_d128(n_ranks, qkv, ld_qkv, T, n_heads, vt, out, ldo, scale_log2e, s);
+  // Fused: one launch over every rank's heads, K and V read as they are.
+  return flash_attention_d128(n_ranks, qkv, ld_qkv, T, n_heads, out, ldo, scale_log2e, s);
 }
 
 }  // namespace
@@ -261,8 +246,7 @@ size_t tp_attention_workspace_bytes(int64_t T, int n_heads, int head_dim) {
 
 size_t tp_attention_ranks_workspace_bytes(int n_ranks, int64_t T, int n_heads, int head_dim) {
   if (n_ranks <= 0 || T <= 0 || n_heads <= 0 || head_dim <= 0) return 0;
-  if (head_dim == 128)  // fused kernel: every rank's V^T
-    return static_cast<size_t>(n_ranks) * tp::fused_vt_bytes(T, n_heads);
+  if (head_dim == 128) return 0;  // the fused kernel reads Q, K and V in place
   const size_t hb = static_cast<size_t>(n_heads < tp::kHeadBatch ? n_heads : tp::kHeadBatch);
   return tp::align256(hb * static_cast<size_t>(T) * static_cast<size_t>(T) * 4) +
          tp::align256(static_cast<size_t>(n_heads) * static_cast<size_t>(head_dim) * static_cast<size_t>(T) * 2);

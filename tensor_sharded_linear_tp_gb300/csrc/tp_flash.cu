@@ -6,10 +6,12 @@
 // of one head of one rank,
 //     O = softmax(Q K^T / sqrt(d)) V
 // without writing scores to memory: scores and probabilities live in tensor
-// memory (TMEM), K and V^T tiles stream through shared memory.
+// memory (TMEM), K and V tiles stream through shared memory, both straight from
+// the rank's QKV buffer (V is the B operand of P.V in its own [key][d] layout,
+// MN-major, so it needs no transpose).
 //
 // CTA (320 threads, one per SM), grid = (query-tile pairs, heads, ranks):
-//   warp 0       TMA producer: both Q tiles once, then K and V^T tiles of 128
+//   warp 0       TMA producer: both Q tiles once, then K and V tiles of 128
 //                keys, each through its own 2-stage ring (128-byte swizzle).
 //   warp 1       one thread issues tcgen05.mma.  For tile g (0, 1) and key tile j:
 //                  S_g = Q_g K_j^T        into TMEM columns [128g, 128g+128)
@@ -49,19 +51,18 @@ constexpr int FD = 128;   // head_dim
 constexpr int FQ = 128;   // queries per tile; two tiles per CTA
 constexpr int FK = 128;   // keys per tile
 constexpr int KS = 2;     // K ring stages
-constexpr int VS = 2;     // V^T ring stages
+constexpr int VS = 2;     // V ring stages
 constexpr int kMaxRanks = 16;
 constexpr uint32_t SUB = 16384;                         // 128 rows x 64 bf16, 128-byte swizzled
 constexpr uint32_t OFF_Q = 0;                           // tile g: 2 sub-tiles (d 0..63, 64..127)
 constexpr uint32_t OFF_K = 2 * 2 * SUB;                 // stage s: 2 sub-tiles
-constexpr uint32_t OFF_V = OFF_K + KS * 2 * SUB;        // stage s: 2 sub-tiles (keys 0..63, 64..127)
+constexpr uint32_t OFF_V = OFF_K + KS * 2 * SUB;        // stage s: 2 sub-tiles (d 0..63, 64..127), 128 key rows
 constexpr uint32_t SMEM_DATA = OFF_V + VS * 2 * SUB;    // 192 KB
 constexpr uint64_t kFlashWaitLimitNs = 2000000000ull;
 constexpr int kThreads = 320;
 
 struct FlashParams {
-  CUtensorMap map_qk[kMaxRanks];  // rank r's QKV output [T, 3*H*d], boxes of 64 columns x 128 rows
-  CUtensorMap map_vt[kMaxRanks];  // rank r's V^T [H*d, T], boxes of 64 keys x 128 rows
+  CUtensorMap map_qk[kMaxRanks];  // rank r's QKV output [T, 3*H*d], boxes of 64 columns x 128 rows (Q, K, V)
   CUtensorMap map_o[kMaxRanks];   // rank r's attention output [T, H*d], boxes of 64 columns x 32 rows
   int T;
   int n_heads;
@@ -263,7 +264,6 @@ __global__ void __launch_bounds__(kThreads, 1) tp_flash_kernel(const __grid_cons
   const int q0 = blockIdx.x * 2 * FQ;
   const int nkv = (p.T + FK - 1) / FK;
   const CUtensorMap* map_qk = &p.map_qk[rank];
-  const CUtensorMap* map_vt = &p.map_vt[rank];
   pdl_launch_dependents();
 
   if (threadIdx.x == 0) {
@@ -294,13 +294,12 @@ __global__ void __launch_bounds__(kThreads, 1) tp_flash_kernel(const __grid_cons
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = ctl->tmem_base;
-  pdl_wait();  // the previous kernel's writes (Q, K, V^T) are complete and visible from here on
+  pdl_wait();  // the previous kernel's writes (Q, K, V) are complete and visible from here on
 
   if (warp == 0) {
     if (lane == 0) {
       // ---------------------------------------------------------------- producer
       ptx::prefetch_tensormap(map_qk);
-      ptx::prefetch_tensormap(map_vt);
       const uint32_t qf = ptx::smem_addr(&ctl->q_full);
       ptx::mbar_arrive_expect_tx(qf, 4 * SUB);
       for (int g = 0; g < 2; ++g) {
@@ -321,9 +320,10 @@ __global__ void __launch_bounds__(kThreads, 1) tp_flash_kernel(const __grid_cons
         if (!fwait(ptx::smem_addr(&ctl->v_empty[vs]), ((j / VS) & 1) ^ 1u, abort_flag, p.status)) break;
         const uint32_t vf = ptx::smem_addr(&ctl->v_full[vs]);
         const uint32_t vdst = sbase + OFF_V + vs * 2 * SUB;
+        const int vx = (2 * p.n_heads + h) * FD;
         ptx::mbar_arrive_expect_tx(vf, 2 * SUB);
-        ptx::tma_load_2d(vdst, map_vt, vf, j * FK, h * FD);
-        ptx::tma_load_2d(vdst + SUB, map_vt, vf, j * FK + 64, h * FD);
+        ptx::tma_load_2d(vdst, map_qk, vf, vx, j * FK);
+        ptx::tma_load_2d(vdst + SUB, map_qk, vf, vx + 64, j * FK);
         ++v_issued;
       }
       // Let every copy land before the CTA can exit.
@@ -337,6 +337,7 @@ __global__ void __launch_bounds__(kThreads, 1) tp_flash_kernel(const __grid_cons
     if (lane == 0) {
       // ---------------------------------------------------------------- MMA issuer
       constexpr uint32_t idesc = ptx::idesc_bf16_f32(FQ, FK);   // M 128, N 128 for both products
+      constexpr uint32_t idesc_pv = idesc | ptx::kIdescMnMajorB;  // V as stored: [key][d], d contiguous
       auto issue_s = [&](int g, int j) {
         const uint32_t kb = sbase + OFF_K + (j % KS) * 2 * SUB;
         const uint32_t qb = sbase + OFF_Q + g * 2 * SUB;
@@ -348,13 +349,14 @@ __global__ void __launch_bounds__(kThreads, 1) tp_flash_kernel(const __grid_cons
         }
       };
       auto issue_pv = [&](int g, int j) {
+        // B = V tile: 128 key rows of 128 B per 64-wide d half; the halves are SUB apart (LBO),
+        // 8-key groups 1024 B apart (SBO); 16 keys per MMA = 2048 B of rows.
         const uint32_t vb = sbase + OFF_V + (j % VS) * 2 * SUB;
+        const uint64_t vdesc = ptx::sw128_mnmajor_desc(vb, SUB, 1024);
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t sub = (kk >> 2) * SUB, k4 = 2u * (kk & 3);
-          ptx::umma_bf16_ts(tmem + 2 * FK + g * FD, tmem + g * FK + kk * 8, ptx::sw128_kmajor_desc(vb + sub) + k4,
-                            idesc, (j > 0 || kk > 0) ? 1u : 0u);
-        }
+        for (int kk = 0; kk < 8; ++kk)
+          ptx::umma_bf16_ts(tmem + 2 * FK + g * FD, tmem + g * FK + kk * 8, vdesc + kk * (2048u >> 4), idesc_pv,
+                            (j > 0 || kk > 0) ? 1u : 0u);
       };
       bool ok = fwait(ptx::smem_addr(&ctl->q_full), 0, abort_flag, p.status) &&
                 fwait(ptx::smem_addr(&ctl->k_full[0]), 0, abort_flag, p.status);
@@ -441,10 +443,9 @@ __global__ void __launch_bounds__(kThreads, 1) tp_flash_kernel(const __grid_cons
 }  // namespace
 
 // Fused attention for head_dim 128 over n_ranks ranks in one launch (see the file comment).
-// vt[r]: rank r's V^T [n_heads*128, T].
+
 tp_status flash_attention_d128(int n_ranks, const void* const* qkv, int64_t ld_qkv, int64_t T, int n_heads,
-                               const void* const* vt, void* const* out, int64_t ldo, float scale_log2e,
-                               cudaStream_t stream) {
+                               void* const* out, int64_t ldo, float scale_log2e, cudaStream_t stream) {
   if (n_ranks < 1 || n_ranks > kMaxRanks)
     return fail(TP_ERR_UNSUPPORTED, "fused attention over %d ranks in one launch (at most %d)", n_ranks, kMaxRanks);
   unsigned int* status = status_word();
@@ -453,7 +454,6 @@ tp_status flash_attention_d128(int n_ranks, const void* const* qkv, int64_t ld_q
   const int64_t width = static_cast<int64_t>(n_heads) * FD;
   for (int r = 0; r < n_ranks; ++r) {
     tp_status st = encode_bf16_2d(&prm.map_qk[r], qkv[r], 3 * width, T, ld_qkv, 64, 128, true);
-    if (st == TP_OK) st = encode_bf16_2d(&prm.map_vt[r], vt[r], T, width, T, 64, 128, true);
     if (st == TP_OK) st = encode_bf16_2d(&prm.map_o[r], out[r], width, T, ldo, 64, 32, true);
     if (st != TP_OK) return st;
   }

@@ -125,6 +125,21 @@ __device__ __forceinline__ uint64_t sw128_kmajor_desc(uint32_t saddr) {
          | (static_cast<uint64_t>(2) << 61);            // 128-byte swizzle
 }
 
+// Shared-memory descriptor for an MN-major operand tile written by TMA with 128-byte swizzle:
+// each 128-byte row holds 64 consecutive bf16 along M or N at one k; rows of consecutive k
+// follow each other, 8-row groups `sbo` bytes apart; the next 64 along M or N start `lbo` bytes
+// further on (the next TMA box).
+__device__ __forceinline__ uint64_t sw128_mnmajor_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  return static_cast<uint64_t>((saddr >> 4) & 0x3FFFu)                  // start address
+         | (static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16)          // leading byte offset: next 64 along M/N
+         | (static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32)          // stride byte offset: next 8 rows along K
+         | (static_cast<uint64_t>(1) << 46)                             // descriptor version for tcgen05
+         | (static_cast<uint64_t>(2) << 61);                            // 128-byte swizzle
+}
+
+// Instruction-descriptor bit that marks B as MN-major (N contiguous) instead of K-major.
+constexpr uint32_t kIdescMnMajorB = 1u << 16;
+
 // Instruction descriptor, kind::f16: bf16 A and B (K-major), fp32 D, M x N tile.
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int m, int n) {
   return (1u << 4)                                  // D format: f32

@@ -67,15 +67,21 @@ def test_attention_of_several_ranks_in_one_call(T, heads, d, n):
 
 
 def test_attention_ranks_workspace_and_limits():
-    assert tp.tp_attention_ranks_workspace_bytes(4, 4608, 12, 128) == 4 * tp.tp_attention_workspace_bytes(4608, 12, 128)
-    assert tp.tp_attention_ranks_workspace_bytes(4, 300, 2, 64) == tp.tp_attention_workspace_bytes(300, 2, 64)
+    # head_dim 128 reads Q, K and V in place: no workspace; other sizes share one across ranks.
+    assert tp.tp_attention_ranks_workspace_bytes(4, 4608, 12, 128) == 0
+    assert tp.tp_attention_workspace_bytes(4608, 12, 128) == 0
+    assert tp.tp_attention_ranks_workspace_bytes(4, 300, 2, 64) == tp.tp_attention_workspace_bytes(300, 2, 64) > 0
     q = torch.zeros((16, 3 * 128), dtype=torch.bfloat16, device=DEV)
     with pytest.raises(tp.TPError) as e:
         tp.tp_attention_heads_ranks([q] * 17, 1, 128)
     assert e.value.name == "TP_ERR_UNSUPPORTED"
+    q64 = torch.zeros((16, 3 * 64), dtype=torch.bfloat16, device=DEV)
     with pytest.raises(tp.TPError) as e:
-        tp.tp_attention_heads_ranks([q, q], 1, 128, workspace=torch.empty(16, dtype=torch.uint8, device=DEV))
+        tp.tp_attention_heads_ranks([q64, q64], 1, 64, workspace=torch.empty(16, dtype=torch.uint8, device=DEV))
     assert e.value.name == "TP_ERR_WORKSPACE"
+    out = tp.tp_attention_heads_ranks([q, q], 1, 128)   # no workspace at all
+    torch.cuda.synchronize()
+    assert all(torch.count_nonzero(o).item() == 0 for o in out)  # zero Q, K, V -> zero output
 
 
 def test_attention_one_dominant_key_returns_its_value():
