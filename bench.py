@@ -483,6 +483,13 @@ class AttnProjWorkload:
         stream.wait_stream(ds)
 
 
+def side_stream(wl):
+    """The workload's second stream (for work that overlaps the main stream's within a step)."""
+    if getattr(wl, "side_stream", None) is None:
+        wl.side_stream = wl.torch.cuda.Stream(wl.device)
+    return wl.side_stream
+
+
 def whole_step(wl, stream):
     """Enqueue one timed step of `wl`: its own step() where it has one, else its phases in order."""
     if hasattr(wl, "step"):
@@ -532,20 +539,36 @@ class MlpWorkload:
         self.flops_out = 2.0 * T * F * H
         self.flops = self.flops_in + self.flops_out
         self.extract_bytes = 2.0 * 2 * (n_in * H + H * F)
-        self.launches_per_step = 3
+        self.launches_per_step = 4  # two extraction launches in the timed step (step()), two projections
 
     def config(self):
         return {"workload": self.name, "tokens": self.T, "hidden": self.H, "ffn": self.F, "act": self.act,
                 "tp_degree": self.p, "rowwise_reduce": "accum",
-                "step": "tp_plan_shard_many (both weights, device) + tp_linear_colwise (act) + tp_linear_rowwise"}
+                "step": "tp_plan_shard_many (in-projection weight, device) + tp_linear_colwise (act), with "
+                        "tp_plan_shard_many (down-projection weight) on a side stream beside it + tp_linear_rowwise"}
+
+    def _extract_requests(self):
+        p = self.p
+        return [dict(weight=self.w_in, style="colwise", tp_degree=p, fused_splits=self.splits, num_heads=self.heads,
+                     outs=self.in_sh),
+                dict(weight=self.w_out, style="rowwise", tp_degree=p, num_heads=self.heads, outs=self.out_sh)]
 
     def phase_extract(self, stream):
-        tp, p = self.tp, self.p
-        tp.tp_plan_shard_many([
-            dict(weight=self.w_in, style="colwise", tp_degree=p, fused_splits=self.splits, num_heads=self.heads,
-                 outs=self.in_sh),
-            dict(weight=self.w_out, style="rowwise", tp_degree=p, num_heads=self.heads, outs=self.out_sh)],
-            stream=stream)
+        self.tp.tp_plan_shard_many(self._extract_requests(), stream=stream)
+
+    def step(self, stream):
+        """One timed step: the phases' work, with the down-projection weight's shards extracted on
+        a side stream launched after the in-projection (the copy, bound by HBM, runs beside it);
+        the down-projection waits for them."""
+        side = side_stream(self)
+        req_in, req_out = self._extract_requests()
+        self.tp.tp_plan_shard_many([req_in], stream=stream)
+        side.wait_stream(stream)
+        self.phase_colwise(stream)
+        with self.torch.cuda.stream(side):
+            self.tp.tp_plan_shard_many([req_out], stream=side)
+        stream.wait_stream(side)
+        self.phase_rowwise(stream)
 
     def phase_colwise(self, stream):
         self.tp.tp_linear_colwise(self.x, self.in_sh, self.act, y_shards=self.h_sh, stream=stream)
@@ -597,27 +620,49 @@ class BlockWorkload:
                        gu=2.0 * T * H * 2 * F, down=2.0 * T * F * H)
         self.flops = sum(self.fl.values())
         self.extract_bytes = 2.0 * 2 * (4 * H * H + 3 * H * F)
-        self.launches_per_step = 1 + 1 + attention_launches(p, hl, self.hd) + 3
+        # Two extraction launches in the timed step (step()), the QKV projection, the attention,
+        # three more projections.
+        self.launches_per_step = 2 + 1 + attention_launches(p, hl, self.hd) + 3
 
     def config(self):
         return {"workload": "block_sweep", "tokens": self.T, "hidden": self.H, "ffn": self.F, "heads": self.heads,
                 "head_dim": self.hd, "tp_degree": self.p, "rowwise_reduce": "accum",
                 "flops": "projections + attention core (4*T^2*head_dim per head)",
-                "step": "tp_plan_shard_many (4 weights) + QKV colwise + tp_attention_heads_ranks (every rank) + out rowwise + "
+                "step": "tp_plan_shard_many (QKV weight) + QKV colwise, with tp_plan_shard_many (the other 3 weights) "
+                        "on a side stream beside it + tp_attention_heads_ranks (every rank) + out rowwise + "
                         "gate/up colwise SwiGLU + down rowwise"}
+
+    def _extract_requests(self):
+        p, H, F = self.p, self.H, self.F
+        return [dict(weight=self.w["wqkv"], style="colwise", tp_degree=p, fused_splits=[H] * 3, num_heads=self.heads,
+                     head_dim=self.hd, outs=self.qkv_sh),
+                dict(weight=self.w["wout"], style="rowwise", tp_degree=p, num_heads=self.heads, head_dim=self.hd,
+                     outs=self.out_sh),
+                dict(weight=self.w["wgu"], style="colwise", tp_degree=p, fused_splits=[F, F], num_heads=self.heads,
+                     outs=self.gu_sh),
+                dict(weight=self.w["wdown"], style="rowwise", tp_degree=p, num_heads=self.heads, outs=self.dn_sh)]
 
     def phase_extract(self, stream):
         # The block's four weights, every rank, in one launch.
-        tp, p, H, F = self.tp, self.p, self.H, self.F
-        tp.tp_plan_shard_many([
-            dict(weight=self.w["wqkv"], style="colwise", tp_degree=p, fused_splits=[H] * 3, num_heads=self.heads,
-                 head_dim=self.hd, outs=self.qkv_sh),
-            dict(weight=self.w["wout"], style="rowwise", tp_degree=p, num_heads=self.heads, head_dim=self.hd,
-                 outs=self.out_sh),
-            dict(weight=self.w["wgu"], style="colwise", tp_degree=p, fused_splits=[F, F], num_heads=self.heads,
-                 outs=self.gu_sh),
-            dict(weight=self.w["wdown"], style="rowwise", tp_degree=p, num_heads=self.heads, outs=self.dn_sh)],
-            stream=stream)
+        self.tp.tp_plan_shard_many(self._extract_requests(), stream=stream)
+
+    def step(self, stream):
+        """One timed step: the phases' work, with only the QKV weight's shards extracted before
+        the QKV projection; the other three weights' shards are extracted on a side stream
+        launched after it, so the copy (bound by HBM) runs beside the projection (bound by the
+        tensor cores) and the attention; the out-projection waits for it."""
+        side = side_stream(self)
+        reqs = self._extract_requests()
+        self.tp.tp_plan_shard_many(reqs[:1], stream=stream)
+        side.wait_stream(stream)
+        self.phase_qkv(stream)
+        with self.torch.cuda.stream(side):
+            self.tp.tp_plan_shard_many(reqs[1:], stream=side)
+        self.phase_attention(stream)
+        stream.wait_stream(side)
+        self.phase_out(stream)
+        self.phase_gate_up(stream)
+        self.phase_down(stream)
 
     def phase_qkv(self, stream):
         self.tp.tp_linear_colwise(self.x, self.qkv_sh, "none", y_shards=self.y_sh, stream=stream)
@@ -693,15 +738,18 @@ class SingleStreamWorkload:
                        out=2.0 * T * (H + F) * H)
         self.flops = sum(self.fl.values())
         self.extract_bytes = 2.0 * 2 * ((3 * H + 2 * F) * H + H * (H + F))
-        self.launches_per_step = 1 + 2 + attention_launches(p, self.heads // p, self.hd) + 1
+        # Two extraction launches in the timed step (step()), two colwise launches, the attention,
+        # the rowwise out-projection.
+        self.launches_per_step = 2 + 2 + attention_launches(p, self.heads // p, self.hd) + 1
 
     def config(self):
         return {"workload": "single_stream_tp4", "tokens": self.T, "hidden": self.H, "mlp_hidden": self.F,
                 "heads": self.heads, "head_dim": self.hd, "tp_degree": self.p, "rowwise_reduce": "accum",
                 "flops": "projections + attention core (4*T^2*head_dim per head)",
-                "step": "tp_plan_shard_many (packed [1,1,1,3,3] colwise, packed [inner, mlp] rowwise) + "
-                        "colwise Q/K/V rows + colwise SwiGLU gate/up rows into [attention, mlp] + "
-                        "tp_attention_heads_ranks into [attention, mlp] + packed rowwise to_out"}
+                "step": "tp_plan_shard_many (Q/K/V blocks of the packed [1,1,1,3,3] colwise weight) + colwise "
+                        "Q/K/V rows, with tp_plan_shard_many (its gate/up blocks, packed [inner, mlp] rowwise) on a "
+                        "side stream beside it + tp_attention_heads_ranks into [attention, mlp] + colwise SwiGLU "
+                        "gate/up rows into [attention, mlp] + packed rowwise to_out"}
 
     def phase_extract(self, stream):
         # Both packed weights, every rank, in one launch.
@@ -711,6 +759,32 @@ class SingleStreamWorkload:
                  outs=self.in_sh),
             dict(weight=self.w_out, style="rowwise", tp_degree=p, fused_splits=self.splits_out, num_heads=self.heads,
                  outs=self.out_sh)], stream=stream)
+
+    def step(self, stream):
+        """One timed step: the phases' work, with only the Q/K/V blocks of the packed in-projection
+        weight extracted before the Q/K/V projection.  Its gate/up blocks and the out-projection
+        weight are extracted on a side stream launched after that projection (the copy, bound by
+        HBM, runs beside it and the attention, which needs only Q/K/V); the gate/up projection
+        waits for them.  A rank's packed shard is
+        its Q/K/V rows followed by its gate/up rows, so the two partial plans (blocks [H, H, H]
+        of rows [0, 3H), blocks [F, F] of the rest) fill the same shard buffers, bit for bit."""
+        tp, p, H, w = self.tp, self.p, self.H, self.w
+        side = side_stream(self)
+        tp.tp_plan_shard_many([
+            dict(weight=self.w_in[:3 * H], style="colwise", tp_degree=p, fused_splits=[H] * 3, num_heads=self.heads,
+                 outs=[s[:3 * w] for s in self.in_sh])], stream=stream)
+        side.wait_stream(stream)
+        self.phase_qkv(stream)
+        with self.torch.cuda.stream(side):
+            tp.tp_plan_shard_many([
+                dict(weight=self.w_in[3 * H:], style="colwise", tp_degree=p, fused_splits=self.splits_in[3:],
+                     num_heads=self.heads, outs=[s[3 * w:] for s in self.in_sh]),
+                dict(weight=self.w_out, style="rowwise", tp_degree=p, fused_splits=self.splits_out,
+                     num_heads=self.heads, outs=self.out_sh)], stream=side)
+        self.phase_attention(stream)
+        stream.wait_stream(side)
+        self.phase_gate_up(stream)
+        self.phase_out(stream)
 
     def phase_qkv(self, stream):
         self.tp.tp_linear_colwise(self.x, [s[:3 * self.w] for s in self.in_sh], "none", y_shards=self.qkv,
@@ -1042,6 +1116,20 @@ def run_ours(args):
     step_ms = np.array([a.elapsed_time(b) for a, b in bounds])
     mean_step_ms = float(step_ms.mean())
 
+    # The timed step (which may reorder or overlap independent work) against the phases run
+    # one after another: the same output, bit for bit.
+    step_matches_phases = None
+    if hasattr(wl, "step") and hasattr(wl, "z"):
+        run_step(wl, stream)
+        stream.synchronize()
+        z_phases = wl.z.clone()
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            wl.z.zero_()
+        whole_step(wl, stream)
+        stream.synchronize()
+        step_matches_phases = bool(torch.equal(wl.z.view(torch.int16), z_phases.view(torch.int16)))
+
     # Per-phase breakdown (not the timed region): each phase alone between events.
     n_phase_steps = min(args.steps, 200)
     marks = [[torch.cuda.Event(enable_timing=True) for _ in range(nph + 1)] for _ in range(n_phase_steps)]
@@ -1231,6 +1319,7 @@ def run_ours(args):
             "gpu_launches": wl.launches_per_step * args.steps, "clocks": clocks,
             "bracket_s": t_wall, "peaks": peaks, "launch": "eager" if args.eager else "cuda_graph_per_step",
             "phase_sum_ms": float(phase.sum(axis=1).mean()),
+            "step_output_bit_identical_to_phases": step_matches_phases,
             "eager_ms_per_step": float(eager_phase.sum(axis=1).mean()),
             "eager_phase_ms": [round(float(v), 5) for v in eager_phase.mean(axis=0)],
             "host_enqueue_ms_per_step": host_enqueue_ms,
