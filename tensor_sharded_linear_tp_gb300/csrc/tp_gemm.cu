@@ -285,15 +285,21 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, SmemCtrl* ctl
   const CUtensorMap* omap = &p.map_out[g];
   if constexpr (kEpi == EPI_SWIGLU) {
     const __nv_bfloat16* bias = p.bias[g];
+    const int n_out = p.N, up_row = p.b_up_row;
     auto swiglu32 = [&](const uint32_t (&gv)[32], const uint32_t (&uv)[32], int col0, float (&f)[32]) {
+      if (bias == nullptr) {  // warp-uniform: no per-element test on the common path
+#pragma unroll
+        for (int j = 0; j < 32; ++j) f[j] = silu_f(__uint_as_float(gv[j])) * __uint_as_float(uv[j]);
+        return;
+      }
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
         const int col = col0 + j;
         float gg = __uint_as_float(gv[j]);
         float uu = __uint_as_float(uv[j]);
-        if (bias != nullptr && col < p.N) {
+        if (col < n_out) {
           gg += __bfloat162float(bias[col]);
-          uu += __bfloat162float(bias[p.b_up_row + col]);
+          uu += __bfloat162float(bias[up_row + col]);
         }
         f[j] = silu_f(gg) * uu;
       }
@@ -321,11 +327,20 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, SmemCtrl* ctl
     }
   } else if constexpr (kEpi == EPI_BF16 || kEpi == EPI_GELU) {
     const __nv_bfloat16* bias = p.bias[g];
+    const int n_out = p.N;
     auto act32 = [&](const uint32_t (&v)[32], int col0, float (&f)[32]) {
+      if (bias == nullptr) {  // warp-uniform: no per-element test on the common path
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const float x = __uint_as_float(v[j]);
+          f[j] = (kEpi == EPI_GELU) ? gelu_tanh_f(x) : x;
+        }
+        return;
+      }
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
         float x = __uint_as_float(v[j]);
-        if (bias != nullptr && col0 + j < p.N) x += __bfloat162float(bias[col0 + j]);
+        if (col0 + j < n_out) x += __bfloat162float(bias[col0 + j]);
         f[j] = (kEpi == EPI_GELU) ? gelu_tanh_f(x) : x;
       }
     };
@@ -365,9 +380,12 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, SmemCtrl* ctl
       if (col0 < p.N) {
         float f[32];
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          f[j] = __uint_as_float(v[j]);
-          if (bias != nullptr && col0 + j < p.N) f[j] += __bfloat162float(bias[col0 + j]);
+        for (int j = 0; j < 32; ++j) f[j] = __uint_as_float(v[j]);
+        if (bias != nullptr) {  // warp-uniform
+          const int n_out = p.N;
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (col0 + j < n_out) f[j] += __bfloat162float(bias[col0 + j]);
         }
         stage_store_f32(omap, wbuf, nchunk, lane, f, col0, row0);
       }

@@ -61,8 +61,12 @@ def test_fuzz_colwise_projection(case):
     shards = tp.tp_plan_shard_ranks(dev(w), "colwise", p, 0, p, splits, device=DEV)
     for r in range(p):
         assert np.array_equal(bits(shards[r]), O.shard(w, "colwise", p, r, splits)), ("extract", case, r)
-    ys = tp.tp_linear_colwise(dev(x), shards, act)
-    want = O.colwise_forward(x, [O.shard(w, "colwise", p, r, splits) for r in range(p)], act)
+    bias_sh = None
+    if case % 3 == 0:   # a bias, sharded like the weight's rows (integer values: sums stay exact)
+        b = tp_inputs.int_bf16(7001, case * 10 + 3, (rows, 1), lim=3)
+        bias_sh = [np.ascontiguousarray(O.shard(b, "colwise", p, r, splits).reshape(-1)) for r in range(p)]
+    ys = tp.tp_linear_colwise(dev(x), shards, act, bias_shards=None if bias_sh is None else [dev(v) for v in bias_sh])
+    want = O.colwise_forward(x, [O.shard(w, "colwise", p, r, splits) for r in range(p)], act, bias_sh)
     for r in range(p):
         if act == "swiglu":
             # SiLU is not exact: within the bar.
@@ -86,10 +90,11 @@ def test_fuzz_rowwise_projection(case):
     x_sh = [O.shard(x, "rowwise", p, r, splits) for r in range(p)]
     for r in range(p):
         assert np.array_equal(bits(w_sh[r]), O.shard(w, "rowwise", p, r, splits)), ("extract", case, r)
-    z = tp.tp_linear_rowwise([dev(a) for a in x_sh], w_sh, mode=mode)
+    b = tp_inputs.int_bf16(7002, case * 10 + 3, (N,), lim=3) if case % 4 == 0 else None  # added once
+    z = tp.tp_linear_rowwise([dev(a) for a in x_sh], w_sh, bias=None if b is None else dev(b), mode=mode)
     if mode == "none":
         z = tp.tp_combine("reduce", list(z))
-    want = O.rowwise_forward(x_sh, [O.shard(w, "rowwise", p, r, splits) for r in range(p)])
+    want = O.rowwise_forward(x_sh, [O.shard(w, "rowwise", p, r, splits) for r in range(p)], b)
     assert np.array_equal(bits(z), O.f64_to_bf16(want)), (case, p, T, K, N, mode)
 
 
