@@ -97,6 +97,9 @@ struct GemmParams {
   int rank_fastest;   // tile order with the rank varying fastest
   int group_m;        // m-tiles per raster group (choose_group_m)
   int a_shared;       // one A map for every rank (colwise)
+  int quad;           // 0: CTA pairs alone; 1: clusters of two pairs on n-adjacent tiles sharing A by
+                      // multicast (A maps of BM/2 rows); 2: on m-adjacent tiles sharing B (B maps of
+                      // a quarter of the tile width)
 };
 
 struct alignas(8) SmemCtrl {
@@ -120,8 +123,15 @@ constexpr size_t smem_bytes() {
   return 1024 /*alignment slack*/ + Cfg<kPair>::STAGES * Cfg<kPair>::STAGE_BYTES + kStagingBytes + sizeof(SmemCtrl);
 }
 
-__device__ __forceinline__ void decode_tile(const GemmParams& p, int t, int& g, int& mb, int& nb) {
-  const int tiles_mn = p.m_tiles * p.n_tiles;
+// (With a multicast launch a work item is two adjacent tiles: the tile counts are then counts of
+// such items along the paired dimension, and mb or nb the item's index.)
+__device__ __forceinline__ void decode_tile(const GemmParams& p, int t, int& g, int& mb, int& nb,
+                                            int n_tiles_override = 0, int m_tiles_override = 0,
+                                            int group_m_override = 0) {
+  const int n_tiles = n_tiles_override > 0 ? n_tiles_override : p.n_tiles;
+  const int m_tiles = m_tiles_override > 0 ? m_tiles_override : p.m_tiles;
+  const int group_m = group_m_override > 0 ? group_m_override : p.group_m;
+  const int tiles_mn = m_tiles * n_tiles;
   int mn;
   if (p.rank_fastest) {
     // The ranks of one (m, n) tile are consecutive work items, so they run at the
@@ -136,10 +146,10 @@ __device__ __forceinline__ void decode_tile(const GemmParams& p, int t, int& g, 
   }
   // Grouped raster: group_m m-tiles sweep the n-tiles together so the CTAs
   // running at the same time share A and B tiles through L2.
-  const int span = p.group_m * p.n_tiles;
+  const int span = group_m * n_tiles;
   const int sr = mn / span;
-  const int first_m = sr * p.group_m;
-  const int gm = min(p.m_tiles - first_m, p.group_m);
+  const int first_m = sr * group_m;
+  const int gm = min(m_tiles - first_m, group_m);
   const int in = mn - sr * span;
   mb = first_m + in % gm;
   nb = in / gm;
@@ -492,7 +502,12 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, SmemCtrl* ctl
 // B, the even CTA issues cta_group::2 MMAs that read both CTAs' shared memory
 // and write both CTAs' tensor memory, and each CTA's epilogue drains its own
 // 128 rows.
-template <int kEpi, bool kPair>
+// kQuad (with kPair): clusters of two CTA pairs that work on n-adjacent tiles of the same 256
+// rows, so their A tiles are the same: each CTA loads half of its A rows and multicasts them to
+// the CTA in the same position of the other pair, halving the A traffic from L2.  A stage of
+// either pair is then written by both pairs' producers, so it is free again only once both
+// pairs' MMAs are done with it (two arrivals on every empty barrier).
+template <int kEpi, bool kPair, bool kQuad = false>
 __global__ void __launch_bounds__(kThreads, 1) tp_gemm_kernel(const __grid_constant__ GemmParams p) {
   using C = Cfg<kPair>;
   extern __shared__ uint8_t smem_raw[];
@@ -502,15 +517,21 @@ __global__ void __launch_bounds__(kThreads, 1) tp_gemm_kernel(const __grid_const
   volatile int* abort_flag = &ctl->abort;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const uint32_t cta = kPair ? ptx::cluster_ctarank() : 0u;  // 0 = leader of the pair
-  const int unit = kPair ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
-  const int nunits = kPair ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
+  static_assert(kPair || !kQuad, "multicast clusters are made of CTA pairs");
+  const uint32_t crank = kPair ? ptx::cluster_ctarank() : 0u;
+  const uint32_t cta = crank & 1u;              // 0 = leader of the pair
+  const uint32_t pq = kQuad ? crank >> 1 : 0u;  // which pair of the cluster
+  const uint32_t leader = crank & ~1u;          // cluster rank of this pair's leader
+  const uint16_t pair_mask = static_cast<uint16_t>(0x3u << (2 * pq));
+  constexpr int kCtasPerUnit = kQuad ? 4 : (kPair ? 2 : 1);
+  const int unit = static_cast<int>(blockIdx.x) / kCtasPerUnit;
+  const int nunits = static_cast<int>(gridDim.x) / kCtasPerUnit;
   pdl_launch_dependents();
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
       ptx::mbar_init(ptx::smem_addr(&ctl->full[s]), 1);
-      ptx::mbar_init(ptx::smem_addr(&ctl->empty[s]), 1);
+      ptx::mbar_init(ptx::smem_addr(&ctl->empty[s]), kQuad ? 2 : 1);
     }
     for (int a = 0; a < 2; ++a) {
       ptx::mbar_init(ptx::smem_addr(&ctl->tfull[a]), 1);
@@ -537,7 +558,13 @@ __global__ void __launch_bounds__(kThreads, 1) tp_gemm_kernel(const __grid_const
   const uint32_t tmem = ctl->tmem_base;
   pdl_wait();  // the previous kernel's writes (operands, output buffers) are complete from here on
 
-  const int total = p.n_groups * p.m_tiles * p.n_tiles;
+  // Work items: tiles, or (kQuad) two adjacent tiles, one per pair: n-adjacent (quad 1, A shared)
+  // or m-adjacent (quad 2, B shared).  The host pairs along a dimension with an even tile count.
+  const int quad = kQuad ? p.quad : 0;
+  const int n_items = quad == 1 ? p.n_tiles / 2 : p.n_tiles;
+  const int m_items = quad == 2 ? p.m_tiles / 2 : p.m_tiles;
+  const int gm_items = quad == 2 ? (p.group_m + 1) / 2 : p.group_m;
+  const int total = p.n_groups * m_items * n_items;
 
   if (warp == 0) {
     if (lane == 0) {
@@ -553,7 +580,9 @@ __global__ void __launch_bounds__(kThreads, 1) tp_gemm_kernel(const __grid_const
       bool ok = true;
       for (int t = unit; t < total && ok; t += nunits) {
         int g, mb, nb;
-        decode_tile(p, t, g, mb, nb);
+        decode_tile(p, t, g, mb, nb, n_items, m_items, gm_items);
+        if (quad == 1) nb = 2 * nb + static_cast<int>(pq);
+        if (quad == 2) mb = 2 * mb + static_cast<int>(pq);
         const int a_row = mb * C::TILE_M + static_cast<int>(cta) * BM;
         for (int seg = 0; seg < p.n_ksegs && ok; ++seg) {
           const int r = (p.n_ksegs > 1) ? seg : g;
@@ -571,15 +600,27 @@ __global__ void __launch_bounds__(kThreads, 1) tp_gemm_kernel(const __grid_const
             const uint32_t sb = sa + C::A_BYTES;
             if constexpr (kPair) {
               // Both CTAs' copies complete on the leader's barrier; the leader expects all of them.
-              const uint32_t full_leader = ptx::mapa_shared(full, 0);
+              const uint32_t full_leader = ptx::mapa_shared(full, leader);
               if (cta == 0) ptx::mbar_arrive_expect_tx(full, 2 * C::A_BYTES + static_cast<uint32_t>(p.bn) * (BK * 2));
-              ptx::tma_load_2d_pair(sa, ma, full_leader, kb * BK, a_row);
+              // quad: half of this CTA's shared operand rows, to the same position in both pairs.
+              const uint16_t qmask = static_cast<uint16_t>((1u << cta) | (1u << (2 + cta)));
+              if (quad == 1)
+                ptx::tma_load_2d_pair_mc(sa + pq * (C::A_BYTES / 2), ma, full_leader, kb * BK,
+                                         a_row + static_cast<int>(pq) * (BM / 2), qmask);
+              else
+                ptx::tma_load_2d_pair(sa, ma, full_leader, kb * BK, a_row);
               int b_row;
               if (kEpi == EPI_SWIGLU)
                 b_row = (cta == 0 ? 0 : p.b_up_row) + nb * (BN / 2);  // leader: gate rows, peer: up rows
               else
                 b_row = nb * p.bn + static_cast<int>(cta) * (p.bn / 2);
-              ptx::tma_load_2d_pair(sb, mbm, full_leader, kb * BK, b_row);
+              if (quad == 2) {
+                const int half = ((kEpi == EPI_SWIGLU) ? BN : p.bn) / 4;  // rows of each pair's part
+                ptx::tma_load_2d_pair_mc(sb + pq * static_cast<uint32_t>(half * BK * 2), mbm, full_leader, kb * BK,
+                                         b_row + static_cast<int>(pq) * half, qmask);
+              } else {
+                ptx::tma_load_2d_pair(sb, mbm, full_leader, kb * BK, b_row);
+              }
             } else {
               ptx::mbar_arrive_expect_tx(full, C::A_BYTES + static_cast<uint32_t>(p.bn) * (BK * 2));
               ptx::tma_load_2d(sa, ma, full, kb * BK, a_row);
@@ -641,8 +682,8 @@ __global__ void __launch_bounds__(kThreads, 1) tp_gemm_kernel(const __grid_const
                 ptx::umma_bf16(d_tmem, adesc + 2u * k, bdesc + 2u * k, idesc, accumulate);
               accumulate = 1;
             }
-            if constexpr (kPair)
-              ptx::umma_commit_pair(ptx::smem_addr(&ctl->empty[s]), 0x3);
+            if constexpr (kPair)  // (kQuad: the stage is free in all four CTAs once both pairs arrive)
+              ptx::umma_commit_pair(ptx::smem_addr(&ctl->empty[s]), kQuad ? 0xF : pair_mask);
             else
               ptx::umma_commit(ptx::smem_addr(&ctl->empty[s]));
             ++it;
@@ -650,13 +691,13 @@ __global__ void __launch_bounds__(kThreads, 1) tp_gemm_kernel(const __grid_const
         }
         if (!ok) break;
         if constexpr (kPair)
-          ptx::umma_commit_pair(ptx::smem_addr(&ctl->tfull[acc]), 0x3);
+          ptx::umma_commit_pair(ptx::smem_addr(&ctl->tfull[acc]), pair_mask);
         else
           ptx::umma_commit(ptx::smem_addr(&ctl->tfull[acc]));
       }
       // Wait for every MMA issued before TMEM and shared memory go away (in both CTAs of a pair).
       if constexpr (kPair)
-        ptx::umma_commit_pair(ptx::smem_addr(&ctl->drain), 0x3);
+        ptx::umma_commit_pair(ptx::smem_addr(&ctl->drain), pair_mask);
       else
         ptx::umma_commit(ptx::smem_addr(&ctl->drain));
       wait_bounded(ptx::smem_addr(&ctl->drain), 0, abort_flag, p.status, true);
@@ -673,7 +714,9 @@ __global__ void __launch_bounds__(kThreads, 1) tp_gemm_kernel(const __grid_const
     uint32_t tcount = 0;
     for (int t = unit; t < total; t += nunits, ++tcount) {
       int g, mb, nb;
-      decode_tile(p, t, g, mb, nb);
+      decode_tile(p, t, g, mb, nb, n_items, m_items, gm_items);
+      if (quad == 1) nb = 2 * nb + static_cast<int>(pq);
+      if (quad == 2) mb = 2 * mb + static_cast<int>(pq);
       const uint32_t acc = tcount & 1u;
       const uint32_t aph = (tcount >> 1) & 1u;
       // Warp-uniform outcome: the epilogue's TMEM loads are warp-collective.
@@ -687,7 +730,7 @@ __global__ void __launch_bounds__(kThreads, 1) tp_gemm_kernel(const __grid_const
       auto release = [&]() {
         ptx::tc_fence_before();
         if constexpr (kPair)
-          ptx::mbar_arrive_cluster(ptx::mapa_shared(tempty, 0));  // the leader's MMA warp owns the accumulator
+          ptx::mbar_arrive_cluster(ptx::mapa_shared(tempty, leader));  // the leader's MMA warp owns the accumulator
         else
           ptx::mbar_arrive(tempty);
       };
@@ -789,8 +832,9 @@ tp_status make_map(CUtensorMap* m, const void* ptr, int64_t inner, int64_t outer
                    static_cast<uint32_t>(box_outer), CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
 }
 
-// Largest number of CTA pairs that can be resident at once (cached per device and epilogue).
-template <int kEpi>
+// Largest number of CTA-pair clusters (kQuad: clusters of two pairs) that can be resident at
+// once (cached per device and kernel).
+template <int kEpi, bool kQuad = false>
 int max_active_pairs(int sms) {
   static int cached[64] = {0};
   static std::mutex mu;
@@ -799,34 +843,35 @@ int max_active_pairs(int sms) {
   std::lock_guard<std::mutex> lock(mu);
   if (cached[dev & 63] == 0) {
     cudaLaunchConfig_t cfg{};
-    cfg.gridDim = dim3(2 * (sms / 2), 1, 1);
+    constexpr int kCluster = kQuad ? 4 : 2;
+    cfg.gridDim = dim3(kCluster * (sms / kCluster), 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = smem_bytes<true>();
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.x = kCluster;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, tp_gemm_kernel<kEpi, true>, &cfg) != cudaSuccess || n <= 0) {
+    if (cudaOccupancyMaxActiveClusters(&n, tp_gemm_kernel<kEpi, true, kQuad>, &cfg) != cudaSuccess || n <= 0) {
       cudaGetLastError();
-      n = sms / 2;
+      n = kQuad ? 0 : sms / 2;  // no multicast launch then (launch_gemm falls back to pairs)
     }
     cached[dev & 63] = n;
   }
   return cached[dev & 63];
 }
 
-template <int kEpi, bool kPair>
+template <int kEpi, bool kPair, bool kQuad = false>
 tp_status set_smem_attr() {
   static std::once_flag once[64];
   int dev = 0;
   cudaGetDevice(&dev);
   cudaError_t err = cudaSuccess;
   std::call_once(once[dev & 63], [&] {
-    err = cudaFuncSetAttribute(tp_gemm_kernel<kEpi, kPair>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    err = cudaFuncSetAttribute(tp_gemm_kernel<kEpi, kPair, kQuad>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                static_cast<int>(smem_bytes<kPair>()));
   });
   if (err != cudaSuccess) return cuda_fail(err, "cudaFuncSetAttribute(max dynamic shared memory)");
@@ -875,6 +920,31 @@ tp_status launch_gemm(const GemmParams& p, bool pair, cudaStream_t stream) {
     ++nattr;
   }
   cudaError_t e;
+  if constexpr (kEpi != EPI_WS_REDUCE) {
+    if (pair && p.quad) {
+      // Clusters of two CTA pairs, A shared by multicast (see tp_gemm_kernel).
+      tp_status st = set_smem_attr<kEpi, true, true>();
+      if (st != TP_OK) return st;
+      const int quads_max = max_active_pairs<kEpi, true>(sms);
+      if (quads_max < 1) return fail(TP_ERR_UNSUPPORTED, "no cluster of four CTAs fits on this device");
+      const int64_t items = static_cast<int64_t>(p.n_groups) * p.m_tiles * p.n_tiles / 2;
+      const int quads = static_cast<int>(items < quads_max ? items : quads_max);
+      cfg.gridDim = dim3(4 * quads, 1, 1);
+      cfg.dynamicSmemBytes = smem_bytes<true>();
+      attr[nattr].id = cudaLaunchAttributeClusterDimension;
+      attr[nattr].val.clusterDim.x = 4;
+      attr[nattr].val.clusterDim.y = 1;
+      attr[nattr].val.clusterDim.z = 1;
+      ++nattr;
+      cfg.attrs = attr;
+      cfg.numAttrs = nattr;
+      e = cudaLaunchKernelEx(&cfg, tp_gemm_kernel<kEpi, true, true>, p);
+      if (e != cudaSuccess) return cuda_fail(e, "GEMM (clusters of CTA pairs) launch");
+      e = cudaGetLastError();
+      if (e != cudaSuccess) return cuda_fail(e, "GEMM kernel launch");
+      return TP_OK;
+    }
+  }
   if (!pair) {
     tp_status st = set_smem_attr<kEpi, false>();
     if (st != TP_OK) return st;
@@ -917,6 +987,19 @@ int resident_units(bool pair) {
   if (!pair) return sms;
   if (set_smem_attr<EPI_BF16, true>() != TP_OK) return sms / 2;
   return max_active_pairs<EPI_BF16>(sms);
+}
+
+// CTA-pair launches run as clusters of two pairs (tp_gemm_kernel's kQuad) whenever such a
+// cluster fits on the device and a tile count is even: 1 = pairs on n-adjacent tiles sharing A
+// (even n_tiles), 2 = on m-adjacent tiles sharing B (even m_tiles), 0 = pairs alone.  Decided
+// before the operand maps are built: the shared operand's boxes are half as high.
+int quad_mode(bool pair, int64_t m_tiles, int64_t n_tiles) {
+  if (!pair) return 0;
+  if (set_smem_attr<EPI_BF16, true, true>() != TP_OK) return 0;
+  if (max_active_pairs<EPI_BF16, true>(sm_count()) < 1) return 0;
+  if (n_tiles % 2 == 0) return 1;
+  if (m_tiles % 2 == 0) return 2;
+  return 0;
 }
 
 // m-tiles per raster group.  When the A rows of every m-tile fit comfortably in L2, one group
@@ -1004,11 +1087,13 @@ tp_status tp_linear_colwise(const void* x, const void* const* w_shards, const vo
 
   const bool pair = use_pair(T);
   GemmParams p{};
-  st = make_map(&p.map_a[0], x, K, T, K, BM);
-  if (st != TP_OK) return st;
   const int64_t m_tiles = (T + (pair ? 2 * BM : BM) - 1) / (pair ? 2 * BM : BM);
   const int bn = (act == TP_ACT_SWIGLU) ? BN : choose_bn(n_out, tp_degree * m_tiles, resident_units(pair));
-  const int box_b = (act == TP_ACT_SWIGLU) ? BN / 2 : (pair ? bn / 2 : bn);
+  const int quad = quad_mode(pair, m_tiles, ceil_div(n_out, (act == TP_ACT_SWIGLU) ? BN / 2 : bn));
+  p.quad = quad;
+  st = make_map(&p.map_a[0], x, K, T, K, quad == 1 ? BM / 2 : BM);
+  if (st != TP_OK) return st;
+  const int box_b = ((act == TP_ACT_SWIGLU) ? BN / 2 : (pair ? bn / 2 : bn)) / (quad == 2 ? 2 : 1);
   for (int r = 0; r < tp_degree; ++r) {
     st = make_map(&p.map_b[r], w_shards[r], K, N_r, K, box_b);
     if (st != TP_OK) return st;
@@ -1133,11 +1218,14 @@ tp_status rowwise_impl(const void* const* x_shards, int64_t ldx, const void* con
   const int64_t m_tiles = (T + (pair ? 2 * BM : BM) - 1) / (pair ? 2 * BM : BM);
   const int groups = (mode == TP_REDUCE_ACCUM) ? 1 : tp_degree;
   const int bn = choose_bn(N, groups * m_tiles, resident_units(pair));
+  // (the workspace mode stays in pairs)
+  const int quad = mode == TP_REDUCE_WORKSPACE ? 0 : quad_mode(pair, m_tiles, ceil_div(N, bn));
   GemmParams p{};
+  p.quad = quad;
   for (int r = 0; r < tp_degree; ++r) {
-    st = make_map(&p.map_a[r], x_shards[r], K_r, T, ldx, BM);
+    st = make_map(&p.map_a[r], x_shards[r], K_r, T, ldx, quad == 1 ? BM / 2 : BM);
     if (st != TP_OK) return st;
-    st = make_map(&p.map_b[r], w_shards[r], K_r, N, K_r, pair ? bn / 2 : bn);
+    st = make_map(&p.map_b[r], w_shards[r], K_r, N, K_r, (pair ? bn / 2 : bn) / (quad == 2 ? 2 : 1));
     if (st != TP_OK) return st;
   }
   p.status = status;
@@ -1277,12 +1365,14 @@ tp_status gemm_batched(int groups, const void* const* a, int64_t lda, const void
   const bool pair = use_pair(M);
   const int64_t m_tiles = (M + (pair ? 2 * BM : BM) - 1) / (pair ? 2 * BM : BM);
   const int bn = choose_bn(N, groups * m_tiles, resident_units(pair));
+  const int quad = quad_mode(pair, m_tiles, ceil_div(N, bn));
   GemmParams p{};
+  p.quad = quad;
   for (int g = 0; g < groups; ++g) {
     if (!aligned16(a[g]) || !aligned16(b[g]) || !aligned16(out[g]))
       return fail(TP_ERR_ALIGNMENT, "batched GEMM operand of group %d is not 16-byte aligned", g);
-    tp_status st = make_map(&p.map_a[g], a[g], K, M, lda, BM);
-    if (st == TP_OK) st = make_map(&p.map_b[g], b[g], K, N, ldb, pair ? bn / 2 : bn);
+    tp_status st = make_map(&p.map_a[g], a[g], K, M, lda, quad == 1 ? BM / 2 : BM);
+    if (st == TP_OK) st = make_map(&p.map_b[g], b[g], K, N, ldb, (pair ? bn / 2 : bn) / (quad == 2 ? 2 : 1));
     if (st == TP_OK) st = make_out_map(&p.map_out[g], out[g], out_f32, N, M, ldo);
     if (st == TP_OK && !out_f32) st = make_out_map(&p.map_out_tail[g], out[g], false, N, M, ldo, true);
     if (st != TP_OK) return st;
