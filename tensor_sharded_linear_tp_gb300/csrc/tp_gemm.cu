@@ -989,17 +989,24 @@ int resident_units(bool pair) {
   return max_active_pairs<EPI_BF16>(sms);
 }
 
-// CTA-pair launches run as clusters of two pairs (tp_gemm_kernel's kQuad) whenever such a
-// cluster fits on the device and a tile count is even: 1 = pairs on n-adjacent tiles sharing A
-// (even n_tiles), 2 = on m-adjacent tiles sharing B (even m_tiles), 0 = pairs alone.  Decided
-// before the operand maps are built: the shared operand's boxes are half as high.
-int quad_mode(bool pair, int64_t m_tiles, int64_t n_tiles) {
+// CTA-pair launches run as clusters of two pairs (tp_gemm_kernel's kQuad) when a tile count is
+// even and the clusters' waves, each about 4 % shorter (measured: fewer operand bytes from L2),
+// take no longer than the pairs' (fewer clusters of four than pairs fit: 36 x 4 CTAs against
+// 76 x 2 on a 152-SM GB300; e.g. 2592 SwiGLU tiles make 36 cluster waves against 35 pair
+// waves, and the clusters still win).  1 = pairs on n-adjacent tiles
+// sharing A (even n_tiles), 2 = on m-adjacent tiles sharing B (even m_tiles), 0 = pairs alone.
+// Decided before the operand maps are built: the shared operand's boxes are half as high.
+int quad_mode(bool pair, int64_t groups, int64_t m_tiles, int64_t n_tiles) {
   if (!pair) return 0;
+  if (n_tiles % 2 != 0 && m_tiles % 2 != 0) return 0;
   if (set_smem_attr<EPI_BF16, true, true>() != TP_OK) return 0;
-  if (max_active_pairs<EPI_BF16, true>(sm_count()) < 1) return 0;
-  if (n_tiles % 2 == 0) return 1;
-  if (m_tiles % 2 == 0) return 2;
-  return 0;
+  const int quads = max_active_pairs<EPI_BF16, true>(sm_count());
+  const int pairs = resident_units(true);
+  if (quads < 1 || pairs < 1) return 0;
+  const int64_t tiles = groups * m_tiles * n_tiles;
+  const int64_t waves_quad = (tiles / 2 + quads - 1) / quads, waves_pair = (tiles + pairs - 1) / pairs;
+  if (waves_quad * 24 > waves_pair * 25) return 0;
+  return (n_tiles % 2 == 0) ? 1 : 2;
 }
 
 // m-tiles per raster group.  When the A rows of every m-tile fit comfortably in L2, one group
@@ -1089,7 +1096,7 @@ tp_status tp_linear_colwise(const void* x, const void* const* w_shards, const vo
   GemmParams p{};
   const int64_t m_tiles = (T + (pair ? 2 * BM : BM) - 1) / (pair ? 2 * BM : BM);
   const int bn = (act == TP_ACT_SWIGLU) ? BN : choose_bn(n_out, tp_degree * m_tiles, resident_units(pair));
-  const int quad = quad_mode(pair, m_tiles, ceil_div(n_out, (act == TP_ACT_SWIGLU) ? BN / 2 : bn));
+  const int quad = quad_mode(pair, tp_degree, m_tiles, ceil_div(n_out, (act == TP_ACT_SWIGLU) ? BN / 2 : bn));
   p.quad = quad;
   st = make_map(&p.map_a[0], x, K, T, K, quad == 1 ? BM / 2 : BM);
   if (st != TP_OK) return st;
@@ -1219,7 +1226,7 @@ tp_status rowwise_impl(const void* const* x_shards, int64_t ldx, const void* con
   const int groups = (mode == TP_REDUCE_ACCUM) ? 1 : tp_degree;
   const int bn = choose_bn(N, groups * m_tiles, resident_units(pair));
   // (the workspace mode stays in pairs)
-  const int quad = mode == TP_REDUCE_WORKSPACE ? 0 : quad_mode(pair, m_tiles, ceil_div(N, bn));
+  const int quad = mode == TP_REDUCE_WORKSPACE ? 0 : quad_mode(pair, groups, m_tiles, ceil_div(N, bn));
   GemmParams p{};
   p.quad = quad;
   for (int r = 0; r < tp_degree; ++r) {
@@ -1365,7 +1372,7 @@ tp_status gemm_batched(int groups, const void* const* a, int64_t lda, const void
   const bool pair = use_pair(M);
   const int64_t m_tiles = (M + (pair ? 2 * BM : BM) - 1) / (pair ? 2 * BM : BM);
   const int bn = choose_bn(N, groups * m_tiles, resident_units(pair));
-  const int quad = quad_mode(pair, m_tiles, ceil_div(N, bn));
+  const int quad = quad_mode(pair, groups, m_tiles, ceil_div(N, bn));
   GemmParams p{};
   p.quad = quad;
   for (int g = 0; g < groups; ++g) {
