@@ -443,3 +443,53 @@ def test_plan_shard_many_refusal_touches_nothing():
     torch.cuda.synchronize()
     for t in outs:
         assert torch.all(t.view(torch.int16) == 7)
+
+
+# CTA-pair launches run as 4-CTA clusters whose two pairs share one operand by multicast:
+# n-adjacent tiles (shared A) when the n-tile count is even, m-adjacent tiles (shared B) when
+# only the m-tile count (256-row tiles) is even.  Shapes that take each form, several k-blocks,
+# every rank; integer inputs, so the results must equal the oracle's bit for bit.
+MULTICAST_COLWISE = [
+    (1024, 320, 2304, 2),   # 4 m-tiles, 9 n-tiles of 256: B shared
+    (1000, 192, 512, 3),    # 4 m-tiles, 2 n-tiles: A shared
+    (1536, 128, 768, 4),    # 6 m-tiles, 3 n-tiles: B shared
+]
+
+
+@pytest.mark.parametrize("shape", MULTICAST_COLWISE, ids=str)
+def test_multicast_clusters_colwise_bit_exact(shape):
+    T, K, N_r, p = shape
+    x = tp_inputs.int_bf16(131, 0, (T, K), lim=3)
+    w = tp_inputs.int_bf16(131, 1, (N_r * p, K), lim=3)
+    shards = [O.shard(w, "colwise", p, r) for r in range(p)]
+    ys = tp.tp_linear_colwise(dev(x), [dev(s) for s in shards], "none")
+    ref = O.colwise_forward(x, shards, "none")
+    for r in range(p):
+        assert np.array_equal(host_bits(ys[r]), O.f64_to_bf16(ref[r])), (shape, r)
+
+
+@pytest.mark.parametrize("T, F_r", [(768, 256), (1024, 384)], ids=str)
+def test_multicast_clusters_swiglu(T, F_r):
+    # (768, 256): 3 m-tiles, 2 n-tiles of 128 gate columns: A shared; (1024, 384): 4 m-tiles,
+    # 3 n-tiles: B shared (each pair's gate and up rows split between the two pairs).
+    p, K = 2, 256
+    x = tp_inputs.activation_bf16(132, 0, (T, K))
+    w = tp_inputs.weight_bf16(132, 1, (2 * F_r * p, K))
+    shards = [O.shard(w, "colwise", p, r, [F_r * p, F_r * p]) for r in range(p)]
+    ys = tp.tp_linear_colwise(dev(x), [dev(s) for s in shards], "swiglu")
+    ref = O.colwise_forward(x, shards, "swiglu")
+    for r in range(p):
+        assert_close(f64(ys[r]), ref[r], f"swiglu T={T} F_r={F_r} rank {r}")
+
+
+@pytest.mark.parametrize("T, N", [(1024, 1536), (1024, 1280), (2048, 768)], ids=str)
+def test_multicast_clusters_rowwise_bit_exact(T, N):
+    # 6 n-tiles: A (every rank's slice in turn) shared; 5 n-tiles, 4 m-tiles: B shared; 8 m-tiles,
+    # 3 n-tiles: B shared.  Three ranks, so the shared operand changes at each rank boundary.
+    p, K_r = 3, 320
+    x = tp_inputs.int_bf16(133, 0, (T, K_r * p), lim=3)
+    w = tp_inputs.int_bf16(133, 1, (N, K_r * p), lim=3)
+    x_sh = [O.shard(x, "rowwise", p, r) for r in range(p)]
+    w_sh = [O.shard(w, "rowwise", p, r) for r in range(p)]
+    z = tp.tp_linear_rowwise([dev(a) for a in x_sh], [dev(b) for b in w_sh], mode="accum")
+    assert np.array_equal(host_bits(z), O.f64_to_bf16(O.rowwise_forward(x_sh, w_sh))), (T, N)
