@@ -19,7 +19,9 @@ tp_degree 4, all four ranks on this GPU):
 ``value`` = the step's GEMM FLOPs (2*T*K*N summed over the projections) per
 second of device time: extraction counts as time, not as work.
 Inputs are resident in HBM when the timed region starts; L2 is flushed
-between steps (a 256 MiB write), so every step reads its operands from HBM.
+between steps (a 256 MiB write, then a 256 MiB read of another buffer), so every
+step reads its operands from HBM and inherits no dirty line of the flush to write
+back.
 The step is captured once as a CUDA graph and each timed step replays it between
 two CUDA events (``--eager`` launches every call from Python instead); a second,
 untimed pass replays each phase as its own graph with events between the phases
@@ -67,6 +69,23 @@ UNIT = "TFLOP/s"
 WORKLOAD = "attn_proj_tp4"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
 L2_FLUSH_BYTES = 256 << 20
+
+
+class L2Flush:
+    """Empties L2 between timed steps: a write larger than L2 evicts whatever the
+    last step left there, and a read of another buffer as large then evicts the
+    write's own dirty lines, so the next step starts from a cold, clean L2 (the
+    state a profiler's cache flush gives) and pays for none of the flush's
+    write-backs."""
+
+    def __init__(self, torch, device):
+        self.w = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+        self.r = torch.zeros(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+
+    def __call__(self):
+        self.w.zero_()
+        self.r.amax()
+
 
 
 # ----------------------------------------------------------------------------- distributed plumbing
@@ -1047,7 +1066,7 @@ def run_ours(args):
     phases = wl.phases()
     nph = len(phases)
     stream = torch.cuda.Stream(device)
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+    flush = L2Flush(torch, device)
     peaks = load_peaks()
 
     for _ in range(args.warmup):
@@ -1062,7 +1081,7 @@ def run_ours(args):
     host_s = 0.0
     for k in range(n_eager):
         with torch.cuda.stream(stream):
-            flush.zero_()
+            flush()
         t0 = time.perf_counter()
         run_step(wl, stream, eager_marks[k])
         host_s += time.perf_counter() - t0
@@ -1101,7 +1120,7 @@ def run_ours(args):
     t_wall0 = time.perf_counter()
     for k in range(args.steps):
         with torch.cuda.stream(stream):
-            flush.zero_()          # L2 flush between steps, outside the step's events
+            flush()          # L2 flush between steps, outside the step's events
             bounds[k][0].record(stream)
             if step_graph is not None:
                 step_graph.replay()
@@ -1135,7 +1154,7 @@ def run_ours(args):
     marks = [[torch.cuda.Event(enable_timing=True) for _ in range(nph + 1)] for _ in range(n_phase_steps)]
     for k in range(n_phase_steps):
         with torch.cuda.stream(stream):
-            flush.zero_()
+            flush()
             if graphs:
                 for i, g in enumerate(graphs):
                     marks[k][i].record(stream)
@@ -1181,7 +1200,7 @@ def run_ours(args):
         for _ in range(reps):
             s_, e_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             with torch.cuda.stream(stream):
-                flush.zero_()
+                flush()
                 s_.record(stream)
                 fn(stream)
                 e_.record(stream)
@@ -1214,7 +1233,7 @@ def run_ours(args):
             for _ in range(20):
                 s_, e_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 with torch.cuda.stream(stream):
-                    flush.zero_()
+                    flush()
                 s_.record(stream)
                 fn(stream)
                 e_.record(stream)
@@ -1253,7 +1272,7 @@ def run_ours(args):
             for _ in range(min(args.steps, 100)):
                 s_, e_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 with torch.cuda.stream(stream):
-                    flush.zero_()
+                    flush()
                     s_.record(stream)
                     run(stream)
                     e_.record(stream)
@@ -1305,7 +1324,7 @@ def run_ours(args):
     if rank == 0:
         cfg = wl.config()
         cfg.update({"parallelism": f"tp{wl.p} simulated on each GPU; replicas across GPUs",
-                    "l2": "flushed between steps (256 MiB write)",
+                    "l2": "flushed between steps (256 MiB write, then 256 MiB read)",
                     "sms": torch.cuda.get_device_properties(device).multi_processor_count})
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
