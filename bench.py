@@ -274,8 +274,8 @@ class AttnProjWorkload:
         self.flops = self.flops_qkv + self.flops_out
         self.extract_bytes = 2.0 * 2 * (3 * H * H + H * H)   # read + write of every shard
         self.gather_bytes = 2.0 * 2 * T * 3 * H
-        # The timed step (step()): two extraction launches (the QKV weight's ranks, then the
-        # out-projection's on a side stream), colwise, rowwise.  Otherwise the phases: one
+        # The timed step (step()): two extraction launches (the out-projection weight's ranks,
+        # then the QKV weight's on a side stream), rowwise, colwise.  Otherwise the phases: one
         # extraction launch, colwise, gather unless fused, rowwise (+ the counter clear of the
         # workspace mode, or the separate reduce of the unfused mode).
         if fused_gather and reduce_mode == "accum":
@@ -289,9 +289,9 @@ class AttnProjWorkload:
         return {"workload": WORKLOAD, "tokens": self.T, "hidden": self.H, "heads": self.heads, "head_dim": self.hd,
                 "tp_degree": self.p, "rowwise_reduce": self.mode,
                 "gather": "fused into the colwise store (ldy)" if self.fused_gather else "tp_combine kernel",
-                "step": "tp_plan_shard_many (fused QKV weight, 4 ranks, from device memory) + tp_linear_colwise "
-                        "writing the gathered QKV [T, 3H], with tp_plan_shard_many (out-projection weight, 4 ranks) "
-                        "on a side stream in the projection's last wave + tp_linear_rowwise"
+                "step": "tp_plan_shard_many (out-projection weight, 4 ranks, from device memory) + "
+                        "tp_linear_rowwise, with tp_plan_shard_many (fused QKV weight, 4 ranks) on a side stream "
+                        "beside it + tp_linear_colwise writing the gathered QKV [T, 3H]"
                         if self.fused_gather and self.mode == "accum" else
                         "tp_plan_shard_many (both weights, 4 ranks each) + tp_linear_colwise "
                         + ("" if self.fused_gather else "+ tp_combine(gather) ") + "+ tp_linear_rowwise"}
@@ -323,23 +323,25 @@ class AttnProjWorkload:
         self.tp.tp_plan_shard_many(list(self._extract_requests()), stream=stream)
 
     def step(self, stream):
-        """One timed step: the phases' work, with the out-projection's shards extracted on a side
-        stream, launched after the QKV projection.  They depend only on the weights, so the copy
-        runs on the SMs that the projection's last, partial wave of tiles leaves idle; the
-        out-projection waits for both."""
+        """One timed step: the phases' work in another order.  The two projections are
+        independent here (the out-projection's input is its own activation), so the smaller
+        weight's shards are extracted first and its rowwise projection runs while the QKV
+        weight's shards are extracted on a side stream, launched after it: the copy runs on
+        the SMs that the projection's clusters and its last, partial wave of tiles leave
+        idle.  The QKV projection waits for both."""
         if not (self.fused_gather and self.mode == "accum"):
             return run_step(self, stream)
         if getattr(self, "side_stream", None) is None:
             self.side_stream = self.torch.cuda.Stream(self.device)
         side = self.side_stream
         req_qkv, req_out = self._extract_requests()
-        self.tp.tp_plan_shard_many([req_qkv], stream=stream)
+        self.tp.tp_plan_shard_many([req_out], stream=stream)
         side.wait_stream(stream)
-        self.phase_colwise(stream)
-        with self.torch.cuda.stream(side):
-            self.tp.tp_plan_shard_many([req_out], stream=side)
-        stream.wait_stream(side)
         self.phase_rowwise(stream)
+        with self.torch.cuda.stream(side):
+            self.tp.tp_plan_shard_many([req_qkv], stream=side)
+        stream.wait_stream(side)
+        self.phase_colwise(stream)
 
     def phase_colwise(self, stream, x=None):
         x = self.x if x is None else x
