@@ -17,6 +17,8 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <mutex>
+
 #include <string>
 
 #include "tp_internal.h"
@@ -182,18 +184,46 @@ __global__ void __launch_bounds__(256) reduce_partials_v8(const __grid_constant_
     float acc[8];
 #pragma unroll
     for (int j = 0; j < 8; ++j) acc[j] = 0.f;
-    for (int r = 0; r < p.p; ++r) {
-      const float4* src = reinterpret_cast<const float4*>(p.part[r]) + 2 * g;
-      float4 a = __ldcs(src);
-      float4 b = __ldcs(src + 1);
-      acc[0] += a.x; acc[1] += a.y; acc[2] += a.z; acc[3] += a.w;
-      acc[4] += b.x; acc[5] += b.y; acc[6] += b.z; acc[7] += b.w;
+    // Four ranks' loads are issued before any of their sums, so a thread keeps up to 128 bytes
+    // in flight; the sums still run in rank order.
+    for (int r0 = 0; r0 < p.p; r0 += 4) {
+      float4 a[4], b[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        if (r0 + k < p.p) {
+          const float4* src = reinterpret_cast<const float4*>(p.part[r0 + k]) + 2 * g;
+          a[k] = __ldcs(src);
+          b[k] = __ldcs(src + 1);
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        if (r0 + k < p.p) {
+          acc[0] += a[k].x; acc[1] += a[k].y; acc[2] += a[k].z; acc[3] += a[k].w;
+          acc[4] += b[k].x; acc[5] += b[k].y; acc[6] += b[k].z; acc[7] += b[k].w;
+        }
+      }
     }
     __align__(16) __nv_bfloat162 o[4];
 #pragma unroll
     for (int j = 0; j < 4; ++j) o[j] = __floats2bfloat162_rn(acc[2 * j], acc[2 * j + 1]);
     reinterpret_cast<uint4*>(p.out)[g] = *reinterpret_cast<const uint4*>(o);
   }
+}
+
+// Resident blocks of 256 threads per SM for reduce_partials_v8 (its register count sets it),
+// queried once.
+int reduce_blocks_per_sm() {
+  static std::once_flag once;
+  static int blocks = 1;
+  std::call_once(once, [] {
+    int b = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, reduce_partials_v8, 256, 0) == cudaSuccess && b > 0)
+      blocks = b;
+    else
+      (void)cudaGetLastError();
+  });
+  return blocks;
 }
 
 __global__ void __launch_bounds__(256) reduce_partials_scalar(const __grid_constant__ ReduceParams p, int64_t begin) {
@@ -440,8 +470,10 @@ tp_status tp_combine(tp_combine_mode mode, const void* const* partials, int tp_d
   int64_t begin = 0;
   if (vec && p.n >= 8) {
     const int64_t groups = p.n >> 3;
+    // One wave: as many blocks as the SMs hold at once (the loop strides over the rest).
     int64_t grid = (groups + 255) / 256;
-    if (grid > static_cast<int64_t>(sms) * 8) grid = static_cast<int64_t>(sms) * 8;
+    const int64_t resident = static_cast<int64_t>(sms) * reduce_blocks_per_sm();
+    if (grid > resident) grid = resident;
     cudaError_t le = launch_pdl(reduce_partials_v8, dim3(static_cast<unsigned>(grid)), dim3(256), 0, s, p);
     if (le != cudaSuccess) return cuda_fail(le, "reduce kernel launch");
     begin = groups << 3;
