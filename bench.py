@@ -290,8 +290,8 @@ class AttnProjWorkload:
                 "tp_degree": self.p, "rowwise_reduce": self.mode,
                 "gather": "fused into the colwise store (ldy)" if self.fused_gather else "tp_combine kernel",
                 "step": "tp_plan_shard_many (out-projection weight, 4 ranks, from device memory) + "
-                        "tp_linear_rowwise, with tp_plan_shard_many (fused QKV weight, 4 ranks) on a side stream "
-                        "beside it + tp_linear_colwise writing the gathered QKV [T, 3H]"
+                        "tp_linear_rowwise, with tp_plan_shard_many (fused QKV weight, 4 ranks) + tp_linear_colwise "
+                        "writing the gathered QKV [T, 3H] on a side stream beside it"
                         if self.fused_gather and self.mode == "accum" else
                         "tp_plan_shard_many (both weights, 4 ranks each) + tp_linear_colwise "
                         + ("" if self.fused_gather else "+ tp_combine(gather) ") + "+ tp_linear_rowwise"}
@@ -328,7 +328,8 @@ class AttnProjWorkload:
         weight's shards are extracted first and its rowwise projection runs while the QKV
         weight's shards are extracted on a side stream, launched after it: the copy runs on
         the SMs that the projection's clusters and its last, partial wave of tiles leave
-        idle.  The QKV projection waits for both."""
+        idle.  The QKV projection follows its extraction on the side stream, so its CTAs
+        take SMs as the out-projection's leave them; the step ends when both are done."""
         if not (self.fused_gather and self.mode == "accum"):
             return run_step(self, stream)
         if getattr(self, "side_stream", None) is None:
@@ -340,8 +341,8 @@ class AttnProjWorkload:
         self.phase_rowwise(stream)
         with self.torch.cuda.stream(side):
             self.tp.tp_plan_shard_many([req_qkv], stream=side)
+            self.phase_colwise(side)
         stream.wait_stream(side)
-        self.phase_colwise(stream)
 
     def phase_colwise(self, stream, x=None):
         x = self.x if x is None else x
