@@ -195,12 +195,18 @@ __device__ __noinline__ bool wait_counter(const int* ctr, int target, volatile i
   }
 }
 
+// GELU with the tanh approximation, 0.5 x (1 + tanh(u)) with u = sqrt(2/pi) (x + 0.044715 x^3),
+// evaluated as x / (1 + e^(-2u)): the same function (1 + tanh(u) = 2 / (1 + e^(-2u))), one fast
+// exponential and one fast division (a reciprocal and a product) instead of a full tanh.  With
+// the correctly rounded division instead, a 64-token GELU launch ran 2.8x slower than with tanh.
+// Large negative u gives x * (1 / inf) = 0, large positive u gives x / 1 = x.
 __device__ __forceinline__ float gelu_tanh_f(float x) {
   const float k0 = 0.7978845608028654f;  // sqrt(2/pi)
   const float k1 = 0.044715f;
-  return 0.5f * x * (1.0f + tanhf(k0 * (x + k1 * x * x * x)));
+  const float u = k0 * (x + k1 * x * x * x);
+  return __fdividef(x, 1.0f + __expf(-2.0f * u));
 }
-__device__ __forceinline__ float silu_f(float x) { return x / (1.0f + __expf(-x)); }
+__device__ __forceinline__ float silu_f(float x) { return __fdividef(x, 1.0f + __expf(-x)); }
 
 // Epilogue output path.  A warp drains its 32 rows (one row per lane) in chunks:
 // 64 bf16 columns or 32 fp32 columns (128-byte rows, 4 KB per chunk), plus a
@@ -527,6 +533,16 @@ __global__ void __launch_bounds__(kThreads, 1) tp_gemm_kernel(const __grid_const
   const int unit = static_cast<int>(blockIdx.x) / kCtasPerUnit;
   const int nunits = static_cast<int>(gridDim.x) / kCtasPerUnit;
   pdl_launch_dependents();
+  if (threadIdx.x == 0) {
+    // Pull every tensor map this launch uses into the TMA descriptor cache while the
+    // prologue runs (the maps are launch parameters, not the previous kernel's output), so
+    // neither the first copy nor a switch of rank inside a tile waits on a descriptor fetch.
+    const int nmaps = (p.n_ksegs > 1) ? p.n_ksegs : p.n_groups;
+    for (int r = 0; r < nmaps; ++r) {
+      ptx::prefetch_tensormap(&p.map_b[r]);
+      if (!p.a_shared || r == 0) ptx::prefetch_tensormap(&p.map_a[r]);
+    }
+  }
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
@@ -569,13 +585,6 @@ __global__ void __launch_bounds__(kThreads, 1) tp_gemm_kernel(const __grid_const
   if (warp == 0) {
     if (lane == 0) {
       // ------------------------------------------------------------ producer
-      // Pull every tensor map this launch uses into the TMA descriptor cache up
-      // front, so switching ranks inside a tile does not stall on a descriptor fetch.
-      const int nmaps = (p.n_ksegs > 1) ? p.n_ksegs : p.n_groups;
-      for (int r = 0; r < nmaps; ++r) {
-        ptx::prefetch_tensormap(&p.map_b[r]);
-        if (!p.a_shared || r == 0) ptx::prefetch_tensormap(&p.map_a[r]);
-      }
       uint32_t it = 0;
       bool ok = true;
       for (int t = unit; t < total && ok; t += nunits) {
