@@ -351,8 +351,7 @@ def combine_reduce(parts: Sequence[np.ndarray]) -> np.ndarray:
 # Attention over a rank's local heads
 # ---------------------------------------------------------------------------
 
-def attention_core(q: np.ndarray, k: np.ndarray, v: np.ndarray, n_heads: int, head_dim: int,
-                   store_p_bf16: bool = False) -> np.ndarray:
+def attention_core(q: np.ndarray, k: np.ndarray, v: np.ndarray, n_heads: int, head_dim: int) -> np.ndarray:
     """softmax(Q_h K_h^T / sqrt(d)) V_h for each of the rank's local heads, float64.
 
     "Tensor parallelism" page, §Colwise and rowwise: colwise Q, K and V give
@@ -361,11 +360,9 @@ def attention_core(q: np.ndarray, k: np.ndarray, v: np.ndarray, n_heads: int, he
     embedding, no QK-norm (norms are replicated and left out of the plan,
     §What to leave out), scale 1/sqrt(head_dim), max-subtracted softmax, head j
     occupying columns [j*d, (j+1)*d) of each of Q, K, V.  ``q`` may hold only
-    some query rows; ``k`` and ``v`` hold every token.
-
-    ``store_p_bf16``: round the probabilities to bf16 before the product with
-    V, for a path that stores them in bf16 (the bf16-storage reading: every
-    tensor a path materialises is bf16).  Off, the result is exact.
+    some query rows; ``k`` and ``v`` hold every token.  The probabilities are
+    never rounded: the pages fix no storage for them, so this is the plain
+    definition, exact in float64.
     """
     q = np.asarray(q, dtype=np.float64)
     k = np.asarray(k, dtype=np.float64)
@@ -378,8 +375,6 @@ def attention_core(q: np.ndarray, k: np.ndarray, v: np.ndarray, n_heads: int, he
         s = s - s.max(axis=1, keepdims=True)
         e = np.exp(s)
         pr = e / e.sum(axis=1, keepdims=True)
-        if store_p_bf16:
-            pr = bf16_to_f64(f64_to_bf16(pr))
         out[:, cols] = pr @ v[:, cols]
     return out
 
@@ -408,13 +403,14 @@ def mlp_forward(x_bits, w_in_shards, w_out_shards, act: str):
 
 
 def attention_block_forward(x_bits, wqkv_shards, wout_shards, n_local_heads: int, head_dim: int,
-                            q_rows: np.ndarray | None = None, store_p_bf16: bool = True):
+                            q_rows: np.ndarray | None = None):
     """QKV colwise -> per-rank attention -> out-projection rowwise + sum.
 
     Returns (qkv_bits per rank, o_bits per rank, Z float64).  With ``q_rows``
     only those token rows are computed for the query side (K and V always use
-    every token), which is exact for those rows.  The attention probabilities
-    are stored in bf16 like every other tensor of the path (``store_p_bf16``).
+    every token), which is exact for those rows.  Q, K, V and the attention
+    output are stored in bf16 like every tensor the path stores; the
+    probabilities are exact (``attention_core``).
     """
     width = n_local_heads * head_dim
     qkv = [f64_to_bf16(y) for y in colwise_forward(x_bits, wqkv_shards, "none")]
@@ -424,14 +420,13 @@ def attention_block_forward(x_bits, wqkv_shards, wout_shards, n_local_heads: int
         if q_rows is not None:
             qb = qb[q_rows]
         o.append(f64_to_bf16(attention_core(bf16_to_f64(qb), bf16_to_f64(kb), bf16_to_f64(vb),
-                                            n_local_heads, head_dim, store_p_bf16=store_p_bf16)))
+                                            n_local_heads, head_dim)))
     z = rowwise_forward(o, wout_shards)
     return qkv, o, z
 
 
 def transformer_block_forward(x_bits, wqkv_shards, wout_shards, wgu_shards, wdown_shards,
-                              n_local_heads: int, head_dim: int, q_rows: np.ndarray | None = None,
-                              store_p_bf16: bool = True):
+                              n_local_heads: int, head_dim: int, q_rows: np.ndarray | None = None):
     """Attention + SwiGLU MLP block, both halves sharded colwise -> rowwise.
 
     x -> QKV (colwise) -> attention over local heads -> out-projection
@@ -441,15 +436,14 @@ def transformer_block_forward(x_bits, wqkv_shards, wout_shards, wgu_shards, wdow
     intermediates and the unrounded final output ``z``.
     """
     qkv, o, z1 = attention_block_forward(x_bits, wqkv_shards, wout_shards, n_local_heads, head_dim,
-                                         q_rows=q_rows, store_p_bf16=store_p_bf16)
+                                         q_rows=q_rows)
     z1_bits = f64_to_bf16(z1)
     h, z2 = mlp_forward(z1_bits, wgu_shards, wdown_shards, "swiglu")
     return dict(qkv=qkv, o=o, z1=z1, z1_bits=z1_bits, h=h, z=z2)
 
 
 def single_stream_block_forward(x_bits, w_in_shards, w_out_shards, n_local_heads: int, head_dim: int,
-                                q_rows: np.ndarray | None = None, store_p_bf16: bool = True,
-                                with_abs_v: bool = False):
+                                q_rows: np.ndarray | None = None):
     """Single-stream block: one fused colwise in-projection and one packed rowwise out-projection.
 
     "Tensor parallelism" page, §Fused projections: [1, 1, 1, 3, 3] packs Q, K,
@@ -462,9 +456,7 @@ def single_stream_block_forward(x_bits, w_in_shards, w_out_shards, n_local_heads
     its packed to_out shard -- feeds the rowwise projection; the partials are
     summed.  Returns a dict: per-rank attention output "o" (float64, before its
     bf16 storage) and "o_bits" (stored), per-rank SwiGLU output "h" and
-    "h_bits" likewise, and the final "z" (float64).  ``with_abs_v`` adds
-    "o_abs_v": the same attention over |V| (exact probabilities), the scale of
-    the error that storing the probabilities in bf16 introduces.
+    "h_bits" likewise, and the final "z" (float64).
     """
     width = n_local_heads * head_dim
     rows = x_bits if q_rows is None else x_bits[q_rows]
@@ -476,12 +468,8 @@ def single_stream_block_forward(x_bits, w_in_shards, w_out_shards, n_local_heads
         kv = y[:, width:3 * width] if q_rows is None else colwise_forward(x_bits, [w[width:3 * width]], "none")[0]
         qb = f64_to_bf16(y[:, :width])
         kb, vb = f64_to_bf16(kv[:, :width]), f64_to_bf16(kv[:, width:])
-        o = attention_core(bf16_to_f64(qb), bf16_to_f64(kb), bf16_to_f64(vb), n_local_heads, head_dim,
-                           store_p_bf16=store_p_bf16)
+        o = attention_core(bf16_to_f64(qb), bf16_to_f64(kb), bf16_to_f64(vb), n_local_heads, head_dim)
         h = apply_act(y[:, 3 * width:], "swiglu")
-        if with_abs_v:
-            res.setdefault("o_abs_v", []).append(
-                attention_core(bf16_to_f64(qb), bf16_to_f64(kb), np.abs(bf16_to_f64(vb)), n_local_heads, head_dim))
         ob, hb = f64_to_bf16(o), f64_to_bf16(h)
         for k, v in (("o", o), ("o_bits", ob), ("h", h), ("h_bits", hb)):
             res[k].append(v)

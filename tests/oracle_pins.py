@@ -397,35 +397,6 @@ def pin_attention():
     assert np.allclose(O.attention_core(q2, k2, v2, h2, d3), ref, rtol=1e-12, atol=1e-13)
 
 
-def pin_attention_p_storage():
-    # Rounding the probabilities to bf16: brute force with the rounding done by hand
-    # (torch's float32 -> bf16 conversion of each probability), and within half a bf16
-    # ulp of the exact attention times sum|P V| per element.
-    rng = np.random.default_rng(53)
-    T, h, d = 6, 2, 4
-    q, k, v = (rng.standard_normal((T, h * d)) for _ in range(3))
-    got = O.attention_core(q, k, v, h, d, store_p_bf16=True)
-    out = np.zeros((T, h * d))
-    for j in range(h):
-        c = slice(j * d, (j + 1) * d)
-        for t in range(T):
-            s_ = [float(q[t, c] @ k[u, c]) / math.sqrt(d) for u in range(T)]
-            m = max(s_)
-            e = [math.exp(x - m) for x in s_]
-            z = sum(e)
-            pr = np.array([float(torch.tensor(x / z, dtype=torch.float64).to(torch.bfloat16).to(torch.float64))
-                           for x in e])
-            out[t, c] = pr @ v[:, c]
-    assert np.allclose(got, out, rtol=1e-12, atol=1e-14)
-    exact = O.attention_core(q, k, v, h, d)
-    bound = np.zeros_like(exact)
-    for j in range(h):
-        c = slice(j * d, (j + 1) * d)
-        bound[:, c] = 2.0 ** -8 * (np.ones((T, T)) @ np.abs(v[:, c]))
-    assert np.all(np.abs(got - exact) <= bound + 1e-12)
-    assert not np.allclose(got, exact, rtol=1e-9, atol=0)   # the rounding is really applied
-
-
 def pin_block_tp_invariance():
     # The sharded block at tp_degree p equals the block at tp_degree 1 (the plain
     # layer) up to float64 reassociation and the bf16 storage between steps.
@@ -440,15 +411,9 @@ def pin_block_tp_invariance():
             wgu_shards=[O.shard(wgu, O.COLWISE, p, r, [F, F]) for r in range(p)],
             wdown_shards=[O.shard(wdown, O.ROWWISE, p, r) for r in range(p)],
         )
-        # Exact attention here (store_p_bf16=False): the reference below is torch's exact SDPA.
-        res = O.transformer_block_forward(x, n_local_heads=h // p, head_dim=d, store_p_bf16=False, **sh)
-        res_p = O.transformer_block_forward(x, n_local_heads=h // p, head_dim=d, **sh)
-        if ref is not None:
-            rms_p = math.sqrt(float(np.mean(ref_p["z"] ** 2)))
-            assert np.max(np.abs(res_p["z"] - ref_p["z"])) <= 1e-2 * rms_p, p
+        res = O.transformer_block_forward(x, n_local_heads=h // p, head_dim=d, **sh)
         if ref is None:
             ref = res
-            ref_p = res_p
             # tp=1: independent plain computation from torch ops in float64.
             xf = torch.from_numpy(O.bf16_to_f64(x))
             wq = torch.from_numpy(O.bf16_to_f64(wqkv))
@@ -474,8 +439,7 @@ def pin_block_tp_invariance():
             for r in range(p):
                 full = ref["qkv"][0]
                 cols = np.concatenate([np.arange(j * H + r * Hp, j * H + (r + 1) * Hp) for j in range(3)])
-                assert np.array_equal(res["qkv"][r], full[:, cols]) or \
-                    np.max(np.abs(O.bf16_to_f64(res["qkv"][r]) - O.bf16_to_f64(full[:, cols]))) < 1e-2
+                assert np.array_equal(res["qkv"][r], full[:, cols]), (p, r)
 
 
 def pin_single_stream_block():
@@ -490,7 +454,7 @@ def pin_single_stream_block():
     for p in (1, 2, 3, 6):
         win = [O.shard(w_in, O.COLWISE, p, r, [H, H, H, F, F], num_heads=h, head_dim=0) for r in range(p)]
         wout = [O.shard(w_out, O.ROWWISE, p, r, [H, F]) for r in range(p)]
-        res[p] = O.single_stream_block_forward(x, win, wout, h // p, d, store_p_bf16=False)["z"]
+        res[p] = O.single_stream_block_forward(x, win, wout, h // p, d)["z"]
     xt = torch.from_numpy(O.bf16_to_f64(x))
     y = xt @ torch.from_numpy(O.bf16_to_f64(w_in)).T
     qkv = torch.from_numpy(O.bf16_to_f64(O.f64_to_bf16(y[:, :3 * H].numpy())))
@@ -545,5 +509,5 @@ def pin_safetensors_reader():
 
 ALL_PINS = [pin_bf16_rounding, pin_plan_rejections, pin_packed_blocks, pin_shard_golden, pin_shard_reassembly,
             pin_whole_heads, pin_linear_bruteforce, pin_activations, pin_colwise_concat, pin_swiglu_packed,
-            pin_rowwise_sum, pin_rowwise_split_input, pin_combine, pin_attention, pin_attention_p_storage, pin_block_tp_invariance,
+            pin_rowwise_sum, pin_rowwise_split_input, pin_combine, pin_attention, pin_block_tp_invariance,
             pin_single_stream_block, pin_safetensors_reader]

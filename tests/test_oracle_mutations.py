@@ -102,15 +102,26 @@ def _attention_wrong_axis(q, k, v, n_heads, head_dim):
     return out
 
 
+def _attention_p_rounded_bf16(q, k, v, n_heads, head_dim):
+    # Rounds the probabilities to bf16 before the product with V.
+    q, k, v = (np.asarray(a, dtype=np.float64) for a in (q, k, v))
+    out = np.empty((q.shape[0], n_heads * head_dim))
+    for j in range(n_heads):
+        c = slice(j * head_dim, (j + 1) * head_dim)
+        s = q[:, c] @ k[:, c].T / np.sqrt(head_dim)
+        e = np.exp(s - s.max(axis=1, keepdims=True))
+        out[:, c] = O.bf16_to_f64(O.f64_to_bf16(e / e.sum(axis=1, keepdims=True))) @ v[:, c]
+    return out
+
+
 def _gather_wrong_axis(parts):
     return np.concatenate(list(parts), axis=0)
 
 
-def _single_stream_concat_swapped(x_bits, w_in_shards, w_out_shards, n_local_heads, head_dim, q_rows=None,
-                                  store_p_bf16=True):
+def _single_stream_concat_swapped(x_bits, w_in_shards, w_out_shards, n_local_heads, head_dim, q_rows=None):
     # Feeds [mlp, attention] to the packed out-projection instead of [attention, mlp].
     res = _orig["single_stream_block_forward"](x_bits, w_in_shards, w_out_shards, n_local_heads, head_dim,
-                                               q_rows=q_rows, store_p_bf16=store_p_bf16)
+                                               q_rows=q_rows)
     res["z"] = O.rowwise_forward([np.concatenate([h, o], axis=1) for o, h in zip(res["o_bits"], res["h_bits"])],
                                  w_out_shards)
     return res
@@ -153,6 +164,7 @@ MUTATIONS = {
     "rowwise_drops_a_partial": ("rowwise_forward", _rowwise_drop_rank0),
     "attention_no_scale": ("attention_core", _attention_no_scale),
     "attention_softmax_wrong_axis": ("attention_core", _attention_wrong_axis),
+    "attention_p_rounded_bf16": ("attention_core", _attention_p_rounded_bf16),
     "gather_wrong_axis": ("combine_gather", _gather_wrong_axis),
     "single_stream_concat_swapped": ("single_stream_block_forward", _single_stream_concat_swapped),
 }
