@@ -10,11 +10,15 @@
 // head_dim 128 runs the fused kernel of tp_flash.cu (scores and probabilities
 // stay on chip).  Other head sizes take these steps, per batch of up to 16 heads:
 //   1. S_h = Q_h . K_h^T   -- batched tcgen05 GEMM, fp32 scores [T, T];
-//   2. P_h = softmax(S_h / sqrt(d)) row by row, fp32 math, written as bf16
-//      over the first half of each score row (one warp per row);
-//   3. O_h = P_h . V_h     -- batched tcgen05 GEMM with B = V_h^T (V is
-//      transposed once per call), bf16 written straight into the rank's
-//      attention output columns [h*d, (h+1)*d).
+//   2. P_h = softmax(S_h / sqrt(d)) row by row, fp32 math, written over its own
+//      score row as two bf16 terms, P = P_hi + P_lo with P_hi = bf16(P) and
+//      P_lo = bf16(P - P_hi) (P to about 2^-17 relative; one bf16 term would
+//      carry 2^-9): each group of 8 scores becomes its 8 P_hi then its 8 P_lo
+//      (one warp per row);
+//   3. O_h = P_h . V_h     -- batched tcgen05 GEMM over K = 2T with B = V_h^T in
+//      the same order (V is transposed once per call, every group of 8 keys
+//      written twice), so one product sums P_hi V + P_lo V; bf16 written
+//      straight into the rank's attention output columns [h*d, (h+1)*d).
 // The score matrices are memory traffic (about 10 bytes per score); a fused
 // kernel that keeps S and P on chip is the next step for this path.
 #include <cuda_bf16.h>
@@ -29,8 +33,10 @@ namespace {
 
 constexpr int kHeadBatch = TP_MAX_DEGREE;
 
-// Vt_r[j][t] = V_r[t][j] for t < T, j < width, for every rank r = blockIdx.z (one launch for
-// all ranks): V_r is [T, width] with row stride ld_v elements, Vt_r dense [width, T].
+// The transpose of V with every group of 8 keys written twice, for the two-term P.V product:
+// Vt_r[j][16c + i] = Vt_r[j][16c + 8 + i] = V_r[8c + i][j] for keys t = 8c + i < T and
+// j < width, for every rank r = blockIdx.z (one launch for all ranks): V_r is [T, width] with
+// row stride ld_v elements, Vt_r dense [width, 2T].
 struct TransposeRanks {
   const __nv_bfloat16* v[TP_MAX_DEGREE];
   __nv_bfloat16* vt[TP_MAX_DEGREE];
@@ -64,7 +70,10 @@ __global__ void __launch_bounds__(256) transpose_ranks_bf16(const __grid_constan
       __nv_bfloat162 pr;
       pr.x = tile[2 * lane][wy + k];
       pr.y = tile[2 * lane + 1][wy + k];
-      *reinterpret_cast<__nv_bfloat162*>(vt + j * p.T + t) = pr;
+      // t is even, so t and t + 1 share a group of 8; the pair is 4-byte aligned.
+      __nv_bfloat162* dst = reinterpret_cast<__nv_bfloat162*>(vt + j * 2 * p.T + 2 * t - (t & 7));
+      dst[0] = pr;
+      dst[4] = pr;
     }
   }
 }
@@ -88,12 +97,12 @@ tp_status transpose_ranks(int n_ranks, const __nv_bfloat16* const* v, int64_t ld
   return TP_OK;
 }
 
-// Row softmax of fp32 scores scaled by `scale`, written as bf16 over the first
-// half of the same row (row i of P starts at byte 4*T*i).  One warp per row;
-// pass 1 keeps a running (max, sum of exponentials) per lane and merges them
-// across the warp, pass 2 writes exp(scale*(s - max)) / sum.  A warp reads a
-// 256-element piece (all lanes) before any lane writes the 512 bytes of P that
-// overlay its first half, so no score is overwritten before it is read.
+// Row softmax of fp32 scores scaled by `scale`, written over the same row as two bf16
+// terms: the 32 bytes of scores 8c..8c+7 become P_hi of those keys (8 bf16) followed by
+// their P_lo (8 bf16), P_hi = bf16(P), P_lo = bf16(P - P_hi).  One warp per row; pass 1
+// keeps a running (max, sum of exponentials) per lane and merges them across the warp,
+// pass 2 writes P = exp(scale*(s - max)) / sum.  Each lane overwrites exactly the 32
+// bytes it has just read, so no score is overwritten before it is read.
 __global__ void __launch_bounds__(256) softmax_rows_inplace(float* s, int64_t rows, int T, float scale_log2e) {
   const int lane = threadIdx.x & 31;
   const int64_t row = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
@@ -123,24 +132,26 @@ __global__ void __launch_bounds__(256) softmax_rows_inplace(float* s, int64_t ro
   __nv_bfloat16* prow = reinterpret_cast<__nv_bfloat16*>(srow);
   for (int base = 0; base < T; base += 256) {
     const int i = base + lane * 8;
-    float x[8];
     if (i < T) {
+      float x[8];
       const float4 a = *reinterpret_cast<const float4*>(srow + i);
       const float4 b = *reinterpret_cast<const float4*>(srow + i + 4);
       x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w; x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
-    }
-    __syncwarp();  // every lane's reads of this piece happen before any lane's writes
-    if (i < T) {
-      uint32_t pk[4];
+      uint32_t hi[4], lo[4];
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
-        __nv_bfloat162 h = __floats2bfloat162_rn(exp2f((x[2 * k] - m) * scale_log2e) * inv,
-                                                 exp2f((x[2 * k + 1] - m) * scale_log2e) * inv);
-        pk[k] = *reinterpret_cast<uint32_t*>(&h);
+        const float p0 = exp2f((x[2 * k] - m) * scale_log2e) * inv;
+        const float p1 = exp2f((x[2 * k + 1] - m) * scale_log2e) * inv;
+        __nv_bfloat162 h = __floats2bfloat162_rn(p0, p1);
+        hi[k] = *reinterpret_cast<uint32_t*>(&h);
+        // bf16 -> fp32 is exact, so p - P_hi is the exact residual before its own rounding.
+        __nv_bfloat162 r = __floats2bfloat162_rn(p0 - __bfloat162float(h.x), p1 - __bfloat162float(h.y));
+        lo[k] = *reinterpret_cast<uint32_t*>(&r);
       }
-      *reinterpret_cast<uint4*>(prow + i) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+      uint4* dst = reinterpret_cast<uint4*>(prow + 2 * static_cast<int64_t>(i));
+      dst[0] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+      dst[1] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
     }
-    __syncwarp();
   }
 }
 
@@ -164,7 +175,7 @@ tp_status attention_unfused(const void* qkv, int64_t ld_qkv, int64_t T, int n_he
   const __nv_bfloat16* k = q + width;
   const __nv_bfloat16* v = q + 2 * width;
   __nv_bfloat16* o = static_cast<__nv_bfloat16*>(out);
-  // V^T once for all heads: [width, T].
+  // V^T once for all heads, each group of 8 keys twice: [width, 2T].
   tp_status ts = transpose_ranks(1, &v, ld_qkv, &vt, T, width, s);
   if (ts != TP_OK) return ts;
   for (int h0 = 0; h0 < n_heads; h0 += kHeadBatch) {
@@ -180,19 +191,19 @@ tp_status attention_unfused(const void* qkv, int64_t ld_qkv, int64_t T, int n_he
     }
     tp_status st = gemm_batched(nb, a, ld_qkv, b, ld_qkv, c, T, true, T, T, head_dim, s);
     if (st != TP_OK) return st;
-    // 2. Softmax rows in place: P (bf16, row stride 2T elements) over S.
+    // 2. Softmax rows in place: P as P_hi/P_lo groups (bf16, row stride 2T elements) over S.
     const int64_t rows = static_cast<int64_t>(nb) * T;
     softmax_rows_inplace<<<static_cast<unsigned>((rows + 7) / 8), 256, 0, s>>>(scores, rows, static_cast<int>(T),
                                                                                 scale_log2e);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "softmax launch");
-    // 3. O_h = P_h . V_h, B = V_h^T [head_dim, T].
+    // 3. O_h = P_h . V_h = P_hi V_h + P_lo V_h: K = 2T, B = V_h^T with doubled key groups [head_dim, 2T].
     for (int j = 0; j < nb; ++j) {
       a[j] = scores + static_cast<int64_t>(j) * T * T;  // bf16 view: row stride 2T elements
-      b[j] = vt + static_cast<int64_t>(h0 + j) * head_dim * T;
+      b[j] = vt + static_cast<int64_t>(h0 + j) * head_dim * 2 * T;
       c[j] = o + static_cast<int64_t>(h0 + j) * head_dim;
     }
-    st = gemm_batched(nb, a, 2 * T, b, T, c, ldo, false, T, head_dim, T, s);
+    st = gemm_batched(nb, a, 2 * T, b, 2 * T, c, ldo, false, T, head_dim, 2 * T, s);
     if (st != TP_OK) return st;
   }
   return TP_OK;
@@ -249,7 +260,7 @@ size_t tp_attention_ranks_workspace_bytes(int n_ranks, int64_t T, int n_heads, i
   if (head_dim == 128) return 0;  // the fused kernel reads Q, K and V in place
   const size_t hb = static_cast<size_t>(n_heads < tp::kHeadBatch ? n_heads : tp::kHeadBatch);
   return tp::align256(hb * static_cast<size_t>(T) * static_cast<size_t>(T) * 4) +
-         tp::align256(static_cast<size_t>(n_heads) * static_cast<size_t>(head_dim) * static_cast<size_t>(T) * 2);
+         tp::align256(static_cast<size_t>(n_heads) * static_cast<size_t>(head_dim) * static_cast<size_t>(T) * 4);
 }
 
 tp_status tp_attention_heads(const void* qkv, int64_t ld_qkv, int64_t T, int n_heads, int head_dim, void* workspace,

@@ -15,9 +15,11 @@
 //                keys, each through its own 2-stage ring (128-byte swizzle).
 //   warp 1       one thread issues tcgen05.mma.  For tile g (0, 1) and key tile j:
 //                  S_g = Q_g K_j^T        into TMEM columns [128g, 128g+128)
-//                  O_g += P_g V_j         P_g read from TMEM (the first 64 columns
-//                                         of S_g's region, bf16 pairs), O_g in
-//                                         columns [256+128g, 256+128g+128).
+//                  O_g += P_g V_j         P_g read from TMEM as two bf16 terms,
+//                                         P_hi (the first 64 columns of S_g's
+//                                         region, bf16 pairs) and P_lo (the last
+//                                         64), two products into O_g in columns
+//                                         [256+128g, 256+128g+128).
 //                Per tile the order is PV_g(j), then S_g(j+1): S_g(j+1) may only
 //                overwrite P_g(j) after PV_g(j) read it, which the tensor core's
 //                in-order execution of one thread's MMAs guarantees.
@@ -28,8 +30,8 @@
 //                running max m by more than 8 (log2 units), m is raised and O
 //                and l rescale by 2^(m_old - m_new) (the whole warp does the TMEM
 //                read-modify-write when any of its rows needs it); P =
-//                2^(s*scale*log2e - m) rounded to bf16 and stored to TMEM; l +=
-//                sum of the unrounded P.  Finally O / l in bf16, staged in the
+//                2^(s*scale*log2e - m) stored to TMEM as P_hi = bf16(P) and
+//                P_lo = bf16(P - P_hi); l += sum of the unrounded P.  Finally O / l in bf16, staged in the
 //                tile's (now idle) Q buffer and written by TMA stores.
 // Keys past the end of the sequence are masked (weight 0); queries past it are
 // computed on zero rows and clipped by the store.  Every wait is bounded (~2 s);
@@ -178,24 +180,37 @@ __device__ __forceinline__ void softmax_tile(uint32_t (&sv)[FK], int j, int T, f
     }
     l *= alpha;
   }
-  // P = 2^(s*k - m) as bf16 pairs into the first 64 columns of S_g's region; l += sum(P)
-  // (the unrounded values, four independent chains).  Masked keys give 2^-inf = 0.
+  // P = 2^(s*k - m) as two bf16 terms, P = P_hi + P_lo: P_hi = bf16(P) as pairs into the
+  // first 64 columns of S_g's region, P_lo = bf16(P - P_hi) into the last 64 (the residual
+  // P - P_hi is exact in fp32, so P_hi + P_lo carries P to about 2^-17 relative instead of
+  // the 2^-9 of one bf16 term); l += sum(P) (the unrounded values, four independent
+  // chains).  Masked keys give 2^-inf = 0 in both terms.
   const uint64_t k2 = f2(k, k), nm2 = f2(-m, -m);
   uint64_t ls[4] = {f2(0.f, 0.f), f2(0.f, 0.f), f2(0.f, 0.f), f2(0.f, 0.f)};
 #pragma unroll
   for (int half = 0; half < 2; ++half) {
     // Packed in place: the pair for column t comes from entries 2t, 2t+1 (>= t), so
-    // entry t of this half is already consumed when it is overwritten.
+    // entry t of this half is already consumed when it is overwritten.  The whole row of
+    // S is in registers, so the P_lo stores may overwrite S columns 64..127 in TMEM.
     uint32_t* pk = &sv[64 * half];
 #pragma unroll
-    for (int t = 0; t < 32; ++t) {
-      const uint64_t x2 = fma2(f2(__uint_as_float(sv[64 * half + 2 * t]), __uint_as_float(sv[64 * half + 2 * t + 1])),
-                               k2, nm2);
-      float x0, x1;
-      f2_split(x2, x0, x1);
-      const float p0 = ex2(x0), p1 = ex2(x1);
-      ls[t & 3] = add2(ls[t & 3], f2(p0, p1));
-      pk[t] = pack_bf16(p0, p1);
+    for (int t8 = 0; t8 < 32; t8 += 8) {
+      uint32_t lo[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int t = t8 + u;
+        const uint64_t x2 = fma2(
+            f2(__uint_as_float(sv[64 * half + 2 * t]), __uint_as_float(sv[64 * half + 2 * t + 1])), k2, nm2);
+        float x0, x1;
+        f2_split(x2, x0, x1);
+        const float p0 = ex2(x0), p1 = ex2(x1);
+        ls[t & 3] = add2(ls[t & 3], f2(p0, p1));
+        const uint32_t hi = pack_bf16(p0, p1);
+        pk[t] = hi;
+        // bf16 -> fp32 is exact: the low half of the pair is p0's, the high half p1's.
+        lo[u] = pack_bf16(p0 - __uint_as_float(hi << 16), p1 - __uint_as_float(hi & 0xffff0000u));
+      }
+      ptx::tmem_st_32x32b_x8(s_addr + 64 + 32 * half + t8, lo);
     }
     ptx::tmem_st_32x32b_x32(s_addr + 32 * half, *reinterpret_cast<uint32_t(*)[32]>(pk));
   }
@@ -353,10 +368,11 @@ __global__ void __launch_bounds__(kThreads, 1) tp_flash_kernel(const __grid_cons
         // 8-key groups 1024 B apart (SBO); 16 keys per MMA = 2048 B of rows.
         const uint32_t vb = sbase + OFF_V + (j % VS) * 2 * SUB;
         const uint64_t vdesc = ptx::sw128_mnmajor_desc(vb, SUB, 1024);
+        // O_g += P_hi V, then O_g += P_lo V (P_lo in columns 64..127 of the region).
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          ptx::umma_bf16_ts(tmem + 2 * FK + g * FD, tmem + g * FK + kk * 8, vdesc + kk * (2048u >> 4), idesc_pv,
-                            (j > 0 || kk > 0) ? 1u : 0u);
+        for (int kk = 0; kk < 16; ++kk)
+          ptx::umma_bf16_ts(tmem + 2 * FK + g * FD, tmem + g * FK + kk * 8, vdesc + (kk & 7) * (2048u >> 4),
+                            idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
       };
       bool ok = fwait(ptx::smem_addr(&ctl->q_full), 0, abort_flag, p.status) &&
                 fwait(ptx::smem_addr(&ctl->k_full[0]), 0, abort_flag, p.status);
