@@ -317,9 +317,18 @@ TP_API size_t tp_rowwise_workspace_bytes(int tp_degree, int64_t T, int64_t N, tp
  * Limits: the call is refused with TP_ERR_WORKSPACE, before any device work,
  * when tp_rowwise_workspace_bytes(tp_degree, T, N, TP_REDUCE_WORKSPACE)
  * exceeds TP_NOALLOC_SCRATCH_BYTES (roughly tp_degree * T * N <= 16M).
- * The first call on a device looks up the array's device address (once per
- * device, with that device current); make that first call before any stream
- * capture.  No allocation happens in this call or the ones it makes.
+ * When the memory is claimed: the array belongs to the library's GEMM
+ * module, and the CUDA driver claims its device memory when it loads that
+ * module on a device -- with lazy module loading (the default) at the first
+ * call on that device that launches one of the library's GEMMs or looks the
+ * array up (this call).  A caller whose memory pool will claim the device's
+ * free memory should make one call of this entry point on each device (any
+ * small problem, e.g. T = 1) before the pool does; from then on no call
+ * claims memory.
+ * The first call on a device (and the first in a new CUDA context, e.g.
+ * after cudaDeviceReset) looks up the array's device address with that
+ * device current; make that first call before any stream capture.  No
+ * allocation happens in this call or the ones it makes.
  * Every call uses the same array and it keeps the last call's contents; the
  * call clears the tile counters itself.  Calls whose kernels overlap on the
  * GPU (other streams, other threads) race on the array: serialise them.
@@ -348,9 +357,12 @@ TP_API tp_status tp_linear_rowwise_noalloc(const void* const* x_shards, const vo
  * workspace: device buffer of tp_attention_workspace_bytes(T, n_heads,
  *       head_dim) bytes, owned by the caller; none (NULL, 0) at head_dim 128,
  *       where the fused kernel reads Q, K and V in place; for other head
- *       sizes V^T and the fp32 scores of up to 16 heads at a time.
- * Scores and softmax are fp32; the probabilities are rounded to bf16 for the
- * P.V product (fp32 accumulation); O is rounded to bf16.
+ *       sizes V^T (each group of 8 keys twice) and the fp32 scores of up to
+ *       16 heads at a time.
+ * Scores and softmax are fp32; the probabilities enter the P.V product (fp32
+ * accumulation) as two bf16 terms, P_hi = bf16(P) and P_lo = bf16(P - P_hi),
+ * which carry P to about 2^-17 relative (one bf16 term would carry 2^-9, an
+ * error that the block's later bf16 roundings amplify); O is rounded to bf16.
  * Alignment (TP_ERR_ALIGNMENT): T, head_dim, ld_qkv, ldo multiples of 8, pointers
  * 16-byte aligned.  T == 0 enqueues nothing.  TP_ERR_WORKSPACE if too small.
  */
@@ -414,6 +426,24 @@ TP_API const char* tp_status_name(tp_status status);
  * reported an error, TP_OK otherwise.
  */
 TP_API tp_status tp_device_status(tp_stream_t stream);
+
+/*
+ * tp_set_tile_wait_limit_ns -- how long a CTA of a TP_REDUCE_WORKSPACE call
+ * waits for the other ranks' partials of its output tile (the one wait of the
+ * library on other CTAs) before it gives up: it then records TP_ERR_TIMEOUT
+ * for tp_device_status, skips its share of the tile's sums, drains its copies
+ * and MMAs and exits.  The output of such a call is not valid.  0 restores
+ * the default of 2 s.  The value is read when a call enqueues its kernel, so
+ * it applies to calls made after this one (and a captured CUDA graph keeps the
+ * value of its capture).  Process-wide; the waits of a CTA on its own copies
+ * and MMAs keep a fixed bound of 2 s.  Exists so that the give-up path can be
+ * exercised: a budget far below the time the ranks of a tile take to arrive
+ * makes the wait run out without any fault.
+ */
+TP_API void tp_set_tile_wait_limit_ns(uint64_t ns);
+
+/* The current tile-wait bound in nanoseconds (see tp_set_tile_wait_limit_ns). */
+TP_API uint64_t tp_tile_wait_limit_ns(void);
 
 /* Library ABI version (major * 100 + minor). */
 TP_API int tp_abi_version(void);

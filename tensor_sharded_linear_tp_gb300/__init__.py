@@ -70,6 +70,8 @@ _SIGS = {
     "tp_status_name": (ctypes.c_char_p, [ctypes.c_int]),
     "tp_device_status": (_status, [_vp]),
     "tp_abi_version": (ctypes.c_int, []),
+    "tp_set_tile_wait_limit_ns": (None, [ctypes.c_uint64]),
+    "tp_tile_wait_limit_ns": (ctypes.c_uint64, []),
     # include/tp_safetensors.h
     "tp_st_dtype_size": (ctypes.c_size_t, [ctypes.c_int]),
     "tp_st_open": (_status, [ctypes.c_char_p, ctypes.c_size_t, ctypes.POINTER(_vp)]),
@@ -446,6 +448,15 @@ def tp_device_status(stream=None) -> None:
 
 def tp_abi_version() -> int:
     return int(lib.tp_abi_version())
+
+
+def tp_set_tile_wait_limit_ns(ns: int) -> None:
+    """Bound, in ns, on a workspace-mode CTA's wait for the other ranks' partials (0: the default 2 s)."""
+    lib.tp_set_tile_wait_limit_ns(int(ns))
+
+
+def tp_tile_wait_limit_ns() -> int:
+    return int(lib.tp_tile_wait_limit_ns())
 
 
 def bf16_from_bits(bits, device=None) -> torch.Tensor:

@@ -267,8 +267,10 @@ tp_status prepare_plan(const void* weight, int64_t rows, int64_t cols, tp_style 
   tp_status st = validate_plan(rows, cols, style, tp_degree, rank_count > 0 ? rank_begin : -1, num_heads, head_dim,
                                fused_splits, n_splits, job->sizes, &job->n);
   if (st != TP_OK) return st;
-  if (rank_count > 0 && rank_begin + rank_count > tp_degree)
-    return fail(TP_ERR_INVALID_ARG, "ranks [%d, %d) outside [0, %d)", rank_begin, rank_begin + rank_count, tp_degree);
+  // rank_begin is in [0, tp_degree) here (validate_plan checked it), so the difference cannot overflow.
+  if (rank_count > 0 && rank_count > tp_degree - rank_begin)
+    return fail(TP_ERR_INVALID_ARG, "ranks [%d, %lld) outside [0, %d)", rank_begin,
+                static_cast<long long>(rank_begin) + rank_count, tp_degree);
   job->rows = rows;
   job->cols = cols;
   job->style = style;

@@ -85,6 +85,7 @@ struct GemmParams {
   __nv_bfloat16* reduce_out;                 // WS_REDUCE: bf16 [M][ldo]
   const __nv_bfloat16* reduce_bias;          // WS_REDUCE: nullable [N]
   unsigned int* status;
+  uint64_t tile_wait_ns;  // WS_REDUCE: bound on the wait for the other ranks' partials of a tile
   int64_t ldo;        // row stride of the outputs, elements
   int M, N;           // output rows; output columns per group
   int n_groups;       // independent outputs (ranks) -- 1 for ACCUM
@@ -178,15 +179,17 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, vola
   }
 }
 
-// Bounded wait until *ctr >= target (a tile counter other CTAs increment); false on abort or timeout.
-__device__ __noinline__ bool wait_counter(const int* ctr, int target, volatile int* abort_flag, unsigned int* status) {
+// Bounded wait until *ctr >= target (a tile counter other CTAs increment); false on abort or
+// timeout.  The bound is the caller's (tp_set_tile_wait_limit_ns), read at launch.
+__device__ __noinline__ bool wait_counter(const int* ctr, int target, volatile int* abort_flag, unsigned int* status,
+                                          uint64_t limit_ns) {
   const uint64_t t0 = ptx::globaltimer_ns();
   for (;;) {
     int v;
     asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(ctr) : "memory");
     if (v >= target) return true;
     if (*abort_flag) return false;
-    if (ptx::globaltimer_ns() - t0 > kWaitLimitNs) {
+    if (ptx::globaltimer_ns() - t0 > limit_ns) {
       *abort_flag = 1;
       atomicOr(status, TP_DEVSTATUS_TIMEOUT);
       return false;
@@ -423,7 +426,8 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, SmemCtrl* ctl
         int* ctr = &p.counters[mb128 * p.n_counters + nb];
         if (epi_tid == 0) {
           atomicAdd(ctr, 1);
-          const bool ready = wait_counter(ctr, p.n_groups, reinterpret_cast<volatile int*>(&ctl->abort), p.status);
+          const bool ready =
+              wait_counter(ctr, p.n_groups, reinterpret_cast<volatile int*>(&ctl->abort), p.status, p.tile_wait_ns);
           *reinterpret_cast<volatile int*>(&ctl->is_last) = ready ? 1 : 0;
         }
         ptx::named_bar_sync(1, 128);
@@ -1120,6 +1124,7 @@ tp_status tp_linear_colwise(const void* x, const void* const* w_shards, const vo
     if (st != TP_OK) return st;
   }
   p.status = status;
+  p.tile_wait_ns = tile_wait_limit_ns();
   p.ldo = ldy;
   p.M = static_cast<int>(T);
   p.N = static_cast<int>(n_out);
@@ -1245,6 +1250,7 @@ tp_status rowwise_impl(const void* const* x_shards, int64_t ldx, const void* con
     if (st != TP_OK) return st;
   }
   p.status = status;
+  p.tile_wait_ns = tile_wait_limit_ns();
   p.M = static_cast<int>(T);
   p.N = static_cast<int>(N);
   p.kblocks = ceil_div(K_r, BK);
@@ -1306,7 +1312,7 @@ tp_status rowwise_impl(const void* const* x_shards, int64_t ldx, const void* con
 // Rowwise workspace mode for callers that cannot allocate: the scratch is a
 // fixed array compiled into the library.  Host code must not pass the
 // array's name to a kernel (on the host it is only a stand-in symbol); its
-// device address is looked up once per device and cached.
+// device address is looked up once per device and context and cached.
 // ---------------------------------------------------------------------------
 
 namespace tp {
@@ -1316,18 +1322,23 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[TP_NOALLOC_SCRA
 
 std::mutex g_noalloc_mutex;
 void* g_noalloc_ptr[64] = {nullptr};
+unsigned long long g_noalloc_ctx[64] = {0};
 
 tp_status noalloc_scratch(void** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
   if (dev < 0 || dev >= 64) return fail(TP_ERR_UNSUPPORTED, "device index %d above 63", dev);
+  const unsigned long long ctx = current_context_id();
   std::lock_guard<std::mutex> lock(g_noalloc_mutex);
-  if (g_noalloc_ptr[dev] == nullptr) {
+  // Looked up again in a new context (after cudaDeviceReset, or a caller's own context): the
+  // module, and with it the array, is loaded anew there.
+  if (g_noalloc_ptr[dev] == nullptr || ctx == 0 || g_noalloc_ctx[dev] != ctx) {
     void* ptr = nullptr;
     e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
     if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(built-in scratch)");
     g_noalloc_ptr[dev] = ptr;
+    g_noalloc_ctx[dev] = current_context_id();
   }
   *out = g_noalloc_ptr[dev];
   return TP_OK;
@@ -1395,6 +1406,7 @@ tp_status gemm_batched(int groups, const void* const* a, int64_t lda, const void
     p.out[g] = out[g];
   }
   p.status = status;
+  p.tile_wait_ns = tile_wait_limit_ns();
   p.ldo = ldo;
   p.M = static_cast<int>(M);
   p.N = static_cast<int>(N);

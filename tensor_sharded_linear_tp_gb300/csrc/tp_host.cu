@@ -7,6 +7,7 @@
 // all checked before any weight is copied).
 #include <cstdio>
 #include <cstring>
+#include <atomic>
 #include <mutex>
 #include <string>
 
@@ -20,6 +21,7 @@ std::mutex g_dev_mutex;
 constexpr int kMaxDevices = 64;
 int g_sm_count[kMaxDevices] = {0};
 unsigned int* g_status_ptr[kMaxDevices] = {nullptr};
+unsigned long long g_status_ctx[kMaxDevices] = {0};
 }  // namespace
 
 // One status word per device: kernels OR flags into it, tp_device_status reads and clears it.
@@ -58,14 +60,47 @@ int sm_count() {
   return g_sm_count[dev];
 }
 
+constexpr uint64_t kDefaultTileWaitNs = 2000000000ull;
+std::atomic<uint64_t> g_tile_wait_ns{kDefaultTileWaitNs};
+
+uint64_t tile_wait_limit_ns() { return g_tile_wait_ns.load(std::memory_order_relaxed); }
+
+unsigned long long current_context_id() {
+  using GetCurrent = CUresult (*)(CUcontext*);
+  using GetId = CUresult (*)(CUcontext, unsigned long long*);
+  static GetCurrent get_current = nullptr;
+  static GetId get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<GetCurrent>(f);
+    f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<GetId>(f);
+  });
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (get_current == nullptr || get_id == nullptr || get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return 0;
+  if (get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
+
 unsigned int* status_word() {
   int dev = current_device();
   if (dev < 0 || dev >= kMaxDevices) return nullptr;
+  const unsigned long long ctx = current_context_id();
   std::lock_guard<std::mutex> lock(g_dev_mutex);
-  if (g_status_ptr[dev] == nullptr) {
+  // Cached per device and context: a new context (after cudaDeviceReset, or a caller's own
+  // context) loads the module again, possibly at another address.
+  if (g_status_ptr[dev] == nullptr || ctx == 0 || g_status_ctx[dev] != ctx) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, tp_kernel_status_word) != cudaSuccess) return nullptr;
     g_status_ptr[dev] = static_cast<unsigned int*>(p);
+    g_status_ctx[dev] = current_context_id();
   }
   return g_status_ptr[dev];
 }
@@ -183,6 +218,12 @@ tp_status tp_device_status(tp_stream_t stream) {
   return TP_OK;
 }
 
-int tp_abi_version(void) { return 101; }
+void tp_set_tile_wait_limit_ns(uint64_t ns) {
+  tp::g_tile_wait_ns.store(ns == 0 ? tp::kDefaultTileWaitNs : ns, std::memory_order_relaxed);
+}
+
+uint64_t tp_tile_wait_limit_ns(void) { return tp::tile_wait_limit_ns(); }
+
+int tp_abi_version(void) { return 102; }
 
 }  // extern "C"

@@ -27,6 +27,14 @@ int sm_count();
 // (bit 0: a kernel gave up on a bounded wait).  Looked up once per device.
 unsigned int* status_word();
 
+// Identity of the calling thread's current CUDA context, unique over the process's lifetime
+// (0 when no context is current).  Device addresses of the library's own arrays are cached
+// under it: a new context loads the library's modules again, possibly elsewhere.
+unsigned long long current_context_id();
+
+// The bound on a CTA's wait for other CTAs' tile partials (tp_set_tile_wait_limit_ns), in ns.
+uint64_t tile_wait_limit_ns();
+
 // Plan validation shared by every entry point.  On TP_OK, `sizes` holds the
 // n_sizes absolute block sizes along the sharded dimension.
 tp_status validate_plan(int64_t rows, int64_t cols, tp_style style, int tp_degree, int rank, int64_t num_heads,

@@ -149,7 +149,8 @@ def test_plan_shard_rejects_bad_plans_before_copying():
 def _shard_request(rows, cols, style, p, splits=None, heads=0, hd=0, rank_begin=0, rank_count=None, w=FAKE, keep=None):
     rc = p - rank_begin if rank_count is None else rank_count
     sp = (ctypes.c_int64 * len(splits))(*splits) if splits else None
-    outs = (ctypes.c_void_p * max(1, rc))(*([FAKE] * max(1, rc)))
+    n_outs = min(max(1, rc), 16)   # a refused request reads none of them
+    outs = (ctypes.c_void_p * n_outs)(*([FAKE] * n_outs))
     if keep is not None:
         keep += [sp, outs]
     return tp.ShardRequest(w, rows, cols, tp.STYLES[style], p, rank_begin, rc, sp, len(splits) if splits else 0,
@@ -169,6 +170,10 @@ def test_plan_shard_many_checks_every_request_first():
     assert tp.STATUS_NAMES[tp.lib.tp_plan_shard_many(arr, -1, None)] == "TP_ERR_INVALID_ARG"
     assert tp.STATUS_NAMES[tp.lib.tp_plan_shard_many(arr, 65, None)] == "TP_ERR_UNSUPPORTED"
     assert tp.STATUS_NAMES[tp.lib.tp_plan_shard_many(None, 2, None)] == "TP_ERR_INVALID_ARG"
+    # A rank range whose end would overflow an int is refused, not wrapped around.
+    huge = (tp.ShardRequest * 1)(_shard_request(16, 8, "colwise", 2, rank_begin=1, rank_count=2 ** 31 - 1,
+                                                keep=keep))
+    assert tp.STATUS_NAMES[tp.lib.tp_plan_shard_many(huge, 1, None)] == "TP_ERR_INVALID_ARG"
     assert tp.lib.tp_plan_shard_many(None, 0, None) == 0
     # Requests with nothing to copy pass without touching memory.
     empty = (tp.ShardRequest * 2)(_shard_request(0, 8, "colwise", 2, w=0, keep=keep),
@@ -224,3 +229,24 @@ def test_combine_argument_checks():
     assert tp.STATUS_NAMES[tp.lib.tp_combine(0, parts, 2, 0, 8, 0, None)] == "TP_OK"
     nulls = (ctypes.c_void_p * 2)(FAKE, None)
     assert tp.STATUS_NAMES[tp.lib.tp_combine(0, nulls, 2, 4, 8, FAKE, None)] == "TP_ERR_INVALID_ARG"
+
+
+def test_tile_wait_limit_round_trips_on_the_host():
+    # Host-side setting only (read by later launches); 0 restores the 2 s default.
+    assert tp.tp_tile_wait_limit_ns() == 2_000_000_000
+    try:
+        tp.tp_set_tile_wait_limit_ns(12345)
+        assert tp.tp_tile_wait_limit_ns() == 12345
+    finally:
+        tp.tp_set_tile_wait_limit_ns(0)
+    assert tp.tp_tile_wait_limit_ns() == 2_000_000_000
+
+
+def test_noalloc_scratch_size_matches_the_header():
+    # The binding's constant is the header's #define, not a second copy that could drift.
+    import os
+    import re
+    hdr = open(os.path.join(os.path.dirname(__file__), "..", "include", "tp.h")).read()
+    m = re.search(r"#define TP_NOALLOC_SCRATCH_BYTES \(\(size_t\)(\d+) << (\d+)\)", hdr)
+    assert m is not None
+    assert tp.NOALLOC_SCRATCH_BYTES == int(m.group(1)) << int(m.group(2))

@@ -189,7 +189,8 @@ def test_plan_refusals_come_before_any_read(tmp_path):
     try:
         def load(name, style, p, rank_begin=0, rank_count=1, splits=None, heads_=0, hd=0):
             arr = (tp._i64 * len(splits))(*splits) if splits else None
-            outs = (tp._vp * max(1, rank_count))(*([FAKE] * max(1, rank_count)))
+            n_outs = min(max(1, rank_count), 16)   # a refused call reads none of them
+            outs = (tp._vp * n_outs)(*([FAKE] * n_outs))
             st = tp.lib.tp_st_plan_shard_ranks(h, name.encode(), tp.STYLES[style], p, rank_begin, rank_count, arr,
                                                len(splits) if splits else 0, heads_, hd, outs, None)
             return tp.STATUS_NAMES[st]
@@ -203,6 +204,8 @@ def test_plan_refusals_come_before_any_read(tmp_path):
         assert load("bytes", "rowwise", 6) == "TP_ERR_UNSUPPORTED"        # 1-byte slices of odd width
         assert load("in", "colwise", 2, rank_begin=1, rank_count=2) == "TP_ERR_INVALID_ARG"
         assert load("in", "colwise", 2, rank_count=-1) == "TP_ERR_INVALID_ARG"
+        # A rank count whose sum with rank_begin would overflow an int is still refused.
+        assert load("in", "colwise", 2, rank_begin=1, rank_count=2 ** 31 - 1) == "TP_ERR_INVALID_ARG"
         # rank_count 0 validates and reads nothing: the binding's pre-allocation check.
         assert load("in", "colwise", 2, rank_count=0, splits=[H, H, H, F, F]) == "TP_OK"
     finally:
