@@ -1,44 +1,45 @@
 #!/usr/bin/env python
-"""Benchmark of the tensor-parallel sharded projection on GB300.
+"""Benchmark of the tensor-parallel sharded projection on one GB300.
 
-One step = one pass of the whole hot path over one batch of synthetic input,
-on the attention-projection workload (tokens 4096, hidden 3072, 24 heads x 128,
-tp_degree 4, all four ranks on this GPU):
+Default workload: a stack of 8 SwiGLU MLP blocks (hidden 6144, ffn 18432,
+tokens 4608, tp_degree 4, all four ranks on this GPU), loaded shard-on-read
+from a page-locked host state dict of 5.44 GB of bf16.
 
-  1. shard extraction of the fused QKV weight [9216, 3072] (colwise, whole
-     heads of Q, K and V per rank) and of the out-projection [3072, 3072]
-     (rowwise) from device-resident full weights -- one tp_plan_shard_many
-     launch covering both weights and all four ranks;
-  2. the colwise QKV projection of every rank, one launch, each rank's tiles
-     stored straight into its column block of the gathered [4096, 9216]
-     output (the AllGather fused into the store; ``--unfused-gather`` runs it
-     as a separate tp_combine kernel);
-  3. the rowwise out-projection of every rank with the partial sums joined on
-     chip in fp32 (tp_linear_rowwise, TP_REDUCE_ACCUM), one launch.
+* ``value`` -- the sharded blocks' throughput: the forward pass through all 8
+  blocks (per block: tp_linear_colwise with the fused SwiGLU epilogue, then
+  tp_linear_rowwise with the ranks' partials summed on chip) is one step; value
+  = its FLOPs (2*T*K*N per projection, summed over ranks) per second of device
+  time, the shards and the input already resident in HBM.  Every step reads
+  5.44 GB of weights, far more than L2, so no flush is needed between steps.
+* ``roofline`` -- the dominant kernel, the gate/up GEMM with the SwiGLU
+  epilogue: its FLOPs per launch over its mean launch time (each launch timed
+  alone with CUDA events), against the measured sustained bf16 peak (the
+  launches run back to back inside a 14 ms pass).
+* ``shard_load`` -- shard-extract GB/s: every rank's slice of all 16 weights
+  read from the page-locked state dict straight into device shards
+  (tp_plan_shard_ranks), against a plain host-to-device copy of 1 GiB measured
+  in the same run (the link, not HBM, bounds it).
+* ``e2e`` -- the same metric through the C-ABI with host buffers: each step
+  reads every rank's slice of every weight from host memory, copies the input
+  in and the output back, pipelined (block b computes while later blocks'
+  slices arrive).
+* ``cpu_baseline`` -- the float64 numpy oracle on a seeded sample of token
+  rows through all 8 blocks (all shards extracted), on the host's cores.
+* ``attn_proj_tp4`` and ``block_tp4`` -- per-kernel figures of the attention
+  projections (tokens 4096, hidden 3072, 24 heads) and of the full attention +
+  SwiGLU MLP block (hidden 6144, 48 heads, tp 4), each step timed with L2
+  flushed between steps (a 256 MiB write, then a 256 MiB read), including the
+  rowwise projection in both join forms (on-chip sum, fp32 partials summed in
+  the GEMM epilogue through an HBM workspace) and the device-to-device
+  extraction GB/s against HBM.
 
-``value`` = the step's GEMM FLOPs (2*T*K*N summed over the projections) per
-second of device time: extraction counts as time, not as work.
-Inputs are resident in HBM when the timed region starts; L2 is flushed
-between steps (a 256 MiB write, then a 256 MiB read of another buffer), so every
-step reads its operands from HBM and inherits no dirty line of the flush to write
-back.
-The step is captured once as a CUDA graph and each timed step replays it between
-two CUDA events (``--eager`` launches every call from Python instead); a second,
-untimed pass replays each phase as its own graph with events between the phases
-for the per-phase breakdown (``kernels``; the eager per-phase times are reported
-too).
+``--workload`` runs one of the other workloads alone with the same machinery.
+``--impl reference`` times the CPU oracle on the default workload, each step a
+bounded sample (one block on sampled token rows).
 
-``e2e`` is the same metric through the same public calls with host buffers:
-the step's activations are copied in from page-locked memory and the output
-is read back, inside the timed region (``e2e.weights_from_host`` also reads
-every rank's weight slices from page-locked host memory every step).
-
-``--impl reference`` times the CPU oracle (float64 numpy) on the same
-workload, each step a bounded sample of token rows.
-
-Under torchrun (N > 1) every GPU runs its own independent replica of the
-block on its own batch (no data-path collective); ``value`` is the total work
-of all GPUs over the slowest GPU's time.
+The library simulates every rank on one GPU; it is a single-GPU library (its
+GEMMs multicast operand tiles inside a thread-block cluster of this GPU), so
+this benchmark refuses to run under torchrun with more than one process.
 """
 from __future__ import annotations
 
@@ -56,6 +57,7 @@ import subprocess
 import sys
 import threading
 import time
+from concurrent.futures import ThreadPoolExecutor
 
 import numpy as np
 
@@ -66,7 +68,8 @@ import tp_inputs  # noqa: E402
 
 METRIC = "sharded-block TFLOP/s & % bf16 tensor peak on 1 GB300; shard-extract GB/s % HBM"
 UNIT = "TFLOP/s"
-WORKLOAD = "attn_proj_tp4"
+WORKLOAD = "stack8_swiglu_tp4"
+ATTN_PROJ = "attn_proj_tp4"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
 L2_FLUSH_BYTES = 256 << 20
 
@@ -87,49 +90,16 @@ class L2Flush:
         self.r.amax()
 
 
-
-# ----------------------------------------------------------------------------- distributed plumbing
-
-def dist_env():
-    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
-            int(os.environ.get("LOCAL_RANK", "0")))
-
-
-def init_dist(world: int, backend: str):
-    if world <= 1:
-        return None
-    import torch.distributed as dist
-    os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
-    dist.init_process_group(backend=backend)
-    return dist
-
-
-def barrier(dist, device=None):
-    if dist is None:
-        return
-    if dist.get_backend() == "nccl" and device is not None:
-        dist.barrier(device_ids=[device.index])
-    else:
-        dist.barrier()
-
-
-def max_over_ranks(dist, value: float, device=None) -> float:
-    """The largest value over all ranks (the slowest rank's time)."""
-    if dist is None:
-        return value
-    import torch
-    t = torch.tensor([value], dtype=torch.float64, device=device if dist.get_backend() == "nccl" else "cpu")
-    dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    return float(t.item())
-
-
-def sum_over_ranks(dist, value: float, device=None) -> float:
-    if dist is None:
-        return value
-    import torch
-    t = torch.tensor([value], dtype=torch.float64, device=device if dist.get_backend() == "nccl" else "cpu")
-    dist.all_reduce(t, op=dist.ReduceOp.SUM)
-    return float(t.item())
+def refuse_multi_gpu(args) -> None:
+    """One process, one GPU: the library is a single-GPU library; more GPUs are refused."""
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if world > 1 or args.gpus != 1:
+        msg = (f"single-GPU benchmark: libtp simulates every tensor-parallel rank on one GPU and its GEMMs "
+               f"multicast operand tiles within a cluster of that GPU; refusing WORLD_SIZE={world}, --gpus {args.gpus}")
+        if int(os.environ.get("RANK", "0")) == 0:
+            print(json.dumps({"metric": METRIC, "value": None, "n_gpus": max(world, args.gpus), "error": msg}))
+        print(msg, file=sys.stderr)
+        sys.exit(2)
 
 
 # ----------------------------------------------------------------------------- peaks, clocks, traffic
@@ -241,7 +211,7 @@ class AttnProjWorkload:
     """Attention projections, tp_degree 4: fused QKV colwise + gather, out-projection rowwise (fused sum)."""
 
     def __init__(self, tp, torch, device, reduce_mode="accum", fused_gather=True):
-        cfg = tp_inputs.WORKLOADS[WORKLOAD]
+        cfg = tp_inputs.WORKLOADS[ATTN_PROJ]
         self.tp, self.torch, self.device = tp, torch, device
         self.fused_gather = fused_gather
         self.p, self.T, self.H = cfg["tp"], cfg["tokens"], cfg["hidden"]
@@ -286,7 +256,7 @@ class AttnProjWorkload:
         self.pin = None
 
     def config(self):
-        return {"workload": WORKLOAD, "tokens": self.T, "hidden": self.H, "heads": self.heads, "head_dim": self.hd,
+        return {"workload": ATTN_PROJ, "tokens": self.T, "hidden": self.H, "heads": self.heads, "head_dim": self.hd,
                 "tp_degree": self.p, "rowwise_reduce": self.mode,
                 "gather": "fused into the colwise store (ldy)" if self.fused_gather else "tp_combine kernel",
                 "step": "tp_plan_shard_many (out-projection weight, 4 ranks, from device memory) + "
@@ -840,193 +810,159 @@ class SingleStreamWorkload:
 
 
 class StackWorkload:
-    """Eight SwiGLU MLP blocks (hidden 6144, ffn 18432, tp 4) from a page-locked host state dict."""
+    """Eight SwiGLU MLP blocks (hidden 6144, ffn 18432, tp 4) from a page-locked host state dict.
+
+    The shards are loaded once (shard-on-read, every rank's slice of every weight
+    straight from host memory); a step is the forward pass through the 8 blocks.
+    Block b reads the previous block's output (x for block 0) and writes one of two
+    ping-pong buffers.
+    """
 
     def __init__(self, tp, torch, device):
-        cfg = tp_inputs.WORKLOADS["stack8_swiglu_tp4"]
+        cfg = tp_inputs.WORKLOADS[WORKLOAD]
         self.tp, self.torch, self.device = tp, torch, device
         self.p, self.nb, self.T, self.H, self.F = cfg["tp"], cfg["blocks"], cfg["tokens"], cfg["hidden"], cfg["ffn"]
-        self.heads = cfg["heads"]
-        seed = cfg["seed"]
+        self.heads, self.seed = cfg["heads"], cfg["seed"]
+        p, H, F, T = self.p, self.H, self.F, self.T
+        # The seeded state dict: 16 tensors, generated side by side (numpy releases the GIL).
+        jobs = [(b, which) for b in range(self.nb) for which in ("gate_up", "down")]
+        with ThreadPoolExecutor(max_workers=min(16, os.cpu_count() or 1)) as ex:
+            bits = list(ex.map(lambda j: tp_inputs.stack_weight(self.seed, j[0], j[1], H, F), jobs))
+        self.host_bits = [(bits[2 * b], bits[2 * b + 1]) for b in range(self.nb)]
         pin = lambda b: torch.empty(b.shape, dtype=torch.bfloat16, pin_memory=True).copy_(  # noqa: E731
             tp.bf16_from_bits(b))
-        self.host = [(pin(tp_inputs.stack_weight(seed, b, "gate_up", self.H, self.F)),
-                      pin(tp_inputs.stack_weight(seed, b, "down", self.H, self.F))) for b in range(self.nb)]
-        x = tp_inputs.stack_input(seed, self.nb, self.T, self.H)
-        self.x_pin = pin(x)
-        self.x = tp.bf16_from_bits(x, device)
-        self.z_pin = torch.empty((self.T, self.H), dtype=torch.bfloat16, pin_memory=True)
-        p, H, F = self.p, self.H, self.F
+        self.host = [(pin(gu), pin(dn)) for gu, dn in self.host_bits]
+        self.x_bits = tp_inputs.stack_input(self.seed, self.nb, T, H)
+        self.x_pin = pin(self.x_bits)
+        self.x = tp.bf16_from_bits(self.x_bits, device)
+        self.z_pin = torch.empty((T, H), dtype=torch.bfloat16, pin_memory=True)
         e = lambda *sh: torch.empty(sh, dtype=torch.bfloat16, device=device)  # noqa: E731
         self.shards = [([e(2 * F // p, H) for _ in range(p)], [e(H, F // p) for _ in range(p)])
                        for _ in range(self.nb)]
-        self.h = [e(self.T, F // p) for _ in range(p)]
-        self.z = [e(self.T, H), e(self.T, H)]
+        self.h = [e(T, F // p) for _ in range(p)]
+        self.zbuf = [e(T, H), e(T, H)]
+        self.z = self.zbuf[(self.nb - 1) % 2]          # the last block's output
+        self.x_in = e(T, H)
         self.shard_bytes = self.nb * (2 * F * H + H * F) * 2
-        self.flops = self.nb * (2.0 * self.T * H * 2 * F + 2.0 * self.T * F * H)
+        self.fl_gu = 2.0 * T * H * 2 * F
+        self.fl_dn = 2.0 * T * F * H
+        self.flops = self.nb * (self.fl_gu + self.fl_dn)
         self.launches_per_step = 2 * self.nb
+        self.copy_stream = None
+
+    def config(self):
+        return {"workload": WORKLOAD, "blocks": self.nb, "tokens": self.T, "hidden": self.H, "ffn": self.F,
+                "heads": self.heads, "tp_degree": self.p, "rowwise_reduce": "accum",
+                "weights": f"{self.shard_bytes / 1e9:.2f} GB of bf16 shards (2.72B parameters)",
+                "step": "8 x (tp_linear_colwise SwiGLU + tp_linear_rowwise accum), shards resident in HBM"}
+
+    # -- shard-on-read ----------------------------------------------------------------------------
+    def load_block(self, b, stream):
+        tp, p, F = self.tp, self.p, self.F
+        gu, dn = self.host[b]
+        gu_sh, dn_sh = self.shards[b]
+        tp.tp_plan_shard_ranks(gu, "colwise", p, 0, p, [F, F], self.heads, 0, outs=gu_sh, stream=stream)
+        tp.tp_plan_shard_ranks(dn, "rowwise", p, 0, p, None, self.heads, 0, outs=dn_sh, stream=stream)
 
     def load(self, stream):
-        tp, p, F = self.tp, self.p, self.F
-        for (gu, dn), (gu_sh, dn_sh) in zip(self.host, self.shards):
-            tp.tp_plan_shard_ranks(gu, "colwise", p, 0, p, [F, F], self.heads, 0, outs=gu_sh, stream=stream)
-            tp.tp_plan_shard_ranks(dn, "rowwise", p, 0, p, None, self.heads, 0, outs=dn_sh, stream=stream)
+        for b in range(self.nb):
+            self.load_block(b, stream)
+
+    # -- the forward pass -------------------------------------------------------------------------
+    def block_input(self, b, x=None):
+        if b == 0:
+            return self.x if x is None else x
+        return self.zbuf[(b - 1) % 2]
+
+    def gate_up(self, b, stream, x=None):
+        self.tp.tp_linear_colwise(self.block_input(b, x), self.shards[b][0], "swiglu", y_shards=self.h,
+                                  stream=stream)
+
+    def down(self, b, stream):
+        self.tp.tp_linear_rowwise(self.h, self.shards[b][1], mode="accum", out=self.zbuf[b % 2], stream=stream)
 
     def forward(self, stream, x=None):
-        tp = self.tp
-        z = self.x if x is None else x
-        for b, (gu_sh, dn_sh) in enumerate(self.shards):
-            tp.tp_linear_colwise(z, gu_sh, "swiglu", y_shards=self.h, stream=stream)
-            out = self.z[b % 2]
-            tp.tp_linear_rowwise(self.h, dn_sh, mode="accum", out=out, stream=stream)
-            z = out
-        return z
+        for b in range(self.nb):
+            self.gate_up(b, stream, x)
+            self.down(b, stream)
+        return self.z
 
+    def step(self, stream):
+        self.forward(stream)
 
-def run_stack(args):
-    """Shard-on-read load of the 8-block state dict, then the forward pass, on one GPU."""
-    import torch
-    from __graft_entry__ import build
-    build()
-    import tensor_sharded_linear_tp_gb300 as tp
-    device = torch.device("cuda", 0)
-    torch.cuda.set_device(device)
-    wl = StackWorkload(tp, torch, device)
-    stream = torch.cuda.Stream(device)
-    ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
-    peaks = load_peaks()
-
-    def timed(fn, reps):
+    def phases(self):
         out = []
-        for _ in range(reps):
-            a, b = ev(), ev()
-            a.record(stream)
-            fn()
-            b.record(stream)
-            b.synchronize()
-            out.append(a.elapsed_time(b))
-        return float(np.mean(out))
+        for b in range(self.nb):
+            out.append(("colwise_swiglu", lambda st, b=b: self.gate_up(b, st), "tensor", self.fl_gu))
+            out.append(("rowwise_down", lambda st, b=b: self.down(b, st), "tensor", self.fl_dn))
+        return out
 
-    # Shard-on-read load over the CPU-GPU link, against a plain page-locked copy of equal size.
-    wl.load(stream)
-    stream.synchronize()
-    load_ms = timed(lambda: wl.load(stream), 3)
-    probe_n = 1 << 30
-    src = torch.empty(probe_n, dtype=torch.uint8, pin_memory=True)
-    dst = torch.empty(probe_n, dtype=torch.uint8, device=device)
-    with torch.cuda.stream(stream):
-        dst.copy_(src, non_blocking=True)
-    def link_copy():
+    # -- end to end: every step from host memory ----------------------------------------------------
+    def step_e2e(self, stream, pipelined=True):
+        """One step through the public calls with host buffers: every rank's slice of every weight
+        read from the page-locked state dict (shard-on-read), the input copied in, the 8 blocks,
+        the output copied back.  Pipelined: the input and the blocks' slices arrive in block order
+        on a copy stream, and block b starts as soon as its own slices have landed, so the
+        compute of block b overlaps the transfer of later blocks' slices.  Unpipelined: the same
+        calls one after another on one stream."""
+        torch = self.torch
+        if not pipelined:
+            self.load(stream)
+            with torch.cuda.stream(stream):
+                self.x_in.copy_(self.x_pin, non_blocking=True)
+            self.forward(stream, self.x_in)
+            with torch.cuda.stream(stream):
+                self.z_pin.copy_(self.z, non_blocking=True)
+            return
+        if self.copy_stream is None:
+            self.copy_stream = torch.cuda.Stream(self.device)
+        cs = self.copy_stream
+        ex = torch.cuda.Event()
+        eb = [torch.cuda.Event() for _ in range(self.nb)]
+        cs.wait_stream(stream)
+        with torch.cuda.stream(cs):
+            self.x_in.copy_(self.x_pin, non_blocking=True)
+            ex.record(cs)
+            for b in range(self.nb):
+                self.load_block(b, cs)
+                eb[b].record(cs)
+        stream.wait_event(ex)
+        for b in range(self.nb):
+            stream.wait_event(eb[b])
+            self.gate_up(b, stream, self.x_in)
+            self.down(b, stream)
         with torch.cuda.stream(stream):
-            dst.copy_(src, non_blocking=True)
+            self.z_pin.copy_(self.z, non_blocking=True)
 
-    copy_ms = timed(link_copy, 3)
-    del dst
-    load_gbs = wl.shard_bytes / (load_ms * 1e-3) / 1e9
-    link_gbs = probe_n / (copy_ms * 1e-3) / 1e9
-
-    for _ in range(args.warmup):
-        wl.forward(stream)
-    stream.synchronize()
-    sampler = ClockSampler(0)
-    sampler.start()
-    time.sleep(0.3)
-    fwd_ms = timed(lambda: wl.forward(stream), max(1, min(args.steps, 50)))
-    clocks = sampler.stop()
-    tp.tp_device_status(stream)
-
-    def e2e_step():
-        wl.load(stream)
-        with torch.cuda.stream(stream):
-            xin = wl.x_pin.to(device, non_blocking=True)
-        z = wl.forward(stream, xin)
-        with torch.cuda.stream(stream):
-            wl.z_pin.copy_(z, non_blocking=True)
-
-    e2e_ms = timed(e2e_step, 3)
-    value = wl.flops / (fwd_ms * 1e-3) / 1e12
-    line = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1, "steps": max(1, min(args.steps, 50)),
-        "warmup": args.warmup, "ms_per_step": fwd_ms, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,0.02) weights, N(0,1) activations)",
-        "config": {"workload": "stack8_swiglu_tp4", "blocks": wl.nb, "tokens": wl.T, "hidden": wl.H, "ffn": wl.F,
-                   "tp_degree": wl.p, "l2": "weights 5.44 GB, larger than L2",
-                   "step": "8 x (tp_linear_colwise SwiGLU + tp_linear_rowwise accum)"},
-        "roofline": {"bound": "tensor", "achieved": value, "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
-                     "frac": value / peaks["bf16_tflops_sustained"], "kernel": "tp_gemm_kernel (16 launches)",
-                     "peak_source": peaks["source"] + " sustained", "traffic": None},
-        "shard_load": {"bytes": wl.shard_bytes, "ms": load_ms, "GB/s": load_gbs,
-                       "link_copy_GB/s": link_gbs, "frac_of_link_copy": load_gbs / link_gbs,
-                       "frac_hbm": load_gbs / peaks["hbm_gbs"]},
-        "e2e": {"value": wl.flops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT, "ms_per_step": e2e_ms,
-                "h2d_bytes_per_step": wl.shard_bytes + wl.T * wl.H * 2, "d2h_bytes_per_step": wl.T * wl.H * 2},
-        "gpu_launches": wl.launches_per_step * max(1, min(args.steps, 50)), "clocks": clocks, "peaks": peaks,
-    }
-    print(json.dumps(line))
+    # -- the oracle on sampled rows -----------------------------------------------------------------
+    def oracle_block(self, b, x_bits):
+        """The oracle's block b on the given input rows: every rank's shards extracted from the
+        host state dict, then the SwiGLU MLP block.  Returns the output's bf16 bits."""
+        from oracle import tp_oracle as O
+        p, F = self.p, self.F
+        gu, dn = self.host_bits[b]
+        with np.errstate(all="ignore"):   # the stacked values leave the bf16 range after block 4
+            _, z = O.mlp_forward(x_bits, [O.shard(gu, "colwise", p, r, [F, F]) for r in range(p)],
+                                 [O.shard(dn, "rowwise", p, r) for r in range(p)], "swiglu")
+            return O.f64_to_bf16(z)
 
 
 # ----------------------------------------------------------------------------- CPU oracle timing
 
-def oracle_sample_step(host, rows, p, H, heads, hd):
-    """The oracle's version of one step, restricted to the given token rows (exact for those rows)."""
-    from oracle import tp_oracle as O
-    qkv = [O.shard(host["w_qkv"], "colwise", p, r, [H] * 3, num_heads=heads, head_dim=hd) for r in range(p)]
-    wo = [O.shard(host["w_out"], "rowwise", p, r, num_heads=heads, head_dim=hd) for r in range(p)]
-    ys = [O.f64_to_bf16(y) for y in O.colwise_forward(host["x"][rows], qkv, "none")]
-    O.combine_gather(ys)
-    a = host["a"][rows]
-    z = O.rowwise_forward([O.shard(a, "rowwise", p, r) for r in range(p)], wo)
-    return O.f64_to_bf16(z)
-
-
-def time_oracle(host, rows, p, H, heads, hd):
+def stack_cpu_baseline(wl, n_rows=32):
+    """The oracle through all 8 blocks on a seeded sample of token rows (exact for those rows)."""
+    rows = tp_inputs.sample_rows(12, wl.T, n_rows)
     t0 = time.perf_counter()
-    oracle_sample_step(host, rows, p, H, heads, hd)
-    return time.perf_counter() - t0
-
-
-def calibrate_rows(host, T, p, H, heads, hd, target_s):
-    rows_n = 32
-    dt = time_oracle(host, tp_inputs.sample_rows(11, T, rows_n), p, H, heads, hd)
-    while dt < target_s / 4 and rows_n < T:
-        rows_n = min(T, rows_n * 4)
-        dt = time_oracle(host, tp_inputs.sample_rows(11, T, rows_n), p, H, heads, hd)
-    return max(1, min(T, int(rows_n * target_s / max(dt, 1e-6))))
-
-
-def cpu_baseline(host, T, p, H, heads, hd, flops_full, target_s=12.0):
-    """The oracle on a bounded sample: whole steps repeated, or a row sample of one, for ~target_s."""
-    rows_n = calibrate_rows(host, T, p, H, heads, hd, target_s)
-    rows = tp_inputs.sample_rows(12, T, rows_n)
-    reps = 1
-    dt = time_oracle(host, rows, p, H, heads, hd)
-    if rows_n == T and dt < target_s:
-        # The whole step is quicker than the target: repeat it.
-        reps = max(1, int(round(target_s / max(dt, 1e-3))))
-        t0 = time.perf_counter()
-        for _ in range(reps):
-            oracle_sample_step(host, rows, p, H, heads, hd)
-        dt = time.perf_counter() - t0
-    flops = flops_full * rows_n / T * reps
-    what = f"{reps} repetitions of the whole step" if rows_n == T else f"{rows_n} of {T} token rows of one step"
+    z = wl.x_bits[rows]
+    for b in range(wl.nb):
+        z = wl.oracle_block(b, z)
+    dt = time.perf_counter() - t0
+    flops = wl.flops * n_rows / wl.T
     return {"value": flops / dt / 1e12, "unit": UNIT, "cores": int(os.environ["OPENBLAS_NUM_THREADS"]),
             "kind": "oracle",
-            "sample": f"{what} (all shards extracted, float64 numpy oracle), {dt:.1f} s; TFLOP/s = the "
-                      f"sample's GEMM FLOPs / its time"}
-
-
-# ----------------------------------------------------------------------------- arms
-
-def make_workload(args, tp, torch, device):
-    if args.workload == WORKLOAD:
-        return AttnProjWorkload(tp, torch, device, args.reduce_mode, fused_gather=not args.unfused_gather)
-    if args.workload in ("tiny_mlp_tp2", "swiglu_mlp_tp4"):
-        return MlpWorkload(tp, torch, device, args.workload)
-    if args.workload == "block_sweep":
-        return BlockWorkload(tp, torch, device, args.tp)
-    if args.workload == "single_stream_tp4":
-        return SingleStreamWorkload(tp, torch, device, args.tp)
-    raise ValueError(args.workload)
+            "sample": f"{n_rows} of {wl.T} token rows through all {wl.nb} blocks, every rank's shards of all "
+                      f"{2 * wl.nb} weights extracted (float64 numpy oracle), {dt:.1f} s; TFLOP/s = the sample's "
+                      f"FLOPs (the step's scaled by rows) / its time"}
 
 
 def generic_cpu_baseline(wl, target_s=12.0):
@@ -1053,49 +989,80 @@ def generic_cpu_baseline(wl, target_s=12.0):
                                         f"FLOPs (the step's FLOPs scaled by rows) / its time"}
 
 
-def run_ours(args):
-    import torch
-    rank, world, local_rank = dist_env()
-    torch.cuda.set_device(local_rank)
-    device = torch.device("cuda", local_rank)
-    dist = init_dist(world, "nccl")
-    from __graft_entry__ import build
-    if rank == 0 or world == 1:
-        build()
-    barrier(dist, device)
-    import tensor_sharded_linear_tp_gb300 as tp
+def oracle_sample_step(host, rows, p, H, heads, hd):
+    """The oracle's attention-projection step, restricted to the given token rows (exact for those rows)."""
+    from oracle import tp_oracle as O
+    qkv = [O.shard(host["w_qkv"], "colwise", p, r, [H] * 3, num_heads=heads, head_dim=hd) for r in range(p)]
+    wo = [O.shard(host["w_out"], "rowwise", p, r, num_heads=heads, head_dim=hd) for r in range(p)]
+    ys = [O.f64_to_bf16(y) for y in O.colwise_forward(host["x"][rows], qkv, "none")]
+    O.combine_gather(ys)
+    a = host["a"][rows]
+    z = O.rowwise_forward([O.shard(a, "rowwise", p, r) for r in range(p)], wo)
+    return O.f64_to_bf16(z)
 
-    wl = make_workload(args, tp, torch, device)
+
+# ----------------------------------------------------------------------------- measurement
+
+def make_workload(name, args, tp, torch, device):
+    if name == WORKLOAD:
+        return StackWorkload(tp, torch, device)
+    if name == ATTN_PROJ:
+        return AttnProjWorkload(tp, torch, device, args.reduce_mode, fused_gather=not args.unfused_gather)
+    if name in ("tiny_mlp_tp2", "swiglu_mlp_tp4"):
+        return MlpWorkload(tp, torch, device, name)
+    if name == "block_sweep":
+        return BlockWorkload(tp, torch, device, args.tp)
+    if name == "single_stream_tp4":
+        return SingleStreamWorkload(tp, torch, device, args.tp)
+    raise ValueError(name)
+
+
+def time_events(torch, stream, fn, reps, before=None):
+    """Mean CUDA-event time (ms) of fn(stream) over reps runs, each alone (before() outside the events)."""
+    ms = []
+    for _ in range(reps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            if before is not None:
+                before()
+            a.record(stream)
+            fn(stream)
+            b.record(stream)
+        b.synchronize()
+        ms.append(a.elapsed_time(b))
+    return float(np.mean(ms))
+
+
+def measure(wl, args, tp, torch, device, stream, peaks, flush=None, steps=None, with_refs=True, sampler=None):
+    """Time `wl`: warm-up, then `steps` whole steps each replayed as one CUDA graph (flush() between
+    them, outside the events, when given), then a per-phase pass (each phase its own graph with
+    events between them).  Returns the figures as a dict."""
+    steps = args.steps if steps is None else steps
     phases = wl.phases()
     nph = len(phases)
-    stream = torch.cuda.Stream(device)
-    flush = L2Flush(torch, device)
-    peaks = load_peaks()
-
+    noop = (lambda: None)
+    fl = flush or noop
     for _ in range(args.warmup):
         whole_step(wl, stream)
     stream.synchronize()
     tp.tp_device_status(stream)
 
-    # Eager launches: host enqueue cost per step, and a per-phase cross-check.
-    n_eager = min(args.steps, 50)
+    # Eager launches: host enqueue cost per step and a per-phase cross-check.
+    n_eager = min(steps, 20)
     eager_marks = [[torch.cuda.Event(enable_timing=True) for _ in range(nph + 1)] for _ in range(n_eager)]
     torch.cuda.synchronize()
     host_s = 0.0
     for k in range(n_eager):
         with torch.cuda.stream(stream):
-            flush()
+            fl()
         t0 = time.perf_counter()
         run_step(wl, stream, eager_marks[k])
         host_s += time.perf_counter() - t0
     torch.cuda.synchronize()
     eager_phase = np.array([[m[i].elapsed_time(m[i + 1]) for i in range(nph)] for m in eager_marks])
-    host_enqueue_ms = host_s / n_eager * 1e3
 
-    # The timed region replays the whole step as one captured CUDA graph (the launches a
-    # serving loop would replay): the GPU runs the step's kernels back to back instead of
-    # waiting on Python.  The per-phase breakdown comes from a second pass that replays
-    # each phase as its own graph with events between them.
+    # The timed steps replay the whole step as one captured CUDA graph (the launches a serving
+    # loop would replay); the per-phase breakdown replays each phase as its own graph.
     graphs, step_graph = [], None
     if not args.eager:
         for _, fn, _, _ in phases:
@@ -1114,16 +1081,15 @@ def run_ours(args):
         stream.synchronize()
         tp.tp_device_status(stream)
 
-    bounds = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    sampler = ClockSampler(local_rank)
-    sampler.start()
-    time.sleep(0.3)
-    barrier(dist, device)
+    bounds = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    if sampler is not None:
+        sampler.start()
+        time.sleep(0.3)
     torch.cuda.synchronize()
     t_wall0 = time.perf_counter()
-    for k in range(args.steps):
+    for k in range(steps):
         with torch.cuda.stream(stream):
-            flush()          # L2 flush between steps, outside the step's events
+            fl()
             bounds[k][0].record(stream)
             if step_graph is not None:
                 step_graph.replay()
@@ -1131,21 +1097,18 @@ def run_ours(args):
                 whole_step(wl, stream)
             bounds[k][1].record(stream)
     torch.cuda.synchronize()
-    barrier(dist, device)
     t_wall = time.perf_counter() - t_wall0
-    clocks = sampler.stop()
+    clocks = sampler.stop() if sampler is not None else None
     tp.tp_device_status(stream)
-    step_ms = np.array([a.elapsed_time(b) for a, b in bounds])
-    mean_step_ms = float(step_ms.mean())
+    step_ms = float(np.mean([a.elapsed_time(b) for a, b in bounds]))
 
-    # The timed step (which may reorder or overlap independent work) against the phases run
-    # one after another: the same output, bit for bit.
+    # The timed step (which may reorder or overlap independent work) against the phases run one
+    # after another: the same output, bit for bit.
     step_matches_phases = None
     if hasattr(wl, "step") and hasattr(wl, "z"):
         run_step(wl, stream)
         stream.synchronize()
         z_phases = wl.z.clone()
-        torch.cuda.synchronize()
         with torch.cuda.stream(stream):
             wl.z.zero_()
         whole_step(wl, stream)
@@ -1153,11 +1116,11 @@ def run_ours(args):
         step_matches_phases = bool(torch.equal(wl.z.view(torch.int16), z_phases.view(torch.int16)))
 
     # Per-phase breakdown (not the timed region): each phase alone between events.
-    n_phase_steps = min(args.steps, 200)
+    n_phase_steps = min(steps, 50)
     marks = [[torch.cuda.Event(enable_timing=True) for _ in range(nph + 1)] for _ in range(n_phase_steps)]
     for k in range(n_phase_steps):
         with torch.cuda.stream(stream):
-            flush()
+            fl()
             if graphs:
                 for i, g in enumerate(graphs):
                     marks[k][i].record(stream)
@@ -1168,55 +1131,43 @@ def run_ours(args):
     torch.cuda.synchronize()
     tp.tp_device_status(stream)
     phase = np.array([[m[i].elapsed_time(m[i + 1]) for i in range(nph)] for m in marks])  # ms
-    slowest_ms = max_over_ranks(dist, mean_step_ms, device)
-    total_flops = sum_over_ranks(dist, wl.flops, device)
-    value = total_flops / (slowest_ms * 1e-3) / 1e12
-
     ph = phase.mean(axis=0)
-    kernels = {}
+
+    # Kernels by label: phases that share a label (the stack's 8 blocks) are pooled.
+    agg = {}
     for (label, _, kind, work), ms in zip(phases, ph):
+        a = agg.setdefault(label, [kind, 0.0, 0.0, 0])
+        a[1] += work
+        a[2] += float(ms)
+        a[3] += 1
+    kernels = {}
+    for label, (kind, work, ms, n) in agg.items():
+        rec = {"ms": round(ms / n, 5)}
+        if n > 1:
+            rec["launches_per_step"] = n
         if kind == "tensor":
             v = work / (ms * 1e-3) / 1e12
-            kernels[label] = {"ms": round(float(ms), 5), "TFLOP/s": v, "frac_tensor": v / peaks["bf16_tflops"]}
+            rec.update({"TFLOP/s": v, "frac_tensor": v / peaks["bf16_tflops"],
+                        "frac_tensor_sustained": v / peaks["bf16_tflops_sustained"]})
         else:
             v = work / (ms * 1e-3) / 1e9
-            kernels[label] = {"ms": round(float(ms), 5), "GB/s": v, "frac_hbm": v / peaks["hbm_gbs"]}
-    tensor_phases = [k for k in kernels if "TFLOP/s" in kernels[k]]
-    dominant = max(kernels, key=lambda k: kernels[k]["ms"])
-    if "TFLOP/s" in kernels[dominant]:
-        achieved = kernels[dominant]["TFLOP/s"]
-        roofline = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                    "frac": achieved / peaks["bf16_tflops"],
-                    "frac_of_sustained": achieved / peaks["bf16_tflops_sustained"],
-                    "kernel": dominant, "peak_source": peaks["source"] + " burst",
-                    "traffic": recorded_traffic(f"{args.workload}:{dominant}", "gemm")}
-    else:
-        achieved = kernels[dominant]["GB/s"]
-        roofline = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                    "frac": achieved / peaks["hbm_gbs"], "kernel": dominant, "peak_source": peaks["source"],
-                    "traffic": recorded_traffic(f"{args.workload}:{dominant}", "copy")}
+            rec.update({"GB/s": v, "frac_hbm": v / peaks["hbm_gbs"]})
+        kernels[label] = rec
+    dominant = max(agg, key=lambda k: agg[k][2])
 
-    def time_alone(fn, reps=20):
-        with torch.cuda.stream(stream):
-            fn(stream)
-        ms = []
-        for _ in range(reps):
-            s_, e_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            with torch.cuda.stream(stream):
-                flush()
-                s_.record(stream)
-                fn(stream)
-                e_.record(stream)
-            e_.synchronize()
-            ms.append(s_.elapsed_time(e_))
-        return float(np.mean(ms))
+    res = {"ms_per_step": step_ms, "value": wl.flops / (step_ms * 1e-3) / 1e12, "kernels": kernels,
+           "dominant": dominant, "phase_sum_ms": float(phase.sum(axis=1).mean()),
+           "step_output_bit_identical_to_phases": step_matches_phases,
+           "eager_ms_per_step": float(eager_phase.sum(axis=1).mean()),
+           "host_enqueue_ms_per_step": host_s / n_eager * 1e3, "bracket_s": t_wall, "clocks": clocks,
+           "launch": "eager" if args.eager else "cuda_graph_per_step"}
 
-    # Reference points (cuBLAS / torch on the same work), L2 flushed before each.
-    refs = None
-    if hasattr(wl, "reference_points"):
+    # Reference points (cuBLAS / torch on the same work) and the join kernels alone, L2 flushed.
+    if with_refs and hasattr(wl, "reference_points"):
         refs = {}
         for label, fn, kind, work in wl.reference_points():
-            t = time_alone(fn)
+            fn(stream)
+            t = time_events(torch, stream, fn, 20, fl)
             if kind == "tensor":
                 v = work / (t * 1e-3) / 1e12
                 refs[label] = {"ms": round(t, 5), "TFLOP/s": v, "frac_tensor": v / peaks["bf16_tflops"]}
@@ -1225,158 +1176,251 @@ def run_ours(args):
                 refs[label] = {"ms": round(t, 5), "GB/s": v, "frac_hbm": v / peaks["hbm_gbs"]}
         wl.phase_extract(stream)   # the shards the reference copy overwrote (same bytes) -- keep them exact
         stream.synchronize()
-
-    # The join kernels on their own (when the step fuses them away), L2 flushed before each.
-    joins = None
-    if hasattr(wl, "join_phases"):
+        res["reference_points"] = refs
+    if with_refs and hasattr(wl, "join_phases"):
         joins = {}
         for label, fn, nbytes in wl.join_phases():
             fn(stream)
-            ms = []
-            for _ in range(20):
-                s_, e_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                with torch.cuda.stream(stream):
-                    flush()
-                s_.record(stream)
-                fn(stream)
-                e_.record(stream)
-                e_.synchronize()
-                ms.append(s_.elapsed_time(e_))
-            t = float(np.mean(ms))
+            t = time_events(torch, stream, fn, 20, fl)
             joins[label] = {"ms": round(t, 5), "GB/s": nbytes / (t * 1e-3) / 1e9,
                             "frac_hbm": nbytes / (t * 1e-3) / 1e9 / peaks["hbm_gbs"]}
         tp.tp_device_status(stream)
+        res["join_kernels"] = joins
+    return res
 
-    # End to end through the same public calls with host buffers (the attention projections):
-    # each step copies its activations in from page-locked host memory and reads Z back, and
-    # is timed alone (no overlap with the next step; inside the step the rowwise inputs are
-    # copied on a second stream while the QKV projection runs).
-    e2e = None
-    if hasattr(wl, "setup_e2e"):
-        wl.setup_e2e()
 
-        def time_e2e(step=None, graph=False, **kw):
-            step = step or (lambda st: wl.step_e2e(st, **kw))
-            run = step
-            if graph:
-                # The whole step (copies in, projections, copies out, on three streams) as one CUDA
-                # graph: replaying it costs the host one launch instead of ~40 enqueues.
-                step(stream)
-                stream.synchronize()
-                g = torch.cuda.CUDAGraph()
-                with torch.cuda.graph(g, stream=stream):
-                    step(stream)
-                run = lambda st: g.replay()  # noqa: E731
-            for _ in range(max(1, args.warmup)):
-                with torch.cuda.stream(stream):
-                    run(stream)
-            stream.synchronize()
-            ms = []
-            for _ in range(min(args.steps, 100)):
-                s_, e_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                with torch.cuda.stream(stream):
-                    flush()
-                    s_.record(stream)
-                    run(stream)
-                    e_.record(stream)
-                e_.synchronize()
-                ms.append(s_.elapsed_time(e_))
-            tp.tp_device_status(stream)
-            return max_over_ranks(dist, float(np.mean(ms)), device)
+def roofline_of(res, workload, peaks, sustained):
+    """The roofline object for the dominant kernel of a measure() result."""
+    label = res["dominant"]
+    k = res["kernels"][label]
+    if "TFLOP/s" in k:
+        peak = peaks["bf16_tflops_sustained"] if sustained else peaks["bf16_tflops"]
+        return {"bound": "tensor", "achieved": k["TFLOP/s"], "peak": peak, "unit": "TFLOP/s",
+                "frac": k["TFLOP/s"] / peak, "frac_of_burst": k["TFLOP/s"] / peaks["bf16_tflops"],
+                "kernel": f"tp_gemm_kernel ({label})" if label != "attention" else "tp_flash_kernel",
+                "peak_source": peaks["source"] + (" sustained" if sustained else " burst"),
+                "launch_ms": k["ms"], "traffic": recorded_traffic(f"{workload}:{label}", "gemm")}
+    return {"bound": "hbm", "achieved": k["GB/s"], "peak": peaks["hbm_gbs"], "unit": "GB/s",
+            "frac": k["GB/s"] / peaks["hbm_gbs"], "kernel": label, "peak_source": peaks["source"],
+            "launch_ms": k["ms"], "traffic": recorded_traffic(f"{workload}:{label}", "copy")}
 
-        e2e_chunked_ms = None
-        chunked_matches = None
-        if hasattr(wl, "step_e2e_chunked") and wl.fused_gather and wl.mode == "accum":
-            e2e_chunked_ms = time_e2e(step=lambda st: wl.step_e2e_chunked(st), graph=True)
-            # The pipelined step's Z (read back to host memory) against the device-resident step's.
-            run_step(wl, stream)
-            stream.synchronize()
-            z_dev = wl.z.clone()
-            wl.step_e2e_chunked(stream)
-            stream.synchronize()
-            chunked_matches = bool(torch.equal(wl.pin["z"].to(device).view(torch.int16), z_dev.view(torch.int16)))
-        e2e_ms = time_e2e()
-        e2e_w_ms = time_e2e(weights_from_host=True)
-        head_ms = e2e_chunked_ms if e2e_chunked_ms is not None else e2e_ms
-        e2e = {"value": total_flops / (head_ms * 1e-3) / 1e12, "unit": UNIT,
-               "h2d_bytes_per_step": int(wl.h2d_bytes), "d2h_bytes_per_step": int(wl.d2h_bytes),
-               "ms_per_step": head_ms,
-               "inputs": "activations X and A_r from page-locked host memory; weights resident in HBM, "
-                         "shards extracted every step",
-               "pipelining": "A (every rank's A_r side by side) copied in first and its out-projection's Z "
-                             "read back while X comes in, in two row blocks, each projected as soon as it "
-                             "has landed; the step replayed as one CUDA graph"
-                             if e2e_chunked_ms is not None else "none",
-               "pipelined_output_bit_identical_to_device_step": chunked_matches,
-               "unchunked": {"value": total_flops / (e2e_ms * 1e-3) / 1e12, "ms_per_step": e2e_ms,
-                             "what": "the same step as one block of rows (copies of A_r overlap the QKV "
-                                     "projection only)"},
-               "weights_from_host": {
-                   "value": total_flops / (e2e_w_ms * 1e-3) / 1e12, "ms_per_step": e2e_w_ms,
-                   "h2d_bytes_per_step": int(wl.h2d_bytes + wl.h2d_bytes_weights),
-                   "what": "the same step with every rank's weight slice read from page-locked host "
-                           "memory (shard-on-read) every step"}}
 
-    cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        if isinstance(wl, AttnProjWorkload):
-            cpu = cpu_baseline(wl.host, wl.T, wl.p, wl.H, wl.heads, wl.hd, wl.flops)
-        else:
-            cpu = generic_cpu_baseline(wl)
+def time_e2e(torch, tp, stream, fn, warmup, reps, flush=None):
+    for _ in range(max(1, warmup)):
+        with torch.cuda.stream(stream):
+            fn(stream)
+    stream.synchronize()
+    t = time_events(torch, stream, fn, reps, flush)
+    tp.tp_device_status(stream)
+    return t
 
-    if rank == 0:
-        cfg = wl.config()
-        cfg.update({"parallelism": f"tp{wl.p} simulated on each GPU; replicas across GPUs",
-                    "l2": "flushed between steps (256 MiB write, then 256 MiB read)",
-                    "sms": torch.cuda.get_device_properties(device).multi_processor_count})
-        line = {
-            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": slowest_ms, "higher_is_better": True, "scaling": "weak",
+
+def attn_proj_extras(args, tp, torch, device, stream, peaks, flush):
+    """Per-kernel figures of the attention projections (tokens 4096, hidden 3072, tp 4), both join
+    forms of the rowwise out-projection, and the end-to-end step with host buffers."""
+    wl = AttnProjWorkload(tp, torch, device, "accum", fused_gather=True)
+    res = measure(wl, args, tp, torch, device, stream, peaks, flush=flush, steps=args.steps)
+    # The rowwise out-projection in its other join form: fp32 partials through an HBM workspace,
+    # summed in the GEMM epilogue (the counters' clear and the GEMM, one phase).
+    ws_bytes = tp.tp_rowwise_workspace_bytes(wl.p, wl.T, wl.H, "workspace")
+    wsbuf = torch.empty(ws_bytes, dtype=torch.uint8, device=device)
+    z_ws = torch.empty_like(wl.z)
+    fn = lambda st: tp.tp_linear_rowwise(wl.a_sh, wl.out_sh, mode="workspace", workspace=wsbuf, out=z_ws,  # noqa
+                                         stream=st)
+    fn(stream)
+    t = time_events(torch, stream, fn, 20, flush)
+    tp.tp_device_status(stream)
+    v = wl.flops_out / (t * 1e-3) / 1e12
+    extra = 2.0 * wl.p * wl.T * wl.H * 4
+    res["kernels"]["rowwise_out_workspace"] = {
+        "ms": round(t, 5), "TFLOP/s": v, "frac_tensor": v / peaks["bf16_tflops"],
+        "workspace_bytes_per_launch": extra,
+        "traffic": recorded_traffic(f"{ATTN_PROJ}:rowwise_out_workspace", "gemm"),
+        "what": "TP_REDUCE_WORKSPACE: every rank's fp32 partial tile written to the workspace and summed back in "
+                "rank order by the tile's CTAs (2*p*T*N*4 bytes more than the on-chip sum)"}
+    with torch.cuda.stream(stream):
+        wl.phase_rowwise(stream)
+    stream.synchronize()
+    res["rowwise_join_forms_bit_identical"] = bool(torch.equal(z_ws.view(torch.int16), wl.z.view(torch.int16)))
+    # End to end (host buffers): activations in, Z out, pipelined over row blocks, one graph.
+    wl.setup_e2e()
+    step = lambda st: wl.step_e2e_chunked(st)  # noqa: E731
+    step(stream)
+    stream.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        step(stream)
+    e2e_ms = time_e2e(torch, tp, stream, lambda st: g.replay(), args.warmup, min(args.steps, 50), flush)
+    res["e2e"] = {"value": wl.flops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT, "ms_per_step": e2e_ms,
+                  "h2d_bytes_per_step": int(wl.h2d_bytes), "d2h_bytes_per_step": int(wl.d2h_bytes)}
+    res["config"] = wl.config()
+    res["flops_per_step"] = wl.flops
+    return res
+
+
+def block_extras(args, tp, torch, device, stream, peaks, flush):
+    """Per-kernel figures of the full attention + SwiGLU MLP block at tp 4."""
+    saved = args.tp
+    args.tp = 4
+    try:
+        wl = BlockWorkload(tp, torch, device, 4)
+    finally:
+        args.tp = saved
+    res = measure(wl, args, tp, torch, device, stream, peaks, flush=flush, steps=args.steps, with_refs=False)
+    res["config"] = wl.config()
+    res["flops_per_step"] = wl.flops
+    return res
+
+
+def run_ours(args):
+    refuse_multi_gpu(args)
+    import torch
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    from __graft_entry__ import build
+    build()
+    import tensor_sharded_linear_tp_gb300 as tp
+    stream = torch.cuda.Stream(device)
+    peaks = load_peaks()
+    if args.workload == WORKLOAD:
+        return run_stack(args, tp, torch, device, stream, peaks)
+    flush = L2Flush(torch, device)
+    wl = make_workload(args.workload, args, tp, torch, device)
+    res = measure(wl, args, tp, torch, device, stream, peaks, flush=flush, sampler=ClockSampler(0))
+    cpu = None if args.no_cpu_baseline else generic_cpu_baseline(wl)
+    cfg = wl.config()
+    cfg.update({"parallelism": f"tp{wl.p} simulated on one GPU", "l2": "flushed between steps "
+                "(256 MiB write, then 256 MiB read)", "sms": torch.cuda.get_device_properties(device).multi_processor_count})
+    line = {"metric": METRIC, "value": res["value"], "unit": UNIT, "n_gpus": 1, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": res["ms_per_step"], "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,0.02) weights, N(0,1) activations)",
-            "config": cfg, "roofline": roofline, "kernels": kernels,
-            "extract_gbs": kernels["extract"]["GB/s"], "extract_frac_hbm": kernels["extract"]["frac_hbm"],
-            "gemm_tflops": sum(wl_work for (lb, _, kd, wl_work) in phases if kd == "tensor") /
-            (sum(kernels[k]["ms"] for k in tensor_phases) * 1e-3) / 1e12,
-            "cpu_baseline": cpu, "e2e": e2e, "join_kernels": joins, "reference_points": refs,
-            "gpu_launches": wl.launches_per_step * args.steps, "clocks": clocks,
-            "bracket_s": t_wall, "peaks": peaks, "launch": "eager" if args.eager else "cuda_graph_per_step",
-            "phase_sum_ms": float(phase.sum(axis=1).mean()),
-            "step_output_bit_identical_to_phases": step_matches_phases,
-            "eager_ms_per_step": float(eager_phase.sum(axis=1).mean()),
-            "eager_phase_ms": [round(float(v), 5) for v in eager_phase.mean(axis=0)],
-            "host_enqueue_ms_per_step": host_enqueue_ms,
-        }
-        print(json.dumps(line))
-    if dist is not None:
-        dist.destroy_process_group()
+            "config": cfg, "roofline": roofline_of(res, args.workload, peaks, sustained=False),
+            "cpu_baseline": cpu, "gpu_launches": wl.launches_per_step * args.steps, "peaks": peaks}
+    line.update({k: v for k, v in res.items() if k not in ("value", "ms_per_step")})
+    print(json.dumps(line))
+
+
+def run_stack(args, tp, torch, device, stream, peaks):
+    """The default line: the 8-block stack, shard-on-read, with the other workloads' kernels beside it."""
+    wl = StackWorkload(tp, torch, device)
+
+    # Shard-on-read of the whole state dict, against a plain page-locked copy of 1 GiB.
+    wl.load(stream)
+    stream.synchronize()
+    tp.tp_device_status(stream)
+    load_ms = time_events(torch, stream, wl.load, 3)
+    probe_n = 1 << 30
+    src = torch.empty(probe_n, dtype=torch.uint8, pin_memory=True)
+    dst = torch.empty(probe_n, dtype=torch.uint8, device=device)
+
+    def link_copy(st):
+        with torch.cuda.stream(st):
+            dst.copy_(src, non_blocking=True)
+    link_copy(stream)
+    copy_ms = time_events(torch, stream, link_copy, 3)
+    del dst, src
+    load_gbs = wl.shard_bytes / (load_ms * 1e-3) / 1e9
+    link_gbs = probe_n / (copy_ms * 1e-3) / 1e9
+
+    # The forward pass (the timed steps), clocks sampled during it.
+    sampler = ClockSampler(0)
+    res = measure(wl, args, tp, torch, device, stream, peaks, flush=None, sampler=sampler)
+    roof = roofline_of(res, WORKLOAD, peaks, sustained=True)
+
+    # End to end with host buffers (every weight slice, the input and the output cross the link).
+    e2e_ms = time_e2e(torch, tp, stream, lambda st: wl.step_e2e(st, pipelined=True), 1, 3)
+    e2e_serial_ms = time_e2e(torch, tp, stream, lambda st: wl.step_e2e(st, pipelined=False), 1, 3)
+    # The pipelined step's output against the device-resident forward's, bit for bit.
+    wl.forward(stream)
+    stream.synchronize()
+    z_dev = wl.z.clone()
+    wl.step_e2e(stream, pipelined=True)
+    stream.synchronize()
+    e2e_same = bool(torch.equal(wl.z_pin.to(device).view(torch.int16), z_dev.view(torch.int16)))
+    h2d = wl.shard_bytes + wl.T * wl.H * 2
+    d2h = wl.T * wl.H * 2
+
+    flush = L2Flush(torch, device)
+    extras = {}
+    if not args.no_extras:
+        extras[ATTN_PROJ] = attn_proj_extras(args, tp, torch, device, stream, peaks, flush)
+        extras["block_tp4"] = block_extras(args, tp, torch, device, stream, peaks, flush)
+    cpu = None if args.no_cpu_baseline else stack_cpu_baseline(wl)
+
+    cfg = wl.config()
+    cfg.update({"parallelism": f"tp{wl.p} simulated on one GPU",
+                "l2": "inputs larger than L2: every step reads 5.44 GB of weight shards (no flush)",
+                "sms": torch.cuda.get_device_properties(device).multi_processor_count})
+    line = {
+        "metric": METRIC, "value": res["value"], "unit": UNIT, "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": res["ms_per_step"], "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,0.02) weights, N(0,1) activations)",
+        "config": cfg, "roofline": roof, "kernels": res["kernels"],
+        "shard_load": {"bytes": wl.shard_bytes, "ms": load_ms, "GB/s": load_gbs, "link_copy_GB/s": link_gbs,
+                       "frac_of_link_copy": load_gbs / link_gbs, "frac_hbm": load_gbs / peaks["hbm_gbs"],
+                       "what": "every rank's slice of all 16 weights from page-locked host memory into device "
+                               "shards (tp_plan_shard_ranks), against a 1 GiB page-locked host-to-device copy"},
+        "e2e": {"value": wl.flops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT, "ms_per_step": e2e_ms,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "inputs": "every rank's weight slices (shard-on-read, 5.44 GB) and X from page-locked host memory "
+                          "every step; Z read back",
+                "pipelining": "X and the blocks' slices arrive in block order on a copy stream; block b computes as "
+                              "soon as its slices have landed",
+                "output_bit_identical_to_device_step": e2e_same,
+                "unpipelined": {"value": wl.flops / (e2e_serial_ms * 1e-3) / 1e12, "ms_per_step": e2e_serial_ms}},
+        "cpu_baseline": cpu,
+        "gpu_launches": wl.launches_per_step * args.steps,
+        "clocks": res["clocks"], "peaks": peaks,
+    }
+    for k in ("phase_sum_ms", "step_output_bit_identical_to_phases", "eager_ms_per_step", "host_enqueue_ms_per_step",
+              "bracket_s", "launch"):
+        line[k] = res[k]
+    for name, r in extras.items():
+        line[name] = {k: v for k, v in r.items() if k not in ("clocks", "dominant")}
+        line[name]["roofline"] = roofline_of(r, ATTN_PROJ if name == ATTN_PROJ else "block_sweep", peaks,
+                                             sustained=False)
+    if ATTN_PROJ in extras:
+        ex = extras[ATTN_PROJ]["kernels"]["extract"]
+        line["extract_gbs"] = ex["GB/s"]
+        line["extract_frac_hbm"] = ex["frac_hbm"]
+    print(json.dumps(line))
 
 
 def run_reference(args):
-    """The CPU oracle as the reference arm: each step is a bounded sample of the same workload."""
-    rank, world, _ = dist_env()
-    if rank != 0:
+    """The CPU oracle as the reference arm, on the default workload: each step one block of the stack
+    (blocks in turn) on a seeded sample of token rows, every rank's shards of its two weights extracted."""
+    if int(os.environ.get("RANK", "0")) != 0:
         return
     cfg = tp_inputs.WORKLOADS[WORKLOAD]
-    p, T, H, heads, hd = cfg["tp"], cfg["tokens"], cfg["hidden"], cfg["heads"], cfg["head_dim"]
-    w_qkv, w_out, x, a = tp_inputs.attn_proj_inputs(cfg["seed"], T, H)
-    host = dict(w_qkv=w_qkv, w_out=w_out, x=x, a=a)
-    flops_full = 2.0 * T * H * 3 * H + 2.0 * T * H * H
-    # Each step a bounded sample so that warmup + steps stay within a few minutes.
-    per_step_s = max(0.05, min(6.0, 150.0 / max(1, args.steps + args.warmup)))
-    rows_n = calibrate_rows(host, T, p, H, heads, hd, per_step_s)
+    p, nb, T, H, F, seed = cfg["tp"], cfg["blocks"], cfg["tokens"], cfg["hidden"], cfg["ffn"], cfg["seed"]
+    from oracle import tp_oracle as O
+    jobs = [(b, which) for b in range(nb) for which in ("gate_up", "down")]
+    with ThreadPoolExecutor(max_workers=min(16, os.cpu_count() or 1)) as ex:
+        bits = list(ex.map(lambda j: tp_inputs.stack_weight(seed, j[0], j[1], H, F), jobs))
+    x = tp_inputs.stack_input(seed, nb, T, H)
+    n_rows = 64
+    flops_block = 2.0 * n_rows * (H * 2 * F + F * H)
+
+    def one(k):
+        b = k % nb
+        gu, dn = bits[2 * b], bits[2 * b + 1]
+        rows = tp_inputs.sample_rows(40 + k, T, n_rows)
+        t0 = time.perf_counter()
+        O.mlp_forward(x[rows], [O.shard(gu, "colwise", p, r, [F, F]) for r in range(p)],
+                      [O.shard(dn, "rowwise", p, r) for r in range(p)], "swiglu")
+        return time.perf_counter() - t0
     for w in range(args.warmup):
-        time_oracle(host, tp_inputs.sample_rows(20 + w, T, rows_n), p, H, heads, hd)
-    times = [time_oracle(host, tp_inputs.sample_rows(40 + k, T, rows_n), p, H, heads, hd)
-             for k in range(args.steps)]
-    flops = flops_full * rows_n / T
-    value = flops / float(np.mean(times)) / 1e12
+        one(w)
+    times = [one(args.warmup + k) for k in range(args.steps)]
+    value = flops_block / float(np.mean(times)) / 1e12
     cores = int(os.environ["OPENBLAS_NUM_THREADS"])
-    sample = f"{rows_n} of {T} token rows per step (all shards extracted, float64 numpy oracle)"
+    sample = (f"one block per step (blocks in turn) on {n_rows} of {T} token rows, every rank's shards of the "
+              f"block's two weights extracted (float64 numpy oracle)")
     line = {
-        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": float(np.mean(times)) * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "tokens": T, "hidden": H, "heads": heads, "head_dim": hd, "tp_degree": p},
+        "config": {"workload": WORKLOAD, "blocks": nb, "tokens": T, "hidden": H, "ffn": F, "tp_degree": p},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -1404,6 +1448,7 @@ def run_st_load(args):
     import shutil
     import tempfile
 
+    refuse_multi_gpu(args)
     import torch
     from __graft_entry__ import build
     build()
@@ -1497,29 +1542,30 @@ def run_st_load(args):
 
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
-    ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=1000)
-    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--gpus", type=int, default=1, help="must be 1: the library runs every rank on one GPU")
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--reduce-mode", choices=["accum", "workspace", "none"], default="accum")
+    ap.add_argument("--reduce-mode", choices=["accum", "workspace", "none"], default="accum",
+                    help="rowwise join of --workload attn_proj_tp4")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing leg")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="default workload: skip the attention-projection and block figures beside the stack")
     ap.add_argument("--eager", action="store_true", help="launch the timed steps eagerly instead of as graphs")
     ap.add_argument("--unfused-gather", action="store_true",
                     help="attention projections: gather the QKV slices with a separate tp_combine kernel instead "
                          "of writing the gathered layout from the colwise GEMM")
     ap.add_argument("--workload", default=WORKLOAD,
-                    choices=[WORKLOAD, "tiny_mlp_tp2", "swiglu_mlp_tp4", "block_sweep", "single_stream_tp4",
-                             "stack8_swiglu_tp4", "st_load_single_stream"],
-                    help="the attention projections (default), the tiny or SwiGLU MLP block, the full block "
-                         "(with --tp), the single-stream block, the 8-block stack loaded shard-on-read from "
-                         "page-locked memory, or shard-on-read from a safetensors file")
+                    choices=[WORKLOAD, ATTN_PROJ, "tiny_mlp_tp2", "swiglu_mlp_tp4", "block_sweep",
+                             "single_stream_tp4", "st_load_single_stream"],
+                    help="the 8-block stack loaded shard-on-read (default), the attention projections, the tiny "
+                         "or SwiGLU MLP block, the full block (with --tp), the single-stream block, or "
+                         "shard-on-read from a safetensors file")
     ap.add_argument("--tp", type=int, default=4, help="tp_degree of --workload block_sweep / single_stream_tp4")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)   # at least three untimed warm-up steps, whatever was asked
     if args.impl == "reference":
         run_reference(args)
-    elif args.workload == "stack8_swiglu_tp4":
-        run_stack(args)
     elif args.workload == "st_load_single_stream":
         run_st_load(args)
     else:
