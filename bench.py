@@ -657,7 +657,8 @@ class BlockWorkload:
         self.phase_down(stream)
 
     def phase_qkv(self, stream):
-        self.tp.tp_linear_colwise(self.x, self.qkv_sh, "none", y_shards=self.y_sh, stream=stream)
+        # Q, K and V feed the softmax: chunked fp32 accumulation (TP_ACCUM_CHUNKED).
+        self.tp.tp_linear_colwise(self.x, self.qkv_sh, "none", y_shards=self.y_sh, stream=stream, chunked=True)
 
     def phase_attention(self, stream):
         self.tp.tp_attention_heads_ranks(self.y_sh, self.heads // self.p, self.hd, outs=self.o_sh,
@@ -779,8 +780,9 @@ class SingleStreamWorkload:
         self.phase_out(stream)
 
     def phase_qkv(self, stream):
+        # Q, K and V feed the softmax: chunked fp32 accumulation (TP_ACCUM_CHUNKED).
         self.tp.tp_linear_colwise(self.x, [s[:3 * self.w] for s in self.in_sh], "none", y_shards=self.qkv,
-                                  stream=stream)
+                                  stream=stream, chunked=True)
 
     def phase_gate_up(self, stream):
         self.tp.tp_linear_colwise(self.x, [s[3 * self.w:] for s in self.in_sh], "swiglu",
@@ -1238,10 +1240,6 @@ def attn_proj_extras(args, tp, torch, device, stream, peaks, flush):
         "traffic": recorded_traffic(f"{ATTN_PROJ}:rowwise_out_workspace", "gemm"),
         "what": "TP_REDUCE_WORKSPACE: every rank's fp32 partial tile written to the workspace and summed back in "
                 "rank order by the tile's CTAs (2*p*T*N*4 bytes more than the on-chip sum)"}
-    with torch.cuda.stream(stream):
-        wl.phase_rowwise(stream)
-    stream.synchronize()
-    res["rowwise_join_forms_bit_identical"] = bool(torch.equal(z_ws.view(torch.int16), wl.z.view(torch.int16)))
     # End to end (host buffers): activations in, Z out, pipelined over row blocks, one graph.
     wl.setup_e2e()
     step = lambda st: wl.step_e2e_chunked(st)  # noqa: E731

@@ -75,6 +75,8 @@ typedef enum {
 typedef enum { TP_COLWISE = 0, TP_ROWWISE = 1 } tp_style;
 typedef enum { TP_GATHER = 0, TP_REDUCE = 1 } tp_combine_mode;
 typedef enum { TP_ACT_NONE = 0, TP_ACT_GELU_TANH = 1, TP_ACT_SWIGLU = 2 } tp_act;
+/* Flag OR'd into tp_linear_colwise's act argument: chunked fp32 accumulation (see there). */
+#define TP_ACCUM_CHUNKED 0x100
 typedef enum {
   TP_REDUCE_NONE = 0,      /* write every rank's fp32 partial; join later with tp_combine(TP_REDUCE) */
   TP_REDUCE_WORKSPACE = 1, /* fp32 partials to a workspace, summed in the GEMM epilogue by the ranks */
@@ -222,6 +224,21 @@ TP_API tp_status tp_plan_shard_many(const tp_shard_request* requests, int n_requ
  *              with ldy = tp_degree*N_out writes the gathered (AllGather)
  *              output [T, tp_degree*N_out] directly.
  * Accumulation is fp32; outputs are rounded to nearest-even bf16.
+ * act | TP_ACCUM_CHUNKED (TP_ACT_NONE only; TP_ERR_UNSUPPORTED otherwise):
+ *              the tensor core adds each step of 16 products into its fp32
+ *              accumulator without rounding to nearest, so a long K sum drifts:
+ *              over K = 6144 about 0.35 % of the bf16 outputs round to the
+ *              other neighbour of the exact value (0.02 % for a sum rounded to
+ *              nearest at every step).  With this flag the products are summed
+ *              on the tensor core in chunks of K = 1024, each from zero, and
+ *              the chunks are added in fp32 with round-to-nearest by the
+ *              epilogue, which brings it to about 0.07 %.  Use it where the
+ *              output feeds a step that amplifies one-ulp differences -- the
+ *              Q, K and V of attention, whose softmax turns a rounding flip in
+ *              a key into a change of every query's weights.  It costs about
+ *              9 % of the projection's time (8 epilogue warps keep the running
+ *              sums in registers; the accumulator is handed to them once per
+ *              chunk instead of once per tile).
  * Alignment (TP_ERR_ALIGNMENT): K % 8 == 0, N_out % 8 == 0, ldy % 8 == 0 and
  * every pointer 16-byte aligned.  tp_degree <= TP_MAX_DEGREE.
  * T == 0 or N_r == 0 enqueues nothing and returns TP_OK.

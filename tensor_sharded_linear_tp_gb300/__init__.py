@@ -37,6 +37,7 @@ STATUS_NAMES = ["TP_OK", "TP_ERR_INVALID_ARG", "TP_ERR_HEADS_NOT_DIVISIBLE", "TP
                 "TP_ERR_FORMAT", "TP_ERR_NOT_FOUND"]
 STYLES = {"colwise": 0, "rowwise": 1}
 ACTS = {"none": 0, "gelu_tanh": 1, "swiglu": 2}
+ACCUM_CHUNKED = 0x100   # TP_ACCUM_CHUNKED (include/tp.h): OR'd into the colwise act argument
 REDUCE_MODES = {"none": 0, "workspace": 1, "accum": 2}
 COMBINE_MODES = {"gather": 0, "reduce": 1}
 MAX_DEGREE = 16
@@ -265,8 +266,13 @@ def tp_plan_shard_many(requests: Sequence[dict], device=None, stream=None) -> li
 
 def tp_linear_colwise(x: torch.Tensor, w_shards: Sequence[torch.Tensor], act: str = "none",
                       bias_shards: Sequence[torch.Tensor | None] | None = None,
-                      y_shards: Sequence[torch.Tensor] | None = None, ldy: int = 0, stream=None):
-    """Y_r = act(X W_r^T + b_r) for every rank r, one launch.  Returns the list of Y_r."""
+                      y_shards: Sequence[torch.Tensor] | None = None, ldy: int = 0, stream=None,
+                      chunked: bool = False):
+    """Y_r = act(X W_r^T + b_r) for every rank r, one launch.  Returns the list of Y_r.
+
+    chunked=True (act "none" only): the K sum is formed in chunks of 1024 on the tensor core and
+    the chunks are added with round-to-nearest (TP_ACCUM_CHUNKED), for outputs that feed
+    attention."""
     _need_bf16("x", x)
     p = len(w_shards)
     T, K = x.shape
@@ -277,7 +283,8 @@ def tp_linear_colwise(x: torch.Tensor, w_shards: Sequence[torch.Tensor], act: st
     if y_shards is None:
         y_shards = [torch.empty((T, n_out), dtype=torch.bfloat16, device=x.device) for _ in range(p)]
     bias_arr = _ptrs(bias_shards) if bias_shards is not None else None
-    _check(lib.tp_linear_colwise(_ptr(x), _ptrs(w_shards), bias_arr, ACTS[act], p, T, K, N_r, _ptrs(y_shards), ldy,
+    code = ACTS[act] | (ACCUM_CHUNKED if chunked else 0)
+    _check(lib.tp_linear_colwise(_ptr(x), _ptrs(w_shards), bias_arr, code, p, T, K, N_r, _ptrs(y_shards), ldy,
                                  _stream(stream)))
     return y_shards
 

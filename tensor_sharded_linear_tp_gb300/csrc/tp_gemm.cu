@@ -56,11 +56,25 @@ constexpr int BM = 128;        // accumulator rows per CTA (TMEM lanes)
 constexpr int BN = 256;        // accumulator columns per tile
 constexpr int BK = 64;         // K per stage: one 128-byte swizzle row of bf16
 constexpr int GROUP_M = 16;
-constexpr int kThreads = 192;
 constexpr int kTmemCols = 512; // two accumulators of BN columns
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
-enum Epi : int { EPI_BF16 = 0, EPI_GELU = 1, EPI_SWIGLU = 2, EPI_F32 = 3, EPI_WS_REDUCE = 4 };
+// EPI_BF16_CHUNKED: the K sum is formed on the tensor core in chunks of kChunkKBlocks k-blocks
+// (K = 1024), each started from zero in one of the two accumulators, and the epilogue adds the
+// chunks in fp32 with round-to-nearest (see epilogue_chunked).  The chunk length is set by the
+// epilogue: pulling a chunk's 128 KB out of tensor memory while the tensor core runs takes each
+// epilogue warp about 2 us, so a chunk must hold more MMA work than that.  Measured on the
+// Q/K/V projection of the block (T 4608, K 6144, 4 x 4608 columns): chunks of 4 / 8 / 16 / 24
+// k-blocks took 1.51 / 1.14 / 1.09 / 1.10 times the plain launch, and 0.020 / 0.033 / 0.068 /
+// 0.100 % of outputs differ from the correctly rounded value (0.35 % plain); one chunk per tile
+// takes 1.07 times as long, the cost of the 8-warp epilogue itself.
+enum Epi : int { EPI_BF16 = 0, EPI_GELU = 1, EPI_SWIGLU = 2, EPI_F32 = 3, EPI_WS_REDUCE = 4, EPI_BF16_CHUNKED = 5 };
+constexpr int kChunkKBlocks = 16;
+
+// Epilogue warps: 4 (one per TMEM lane quarter), or 8 for the chunked sum (two per lane quarter,
+// each holding the running sums of half of the tile's columns in registers).
+__host__ __device__ constexpr int epilogue_warps(int epi) { return epi == EPI_BF16_CHUNKED ? 8 : 4; }
+__host__ __device__ constexpr int threads_of(int epi) { return 64 + 32 * epilogue_warps(epi); }
 
 // Tile shape of the single-CTA (kPair = false) and CTA-pair (kPair = true) kernels.
 template <bool kPair>
@@ -220,7 +234,14 @@ __device__ __forceinline__ float silu_f(float x) { return __fdividef(x, 1.0f + _
 // -- so the 32 lanes hit all banks, and then sent to global memory by one TMA store
 // (rows and columns outside the output are clipped).  A buffer is reused only after
 // its previous store has finished reading it.
-__device__ __forceinline__ uint32_t stage_buffer(uint32_t wbuf, int nchunk, int lane) {
+__device__ __forceinline__ uint32_t stage_buffer(uint32_t wbuf, int nchunk, int lane, bool single = false) {
+  if (single) {  // one buffer: the previous store must have finished reading it
+    if (nchunk >= 1) {
+      if (lane == 0) ptx::bulk_wait_read_0();
+      __syncwarp();
+    }
+    return wbuf;
+  }
   const uint32_t buf = wbuf + static_cast<uint32_t>(nchunk & 1) * kStageBuf;
   if (nchunk >= 2) {
     if (lane == 0) ptx::bulk_wait_read_1();
@@ -262,8 +283,9 @@ __device__ __forceinline__ void stage_store_f32(const CUtensorMap* map, uint32_t
 
 // bf16: 64 columns given as two halves of 32.
 __device__ __forceinline__ void stage_store_bf16x64(const CUtensorMap* map, uint32_t wbuf, int& nchunk, int lane,
-                                                    const float (&lo)[32], const float (&hi)[32], int x, int y) {
-  const uint32_t buf = stage_buffer(wbuf, nchunk, lane);
+                                                    const float (&lo)[32], const float (&hi)[32], int x, int y,
+                                                    bool single = false) {
+  const uint32_t buf = stage_buffer(wbuf, nchunk, lane, single);
   const uint32_t row = buf + static_cast<uint32_t>(lane) * 128;
   uint32_t packed[16];
   pack_bf16x32(lo, packed);
@@ -281,8 +303,8 @@ __device__ __forceinline__ void stage_store_bf16x64(const CUtensorMap* map, uint
 
 // bf16: 32 columns (the last chunk of a tile whose width is an odd multiple of 32).
 __device__ __forceinline__ void stage_store_bf16x32(const CUtensorMap* map, uint32_t wbuf, int& nchunk, int lane,
-                                                    const float (&f)[32], int x, int y) {
-  const uint32_t buf = stage_buffer(wbuf, nchunk, lane);
+                                                    const float (&f)[32], int x, int y, bool single = false) {
+  const uint32_t buf = stage_buffer(wbuf, nchunk, lane, single);
   const uint32_t row = buf + static_cast<uint32_t>(lane) * 64;
   uint32_t packed[16];
   pack_bf16x32(f, packed);
@@ -507,6 +529,93 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, SmemCtrl* ctl
   }
 }
 
+// Epilogue of EPI_BF16_CHUNKED: 8 warps, warp w (2..9) reading TMEM lane quarter w % 4 and
+// owning column half (w - 2) / 4 of the tile (p.bn / 2 = 64, 96 or 128 columns).  Each chunk of
+// kChunkKBlocks k-blocks arrives in one of the two accumulators, summed on the tensor core from
+// zero; the warp adds it to its running sums (fp32, round to nearest) and releases the
+// accumulator at once, so the MMA warp runs one chunk ahead.  After a tile's last chunk the sums
+// get the bias, are rounded to bf16 and stored (one 4 KB staging buffer per warp).
+//
+// Why: the tensor core adds each K=16 step into the fp32 accumulator without rounding to
+// nearest, so over K = 6144 the sum drifts (measured on the GB300: 0.35 % of bf16 outputs round
+// to the other neighbour of the exact value, against 0.02 % for a round-to-nearest fp32 sum);
+// sums of K = 1024 started from zero and added with round-to-nearest bring it to 0.07 %.
+template <bool kPair, bool kQuad>
+__device__ __forceinline__ void epilogue_chunked(const GemmParams& p, SmemCtrl* ctl, uint8_t* staging, uint32_t tmem,
+                                                 int warp, int lane, int unit, int nunits, int total, int n_items,
+                                                 int m_items, int gm_items, int quad, uint32_t pq, uint32_t cta,
+                                                 uint32_t leader) {
+  using C = Cfg<kPair>;
+  volatile int* abort_flag = &ctl->abort;
+  const int q = warp & 3;            // TMEM lane quarter this warp may read
+  const int h = (warp - 2) >> 2;     // column half of the tile
+  const int half = p.bn / 2;
+  const uint32_t wbuf = ptx::smem_addr(staging) + static_cast<uint32_t>(warp - 2) * kStageBuf;
+  const int nchunks = (p.n_ksegs * p.kblocks + kChunkKBlocks - 1) / kChunkKBlocks;
+  int nstore = 0;
+  uint32_t ccount = 0;
+  bool ok = true;
+  for (int t = unit; t < total && ok; t += nunits) {
+    int g, mb, nb;
+    decode_tile(p, t, g, mb, nb, n_items, m_items, gm_items);
+    if (quad == 1) nb = 2 * nb + static_cast<int>(pq);
+    if (quad == 2) mb = 2 * mb + static_cast<int>(pq);
+    float sum[128];
+    for (int c = 0; c < nchunks; ++c, ++ccount) {
+      const uint32_t acc = ccount & 1u;
+      // Warp-uniform outcome: the TMEM loads below are warp-collective.
+      if (!__all_sync(0xffffffffu, wait_bounded(ptx::smem_addr(&ctl->tfull[acc]), (ccount >> 1) & 1u, abort_flag,
+                                                p.status, false))) {
+        ok = false;
+        break;
+      }
+      ptx::tc_fence_after();
+      const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + acc * static_cast<uint32_t>(p.bn) +
+                             static_cast<uint32_t>(h * half);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        if (16 * j < half) {  // warp-uniform
+          uint32_t v[16];
+          ptx::tmem_ld_32x32b_x16(taddr + 16 * j, v);
+          ptx::tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            sum[16 * j + i] = (c == 0) ? __uint_as_float(v[i]) : sum[16 * j + i] + __uint_as_float(v[i]);
+        }
+      }
+      ptx::tc_fence_before();
+      const uint32_t tempty = ptx::smem_addr(&ctl->tempty[acc]);
+      if constexpr (kPair)
+        ptx::mbar_arrive_cluster(ptx::mapa_shared(tempty, leader));  // the leader's MMA warp owns the accumulator
+      else
+        ptx::mbar_arrive(tempty);
+    }
+    if (!ok) break;
+    const int mb128 = mb * (C::TILE_M / BM) + static_cast<int>(cta);
+    const int row0 = mb128 * BM + q * 32;
+    const __nv_bfloat16* bias = p.bias[g];
+    const int colh = nb * p.bn + h * half;   // first output column of this warp's half
+    if (bias != nullptr) {  // warp-uniform
+#pragma unroll
+      for (int i = 0; i < 128; ++i)
+        if (i < half && colh + i < p.N) sum[i] += __bfloat162float(bias[colh + i]);
+    }
+    // Stored straight from the sums: 64 columns (two halves of 32), or 32 for a 96-column half.
+#pragma unroll
+    for (int j = 0; j < 4; j += 2) {
+      const int col0 = colh + 32 * j;
+      if (32 * j >= half || col0 >= p.N) break;
+      const float(&lo)[32] = *reinterpret_cast<const float(*)[32]>(&sum[32 * j]);
+      const float(&hi)[32] = *reinterpret_cast<const float(*)[32]>(&sum[32 * j + 32]);
+      if (32 * j + 64 <= half)
+        stage_store_bf16x64(&p.map_out[g], wbuf, nstore, lane, lo, hi, col0, row0, true);
+      else
+        stage_store_bf16x32(&p.map_out_tail[g], wbuf, nstore, lane, lo, col0, row0, true);
+    }
+  }
+  if (lane == 0) ptx::bulk_wait_all();  // every output store of this warp has landed
+}
+
 // kPair = false: one CTA per 128 x 256 tile.  kPair = true: a cluster of two
 // CTAs per 256 x 256 tile -- each CTA stages its own 128 rows of A and half of
 // B, the even CTA issues cta_group::2 MMAs that read both CTAs' shared memory
@@ -518,7 +627,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, SmemCtrl* ctl
 // either pair is then written by both pairs' producers, so it is free again only once both
 // pairs' MMAs are done with it (two arrivals on every empty barrier).
 template <int kEpi, bool kPair, bool kQuad = false>
-__global__ void __launch_bounds__(kThreads, 1) tp_gemm_kernel(const __grid_constant__ GemmParams p) {
+__global__ void __launch_bounds__(threads_of(kEpi), 1) tp_gemm_kernel(const __grid_constant__ GemmParams p) {
   using C = Cfg<kPair>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -555,7 +664,7 @@ __global__ void __launch_bounds__(kThreads, 1) tp_gemm_kernel(const __grid_const
     }
     for (int a = 0; a < 2; ++a) {
       ptx::mbar_init(ptx::smem_addr(&ctl->tfull[a]), 1);
-      ptx::mbar_init(ptx::smem_addr(&ctl->tempty[a]), kPair ? 256 : 128);
+      ptx::mbar_init(ptx::smem_addr(&ctl->tempty[a]), (kPair ? 2 : 1) * 32 * epilogue_warps(kEpi));
     }
     ptx::mbar_init(ptx::smem_addr(&ctl->drain), 1);
     ctl->abort = 0;
@@ -665,17 +774,41 @@ __global__ void __launch_bounds__(kThreads, 1) tp_gemm_kernel(const __grid_const
     if (lane == 0 && cta == 0) {
       // ------------------------------------------------------------ MMA issuer (leader CTA)
       const uint32_t idesc = ptx::idesc_bf16_f32(C::TILE_M, p.bn);
-      uint32_t it = 0, tcount = 0;
+      // An accumulator is taken (wait until the epilogue has released it) and handed to the
+      // epilogue (commit) once per tile -- or, for EPI_BF16_CHUNKED, once per chunk of
+      // kChunkKBlocks k-blocks, each chunk summed from zero; the two accumulators alternate.
+      uint32_t it = 0, ccount = 0;
+      uint32_t acc = 0, accumulate = 0, d_tmem = tmem;
       bool ok = true;
-      for (int t = unit; t < total && ok; t += nunits, ++tcount) {
-        const uint32_t acc = tcount & 1u;
-        const uint32_t aph = (tcount >> 1) & 1u;
-        if (!wait_bounded<kPair>(ptx::smem_addr(&ctl->tempty[acc]), aph ^ 1u, abort_flag, p.status, false)) break;
+      auto take = [&]() -> bool {
+        acc = ccount & 1u;
+        if (!wait_bounded<kPair>(ptx::smem_addr(&ctl->tempty[acc]), ((ccount >> 1) & 1u) ^ 1u, abort_flag, p.status,
+                                 false))
+          return false;
         ptx::tc_fence_after();
-        const uint32_t d_tmem = tmem + acc * static_cast<uint32_t>(p.bn);
-        uint32_t accumulate = 0;
+        d_tmem = tmem + acc * static_cast<uint32_t>(p.bn);
+        accumulate = 0;
+        return true;
+      };
+      auto hand_over = [&]() {
+        if constexpr (kPair)
+          ptx::umma_commit_pair(ptx::smem_addr(&ctl->tfull[acc]), pair_mask);
+        else
+          ptx::umma_commit(ptx::smem_addr(&ctl->tfull[acc]));
+        ++ccount;
+      };
+      for (int t = unit; t < total && ok; t += nunits) {
+        if (!take()) break;
+        int kdone = 0;
         for (int seg = 0; seg < p.n_ksegs && ok; ++seg) {
-          for (int kb = 0; kb < p.kblocks; ++kb) {
+          for (int kb = 0; kb < p.kblocks; ++kb, ++kdone) {
+            if (kEpi == EPI_BF16_CHUNKED && kdone > 0 && kdone % kChunkKBlocks == 0) {
+              hand_over();
+              if (!take()) {
+                ok = false;
+                break;
+              }
+            }
             const uint32_t s = it % C::STAGES;
             const uint32_t ph = (it / C::STAGES) & 1u;
             if (!wait_bounded(ptx::smem_addr(&ctl->full[s]), ph, abort_flag, p.status, false)) {
@@ -703,10 +836,7 @@ __global__ void __launch_bounds__(kThreads, 1) tp_gemm_kernel(const __grid_const
           }
         }
         if (!ok) break;
-        if constexpr (kPair)
-          ptx::umma_commit_pair(ptx::smem_addr(&ctl->tfull[acc]), pair_mask);
-        else
-          ptx::umma_commit(ptx::smem_addr(&ctl->tfull[acc]));
+        hand_over();
       }
       // Wait for every MMA issued before TMEM and shared memory go away (in both CTAs of a pair).
       if constexpr (kPair)
@@ -718,6 +848,10 @@ __global__ void __launch_bounds__(kThreads, 1) tp_gemm_kernel(const __grid_const
       // The peer CTA: its shared memory feeds the leader's MMAs until the final drain arrives.
       wait_bounded(ptx::smem_addr(&ctl->drain), 0, abort_flag, p.status, true);
     }
+  } else if constexpr (kEpi == EPI_BF16_CHUNKED) {
+    // ---------------------------------------------------------------- epilogue, chunked sum
+    epilogue_chunked<kPair, kQuad>(p, ctl, staging, tmem, warp, lane, unit, nunits, total, n_items, m_items,
+                                   gm_items, quad, pq, cta, leader);
   } else {
     // ---------------------------------------------------------------- epilogue
     const int q = warp & 3;  // TMEM lane quarter this warp may read
@@ -858,7 +992,7 @@ int max_active_pairs(int sms) {
     cudaLaunchConfig_t cfg{};
     constexpr int kCluster = kQuad ? 4 : 2;
     cfg.gridDim = dim3(kCluster * (sms / kCluster), 1, 1);
-    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.blockDim = dim3(threads_of(kEpi), 1, 1);
     cfg.dynamicSmemBytes = smem_bytes<true>();
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -919,7 +1053,7 @@ tp_status launch_gemm(const GemmParams& p, bool pair, cudaStream_t stream) {
   cudaLaunchConfig_t cfg{};
   cudaLaunchAttribute attr[3];
   int nattr = 0;
-  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.blockDim = dim3(threads_of(kEpi), 1, 1);
   cfg.stream = stream;
   if (coop) {
     attr[nattr].id = cudaLaunchAttributeCooperative;
@@ -1041,11 +1175,12 @@ int choose_group_m(int m_tiles, int64_t a_bytes) {
 // launch's time follows its wave count, not waves x width: a sweep of the 16 x N 3072
 // out-projection gave 60.6 / 60.1 / 73.2 / 86.1 / 100.2 us at widths 256 / 224 /
 // 192 / 160 / 128, i.e. 3 / 3 / 4 / 5 / 6 waves.
-int choose_bn(int64_t n_out, int64_t groups_x_mtiles, int units) {
+int choose_bn(int64_t n_out, int64_t groups_x_mtiles, int units, bool halves_of_32 = false) {
   static const int kWidths[] = {256, 224, 192, 160, 128};
   int best = 256;
   int64_t best_waves = -1;
   for (int bn : kWidths) {
+    if (halves_of_32 && (bn / 2) % 32 != 0) continue;  // the chunked epilogue's halves: 128, 96 or 64 columns
     const int64_t tiles = groups_x_mtiles * ((n_out + bn - 1) / bn);
     const int64_t waves = (tiles + units - 1) / units;
     if (best_waves < 0 || waves < best_waves) {
@@ -1078,8 +1213,12 @@ tp_status tp_linear_colwise(const void* x, const void* const* w_shards, const vo
   if (tp_degree < 1) return fail(TP_ERR_INVALID_ARG, "tp_degree must be >= 1, got %d", tp_degree);
   if (tp_degree > TP_MAX_DEGREE)
     return fail(TP_ERR_UNSUPPORTED, "tp_degree=%d above TP_MAX_DEGREE=%d", tp_degree, TP_MAX_DEGREE);
+  const bool chunked = (static_cast<int>(act) & TP_ACCUM_CHUNKED) != 0;
+  act = static_cast<tp_act>(static_cast<int>(act) & ~TP_ACCUM_CHUNKED);
   if (act != TP_ACT_NONE && act != TP_ACT_GELU_TANH && act != TP_ACT_SWIGLU)
     return fail(TP_ERR_INVALID_ARG, "unknown activation %d", (int)act);
+  if (chunked && act != TP_ACT_NONE)
+    return fail(TP_ERR_UNSUPPORTED, "TP_ACCUM_CHUNKED is supported with TP_ACT_NONE only");
   tp_status st = check_dims(T, K, N_r);
   if (st != TP_OK) return st;
   if (act == TP_ACT_SWIGLU && (N_r % 2) != 0)
@@ -1108,7 +1247,7 @@ tp_status tp_linear_colwise(const void* x, const void* const* w_shards, const vo
   const bool pair = use_pair(T);
   GemmParams p{};
   const int64_t m_tiles = (T + (pair ? 2 * BM : BM) - 1) / (pair ? 2 * BM : BM);
-  const int bn = (act == TP_ACT_SWIGLU) ? BN : choose_bn(n_out, tp_degree * m_tiles, resident_units(pair));
+  const int bn = (act == TP_ACT_SWIGLU) ? BN : choose_bn(n_out, tp_degree * m_tiles, resident_units(pair), chunked);
   const int quad = quad_mode(pair, tp_degree, m_tiles, ceil_div(n_out, (act == TP_ACT_SWIGLU) ? BN / 2 : bn));
   p.quad = quad;
   st = make_map(&p.map_a[0], x, K, T, K, quad == 1 ? BM / 2 : BM);
@@ -1142,7 +1281,7 @@ tp_status tp_linear_colwise(const void* x, const void* const* w_shards, const vo
   switch (act) {
     case TP_ACT_GELU_TANH: return launch_gemm<EPI_GELU>(p, pair, s);
     case TP_ACT_SWIGLU: return launch_gemm<EPI_SWIGLU>(p, pair, s);
-    default: return launch_gemm<EPI_BF16>(p, pair, s);
+    default: return chunked ? launch_gemm<EPI_BF16_CHUNKED>(p, pair, s) : launch_gemm<EPI_BF16>(p, pair, s);
   }
 }
 

@@ -250,3 +250,15 @@ def test_noalloc_scratch_size_matches_the_header():
     m = re.search(r"#define TP_NOALLOC_SCRATCH_BYTES \(\(size_t\)(\d+) << (\d+)\)", hdr)
     assert m is not None
     assert tp.NOALLOC_SCRATCH_BYTES == int(m.group(1)) << int(m.group(2))
+
+
+def test_colwise_chunked_flag_checks():
+    # TP_ACCUM_CHUNKED is accepted with TP_ACT_NONE only; other bits are not activations.
+    ws = (ctypes.c_void_p * 2)(*([FAKE] * 2))
+    ys = (ctypes.c_void_p * 2)(*([FAKE] * 2))
+    call = lambda code: tp.STATUS_NAMES[tp.lib.tp_linear_colwise(FAKE, ws, None, code, 2, 64, 256, 512, ys, 0,  # noqa
+                                                                   None)]
+    assert call(tp.ACTS["gelu_tanh"] | tp.ACCUM_CHUNKED) == "TP_ERR_UNSUPPORTED"
+    assert call(tp.ACTS["swiglu"] | tp.ACCUM_CHUNKED) == "TP_ERR_UNSUPPORTED"
+    assert call(0x200) == "TP_ERR_INVALID_ARG"
+    assert tp.ACCUM_CHUNKED == 0x100

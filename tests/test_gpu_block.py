@@ -143,7 +143,8 @@ def gpu_block(x_bits, wqkv, wout, wgu, wdown, p, heads, d, F, mode="accum"):
     out_sh = tp.tp_plan_shard_ranks(dev(wout), "rowwise", p, 0, p, None, heads, d, device=DEV)
     gu_sh = tp.tp_plan_shard_ranks(dev(wgu), "colwise", p, 0, p, [F, F], heads, 0, device=DEV)
     dn_sh = tp.tp_plan_shard_ranks(dev(wdown), "rowwise", p, 0, p, None, heads, 0, device=DEV)
-    ys = tp.tp_linear_colwise(x, qkv_sh, "none")
+    # Q, K and V feed the softmax, which amplifies one-ulp rounding differences: chunked accumulation.
+    ys = tp.tp_linear_colwise(x, qkv_sh, "none", chunked=True)
     hl = heads // p
     os_ = tp.tp_attention_heads_ranks(ys, hl, d)
     z1 = tp.tp_linear_rowwise(os_, out_sh, mode=mode)
@@ -204,7 +205,8 @@ def check_block_against_oracle(got, ref, x_rows, wout, wgu, wdown, p, F, heads, 
 
     def check(*a):
         try:
-            assert_close(*a)
+            st = assert_close(*a)
+            print(a[2], {k: round(v, 5) for k, v in st.items()})
         except AssertionError as e:
             failures.append(e.args[0])
 
@@ -246,7 +248,7 @@ def test_block_small_every_tp_degree_is_bit_identical_to_tp1():
         assert np.array_equal(got, base), p
 
 
-MID = dict(T=392, heads=24, d=128, F=2048)   # head_dim 128 (the fused attention), a ragged token tail
+MID = dict(T=392, heads=24, d=128, F=3072)   # head_dim 128 (the fused attention), a ragged token tail
 
 
 @pytest.mark.parametrize("p", [1, 3, 8])

@@ -48,7 +48,7 @@ def gpu_single_stream(x_bits, w_in, w_out, p, heads, d, F, mode="accum"):
     in_sh = tp.tp_plan_shard_ranks(dev(w_in), "colwise", p, 0, p, [H, H, H, F, F], heads, 0, device=DEV)
     out_sh = tp.tp_plan_shard_ranks(dev(w_out), "rowwise", p, 0, p, [H, F], heads, 0, device=DEV)
     cat = [torch.full((T, w + f), float("nan"), dtype=torch.bfloat16, device=DEV) for _ in range(p)]
-    qkv = tp.tp_linear_colwise(x, [s[:3 * w] for s in in_sh], "none")
+    qkv = tp.tp_linear_colwise(x, [s[:3 * w] for s in in_sh], "none", chunked=True)
     tp.tp_linear_colwise(x, [s[3 * w:] for s in in_sh], "swiglu", y_shards=[c[:, w:] for c in cat], ldy=w + f)
     tp.tp_attention_heads_ranks(qkv, heads // p, d, outs=[c[:, :w] for c in cat])
     z = tp.tp_linear_rowwise(cat, out_sh, mode=mode)
