@@ -136,8 +136,10 @@ TP_API tp_status tp_shard_shape(int64_t rows, int64_t cols, tp_style style, int 
  * full-size weight is ever staged there; §Limitations: enable_parallelism()
  * shards a model already in memory.  Both are this call: `weight` may be
  * page-locked host memory (the slice is read over the CPU-GPU link straight
- * into `dev_out`; nothing else reaches the device) or device memory (a
- * device-to-device copy).  Pageable host memory is rejected with
+ * into `dev_out` by the copy engines, one transfer per packed block -- a
+ * column window of every row for TP_ROWWISE -- so no SM is taken from kernels
+ * running beside the load; nothing else reaches the device) or device memory
+ * (a device-to-device copy kernel).  Pageable host memory is rejected with
  * TP_ERR_NOT_PINNED.
  *
  * Slice definition (§Colwise and rowwise, §Fused projections): with packed
@@ -178,9 +180,9 @@ TP_API tp_status tp_plan_shard_ranks(const void* weight, int64_t rows, int64_t c
  * with the same slice definition, checks and errors.  All requests are
  * checked before anything is copied; a refused request leaves every output
  * untouched and the error message names the request's index.  Requests from
- * device memory share one launch and requests from page-locked host memory
- * another (more launches only beyond 64 copy segments: one per packed block
- * per rank).  1 <= n_requests <= TP_MAX_SHARD_REQUESTS (0 is a no-op);
+ * device memory share one copy-kernel launch (more only beyond 64 copy
+ * segments: one per packed block per rank); requests from page-locked host
+ * memory are one copy-engine transfer per segment.  1 <= n_requests <= TP_MAX_SHARD_REQUESTS (0 is a no-op);
  * `requests` and the arrays it points to are read during the call only.
  */
 #define TP_MAX_SHARD_REQUESTS 64

@@ -9,11 +9,15 @@
 //   * gather: one segment per rank -- rank r's [T, N_each] into columns
 //     [r*N_each, (r+1)*N_each) of the joined output.
 // A segment whose rows are back to back in both source and destination is
-// copied as one long row.  Rows are cut into pieces of at most 4 KiB; a warp
-// copies one piece with 16-byte vector loads and stores, all of the piece's
-// loads (up to 8 per lane) issued before its stores.  Grid: up to 8 blocks of
-// 256 threads per SM, grid-stride over pieces.  HBM-bound: the algorithmic
-// traffic is exactly 2 x the bytes copied.
+// copied as one long row.  From device memory, rows are cut into pieces of at
+// most 4 KiB; a warp copies one piece with 16-byte vector loads and stores, all
+// of the piece's loads (up to 8 per lane) issued before its stores.  Grid: up to
+// 8 blocks of 256 threads per SM, grid-stride over pieces.  HBM-bound: the
+// algorithmic traffic is exactly 2 x the bytes copied.  From page-locked host
+// memory (shard-on-read), each segment is one copy-engine transfer
+// (cudaMemcpyAsync, or cudaMemcpy2DAsync for a column window of every row): the
+// CPU-GPU link bounds it either way, and the copy engines leave the SMs to the
+// GEMMs that run beside a load.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -47,21 +51,15 @@ struct CopyParams {
   int64_t total_units;
 };
 
-__device__ __forceinline__ uint4 load16(const uint4* p, bool host_src) {
+__device__ __forceinline__ uint4 load16(const uint4* p) {
   uint4 v;
-  if (host_src) {
-    // Mapped page-locked host memory: plain coherent load over the CPU-GPU link.
-    asm volatile("ld.global.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
-  } else {
-    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "l"(p));
-  }
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
   return v;
 }
 
 // 16-byte path: every pointer, stride and row length is a multiple of 16 bytes.
-template <bool kHostSrc>
 __global__ void __launch_bounds__(kCopyThreads) copy_segments_v16(const __grid_constant__ CopyParams p) {
   pdl_launch_dependents();
   pdl_wait();
@@ -83,7 +81,7 @@ __global__ void __launch_bounds__(kCopyThreads) copy_segments_v16(const __grid_c
     uint4 v[8];
 #pragma unroll
     for (int j = 0; j < 8; ++j)
-      if (lane + 32 * j < n) v[j] = load16(src + lane + 32 * j, kHostSrc);
+      if (lane + 32 * j < n) v[j] = load16(src + lane + 32 * j);
 #pragma unroll
     for (int j = 0; j < 8; ++j)
       if (lane + 32 * j < n) dst[lane + 32 * j] = v[j];
@@ -145,6 +143,20 @@ struct SegBuilder {
 
 tp_status launch_copy(SegBuilder& b, bool host_src, cudaStream_t stream) {
   if (b.p.total_units == 0) return TP_OK;
+  if (host_src) {
+    // Page-locked host source: one copy-engine transfer per segment (segment sources are host
+    // addresses here).
+    for (int i = 0; i < b.p.nseg; ++i) {
+      const CopySeg& g = b.p.seg[i];
+      const cudaError_t e =
+          g.rows == 1 ? cudaMemcpyAsync(g.dst, g.src, static_cast<size_t>(g.row_bytes), cudaMemcpyHostToDevice, stream)
+                      : cudaMemcpy2DAsync(g.dst, static_cast<size_t>(g.dst_stride), g.src,
+                                          static_cast<size_t>(g.src_stride), static_cast<size_t>(g.row_bytes),
+                                          static_cast<size_t>(g.rows), cudaMemcpyHostToDevice, stream);
+      if (e != cudaSuccess) return cuda_fail(e, "host-to-device shard copy");
+    }
+    return TP_OK;
+  }
   const int sms = sm_count();
   if (sms <= 0) return fail(TP_ERR_CUDA, "cannot query the SM count of the current device");
   const int64_t warps_needed = b.p.total_units;
@@ -156,7 +168,7 @@ tp_status launch_copy(SegBuilder& b, bool host_src, cudaStream_t stream) {
   const dim3 g(static_cast<unsigned>(grid)), blk(kCopyThreads);
   cudaError_t e;
   if (b.vec_ok)
-    e = launch_pdl(host_src ? copy_segments_v16<true> : copy_segments_v16<false>, g, blk, 0, stream, b.p);
+    e = launch_pdl(copy_segments_v16, g, blk, 0, stream, b.p);
   else
     e = launch_pdl(copy_segments_b16, g, blk, 0, stream, b.p);
   if (e == cudaSuccess) e = cudaGetLastError();
@@ -243,8 +255,8 @@ __global__ void __launch_bounds__(256) reduce_partials_scalar(const __grid_const
 namespace tp {
 namespace {
 
-// One validated extraction: the source (device pointer or the device mapping of
-// page-locked host memory), the plan's block sizes and the ranks' outputs.
+// One validated extraction: the source (device memory, or page-locked host memory that the
+// copy engines read), the plan's block sizes and the ranks' outputs.
 struct ShardJob {
   const uint8_t* src = nullptr;
   bool host_src = false;
@@ -290,16 +302,14 @@ tp_status prepare_pointers(const void* weight, void* const* dev_outs, ShardJob* 
   for (int i = 0; i < rank_count; ++i)
     if (dev_outs[i] == nullptr) return fail(TP_ERR_INVALID_ARG, "dev_outs[%d] is NULL", i);
 
-  // Where does the source live?  Page-locked host memory is read through its
-  // device mapping; pageable host memory is refused rather than staged.
+  // Where does the source live?  Page-locked host memory is read by the copy engines;
+  // pageable host memory is refused rather than staged.
   cudaPointerAttributes attr{};
   cudaError_t e = cudaPointerGetAttributes(&attr, weight);
   if (e != cudaSuccess) return cuda_fail(e, "cudaPointerGetAttributes(weight)");
   job->src = static_cast<const uint8_t*>(weight);
   job->host_src = false;
   if (attr.type == cudaMemoryTypeHost) {
-    if (attr.devicePointer == nullptr) return fail(TP_ERR_NOT_PINNED, "page-locked weight has no device mapping");
-    job->src = static_cast<const uint8_t*>(attr.devicePointer);
     job->host_src = true;
   } else if (attr.type == cudaMemoryTypeUnregistered) {
     return fail(TP_ERR_NOT_PINNED, "weight is pageable host memory; page-lock it (cudaHostAlloc/cudaHostRegister)");
