@@ -379,9 +379,10 @@ TP_API tp_status tp_linear_rowwise_noalloc(const void* const* x_shards, const vo
  *       sizes V^T (each group of 8 keys twice) and the fp32 scores of up to
  *       16 heads at a time.
  * Scores and softmax are fp32; the probabilities enter the P.V product (fp32
- * accumulation) as two bf16 terms, P_hi = bf16(P) and P_lo = bf16(P - P_hi),
- * which carry P to about 2^-17 relative (one bf16 term would carry 2^-9, an
- * error that the block's later bf16 roundings amplify); O is rounded to bf16.
+ * accumulation) as two bf16 terms, P_hi (P truncated to bf16 in the fused
+ * head_dim-128 kernel, rounded elsewhere) and P_lo = bf16(P - P_hi), which
+ * carry P to about 2^-16 relative (one bf16 term would carry 2^-9, an error
+ * that the block's later bf16 roundings amplify); O is rounded to bf16.
  * Alignment (TP_ERR_ALIGNMENT): T, head_dim, ld_qkv, ldo multiples of 8, pointers
  * 16-byte aligned.  T == 0 enqueues nothing.  TP_ERR_WORKSPACE if too small.
  */

@@ -30,8 +30,8 @@
 //                running max m by more than 8 (log2 units), m is raised and O
 //                and l rescale by 2^(m_old - m_new) (the whole warp does the TMEM
 //                read-modify-write when any of its rows needs it); P =
-//                2^(s*scale*log2e - m) stored to TMEM as P_hi = bf16(P) and
-//                P_lo = bf16(P - P_hi); l += sum of the unrounded P.  Finally O / l in bf16, staged in the
+//                2^(s*scale*log2e - m) stored to TMEM as P_hi (P truncated to bf16)
+//                and P_lo = bf16(P - P_hi); l += sum of the unrounded P.  Finally O / l in bf16, staged in the
 //                tile's (now idle) Q buffer and written by TMA stores.
 // Keys past the end of the sequence are masked (weight 0); queries past it are
 // computed on zero rows and clipped by the store.  Every wait is bounded (~2 s);
@@ -180,11 +180,12 @@ __device__ __forceinline__ void softmax_tile(uint32_t (&sv)[FK], int j, int T, f
     }
     l *= alpha;
   }
-  // P = 2^(s*k - m) as two bf16 terms, P = P_hi + P_lo: P_hi = bf16(P) as pairs into the
-  // first 64 columns of S_g's region, P_lo = bf16(P - P_hi) into the last 64 (the residual
-  // P - P_hi is exact in fp32, so P_hi + P_lo carries P to about 2^-17 relative instead of
-  // the 2^-9 of one bf16 term); l += sum(P) (the unrounded values, four independent
-  // chains).  Masked keys give 2^-inf = 0 in both terms.
+  // P = 2^(s*k - m) as two bf16 terms, P = P_hi + P_lo: P_hi = P truncated to bf16 (its top
+  // 16 bits) as pairs into the first 64 columns of S_g's region, P_lo = bf16(P - P_hi) into
+  // the last 64.  The residual P - P_hi is exact in fp32 and below one bf16 ulp of P, so
+  // P_hi + P_lo carries P to about 2^-16 relative instead of the 2^-9 of one bf16 term;
+  // l += sum(P) (the unrounded values, four independent chains).  Masked keys give
+  // 2^-inf = 0 in both terms.
   const uint64_t k2 = f2(k, k), nm2 = f2(-m, -m);
   uint64_t ls[4] = {f2(0.f, 0.f), f2(0.f, 0.f), f2(0.f, 0.f), f2(0.f, 0.f)};
 #pragma unroll
@@ -204,11 +205,18 @@ __device__ __forceinline__ void softmax_tile(uint32_t (&sv)[FK], int j, int T, f
         float x0, x1;
         f2_split(x2, x0, x1);
         const float p0 = ex2(x0), p1 = ex2(x1);
-        ls[t & 3] = add2(ls[t & 3], f2(p0, p1));
-        const uint32_t hi = pack_bf16(p0, p1);
-        pk[t] = hi;
-        // bf16 -> fp32 is exact: the low half of the pair is p0's, the high half p1's.
-        lo[u] = pack_bf16(p0 - __uint_as_float(hi << 16), p1 - __uint_as_float(hi & 0xffff0000u));
+        const uint64_t pp = f2(p0, p1);
+        ls[t & 3] = add2(ls[t & 3], pp);
+        const uint32_t u0 = __float_as_uint(p0), u1 = __float_as_uint(p1);
+        pk[t] = __byte_perm(u0, u1, 0x7632);   // the top halves: P_hi of p0 (low), of p1 (high)
+        // -P_hi in one logic operation each (keep the top 16 bits, flip the sign), then both
+        // residuals P - P_hi in one two-wide add (5 % faster than rounding P_hi and shifting
+        // it back, measured on the block's attention).
+        const uint64_t res = add2(pp, f2(__uint_as_float((u0 & 0xffff0000u) ^ 0x80000000u),
+                                         __uint_as_float((u1 & 0xffff0000u) ^ 0x80000000u)));
+        float r0, r1;
+        f2_split(res, r0, r1);
+        lo[u] = pack_bf16(r0, r1);
       }
       ptx::tmem_st_32x32b_x8(s_addr + 64 + 32 * half + t8, lo);
     }
