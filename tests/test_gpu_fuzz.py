@@ -1,8 +1,8 @@
 """Seeded random shapes through every entry point, against the oracle.
 
 Each case draws a plan and a shape (ragged token counts, widths that are not
-multiples of the tile sizes, packed blocks, every join mode) from a seeded
-generator.  Inputs are small integers, so every product sum is exact in fp32
+multiples of the tile sizes, packed blocks, every join mode, plain and chunked
+accumulation) from a seeded generator.  Inputs are small integers, so every product sum is exact in fp32
 and the bf16 results must equal the oracle's bit for bit, whatever the
 kernels' summation order.  Attention cases use normal inputs and the
 tolerance of tests/tolerance.py.
@@ -49,7 +49,10 @@ def test_fuzz_colwise_projection(case):
     p = int(rng.integers(1, 9))
     T = int(rng.integers(1, 700))
     K = 8 * int(rng.integers(1, 80))
-    act = ["none", "swiglu"][case % 2]
+    act = ["none", "swiglu", "none"][case % 3]
+    chunked = case % 3 == 2          # chunked fp32 accumulation (TP_ACCUM_CHUNKED)
+    if chunked:
+        K = 8 * int(rng.integers(1, 400))   # up to 50 k-blocks: several chunks of 16 and a tail
     if act == "swiglu":
         F = 8 * p * int(rng.integers(1, 40))
         splits = [F, F]
@@ -65,7 +68,8 @@ def test_fuzz_colwise_projection(case):
     if case % 3 == 0:   # a bias, sharded like the weight's rows (integer values: sums stay exact)
         b = tp_inputs.int_bf16(7001, case * 10 + 3, (rows, 1), lim=3)
         bias_sh = [np.ascontiguousarray(O.shard(b, "colwise", p, r, splits).reshape(-1)) for r in range(p)]
-    ys = tp.tp_linear_colwise(dev(x), shards, act, bias_shards=None if bias_sh is None else [dev(v) for v in bias_sh])
+    ys = tp.tp_linear_colwise(dev(x), shards, act, bias_shards=None if bias_sh is None else [dev(v) for v in bias_sh],
+                              chunked=chunked)
     want = O.colwise_forward(x, [O.shard(w, "colwise", p, r, splits) for r in range(p)], act, bias_sh)
     for r in range(p):
         if act == "swiglu":
