@@ -33,6 +33,10 @@
 //               epilogue of tile i overlaps the main loop of tile i+1.
 //   warps 2..5  epilogue: tcgen05.ld 32 columns at a time, bias, activation
 //               (GELU-tanh or SwiGLU) in fp32, round to bf16, store.
+// Chunked accumulation (EPI_BF16_CHUNKED, 320 threads): the MMA warp hands an
+// accumulator to the epilogue every 16 k-blocks, each chunk summed from zero,
+// and warps 2..9 (two per TMEM lane quarter, half of the tile's columns each)
+// add the chunks into fp32 registers with round-to-nearest (epilogue_chunked).
 //
 // Every mbarrier wait is bounded (about 2 s of %globaltimer); a wait that
 // gives up sets a flag in the library's status word and the CTA drains its
