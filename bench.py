@@ -859,11 +859,15 @@ class StackWorkload:
                 "step": "8 x (tp_linear_colwise SwiGLU + tp_linear_rowwise accum), shards resident in HBM"}
 
     # -- shard-on-read ----------------------------------------------------------------------------
-    def load_block(self, b, stream):
+    def load_block(self, b, stream, after_gate_up=None):
+        """Every rank's slices of block b's two weights, gate/up first (`after_gate_up`, an
+        event, is recorded between the two)."""
         tp, p, F = self.tp, self.p, self.F
         gu, dn = self.host[b]
         gu_sh, dn_sh = self.shards[b]
         tp.tp_plan_shard_ranks(gu, "colwise", p, 0, p, [F, F], self.heads, 0, outs=gu_sh, stream=stream)
+        if after_gate_up is not None:
+            after_gate_up.record(stream)
         tp.tp_plan_shard_ranks(dn, "rowwise", p, 0, p, None, self.heads, 0, outs=dn_sh, stream=stream)
 
     def load(self, stream):
@@ -904,9 +908,10 @@ class StackWorkload:
         """One step through the public calls with host buffers: every rank's slice of every weight
         read from the page-locked state dict (shard-on-read), the input copied in, the 8 blocks,
         the output copied back.  Pipelined: the input and the blocks' slices arrive in block order
-        on a copy stream, and block b starts as soon as its own slices have landed, so the
-        compute of block b overlaps the transfer of later blocks' slices.  Unpipelined: the same
-        calls one after another on one stream."""
+        on a copy stream; block b's gate/up projection starts as soon as its gate/up slices
+        have landed and its down-projection once its down slices have, so the compute overlaps
+        the transfer of the later slices (the last block's gate/up, that of its own down
+        weight).  Unpipelined: the same calls one after another on one stream."""
         torch = self.torch
         if not pipelined:
             self.load(stream)
@@ -920,18 +925,20 @@ class StackWorkload:
             self.copy_stream = torch.cuda.Stream(self.device)
         cs = self.copy_stream
         ex = torch.cuda.Event()
-        eb = [torch.cuda.Event() for _ in range(self.nb)]
+        egu = [torch.cuda.Event() for _ in range(self.nb)]
+        edn = [torch.cuda.Event() for _ in range(self.nb)]
         cs.wait_stream(stream)
         with torch.cuda.stream(cs):
             self.x_in.copy_(self.x_pin, non_blocking=True)
             ex.record(cs)
             for b in range(self.nb):
-                self.load_block(b, cs)
-                eb[b].record(cs)
+                self.load_block(b, cs, after_gate_up=egu[b])
+                edn[b].record(cs)
         stream.wait_event(ex)
         for b in range(self.nb):
-            stream.wait_event(eb[b])
+            stream.wait_event(egu[b])
             self.gate_up(b, stream, self.x_in)
+            stream.wait_event(edn[b])
             self.down(b, stream)
         with torch.cuda.stream(stream):
             self.z_pin.copy_(self.z, non_blocking=True)
@@ -1367,8 +1374,8 @@ def run_stack(args, tp, torch, device, stream, peaks):
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "inputs": "every rank's weight slices (shard-on-read, 5.44 GB) and X from page-locked host memory "
                           "every step; Z read back",
-                "pipelining": "X and the blocks' slices arrive in block order on a copy stream; block b computes as "
-                              "soon as its slices have landed",
+                "pipelining": "X and the blocks' slices arrive in block order on a copy stream; each projection "
+                              "starts as soon as its own weight's slices have landed",
                 "output_bit_identical_to_device_step": e2e_same,
                 "unpipelined": {"value": wl.flops / (e2e_serial_ms * 1e-3) / 1e12, "ms_per_step": e2e_serial_ms}},
         "cpu_baseline": cpu,
