@@ -1437,12 +1437,20 @@ def run_reference(args):
     print(json.dumps(line))
 
 
-def _vm_hwm_bytes():
-    with open("/proc/self/status") as fh:
-        for line in fh:
-            if line.startswith("VmHWM:"):
-                return int(line.split()[1]) * 1024
+def _status_bytes(key):
+    """A size line of /proc/self/status (VmHWM, RssAnon, ...) in bytes, or None."""
+    try:
+        with open("/proc/self/status") as fh:
+            for line in fh:
+                if line.startswith(key + ":"):
+                    return int(line.split()[1]) * 1024
+    except OSError:
+        pass
     return None
+
+
+def _vm_hwm_bytes():
+    return _status_bytes("VmHWM")
 
 
 def run_st_load(args):
@@ -1490,6 +1498,7 @@ def run_st_load(args):
                 for _ in range(nb)]
         stream = torch.cuda.Stream(device)
         f = tp.SafetensorsFile(path)
+        read_mode = f.read_mode_on_device()
 
         def load():
             for b, (o_in, o_out) in enumerate(outs):
@@ -1509,13 +1518,29 @@ def run_st_load(args):
                 fh.write("5")
         except OSError:
             hwm_reset = False
-        hwm0 = _vm_hwm_bytes()
+        hwm0, anon0 = _vm_hwm_bytes(), _status_bytes("RssAnon")
         reps = max(1, min(args.steps, 5))
-        t0 = time.perf_counter()
-        for _ in range(reps):
+
+        def timed_loads():
+            times = []
+            for _ in range(reps):
+                t0 = time.perf_counter()
+                load()
+                times.append(time.perf_counter() - t0)
+            return times
+
+        load_runs = timed_loads()
+        load_s = statistics.median(load_runs)
+        hwm1, anon1 = _vm_hwm_bytes(), _status_bytes("RssAnon")
+        # The other way of reading, for comparison: staged through page-locked buffers by host
+        # threads (bounded by the host's file-read rate), where the default maps the file.
+        other = "staged" if read_mode == "mapped" else None
+        other_s = None
+        if other is not None:
+            f.close()
+            f = tp.SafetensorsFile(path, read_mode=other)
             load()
-        load_s = (time.perf_counter() - t0) / reps
-        hwm1 = _vm_hwm_bytes()
+            other_s = statistics.median(timed_loads())
         f.close()
         tp.tp_device_status(stream)
 
@@ -1535,16 +1560,25 @@ def run_st_load(args):
         line = {
             "metric": "shard-on-read load GB/s from a safetensors file", "value": value, "unit": "GB/s",
             "n_gpus": 1, "steps": reps, "warmup": 1, "ms_per_step": load_s * 1e3, "higher_is_better": True,
+            "ms_runs": [round(t * 1e3, 2) for t in load_runs], "timing": "median of the loads",
             "dtype": "bf16", "data": "synthetic (seeded N(0,0.02) weights)",
             "config": {"workload": "st_load_single_stream", "blocks": nb, "hidden": H, "mlp_hidden": F,
                        "tp_degree": p, "ranks_loaded": p, "file_bytes": total,
                        "staging_bytes": 2 * (64 << 20), "page_cache": "warm",
                        "step": "every rank's shard of every tensor: packed [1,1,1,3,3] colwise in-projection "
                                "and packed [inner, mlp] rowwise to_out, 4 blocks"},
+            "read_mode": read_mode,
             "link_copy_GB/s": link_gbs, "frac_of_link_copy": value / link_gbs,
             "peak_host_rss_growth_bytes": (hwm1 - hwm0) if (hwm_reset and hwm0 is not None) else None,
+            "host_anon_growth_bytes": (anon1 - anon0) if (anon0 is not None and anon1 is not None) else None,
+            "host_memory_note": "mapped reads keep the file's pages mapped (page cache, shared, reclaimable) "
+                                "until the file is closed, so the peak resident size counts them; anonymous "
+                                "memory is what the loader itself holds",
             "gpu_launches": nb * (-(-((H + F) * 2 * H) // (64 << 20))) * reps,
         }
+        if other_s is not None:
+            line[f"{other}_GB/s"] = total / other_s / 1e9
+            line[f"{other}_ms_per_step"] = other_s * 1e3
         print(json.dumps(line))
     finally:
         shutil.rmtree(tmp, ignore_errors=True)

@@ -11,12 +11,24 @@
  * Here one process plays every rank on one GPU (tp.h), so "rank r's slice"
  * is the slice tp_plan_shard() defines, for any range of ranks.  A file is
  * opened once (its header parsed and checked), then each weight is loaded
- * with tp_st_plan_shard_ranks(): the bytes of the requested ranks' slices are
- * read from the file into a small page-locked staging ring owned by the file
- * handle, and copied from there into the caller's device shards while the
- * next part is read.  Host memory stays at the staging size whatever the
- * checkpoint's size; the full weight is never assembled in host or device
- * memory.
+ * with tp_st_plan_shard_ranks(), which reads the file in one of two ways
+ * (tp_st_set_read_mode):
+ *   staged: the bytes of the requested ranks' slices are read (pread, several
+ *           threads) into a small page-locked staging ring owned by the file
+ *           handle, and copied from there into the caller's device shards
+ *           while the next part is read;
+ *   mapped: where the GPU reads pageable host memory through the host's own
+ *           page tables (cudaDevAttrPageableMemoryAccessUsesHostPageTables,
+ *           e.g. a Grace host), the file is memory-mapped and the copy engine
+ *           reads the slices straight out of the page cache (each range's
+ *           pages populated first): no host-side copy, so the load runs at
+ *           the CPU-GPU link's rate instead of the host's file-read rate.
+ * Staged reads hold two staging buffers of host memory whatever the
+ * checkpoint's size.  Mapped reads allocate no host memory for the data, but
+ * the pages they read stay mapped into the process until tp_st_close(), so
+ * its resident size counts them: they are the page cache's own pages, shared
+ * and reclaimable, not copies.  The full weight is never assembled in host or
+ * device memory.
  *
  * File format (the published safetensors layout; not defined by the page):
  *   bytes [0, 8)       little-endian uint64 N, the header length;
@@ -36,11 +48,14 @@
  *
  * Ownership and lifetime: unlike the rest of the library (tp.h), a file
  * handle owns host resources: the open file descriptor, the parsed table and,
- * after the first load, two page-locked staging buffers and two CUDA events.
- * tp_st_close() waits for copies still in flight from the staging buffers and
- * releases everything.  A handle is not thread-safe: use one per thread.
- * Loads are host-synchronous reads feeding asynchronous copies; they cannot be
- * captured into a CUDA graph.
+ * after the first load, two CUDA events and either two page-locked staging
+ * buffers (staged reads) or a read-only mapping of the file plus, for
+ * rowwise loads, two device staging buffers of the staging size (mapped
+ * reads).  tp_st_close() waits for copies still in flight and releases
+ * everything.  A handle is not thread-safe: use one per thread.  Loads are
+ * host-synchronous reads feeding asynchronous copies (a mapped load's copies
+ * from pageable memory return only when the bytes have left the page cache);
+ * they cannot be captured into a CUDA graph.
  */
 #ifndef TP_SAFETENSORS_H_
 #define TP_SAFETENSORS_H_
@@ -74,6 +89,13 @@ typedef enum {
   TP_ST_F64 = 14
 } tp_st_dtype;
 
+/* How tp_st_plan_shard_ranks reads the file (see the top of this header). */
+typedef enum {
+  TP_ST_READ_AUTO = 0,   /* mapped where the current device supports it, else staged (the default) */
+  TP_ST_READ_STAGED = 1, /* pread into page-locked staging buffers, then the copy engine */
+  TP_ST_READ_MAPPED = 2  /* the copy engine reads a read-only mapping of the file */
+} tp_st_read_mode;
+
 /* Bytes per element of a dtype (0 for an unknown value). */
 TP_API size_t tp_st_dtype_size(tp_st_dtype dtype);
 
@@ -98,6 +120,27 @@ TP_API tp_status tp_st_open(const char* path, size_t staging_bytes, tp_st_file**
  * released anyway).
  */
 TP_API tp_status tp_st_close(tp_st_file* file);
+
+/*
+ * tp_st_set_read_mode -- choose how the following loads read the file.
+ * Takes effect at the next tp_st_plan_shard_ranks; buffers of the other mode
+ * are kept until tp_st_close.  Needs no GPU.
+ * Errors: TP_ERR_INVALID_ARG (NULL file, a value outside tp_st_read_mode).
+ */
+TP_API tp_status tp_st_set_read_mode(tp_st_file* file, tp_st_read_mode mode);
+
+/*
+ * tp_st_read_mode_on_device -- the mode a load on the current device would
+ * use: TP_ST_READ_STAGED or TP_ST_READ_MAPPED (TP_ST_READ_AUTO resolved).
+ * Mapped reads need the device to read pageable memory through the host's
+ * page tables and the kernel to populate a mapping on request
+ * (MADV_POPULATE_READ, Linux 5.14); the file is mapped by this call if it is
+ * not yet.
+ * Errors: TP_ERR_INVALID_ARG (NULL argument), TP_ERR_UNSUPPORTED (mode
+ * TP_ST_READ_MAPPED where mapped reads are not available), TP_ERR_IO (the
+ * mapping failed), TP_ERR_CUDA (no current device).
+ */
+TP_API tp_status tp_st_read_mode_on_device(tp_st_file* file, tp_st_read_mode* mode);
 
 /* Number of tensors in the file (the "__metadata__" entry is not one); -1 for NULL. */
 TP_API int64_t tp_st_count(const tp_st_file* file);
@@ -135,7 +178,8 @@ TP_API int64_t tp_st_find(const tp_st_file* file, const char* name);
  * file); for TP_ROWWISE, whole rows in chunks of the staging size, from which
  * the requested ranks' columns are extracted on the GPU by the same kernel as
  * tp_plan_shard (the row segments of one rank are short and scattered, so
- * reading whole rows is the faster way even for a single rank).
+ * reading whole rows is the faster way even for a single rank).  Mapped
+ * reads copy those chunks into a device staging buffer first.
  *
  * dev_outs: host array of rank_count device buffers; dev_outs[i] receives rank
  *           (rank_begin + i)'s dense shard (tp_shard_shape() rows and cols of
@@ -149,9 +193,13 @@ TP_API int64_t tp_st_find(const tp_st_file* file, const char* name);
  * (TP_ERR_UNSUPPORTED otherwise).
  * Errors: TP_ERR_INVALID_ARG (NULL file/name/dev_outs entry, dev_outs not
  * device memory, a bad rank range), TP_ERR_NOT_FOUND, everything
- * tp_validate() returns, TP_ERR_UNSUPPORTED, TP_ERR_IO (a read failed or came
- * up short), TP_ERR_CUDA.  A plan error leaves device memory untouched; an
- * I/O error part way through leaves the shards partly written.
+ * tp_validate() returns, TP_ERR_UNSUPPORTED (also: mode TP_ST_READ_MAPPED
+ * where it is not available), TP_ERR_IO (a read failed or came up short; in
+ * mapped mode a window that the kernel could not populate), TP_ERR_CUDA.  A
+ * plan error leaves device memory untouched; an I/O error part way through
+ * leaves the shards partly written.  The file must not be truncated or
+ * rewritten while a handle is open on it: mapped loads read its pages in
+ * place.
  */
 TP_API tp_status tp_st_plan_shard_ranks(tp_st_file* file, const char* name, tp_style style, int tp_degree,
                                         int rank_begin, int rank_count, const int64_t* fused_splits, int n_splits,

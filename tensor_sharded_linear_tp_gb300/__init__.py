@@ -77,6 +77,8 @@ _SIGS = {
     "tp_st_dtype_size": (ctypes.c_size_t, [ctypes.c_int]),
     "tp_st_open": (_status, [ctypes.c_char_p, ctypes.c_size_t, ctypes.POINTER(_vp)]),
     "tp_st_close": (_status, [_vp]),
+    "tp_st_set_read_mode": (_status, [_vp, ctypes.c_int]),
+    "tp_st_read_mode_on_device": (_status, [_vp, ctypes.POINTER(ctypes.c_int)]),
     "tp_st_count": (_i64, [_vp]),
     "tp_st_info": (_status, [_vp, _i64, ctypes.POINTER(ctypes.c_char_p), ctypes.POINTER(ctypes.c_int),
                              ctypes.POINTER(ctypes.c_int), ctypes.POINTER(_i64), ctypes.POINTER(ctypes.c_uint64),
@@ -511,6 +513,21 @@ def tp_st_close(handle: int) -> None:
     _check(lib.tp_st_close(handle))
 
 
+ST_READ_MODES = ["auto", "staged", "mapped"]   # tp_st_read_mode order
+
+
+def tp_st_set_read_mode(handle: int, mode: str) -> None:
+    """How the following loads read the file: "auto", "staged" or "mapped"."""
+    _check(lib.tp_st_set_read_mode(handle, ST_READ_MODES.index(mode)))
+
+
+def tp_st_read_mode_on_device(handle: int) -> str:
+    """The mode a load on the current device uses ("staged" or "mapped")."""
+    m = ctypes.c_int(-1)
+    _check(lib.tp_st_read_mode_on_device(handle, ctypes.byref(m)))
+    return ST_READ_MODES[m.value]
+
+
 def tp_st_count(handle: int) -> int:
     return int(lib.tp_st_count(handle))
 
@@ -566,8 +583,17 @@ def tp_st_plan_shard_ranks(handle: int, name: str, style: str, tp_degree: int, r
 class SafetensorsFile:
     """A safetensors file opened for shard-on-read (closes on exit of a ``with`` block)."""
 
-    def __init__(self, path: str, staging_bytes: int = 0):
+    def __init__(self, path: str, staging_bytes: int = 0, read_mode: str = "auto"):
         self.handle = tp_st_open(path, staging_bytes)
+        if read_mode != "auto":
+            try:
+                tp_st_set_read_mode(self.handle, read_mode)
+            except BaseException:
+                self.close()
+                raise
+
+    def read_mode_on_device(self) -> str:
+        return tp_st_read_mode_on_device(self.handle)
 
     def tensors(self) -> list[dict]:
         return [tp_st_info(self.handle, i) for i in range(tp_st_count(self.handle))]

@@ -224,6 +224,6 @@ void tp_set_tile_wait_limit_ns(uint64_t ns) {
 
 uint64_t tp_tile_wait_limit_ns(void) { return tp::tile_wait_limit_ns(); }
 
-int tp_abi_version(void) { return 102; }
+int tp_abi_version(void) { return 103; }
 
 }  // extern "C"

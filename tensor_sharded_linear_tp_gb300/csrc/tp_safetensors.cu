@@ -2,18 +2,31 @@
 //
 // diffusers "Tensor parallelism" page, §Load a sharded model: every rank reads
 // only its slice of each weight and places it straight on its device.  The
-// header is parsed once; each load streams the bytes of the requested ranks'
-// slices through two page-locked staging buffers: while the copy engine moves
-// one buffer to the device, host threads read the next part of the file into
-// the other.  Colwise slices are contiguous row ranges of the file and are
-// copied as they are; rowwise slices are scattered column segments, so whole
-// rows are staged and the ranks' columns extracted by tp_plan_shard_ranks.
+// header is parsed once; each load moves the bytes of the requested ranks'
+// slices in windows of the staging size, through one of two slot pairs:
+//   staged: two page-locked staging buffers; while the copy engine moves one
+//           buffer to the device, host threads read the next part of the file
+//           into the other;
+//   mapped: where the GPU reads pageable memory through the host's page
+//           tables, the copy engine reads straight from a read-only mapping
+//           of the file; the pages of each range are populated first, so the
+//           copy finds them mapped (a copy that has to fault them in through
+//           the GPU's address translation runs at about half the rate) and a
+//           read error is reported instead of faulted on.  Pages stay mapped
+//           until the file is closed: unmapping them after each copy costs
+//           the TLB invalidations of every page, about as long as the copy.
+// Colwise slices are contiguous row ranges of the file and are copied as they
+// are; rowwise slices are scattered column segments, so whole rows are moved
+// (to the pinned staging buffer, or to a device staging buffer when mapped)
+// and the ranks' columns extracted by tp_plan_shard_ranks.
 #include <fcntl.h>
+#include <sys/mman.h>
 #include <sys/stat.h>
 #include <unistd.h>
 
 #include <algorithm>
 #include <condition_variable>
+#include <future>
 #include <memory>
 #include <mutex>
 #include <cerrno>
@@ -26,6 +39,10 @@
 
 #include "tp_internal.h"
 #include "tp_safetensors.h"
+
+#ifndef MADV_POPULATE_READ
+#define MADV_POPULATE_READ 22  // Linux 5.14 and later
+#endif
 
 namespace tp {
 namespace stf {
@@ -463,68 +480,201 @@ struct tp_st_file {
   std::vector<tp::stf::Entry> entries;  // in order of increasing offset
   std::unordered_map<std::string, int64_t> index;
   size_t staging_bytes = 0;
-  void* staging[2] = {nullptr, nullptr};
+  tp_st_read_mode mode = TP_ST_READ_AUTO;
+  // Slots: one event each, recorded after the slot's copies; a slot is reused once it fired.
   cudaEvent_t done[2] = {nullptr, nullptr};
   bool pending[2] = {false, false};
-  int device = -1;
+  int device = -1;  // the device the events and staging buffers belong to
   int slot = 0;
+  // Staged reads: page-locked staging buffers and the reader threads.
+  void* staging[2] = {nullptr, nullptr};
   int io_threads = 1;
   std::unique_ptr<tp::stf::ReadPool> pool;
+  // Mapped reads: the whole file mapped read-only (map_state 1), or found unusable (-1, reason
+  // in map_error); device staging buffers for rowwise loads.
+  const uint8_t* map = nullptr;
+  int map_state = 0;
+  std::string map_error;
+  uint64_t page = 4096;
+  void* dstage[2] = {nullptr, nullptr};
 };
 
 namespace {
 
 using tp::fail;
 
+// The whole pages of the mapping that cover file bytes [off, off + len).
+void page_span(const tp_st_file* f, uint64_t off, uint64_t len, uint8_t** start, size_t* bytes) {
+  const uint64_t b = off & ~(f->page - 1);
+  const uint64_t e = (off + len + f->page - 1) & ~(f->page - 1);
+  *start = const_cast<uint8_t*>(f->map) + b;
+  *bytes = static_cast<size_t>(e - b);
+}
+
 tp_status wait_slot(tp_st_file* f, int s) {
   if (!f->pending[s]) return TP_OK;
   f->pending[s] = false;
   cudaError_t e = cudaEventSynchronize(f->done[s]);
-  if (e != cudaSuccess) return tp::cuda_fail(e, "waiting for a staged copy");
+  if (e != cudaSuccess) return tp::cuda_fail(e, "waiting for a shard copy");
   return TP_OK;
 }
 
+// Wait for both slots and free the events and staging buffers (the mapping stays).
 tp_status release_staging(tp_st_file* f) {
   tp_status st = TP_OK;
+  int cur = -1;
+  const bool switch_back = f->device >= 0 && cudaGetDevice(&cur) == cudaSuccess && cur != f->device &&
+                           cudaSetDevice(f->device) == cudaSuccess;
   for (int s = 0; s < 2; ++s) {
     tp_status w = wait_slot(f, s);
     if (st == TP_OK) st = w;
     if (f->done[s]) cudaEventDestroy(f->done[s]);
     if (f->staging[s]) cudaFreeHost(f->staging[s]);
+    if (f->dstage[s]) cudaFree(f->dstage[s]);
     f->done[s] = nullptr;
     f->staging[s] = nullptr;
+    f->dstage[s] = nullptr;
   }
+  if (switch_back) cudaSetDevice(cur);
   f->device = -1;
   return st;
 }
 
-// Page-locked staging and events on the current device (re-made if the device changed).
-tp_status ensure_staging(tp_st_file* f) {
+// Events on the current device (everything re-made if the device changed), and the buffers a
+// load needs: page-locked staging for staged reads, device staging for mapped rowwise reads.
+tp_status ensure_slots(tp_st_file* f, bool mapped, bool device_staging) {
   int dev = -1;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return tp::cuda_fail(e, "cudaGetDevice");
-  if (f->staging[0] != nullptr && f->device == dev) return TP_OK;
-  if (f->staging[0] != nullptr) {
+  if (f->device >= 0 && f->device != dev) {
     tp_status st = release_staging(f);
     if (st != TP_OK) return st;
   }
-  for (int s = 0; s < 2; ++s) {
-    e = cudaHostAlloc(&f->staging[s], f->staging_bytes, cudaHostAllocPortable);
-    if (e != cudaSuccess) {
-      f->staging[s] = nullptr;
-      release_staging(f);
-      return tp::cuda_fail(e, "cudaHostAlloc(staging)");
+  if (f->done[0] == nullptr) {
+    for (int s = 0; s < 2; ++s) {
+      e = cudaEventCreateWithFlags(&f->done[s], cudaEventDisableTiming);
+      if (e != cudaSuccess) {
+        f->done[s] = nullptr;
+        release_staging(f);
+        return tp::cuda_fail(e, "cudaEventCreate");
+      }
     }
-    e = cudaEventCreateWithFlags(&f->done[s], cudaEventDisableTiming);
-    if (e != cudaSuccess) {
-      f->done[s] = nullptr;
-      release_staging(f);
-      return tp::cuda_fail(e, "cudaEventCreate");
+    f->device = dev;
+  }
+  for (int s = 0; s < 2; ++s) {
+    if (!mapped && f->staging[s] == nullptr) {
+      e = cudaHostAlloc(&f->staging[s], f->staging_bytes, cudaHostAllocPortable);
+      if (e != cudaSuccess) {
+        f->staging[s] = nullptr;
+        release_staging(f);
+        return tp::cuda_fail(e, "cudaHostAlloc(staging)");
+      }
+    }
+    if (mapped && device_staging && f->dstage[s] == nullptr) {
+      e = cudaMalloc(&f->dstage[s], f->staging_bytes);
+      if (e != cudaSuccess) {
+        f->dstage[s] = nullptr;
+        release_staging(f);
+        return tp::cuda_fail(e, "cudaMalloc(device staging)");
+      }
     }
   }
-  f->device = dev;
   return TP_OK;
 }
+
+// Map the file once.  Mapped reads are unusable (map_state -1, reason kept) if the mapping
+// fails or the kernel cannot populate a mapping on request.
+void ensure_map(tp_st_file* f) {
+  if (f->map_state != 0) return;
+  const long pg = sysconf(_SC_PAGESIZE);
+  f->page = pg > 0 ? static_cast<uint64_t>(pg) : 4096;
+  void* m = mmap(nullptr, static_cast<size_t>(f->file_size), PROT_READ, MAP_SHARED, f->fd, 0);
+  if (m == MAP_FAILED) {
+    f->map_state = -1;
+    f->map_error = std::string("mmap failed: ") + strerror(errno);
+    return;
+  }
+  int rc;
+  do {
+    rc = madvise(m, static_cast<size_t>(std::min<uint64_t>(f->page, f->file_size)), MADV_POPULATE_READ);
+  } while (rc != 0 && errno == EINTR);
+  if (rc != 0) {
+    f->map_error = std::string("madvise(MADV_POPULATE_READ) failed: ") + strerror(errno);
+    munmap(m, static_cast<size_t>(f->file_size));
+    f->map_state = -1;
+    return;
+  }
+  madvise(m, static_cast<size_t>(std::min<uint64_t>(f->page, f->file_size)), MADV_DONTNEED);
+  f->map = static_cast<const uint8_t*>(m);
+  f->map_state = 1;
+}
+
+// The mode a load on the current device uses (TP_ST_READ_AUTO resolved).
+tp_status resolve_mode(tp_st_file* f, tp_st_read_mode* out) {
+  *out = TP_ST_READ_STAGED;
+  if (f->mode == TP_ST_READ_STAGED) return TP_OK;
+  int dev = -1, host_tables = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return tp::cuda_fail(e, "cudaGetDevice");
+  e = cudaDeviceGetAttribute(&host_tables, cudaDevAttrPageableMemoryAccessUsesHostPageTables, dev);
+  if (e != cudaSuccess) return tp::cuda_fail(e, "cudaDeviceGetAttribute(PageableMemoryAccessUsesHostPageTables)");
+  std::string why;
+  if (host_tables != 1) {
+    why = "device " + std::to_string(dev) + " does not read pageable memory through the host's page tables";
+  } else {
+    ensure_map(f);
+    if (f->map_state != 1) why = f->map_error;
+  }
+  if (why.empty()) {
+    *out = TP_ST_READ_MAPPED;
+    return TP_OK;
+  }
+  if (f->mode == TP_ST_READ_MAPPED)
+    return tp::fail(TP_ERR_UNSUPPORTED, "%s: mapped reads are not available: %s", f->path.c_str(), why.c_str());
+  return TP_OK;
+}
+
+// Fault in the pages of file bytes [off, off + len) (reading them from disk if need be), so
+// that the copy engine finds them mapped and a read error surfaces here.  Returns 0 or errno.
+int populate(const tp_st_file* f, uint64_t off, uint64_t len) {
+  uint8_t* p = nullptr;
+  size_t n = 0;
+  page_span(f, off, len, &p, &n);
+  int rc;
+  do {
+    rc = madvise(p, n, MADV_POPULATE_READ);
+  } while (rc != 0 && errno == EINTR);
+  return rc == 0 ? 0 : errno;
+}
+
+// Populates the file ranges of a mapped load one ahead of their copies, on a helper thread:
+// take(i) waits for range i's pages (and starts range i + 1's).
+class PopulateAhead {
+ public:
+  PopulateAhead(const tp_st_file* f, const char* name, std::vector<std::pair<uint64_t, uint64_t>> ranges)
+      : f_(f), name_(name), ranges_(std::move(ranges)) {
+    if (!ranges_.empty()) next_ = start(0);
+  }
+  tp_status take(size_t i) {
+    const int err = next_.get();
+    if (i + 1 < ranges_.size()) next_ = start(i + 1);
+    if (err == 0) return TP_OK;
+    return tp::fail(TP_ERR_IO, "%s: tensor \"%s\": cannot read file bytes [%llu, %llu): %s", f_->path.c_str(), name_,
+                    (unsigned long long)ranges_[i].first, (unsigned long long)(ranges_[i].first + ranges_[i].second),
+                    strerror(err));
+  }
+
+ private:
+  std::future<int> start(size_t i) {
+    const tp_st_file* f = f_;
+    const auto r = ranges_[i];
+    return std::async(std::launch::async, [f, r] { return populate(f, r.first, r.second); });
+  }
+  const tp_st_file* f_;
+  const char* name_;
+  std::vector<std::pair<uint64_t, uint64_t>> ranges_;
+  std::future<int> next_;
+};
 
 // Take the next staging buffer once its previous copy has finished.
 tp_status next_slot(tp_st_file* f, int* s) {
@@ -655,9 +805,25 @@ tp_status tp_st_close(tp_st_file* file) {
   tp::clear_error();
   if (file == nullptr) return TP_OK;
   tp_status st = release_staging(file);
+  if (file->map != nullptr) munmap(const_cast<uint8_t*>(file->map), static_cast<size_t>(file->file_size));
   if (file->fd >= 0) close(file->fd);
   delete file;
   return st;
+}
+
+tp_status tp_st_set_read_mode(tp_st_file* file, tp_st_read_mode mode) {
+  tp::clear_error();
+  if (file == nullptr) return tp::fail(TP_ERR_INVALID_ARG, "file is NULL");
+  if (mode != TP_ST_READ_AUTO && mode != TP_ST_READ_STAGED && mode != TP_ST_READ_MAPPED)
+    return tp::fail(TP_ERR_INVALID_ARG, "read mode %d is not a tp_st_read_mode", static_cast<int>(mode));
+  file->mode = mode;
+  return TP_OK;
+}
+
+tp_status tp_st_read_mode_on_device(tp_st_file* file, tp_st_read_mode* mode) {
+  tp::clear_error();
+  if (file == nullptr || mode == nullptr) return tp::fail(TP_ERR_INVALID_ARG, "file or mode is NULL");
+  return resolve_mode(file, mode);
 }
 
 int64_t tp_st_count(const tp_st_file* file) {
@@ -744,7 +910,11 @@ tp_status tp_st_plan_shard_ranks(tp_st_file* file, const char* name, tp_style st
     if (a.type != cudaMemoryTypeDevice && a.type != cudaMemoryTypeManaged)
       return fail(TP_ERR_INVALID_ARG, "dev_outs[%d] is not device memory", i);
   }
-  st = ensure_staging(file);
+  tp_st_read_mode mode = TP_ST_READ_STAGED;
+  st = resolve_mode(file, &mode);
+  if (st != TP_OK) return st;
+  const bool mapped = mode == TP_ST_READ_MAPPED;
+  st = ensure_slots(file, mapped, style == TP_ROWWISE);
   if (st != TP_OK) return st;
 
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -752,7 +922,7 @@ tp_status tp_st_plan_shard_ranks(tp_st_file* file, const char* name, tp_style st
   const uint64_t chunk = file->staging_bytes;
   std::string err;
 
-  if (!file->pool) file->pool.reset(new stf::ReadPool(file->io_threads));
+  if (!mapped && !file->pool) file->pool.reset(new stf::ReadPool(file->io_threads));
 
   if (style == TP_COLWISE) {
     // Rank r's part of block b: rows [o_b + r*s_b/p, o_b + (r+1)*s_b/p), one byte range of the
@@ -780,6 +950,24 @@ tp_status tp_st_plan_shard_ranks(tp_st_file* file, const char* name, tp_style st
         block_off += sizes[b];
         out_row += part;
       }
+    }
+    if (mapped) {
+      // Each piece is populated, then copied by the copy engine straight from the mapping; a
+      // slot's event marks the end, so that closing the file waits for the copies.
+      int slot = 0;
+      st = next_slot(file, &slot);
+      if (st != TP_OK) return st;
+      std::vector<std::pair<uint64_t, uint64_t>> spans;
+      for (const Piece& pc : pieces) spans.emplace_back(pc.src, pc.len);
+      PopulateAhead ahead(file, name, std::move(spans));
+      for (size_t i = 0; i < pieces.size(); ++i) {
+        const Piece& pc = pieces[i];
+        st = ahead.take(i);
+        if (st != TP_OK) return st;
+        cudaError_t e = cudaMemcpyAsync(pc.dst, file->map + pc.src, pc.len, cudaMemcpyHostToDevice, s);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyAsync(mapped file to shard)");
+      }
+      return mark_slot(file, slot, s);
     }
     std::vector<stf::Range> ranges;
     std::vector<std::pair<uint8_t*, stf::Range>> copies;
@@ -832,17 +1020,36 @@ tp_status tp_st_plan_shard_ranks(tp_st_file* file, const char* name, tp_style st
   void* outs[TP_MAX_DEGREE > 64 ? TP_MAX_DEGREE : 64];
   if (rank_count > static_cast<int>(sizeof(outs) / sizeof(outs[0])))
     return fail(TP_ERR_UNSUPPORTED, "%d ranks in one rowwise load", rank_count);
+  std::unique_ptr<PopulateAhead> ahead;
+  if (mapped) {
+    std::vector<std::pair<uint64_t, uint64_t>> spans;
+    for (int64_t r0 = 0; r0 < rows; r0 += chunk_rows)
+      spans.emplace_back(base + static_cast<uint64_t>(r0 * row_bytes),
+                         static_cast<uint64_t>(std::min(chunk_rows, rows - r0) * row_bytes));
+    ahead.reset(new PopulateAhead(file, name, std::move(spans)));
+  }
   for (int64_t r0 = 0; r0 < rows; r0 += chunk_rows) {
     const int64_t nr = std::min(chunk_rows, rows - r0);
     int slot = 0;
     st = next_slot(file, &slot);
     if (st != TP_OK) return st;
-    const std::vector<stf::Range> rows_range{
-        {base + static_cast<uint64_t>(r0 * row_bytes), static_cast<uint64_t>(nr * row_bytes), 0}};
-    if (!file->pool->run(file->fd, static_cast<uint8_t*>(file->staging[slot]), rows_range, &err))
-      return fail(TP_ERR_IO, "%s: tensor \"%s\": %s", file->path.c_str(), name, err.c_str());
+    const uint64_t off = base + static_cast<uint64_t>(r0 * row_bytes), len = static_cast<uint64_t>(nr * row_bytes);
+    void* rows_buf = nullptr;
+    if (mapped) {
+      // The rows go to a device staging buffer; the extraction kernel then reads device memory.
+      st = ahead->take(static_cast<size_t>(r0 / chunk_rows));
+      if (st != TP_OK) return st;
+      cudaError_t e = cudaMemcpyAsync(file->dstage[slot], file->map + off, len, cudaMemcpyHostToDevice, s);
+      if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyAsync(mapped file to device staging)");
+      rows_buf = file->dstage[slot];
+    } else {
+      const std::vector<stf::Range> rows_range{{off, len, 0}};
+      if (!file->pool->run(file->fd, static_cast<uint8_t*>(file->staging[slot]), rows_range, &err))
+        return fail(TP_ERR_IO, "%s: tensor \"%s\": %s", file->path.c_str(), name, err.c_str());
+      rows_buf = file->staging[slot];
+    }
     for (int i = 0; i < rank_count; ++i) outs[i] = static_cast<uint8_t*>(dev_outs[i]) + r0 * shard_row_bytes;
-    st = tp_plan_shard_ranks(file->staging[slot], nr, units, TP_ROWWISE, tp_degree, rank_begin, rank_count,
+    st = tp_plan_shard_ranks(rows_buf, nr, units, TP_ROWWISE, tp_degree, rank_begin, rank_count,
                              n_splits > 0 ? unit_sizes : nullptr, n_splits > 0 ? n : 0, 0, 0, outs, stream);
     if (st != TP_OK) return st;
     st = mark_slot(file, slot, s);

@@ -72,15 +72,47 @@ PLAN = [
 ]
 
 
+READ_MODES = ["staged", "mapped"]
+
+
+def open_file(path, staging, mode):
+    """The file opened in `mode`; skips where mapped reads are not available on this device."""
+    f = tp.SafetensorsFile(path, staging, read_mode=mode)
+    try:
+        got = f.read_mode_on_device()
+    except tp.TPError as e:
+        f.close()
+        if mode == "mapped" and e.name == "TP_ERR_UNSUPPORTED":
+            pytest.skip(f"mapped reads not available: {e}")
+        raise
+    assert got == mode
+    return f
+
+
+def test_auto_mode_takes_mapped_reads_where_available(tmp_path):
+    path = str(tmp_path / "model.safetensors")
+    tp_inputs.write_safetensors(path, model_tensors())
+    with tp.SafetensorsFile(path, read_mode="mapped") as f:
+        try:
+            available = f.read_mode_on_device() == "mapped"
+        except tp.TPError as e:
+            assert e.name == "TP_ERR_UNSUPPORTED", e
+            assert "mapped reads are not available" in str(e)
+            available = False
+    with tp.SafetensorsFile(path) as f:
+        assert f.read_mode_on_device() == ("mapped" if available else "staged")
+
+
+@pytest.mark.parametrize("mode", READ_MODES)
 @pytest.mark.parametrize("staging", [0, 8192])
 @pytest.mark.parametrize("p", [1, 2, 3, 6])
-def test_every_rank_bit_exact(tmp_path, p, staging):
+def test_every_rank_bit_exact(tmp_path, p, staging, mode):
     # staging 8192 bytes: every tensor crosses several staging buffers (chunk boundaries
     # inside rows for colwise, several row chunks for rowwise).
     path = str(tmp_path / "model.safetensors")
     tp_inputs.write_safetensors(path, model_tensors())
     ref, _ = st_oracle.read_safetensors(path)
-    with tp.SafetensorsFile(path, staging) as f:
+    with open_file(path, staging, mode) as f:
         for name, style, splits, heads in PLAN:
             shards = f.shard_ranks(name, style, p, fused_splits=splits, num_heads=heads, device=DEV)
             for r, t in enumerate(shards):
@@ -90,12 +122,13 @@ def test_every_rank_bit_exact(tmp_path, p, staging):
         assert host_bytes(full) == ref["single.0.norm.weight"].tobytes()
 
 
-def test_rank_subsets_and_given_outputs(tmp_path):
+@pytest.mark.parametrize("mode", READ_MODES)
+def test_rank_subsets_and_given_outputs(tmp_path, mode):
     path = str(tmp_path / "model.safetensors")
     tp_inputs.write_safetensors(path, model_tensors(1))
     ref, _ = st_oracle.read_safetensors(path)
     p = 6
-    with tp.SafetensorsFile(path, 16384) as f:
+    with open_file(path, 16384, mode) as f:
         for name, style, splits, heads in PLAN[:4]:
             outs = f.shard_ranks(name, style, p, rank_begin=2, rank_count=3, fused_splits=splits, num_heads=heads,
                                  device=DEV)
@@ -111,7 +144,8 @@ def test_rank_subsets_and_given_outputs(tmp_path):
             assert host_bytes(t) == want_shard(ref[name], style, p, r, splits)
 
 
-def test_shards_match_the_in_memory_extraction(tmp_path):
+@pytest.mark.parametrize("mode", READ_MODES)
+def test_shards_match_the_in_memory_extraction(tmp_path, mode):
     # Loading from the file and extracting from a device copy of the same weight give the
     # same shards: the two loading routes the page describes agree.
     w_in, w_out, _ = tp_inputs.single_stream_inputs(7, tokens=8, hidden=768, mlp_ratio=3)
@@ -119,7 +153,7 @@ def test_shards_match_the_in_memory_extraction(tmp_path):
     path = str(tmp_path / "block.safetensors")
     tp_inputs.write_safetensors(path, [("w_in", "BF16", w_in), ("w_out", "BF16", w_out)])
     p = 3
-    with tp.SafetensorsFile(path) as f:
+    with open_file(path, 0, mode) as f:
         a = f.shard_ranks("w_in", "colwise", p, fused_splits=[Hh, Hh, Hh, Ff, Ff], num_heads=6, device=DEV)
         b = f.shard_ranks("w_out", "rowwise", p, fused_splits=[Hh, Ff], num_heads=6, device=DEV)
     a2 = tp.tp_plan_shard_ranks(tp.bf16_from_bits(w_in, DEV), "colwise", p, 0, p, [Hh, Hh, Hh, Ff, Ff], 6, 0)
@@ -137,6 +171,14 @@ def _hwm_reset_supported():
         return False
 
 
+def _rss_anon_bytes():
+    with open("/proc/self/status") as fh:
+        for line in fh:
+            if line.startswith("RssAnon:"):
+                return int(line.split()[1]) * 1024
+    return None
+
+
 def _vm_hwm_bytes():
     with open("/proc/self/status") as fh:
         for line in fh:
@@ -146,10 +188,12 @@ def _vm_hwm_bytes():
 
 
 @pytest.mark.slow
-def test_large_weight_host_memory_stays_at_staging_size(tmp_path):
+@pytest.mark.parametrize("mode", READ_MODES)
+def test_large_weight_host_memory_stays_at_staging_size(tmp_path, mode):
     # A 302 MB packed to_out weight (hidden 6144, mlp_hidden 18432) loaded for all 4 ranks
-    # with 8 MiB staging buffers: the process's peak resident memory grows by about the
-    # staging size, not by the weight's size.
+    # with 8 MiB staging buffers.  Staged: the process's peak resident memory grows by about
+    # the staging size, not by the weight's size.  Mapped: its anonymous memory does not grow
+    # (the pages it reads are the page cache's, mapped in, not copies of them).
     Hh, Ff, p = 6144, 18432, 4
     path = str(tmp_path / "big.safetensors")
     w = tp_inputs.random_bits(9, 0, (Hh, Hh + Ff))
@@ -159,16 +203,20 @@ def test_large_weight_host_memory_stays_at_staging_size(tmp_path):
     staging = 8 << 20
     outs_row = [torch.empty((Hh, (Hh + Ff) // p), dtype=torch.bfloat16, device=DEV) for _ in range(p)]
     outs_col = [torch.empty(((3 * Hh + 2 * Ff) // p, 1024), dtype=torch.bfloat16, device=DEV) for _ in range(p)]
-    with tp.SafetensorsFile(path, staging) as f:
+    with open_file(path, staging, mode) as f:
         f.shard_ranks("to_out", "rowwise", p, fused_splits=[Hh, Ff], outs=outs_row)   # warm-up: staging allocated
         torch.cuda.synchronize()
-        if not _hwm_reset_supported():
+        f.shard_ranks("in_proj", "colwise", p, fused_splits=[Hh, Hh, Hh, Ff, Ff], outs=outs_col)
+        torch.cuda.synchronize()
+        if mode == "staged" and not _hwm_reset_supported():
             pytest.skip("cannot reset the peak-RSS counter on this kernel")
-        base = _vm_hwm_bytes()
+        if mode == "mapped" and _rss_anon_bytes() is None:
+            pytest.skip("no RssAnon line in /proc/self/status")
+        base = _vm_hwm_bytes() if mode == "staged" else _rss_anon_bytes()
         f.shard_ranks("to_out", "rowwise", p, fused_splits=[Hh, Ff], outs=outs_row)
         f.shard_ranks("in_proj", "colwise", p, fused_splits=[Hh, Hh, Hh, Ff, Ff], outs=outs_col)
         torch.cuda.synchronize()
-        grew = _vm_hwm_bytes() - base
+        grew = (_vm_hwm_bytes() if mode == "staged" else _rss_anon_bytes()) - base
     weight_bytes = Hh * (Hh + Ff) * 2
     assert grew < 4 * staging, (grew, weight_bytes)
     ref, _ = st_oracle.read_safetensors(path)

@@ -236,3 +236,20 @@ def test_dtype_sizes():
     for name, size in sizes.items():
         assert tp.tp_st_dtype_size(name) == size
         assert np.dtype(st_oracle.DTYPES[name]).itemsize == size
+
+
+def test_read_mode_choice_needs_no_gpu(tmp_path):
+    path = _write(tmp_path, [("w", "BF16", tp_inputs.random_bits(3, 0, (4, 8)))])
+    h = tp.tp_st_open(path)
+    try:
+        tp.tp_st_set_read_mode(h, "staged")
+        assert tp.tp_st_read_mode_on_device(h) == "staged"   # staged is never resolved against a device
+        for bad in (-1, 3, 1000):
+            assert tp.STATUS_NAMES[tp.lib.tp_st_set_read_mode(h, bad)] == "TP_ERR_INVALID_ARG"
+        assert tp.tp_st_read_mode_on_device(h) == "staged"   # a refused value changes nothing
+        assert tp.STATUS_NAMES[tp.lib.tp_st_set_read_mode(None, 0)] == "TP_ERR_INVALID_ARG"
+        assert tp.STATUS_NAMES[tp.lib.tp_st_read_mode_on_device(h, None)] == "TP_ERR_INVALID_ARG"
+    finally:
+        tp.tp_st_close(h)
+    with pytest.raises(ValueError):
+        tp.SafetensorsFile(path, read_mode="mmap")
