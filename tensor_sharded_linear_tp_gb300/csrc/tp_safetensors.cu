@@ -33,6 +33,7 @@
 #include <cstdio>
 #include <cstring>
 #include <string>
+#include <system_error>
 #include <thread>
 #include <unordered_map>
 #include <vector>
@@ -370,8 +371,18 @@ struct Range {
 // full parallel rate.
 class ReadPool {
  public:
-  explicit ReadPool(int threads) : n_(std::max(1, threads)) {
-    for (int i = 1; i < n_; ++i) workers_.emplace_back([this, i] { loop(i); });
+  // Starts up to threads - 1 workers (the caller is the first reader); if the system refuses a
+  // thread, the pool runs with the workers it got.
+  explicit ReadPool(int threads) {
+    const int want = std::max(1, threads);
+    for (int i = 1; i < want; ++i) {
+      try {
+        workers_.emplace_back([this, i] { loop(i); });
+      } catch (const std::system_error&) {
+        break;
+      }
+    }
+    n_ = 1 + static_cast<int>(workers_.size());
   }
   ~ReadPool() {
     {
@@ -453,7 +464,7 @@ class ReadPool {
     }
   }
 
-  int n_;
+  int n_ = 1;
   std::vector<std::thread> workers_;
   std::mutex m_;
   std::condition_variable cv_job_, cv_done_;
@@ -668,7 +679,12 @@ class PopulateAhead {
   std::future<int> start(size_t i) {
     const tp_st_file* f = f_;
     const auto r = ranges_[i];
-    return std::async(std::launch::async, [f, r] { return populate(f, r.first, r.second); });
+    auto job = [f, r] { return populate(f, r.first, r.second); };
+    try {
+      return std::async(std::launch::async, job);
+    } catch (const std::system_error&) {  // no thread to be had: populate when the range is taken
+      return std::async(std::launch::deferred, job);
+    }
   }
   const tp_st_file* f_;
   const char* name_;
