@@ -6,6 +6,7 @@ memory per rank stays far below the checkpoint's size.  Every loaded shard
 must equal, byte for byte, the oracle's shard of the tensor the oracle reads
 from the same file.
 """
+import os
 import resource
 
 import numpy as np
@@ -230,3 +231,23 @@ def test_large_weight_host_memory_stays_at_staging_size(tmp_path, mode):
         got = outs_col[r][torch.from_numpy(rows).to(DEV)].view(torch.int16).cpu().numpy().view(np.uint16)
         want = O.shard(ref["in_proj"], "colwise", p, r, [Hh, Hh, Hh, Ff, Ff])[rows]
         assert np.array_equal(got, want), r
+
+
+@pytest.mark.parametrize("mode", READ_MODES)
+def test_file_truncated_after_open_is_an_io_error(tmp_path, mode):
+    # The header was checked at open; the data then shrinks under the handle.  Staged reads
+    # come up short; mapped reads find the missing pages when they populate a range, on the
+    # host, before the copy of that range is issued.
+    path = str(tmp_path / "model.safetensors")
+    w = tp_inputs.random_bits(4, 0, (1024, 512))
+    tp_inputs.write_safetensors(path, [("w", "BF16", w)])
+    f = open_file(path, 1 << 20, mode)
+    try:
+        size = os.path.getsize(path)
+        os.truncate(path, size - 600 * 512 * 2)       # the last 600 rows are gone
+        with pytest.raises(tp.TPError) as e:
+            f.shard_ranks("w", "colwise", 2, device=DEV)
+        assert e.value.name == "TP_ERR_IO", e.value
+        torch.cuda.synchronize()
+    finally:
+        f.close()
