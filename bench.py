@@ -968,7 +968,7 @@ class StackWorkload:
 
 # ----------------------------------------------------------------------------- CPU oracle timing
 
-def stack_cpu_baseline(wl, n_rows=32):
+def stack_cpu_baseline(wl, n_rows=128):
     """The oracle through all 8 blocks on a seeded sample of token rows (exact for those rows)."""
     rows = tp_inputs.sample_rows(12, wl.T, n_rows)
     t0 = time.perf_counter()
@@ -981,7 +981,10 @@ def stack_cpu_baseline(wl, n_rows=32):
             "kind": "oracle",
             "sample": f"{n_rows} of {wl.T} token rows through all {wl.nb} blocks, every rank's shards of all "
                       f"{2 * wl.nb} weights extracted (float64 numpy oracle), {dt:.1f} s; TFLOP/s = the sample's "
-                      f"FLOPs (the step's scaled by rows) / its time"}
+                      f"FLOPs (the step's scaled by rows) / its time",
+            "per_row_s": dt / n_rows, "extrapolated_full_step_s": dt / n_rows * wl.T,
+            "extrapolation": "per-row time x all token rows (extrapolated, not run; the shard extraction it "
+                             "includes would not grow with the rows)"}
 
 
 def generic_cpu_baseline(wl, target_s=12.0):
