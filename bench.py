@@ -968,7 +968,7 @@ class StackWorkload:
 
 # ----------------------------------------------------------------------------- CPU oracle timing
 
-def stack_cpu_baseline(wl, n_rows=128):
+def stack_cpu_baseline(wl, n_rows=256):
     """The oracle through all 8 blocks on a seeded sample of token rows (exact for those rows)."""
     rows = tp_inputs.sample_rows(12, wl.T, n_rows)
     t0 = time.perf_counter()
@@ -1227,14 +1227,19 @@ def roofline_of(res, workload, peaks, sustained):
             "launch_ms": k["ms"], "traffic": recorded_traffic(f"{workload}:{label}", "copy")}
 
 
-def time_e2e(torch, tp, stream, fn, warmup, reps, flush=None):
+def time_e2e(torch, tp, stream, fn, warmup, reps, flush=None, runs=None):
+    """Median CUDA-event time (ms) of `reps` end-to-end steps, each alone: a step crosses the
+    CPU-GPU link, whose copies now and then stall for tens of milliseconds on this machine.
+    The single times go to `runs` when given."""
     for _ in range(max(1, warmup)):
         with torch.cuda.stream(stream):
             fn(stream)
     stream.synchronize()
-    t = time_events(torch, stream, fn, reps, flush)
+    ts = [time_events(torch, stream, fn, 1, flush) for _ in range(reps)]
     tp.tp_device_status(stream)
-    return t
+    if runs is not None:
+        runs.extend(round(t, 3) for t in ts)
+    return float(np.median(ts))
 
 
 def attn_proj_extras(args, tp, torch, device, stream, peaks, flush):
@@ -1361,10 +1366,12 @@ def run_stack(args, tp, torch, device, stream, peaks):
     roof = roofline_of(res, WORKLOAD, peaks, sustained=True)
 
     # End to end with host buffers (every weight slice, the input and the output cross the link).
-    e2e_ms = time_e2e(torch, tp, stream, lambda st: wl.step_e2e(st, pipelined=True), 1, 3)
-    e2e_serial_ms = time_e2e(torch, tp, stream, lambda st: wl.step_e2e(st, pipelined=False), 1, 3)
+    e2e_runs, serial_runs, resident_runs = [], [], []
+    e2e_ms = time_e2e(torch, tp, stream, lambda st: wl.step_e2e(st, pipelined=True), 1, 5, runs=e2e_runs)
+    e2e_serial_ms = time_e2e(torch, tp, stream, lambda st: wl.step_e2e(st, pipelined=False), 1, 5,
+                             runs=serial_runs)
     wl.load(stream)
-    e2e_resident_ms = time_e2e(torch, tp, stream, wl.step_e2e_resident, 2, 10)
+    e2e_resident_ms = time_e2e(torch, tp, stream, wl.step_e2e_resident, 2, 9, runs=resident_runs)
     # The pipelined step's output against the device-resident forward's, bit for bit.
     wl.forward(stream)
     stream.synchronize()
@@ -1398,14 +1405,17 @@ def run_stack(args, tp, torch, device, stream, peaks):
                                "shards (tp_plan_shard_ranks: copy-engine transfers, one per packed block and rank), "
                                "median of 5, against a 1 GiB page-locked host-to-device copy"},
         "e2e": {"value": wl.flops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT, "ms_per_step": e2e_ms,
+                "ms_runs": e2e_runs, "timing": "median of 5 steps, each alone between events",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "inputs": "every rank's weight slices (shard-on-read, 5.44 GB) and X from page-locked host memory "
                           "every step; Z read back",
                 "pipelining": "X and the blocks' slices arrive in block order on a copy stream; each projection "
                               "starts as soon as its own weight's slices have landed",
                 "output_bit_identical_to_device_step": e2e_same,
-                "unpipelined": {"value": wl.flops / (e2e_serial_ms * 1e-3) / 1e12, "ms_per_step": e2e_serial_ms},
+                "unpipelined": {"value": wl.flops / (e2e_serial_ms * 1e-3) / 1e12, "ms_per_step": e2e_serial_ms,
+                                "ms_runs": serial_runs},
                 "weights_resident": {"value": wl.flops / (e2e_resident_ms * 1e-3) / 1e12, "ms_per_step": e2e_resident_ms,
+                                     "ms_runs": resident_runs,
                                      "h2d_bytes_per_step": wl.T * wl.H * 2, "d2h_bytes_per_step": d2h,
                                      "what": "a serving step with the shards loaded once: X in from page-locked "
                                              "host memory, the 8 blocks, Z back"}},
