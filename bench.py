@@ -968,7 +968,7 @@ class StackWorkload:
 
 # ----------------------------------------------------------------------------- CPU oracle timing
 
-def stack_cpu_baseline(wl, n_rows=256):
+def stack_cpu_baseline(wl, n_rows=512):
     """The oracle through all 8 blocks on a seeded sample of token rows (exact for those rows)."""
     rows = tp_inputs.sample_rows(12, wl.T, n_rows)
     t0 = time.perf_counter()
