@@ -903,6 +903,21 @@ class StackWorkload:
             out.append(("rowwise_down", lambda st, b=b: self.down(b, st), "tensor", self.fl_dn))
         return out
 
+    def reference_points(self):
+        """cuBLAS (torch.matmul) on block 0's unsharded projections, the same FLOPs as the two
+        phases (a reference point, not a target: no SwiGLU, no sharding, no join)."""
+        torch = self.torch
+        if getattr(self, "_ref_bufs", None) is None:
+            gu, dn = self.host[0]
+            w_gu, w_dn = gu.to(self.device), dn.to(self.device)
+            y = torch.empty((self.T, 2 * self.F), dtype=torch.bfloat16, device=self.device)
+            h = torch.empty((self.T, self.F), dtype=torch.bfloat16, device=self.device).normal_()
+            z = torch.empty((self.T, self.H), dtype=torch.bfloat16, device=self.device)
+            self._ref_bufs = (w_gu, w_dn, y, h, z)
+        w_gu, w_dn, y, h, z = self._ref_bufs
+        return [("cublas_gate_up", lambda st: torch.matmul(self.x, w_gu.t(), out=y), "tensor", self.fl_gu),
+                ("cublas_down", lambda st: torch.matmul(h, w_dn.t(), out=z), "tensor", self.fl_dn)]
+
     # -- end to end: every step from host memory ----------------------------------------------------
     def step_e2e(self, stream, pipelined=True):
         """One step through the public calls with host buffers: every rank's slice of every weight
@@ -1196,7 +1211,8 @@ def measure(wl, args, tp, torch, device, stream, peaks, flush=None, steps=None, 
             else:
                 v = work / (t * 1e-3) / 1e9
                 refs[label] = {"ms": round(t, 5), "GB/s": v, "frac_hbm": v / peaks["hbm_gbs"]}
-        wl.phase_extract(stream)   # the shards the reference copy overwrote (same bytes) -- keep them exact
+        if hasattr(wl, "phase_extract"):
+            wl.phase_extract(stream)   # the shards the reference copy overwrote (same bytes) -- keep them exact
         stream.synchronize()
         res["reference_points"] = refs
     if with_refs and hasattr(wl, "join_phases"):
@@ -1398,6 +1414,7 @@ def run_stack(args, tp, torch, device, stream, peaks):
         "warmup": args.warmup, "ms_per_step": res["ms_per_step"], "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,0.02) weights, N(0,1) activations)",
         "config": cfg, "roofline": roof, "kernels": res["kernels"],
+        "reference_points": res.get("reference_points"),
         "shard_load": {"bytes": wl.shard_bytes, "ms": load_ms, "ms_runs": [round(v, 3) for v in load_runs],
                        "GB/s": load_gbs, "link_copy_GB/s": link_gbs,
                        "frac_of_link_copy": load_gbs / link_gbs, "frac_hbm": load_gbs / peaks["hbm_gbs"],
