@@ -573,6 +573,20 @@ class MlpWorkload:
                 ("colwise_" + self.act, self.phase_colwise, "tensor", self.flops_in),
                 ("rowwise_down", self.phase_rowwise, "tensor", self.flops_out)]
 
+    def reference_points(self):
+        """cuBLAS (torch.matmul) on the unsharded in- and out-projections: the same FLOPs as the
+        two projection phases (reference points, not targets: no activation, no sharding)."""
+        torch = self.torch
+        if getattr(self, "_ref_bufs", None) is None:
+            y = torch.empty((self.T, self.w_in.shape[0]), dtype=torch.bfloat16, device=self.device)
+            h = torch.empty((self.T, self.F), dtype=torch.bfloat16, device=self.device).normal_()
+            z = torch.empty((self.T, self.H), dtype=torch.bfloat16, device=self.device)
+            self._ref_bufs = (y, h, z)
+        y, h, z = self._ref_bufs
+        return [("cublas_colwise", lambda st: torch.matmul(self.x, self.w_in.t(), out=y), "tensor", self.flops_in),
+                ("cublas_rowwise_down", lambda st: torch.matmul(h, self.w_out.t(), out=z), "tensor",
+                 self.flops_out)]
+
     def oracle_step(self, rows):
         from oracle import tp_oracle as O
         p, h = self.p, self.host
