@@ -121,9 +121,13 @@ struct GemmParams {
                       // a quarter of the tile width)
 };
 
+constexpr int kMaxStages = 8;  // stage barriers held in SmemCtrl
+static_assert(Cfg<true>::STAGES <= kMaxStages && Cfg<false>::STAGES <= kMaxStages,
+              "the control block holds kMaxStages full/empty barrier pairs");
+
 struct alignas(8) SmemCtrl {
-  uint64_t full[8];
-  uint64_t empty[8];
+  uint64_t full[kMaxStages];
+  uint64_t empty[kMaxStages];
   uint64_t tfull[2];
   uint64_t tempty[2];
   uint64_t drain;
