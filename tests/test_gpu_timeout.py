@@ -20,9 +20,12 @@ pytestmark = pytest.mark.gpu
 tp = pytest.importorskip("tensor_sharded_linear_tp_gb300")
 
 
-def _integer_case(p=4, T=128, K_r=64, N=1024):
-    # Integer-valued inputs: every product sum is exact in fp32, so a valid result equals the
-    # oracle's bit for bit.  T <= 128 runs single CTAs (no CTA pairs).
+def _integer_case(p=4, T=128, K_r=4096, N=4096):
+    # Integer-valued inputs: every product sum is exact in fp32 (|sum| <= 16 * 4 * 4096 < 2^24),
+    # so a valid result equals the oracle's bit for bit.  T <= 128 runs single CTAs (no CTA
+    # pairs).  The K slices are long (64 k-blocks per rank), so the ranks' CTAs of a tile
+    # publish their partials microseconds apart, more than the device timer's tick: the first
+    # to arrive then always waits long enough for a bound of 1 ns to run out.
     x = tp_inputs.int_bf16(170, 0, (T, K_r * p))
     w = tp_inputs.int_bf16(170, 1, (N, K_r * p))
     xs = [O.shard(x, "rowwise", p, r) for r in range(p)]
@@ -40,11 +43,11 @@ def test_tile_wait_runs_out_and_is_reported_then_recovers():
         assert tp.tp_tile_wait_limit_ns() == 1
         # A CTA gives up unless every other rank's partial of its tile is already in when it
         # first looks; the ranks' CTAs run side by side, so some CTA nearly always looks too
-        # early.  A few tries make the outcome certain.
+        # early.  Several tries make the outcome certain.
         reported = []
-        for _ in range(5):
+        for _ in range(10):
             out = tp.tp_linear_rowwise(xs, ws, mode="workspace")   # returns: the kernel gives up, drains, exits
-            assert out.shape == (128, 1024)
+            assert out.shape == (128, 4096)
             try:
                 tp.tp_device_status()
             except tp.TPError as e:
