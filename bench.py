@@ -708,8 +708,8 @@ class BlockWorkload:
 
 def attention_launches(ranks, local_heads, head_dim):
     """Kernels one tp_attention_heads_ranks call launches: one fused kernel for every rank at
-    head_dim 128, else per rank V^T plus scores / softmax / PV per 16 heads."""
-    if head_dim == 128:
+    head_dim 64 or 128, else per rank V^T plus scores / softmax / PV per 16 heads."""
+    if head_dim in (64, 128):
         return 1
     return ranks * (1 + 3 * ((local_heads + 15) // 16))
 

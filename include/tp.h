@@ -374,13 +374,13 @@ TP_API tp_status tp_linear_rowwise_noalloc(const void* const* x_shards, const vo
  *       (0 = dense): Q, then K, then V -- the rank's colwise QKV output.
  * out:  device bf16 [T, n_heads*head_dim] with row stride ldo (0 = dense).
  * workspace: device buffer of tp_attention_workspace_bytes(T, n_heads,
- *       head_dim) bytes, owned by the caller; none (NULL, 0) at head_dim 128,
- *       where the fused kernel reads Q, K and V in place; for other head
+ *       head_dim) bytes, owned by the caller; none (NULL, 0) at head_dim 64 and
+ *       128, where the fused kernel reads Q, K and V in place; for other head
  *       sizes V^T (each group of 8 keys twice) and the fp32 scores of up to
  *       16 heads at a time.
  * Scores and softmax are fp32; the probabilities enter the P.V product (fp32
  * accumulation) as two bf16 terms, P_hi (P truncated to bf16 in the fused
- * head_dim-128 kernel, rounded elsewhere) and P_lo = bf16(P - P_hi), which
+ * kernel of head_dim 64 and 128, rounded elsewhere) and P_lo = bf16(P - P_hi), which
  * carry P to about 2^-16 relative (one bf16 term would carry 2^-9, an error
  * that the block's later bf16 roundings amplify); O is rounded to bf16.
  * Alignment (TP_ERR_ALIGNMENT): T, head_dim, ld_qkv, ldo multiples of 8, pointers
@@ -389,14 +389,14 @@ TP_API tp_status tp_linear_rowwise_noalloc(const void* const* x_shards, const vo
 TP_API tp_status tp_attention_heads(const void* qkv, int64_t ld_qkv, int64_t T, int n_heads, int head_dim,
                                     void* workspace, size_t ws_bytes, void* out, int64_t ldo, tp_stream_t stream);
 
-/* Bytes of device workspace tp_attention_heads needs (0 at head_dim 128). */
+/* Bytes of device workspace tp_attention_heads needs (0 at head_dim 64 and 128). */
 TP_API size_t tp_attention_workspace_bytes(int64_t T, int n_heads, int head_dim);
 
 /*
  * tp_attention_heads_ranks -- tp_attention_heads for n_ranks ranks in one
  * call: qkv[r] and out[r] (host arrays of n_ranks device pointers) are rank
  * r's QKV output and attention output, every rank with the same T, n_heads,
- * head_dim, ld_qkv and ldo.  With head_dim 128 one kernel launch covers every
+ * head_dim, ld_qkv and ldo.  With head_dim 64 or 128 one kernel launch covers every
  * rank's heads, so a small per-rank head count still fills the GPU, and no
  * workspace is needed; other head sizes run the ranks one after another
  * through the same workspace.  Same arithmetic, checks and errors as
@@ -407,7 +407,7 @@ TP_API tp_status tp_attention_heads_ranks(int n_ranks, const void* const* qkv, i
                                           int head_dim, void* workspace, size_t ws_bytes, void* const* out,
                                           int64_t ldo, tp_stream_t stream);
 
-/* Bytes of device workspace tp_attention_heads_ranks needs (0 at head_dim 128, and for an empty or
+/* Bytes of device workspace tp_attention_heads_ranks needs (0 at head_dim 64 and 128, and for an empty or
  * invalid call). */
 TP_API size_t tp_attention_ranks_workspace_bytes(int n_ranks, int64_t T, int n_heads, int head_dim);
 

@@ -401,7 +401,7 @@ def tp_attention_ranks_workspace_bytes(n_ranks: int, T: int, n_heads: int, head_
 def tp_attention_heads_ranks(qkv: Sequence[torch.Tensor], n_heads: int, head_dim: int,
                              outs: Sequence[torch.Tensor] | None = None, workspace: torch.Tensor | None = None,
                              stream=None) -> list[torch.Tensor]:
-    """tp_attention_heads for every rank's QKV output in one call (one launch at head_dim 128)."""
+    """tp_attention_heads for every rank's QKV output in one call (one launch at head_dim 64 or 128)."""
     n = len(qkv)
     for t in qkv:
         _need_bf16_rows("qkv[r]", t)

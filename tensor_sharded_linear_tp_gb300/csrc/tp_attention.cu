@@ -7,8 +7,9 @@
 // [h*d, (h+1)*d) of each of Q, K, V in the rank's QKV output):
 //     O_h = softmax(Q_h K_h^T / sqrt(d)) V_h        (no mask)
 //
-// head_dim 128 runs the fused kernel of tp_flash.cu (scores and probabilities
-// stay on chip).  Other head sizes take these steps, per batch of up to 16 heads:
+// head_dim 64 and 128 run the fused kernel of tp_flash.cu (scores and
+// probabilities stay on chip).  Other head sizes take these steps, per batch of
+// up to 16 heads:
 //   1. S_h = Q_h . K_h^T   -- batched tcgen05 GEMM, fp32 scores [T, T];
 //   2. P_h = softmax(S_h / sqrt(d)) row by row, fp32 math, written over its own
 //      score row as two bf16 terms, P = P_hi + P_lo with P_hi = bf16(P) and
@@ -19,8 +20,7 @@
 //      the same order (V is transposed once per call, every group of 8 keys
 //      written twice), so one product sums P_hi V + P_lo V; bf16 written
 //      straight into the rank's attention output columns [h*d, (h+1)*d).
-// The score matrices are memory traffic (about 10 bytes per score); a fused
-// kernel that keeps S and P on chip is the next step for this path.
+// The score matrices are memory traffic (about 10 bytes per score).
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -163,7 +163,7 @@ size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 namespace tp {
 namespace {
 
-// Unfused path for one rank (head sizes other than 128), using the whole workspace.
+// Unfused path for one rank (head sizes other than 64 and 128), using the whole workspace.
 tp_status attention_unfused(const void* qkv, int64_t ld_qkv, int64_t T, int n_heads, int head_dim, void* workspace,
                             void* out, int64_t ldo, float scale_log2e, cudaStream_t s) {
   const int64_t width = static_cast<int64_t>(n_heads) * head_dim;
@@ -234,7 +234,7 @@ tp_status attention_ranks(int n_ranks, const void* const* qkv, int64_t ld_qkv, i
   if (need > 0 && (workspace == nullptr || ws_bytes < need))
     return fail(TP_ERR_WORKSPACE, "workspace of %zu bytes given, %zu needed", workspace ? ws_bytes : 0, need);
   const float scale_log2e = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(head_dim)));
-  if (head_dim != 128) {
+  if (!fused_attention_head_dim(head_dim)) {
     // One rank after another through the same workspace (stream order keeps them apart).
     for (int r = 0; r < n_ranks; ++r) {
       tp_status st = attention_unfused(qkv[r], ld_qkv, T, n_heads, head_dim, workspace, out[r], ldo, scale_log2e, s);
@@ -243,7 +243,7 @@ tp_status attention_ranks(int n_ranks, const void* const* qkv, int64_t ld_qkv, i
     return TP_OK;
   }
   // Fused: one launch over every rank's heads, K and V read as they are.
-  return flash_attention_d128(n_ranks, qkv, ld_qkv, T, n_heads, out, ldo, scale_log2e, s);
+  return flash_attention_fused(head_dim, n_ranks, qkv, ld_qkv, T, n_heads, out, ldo, scale_log2e, s);
 }
 
 }  // namespace
@@ -257,7 +257,7 @@ size_t tp_attention_workspace_bytes(int64_t T, int n_heads, int head_dim) {
 
 size_t tp_attention_ranks_workspace_bytes(int n_ranks, int64_t T, int n_heads, int head_dim) {
   if (n_ranks <= 0 || T <= 0 || n_heads <= 0 || head_dim <= 0) return 0;
-  if (head_dim == 128) return 0;  // the fused kernel reads Q, K and V in place
+  if (tp::fused_attention_head_dim(head_dim)) return 0;  // the fused kernel reads Q, K and V in place
   const size_t hb = static_cast<size_t>(n_heads < tp::kHeadBatch ? n_heads : tp::kHeadBatch);
   return tp::align256(hb * static_cast<size_t>(T) * static_cast<size_t>(T) * 4) +
          tp::align256(static_cast<size_t>(n_heads) * static_cast<size_t>(head_dim) * static_cast<size_t>(T) * 4);

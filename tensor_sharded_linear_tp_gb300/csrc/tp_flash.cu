@@ -1,4 +1,4 @@
-// Fused attention over the local heads of one or more ranks, head_dim 128 (tp_attention_heads*).
+// Fused attention over the local heads of one or more ranks, head_dim 64 or 128 (tp_attention_heads*).
 //
 // diffusers "Tensor parallelism" page, §Colwise and rowwise: the colwise Q, K
 // and V projections give each rank a subset of heads; each rank attends over
@@ -19,7 +19,7 @@
 //                                         P_hi (the first 64 columns of S_g's
 //                                         region, bf16 pairs) and P_lo (the last
 //                                         64), two products into O_g in columns
-//                                         [256+128g, 256+128g+128).
+//                                         [256+d*g, 256+d*g+d) (d = head_dim)
 //                Per tile the order is PV_g(j), then S_g(j+1): S_g(j+1) may only
 //                overwrite P_g(j) after PV_g(j) read it, which the tensor core's
 //                in-order execution of one thread's MMAs guarantees.
@@ -41,6 +41,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "tp_internal.h"
@@ -49,17 +50,12 @@
 namespace tp {
 namespace {
 
-constexpr int FD = 128;   // head_dim
 constexpr int FQ = 128;   // queries per tile; two tiles per CTA
 constexpr int FK = 128;   // keys per tile
 constexpr int KS = 2;     // K ring stages
 constexpr int VS = 2;     // V ring stages
 constexpr int kMaxRanks = 16;
 constexpr uint32_t SUB = 16384;                         // 128 rows x 64 bf16, 128-byte swizzled
-constexpr uint32_t OFF_Q = 0;                           // tile g: 2 sub-tiles (d 0..63, 64..127)
-constexpr uint32_t OFF_K = 2 * 2 * SUB;                 // stage s: 2 sub-tiles
-constexpr uint32_t OFF_V = OFF_K + KS * 2 * SUB;        // stage s: 2 sub-tiles (d 0..63, 64..127), 128 key rows
-constexpr uint32_t SMEM_DATA = OFF_V + VS * 2 * SUB;    // 192 KB
 constexpr uint64_t kFlashWaitLimitNs = 2000000000ull;
 constexpr int kThreads = 320;
 
@@ -84,8 +80,20 @@ struct alignas(8) FlashCtrl {
   int abort;
 };
 
-constexpr size_t kFlashSmem = 1024 + SMEM_DATA + sizeof(FlashCtrl);
-static_assert(kFlashSmem <= 232448, "flash attention shared memory exceeds the per-CTA limit");
+// Shared-memory layout for head_dim kFD (64 or 128): a 128-row tile of Q, K or V is kFD / 64
+// sub-tiles of 64 columns (d 0..63, then 64..127), each 128 rows x 128 B, 128-byte swizzled.
+template <int kFD>
+struct FlashDims {
+  static_assert(kFD == 64 || kFD == 128, "the fused kernel covers head_dim 64 and 128");
+  static constexpr int HALVES = kFD / 64;
+  static constexpr uint32_t TILE = HALVES * SUB;
+  static constexpr uint32_t OFF_Q = 0;                     // query tile g at g * TILE
+  static constexpr uint32_t OFF_K = 2 * TILE;              // K stage s at OFF_K + s * TILE
+  static constexpr uint32_t OFF_V = OFF_K + KS * TILE;     // V stage s, 128 key rows
+  static constexpr uint32_t SMEM_DATA = OFF_V + VS * TILE; // 192 KB at head_dim 128, 96 KB at 64
+  static constexpr size_t SMEM = 1024 + SMEM_DATA + sizeof(FlashCtrl);
+  static_assert(SMEM <= 232448, "flash attention shared memory exceeds the per-CTA limit");
+};
 
 __device__ __forceinline__ bool fwait(uint32_t bar, uint32_t parity, volatile int* abort_flag, unsigned int* status,
                                       bool ignore_abort = false) {
@@ -148,6 +156,7 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
 // max m (raising it, and rescaling l and O in TMEM, only when the tile's max exceeds it by more
 // than 8 in log2 units), writes P = 2^(s*k - m) as bf16 pairs over the first 64 columns of the
 // tile's S region and adds the unrounded P to l.  Warp-collective (TMEM access).
+template <int FD>
 __device__ __forceinline__ void softmax_tile(uint32_t (&sv)[FK], int j, int T, float k, uint32_t s_addr,
                                              uint32_t o_addr, float& m, float& l) {
   const int valid = min(FK, T - j * FK);
@@ -244,12 +253,13 @@ __device__ __forceinline__ void softmax_tile(uint32_t (&sv)[FK], int j, int T, f
 // The tile's output rows of this warp: O / l in bf16, staged in the (idle) Q buffer `qbuf` of
 // the tile and written by two TMA stores of 32 rows x 64 columns (rows past T are skipped or
 // clipped).  Warp-collective.
+template <int FD>
 __device__ __forceinline__ void write_output(const CUtensorMap& map_o, uint32_t o_addr, float l, uint32_t qbuf,
                                              int q, int lane, int h, int row0, int T) {
   // Epilogue: O / l in bf16, staged in the tile's Q buffer (idle: every S MMA of this tile
   // completed before o_done), written by TMA stores of 32 rows x 64 columns.
   const float inv = 1.0f / l;
-  const uint32_t stage = qbuf + static_cast<uint32_t>(q) * 8192;
+  const uint32_t stage = qbuf + static_cast<uint32_t>(q) * (FD / 64) * 4096;  // 32 rows x FD bf16 per warp
 #pragma unroll 1
   for (int c = 0; c < FD; c += 32) {
     uint32_t v[32];
@@ -268,18 +278,21 @@ __device__ __forceinline__ void write_output(const CUtensorMap& map_o, uint32_t 
   ptx::fence_proxy_async_smem();
   __syncwarp();
   if (lane == 0 && row0 < T) {
-    ptx::tma_store_2d(&map_o, stage, h * FD, row0);
-    ptx::tma_store_2d(&map_o, stage + 4096, h * FD + 64, row0);
+#pragma unroll
+    for (int h2 = 0; h2 < FD / 64; ++h2) ptx::tma_store_2d(&map_o, stage + h2 * 4096, h * FD + 64 * h2, row0);
     ptx::bulk_commit();
     ptx::bulk_wait_all();
   }
   __syncwarp();
 }
 
+template <int kFD>
 __global__ void __launch_bounds__(kThreads, 1) tp_flash_kernel(const __grid_constant__ FlashParams p) {
+  using D = FlashDims<kFD>;
+  constexpr int FD = kFD;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  FlashCtrl* ctl = reinterpret_cast<FlashCtrl*>(base + SMEM_DATA);
+  FlashCtrl* ctl = reinterpret_cast<FlashCtrl*>(base + D::SMEM_DATA);
   volatile int* abort_flag = &ctl->abort;
   const uint32_t sbase = ptx::smem_addr(base);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -324,29 +337,26 @@ __global__ void __launch_bounds__(kThreads, 1) tp_flash_kernel(const __grid_cons
       // ---------------------------------------------------------------- producer
       ptx::prefetch_tensormap(map_qk);
       const uint32_t qf = ptx::smem_addr(&ctl->q_full);
-      ptx::mbar_arrive_expect_tx(qf, 4 * SUB);
-      for (int g = 0; g < 2; ++g) {
-        ptx::tma_load_2d(sbase + OFF_Q + g * 2 * SUB, map_qk, qf, h * FD, q0 + g * FQ);
-        ptx::tma_load_2d(sbase + OFF_Q + g * 2 * SUB + SUB, map_qk, qf, h * FD + 64, q0 + g * FQ);
-      }
+      ptx::mbar_arrive_expect_tx(qf, 2 * D::TILE);
+      for (int g = 0; g < 2; ++g)
+        for (int h2 = 0; h2 < D::HALVES; ++h2)
+          ptx::tma_load_2d(sbase + D::OFF_Q + g * D::TILE + h2 * SUB, map_qk, qf, h * FD + 64 * h2, q0 + g * FQ);
       int k_issued = 0, v_issued = 0;
       for (int j = 0; j < nkv; ++j) {
         const int ks = j % KS, vs = j % VS;
         if (!fwait(ptx::smem_addr(&ctl->k_empty[ks]), ((j / KS) & 1) ^ 1u, abort_flag, p.status)) break;
         const uint32_t kf = ptx::smem_addr(&ctl->k_full[ks]);
-        const uint32_t kdst = sbase + OFF_K + ks * 2 * SUB;
+        const uint32_t kdst = sbase + D::OFF_K + ks * D::TILE;
         const int kx = (p.n_heads + h) * FD;
-        ptx::mbar_arrive_expect_tx(kf, 2 * SUB);
-        ptx::tma_load_2d(kdst, map_qk, kf, kx, j * FK);
-        ptx::tma_load_2d(kdst + SUB, map_qk, kf, kx + 64, j * FK);
+        ptx::mbar_arrive_expect_tx(kf, D::TILE);
+        for (int h2 = 0; h2 < D::HALVES; ++h2) ptx::tma_load_2d(kdst + h2 * SUB, map_qk, kf, kx + 64 * h2, j * FK);
         ++k_issued;
         if (!fwait(ptx::smem_addr(&ctl->v_empty[vs]), ((j / VS) & 1) ^ 1u, abort_flag, p.status)) break;
         const uint32_t vf = ptx::smem_addr(&ctl->v_full[vs]);
-        const uint32_t vdst = sbase + OFF_V + vs * 2 * SUB;
+        const uint32_t vdst = sbase + D::OFF_V + vs * D::TILE;
         const int vx = (2 * p.n_heads + h) * FD;
-        ptx::mbar_arrive_expect_tx(vf, 2 * SUB);
-        ptx::tma_load_2d(vdst, map_qk, vf, vx, j * FK);
-        ptx::tma_load_2d(vdst + SUB, map_qk, vf, vx + 64, j * FK);
+        ptx::mbar_arrive_expect_tx(vf, D::TILE);
+        for (int h2 = 0; h2 < D::HALVES; ++h2) ptx::tma_load_2d(vdst + h2 * SUB, map_qk, vf, vx + 64 * h2, j * FK);
         ++v_issued;
       }
       // Let every copy land before the CTA can exit.
@@ -359,13 +369,14 @@ __global__ void __launch_bounds__(kThreads, 1) tp_flash_kernel(const __grid_cons
   } else if (warp == 1) {
     if (lane == 0) {
       // ---------------------------------------------------------------- MMA issuer
-      constexpr uint32_t idesc = ptx::idesc_bf16_f32(FQ, FK);   // M 128, N 128 for both products
-      constexpr uint32_t idesc_pv = idesc | ptx::kIdescMnMajorB;  // V as stored: [key][d], d contiguous
+      constexpr uint32_t idesc = ptx::idesc_bf16_f32(FQ, FK);   // S: M 128 queries, N 128 keys
+      constexpr uint32_t idesc_pv = ptx::idesc_bf16_f32(FQ, FD) | ptx::kIdescMnMajorB;  // P.V: N = head_dim;
+                                                                                      // V as stored, d contiguous
       auto issue_s = [&](int g, int j) {
-        const uint32_t kb = sbase + OFF_K + (j % KS) * 2 * SUB;
-        const uint32_t qb = sbase + OFF_Q + g * 2 * SUB;
+        const uint32_t kb = sbase + D::OFF_K + (j % KS) * D::TILE;
+        const uint32_t qb = sbase + D::OFF_Q + g * D::TILE;
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
+        for (int kk = 0; kk < FD / 16; ++kk) {
           const uint32_t sub = (kk >> 2) * SUB, k4 = 2u * (kk & 3);
           ptx::umma_bf16(tmem + g * FK, ptx::sw128_kmajor_desc(qb + sub) + k4, ptx::sw128_kmajor_desc(kb + sub) + k4,
                          idesc, kk > 0 ? 1u : 0u);
@@ -374,7 +385,7 @@ __global__ void __launch_bounds__(kThreads, 1) tp_flash_kernel(const __grid_cons
       auto issue_pv = [&](int g, int j) {
         // B = V tile: 128 key rows of 128 B per 64-wide d half; the halves are SUB apart (LBO),
         // 8-key groups 1024 B apart (SBO); 16 keys per MMA = 2048 B of rows.
-        const uint32_t vb = sbase + OFF_V + (j % VS) * 2 * SUB;
+        const uint32_t vb = sbase + D::OFF_V + (j % VS) * D::TILE;
         const uint64_t vdesc = ptx::sw128_mnmajor_desc(vb, SUB, 1024);
         // O_g += P_hi V, then O_g += P_lo V (P_lo in columns 64..127 of the region).
 #pragma unroll
@@ -445,13 +456,14 @@ __global__ void __launch_bounds__(kThreads, 1) tp_flash_kernel(const __grid_cons
       ptx::tmem_ld_32x32b_x32(s_addr + 64, *reinterpret_cast<uint32_t(*)[32]>(&sv[64]));
       ptx::tmem_ld_32x32b_x32(s_addr + 96, *reinterpret_cast<uint32_t(*)[32]>(&sv[96]));
       ptx::tmem_ld_wait();
-      softmax_tile(sv, j, p.T, k, s_addr, o_addr, m, l);
+      softmax_tile<FD>(sv, j, p.T, k, s_addr, o_addr, m, l);
       ptx::tc_fence_before();
       ptx::mbar_arrive(ptx::smem_addr(&ctl->p_full[g]));
     }
     if (ok && __all_sync(0xffffffffu, fwait(ptx::smem_addr(&ctl->o_done[g]), 0, abort_flag, p.status))) {
       ptx::tc_fence_after();
-      write_output(p.map_o[rank], o_addr, l, sbase + OFF_Q + g * 2 * SUB, q, lane, h, q0 + g * FQ + q * 32, p.T);
+      write_output<FD>(p.map_o[rank], o_addr, l, sbase + D::OFF_Q + g * D::TILE, q, lane, h, q0 + g * FQ + q * 32,
+                       p.T);
     }
   }
 
@@ -464,18 +476,17 @@ __global__ void __launch_bounds__(kThreads, 1) tp_flash_kernel(const __grid_cons
   }
 }
 
-}  // namespace
-
-// Fused attention for head_dim 128 over n_ranks ranks in one launch (see the file comment).
-
-tp_status flash_attention_d128(int n_ranks, const void* const* qkv, int64_t ld_qkv, int64_t T, int n_heads,
-                               void* const* out, int64_t ldo, float scale_log2e, cudaStream_t stream) {
+// Fused attention for head_dim 64 or 128 over n_ranks ranks in one launch (see the file comment).
+template <int kFD>
+tp_status flash_attention(int n_ranks, const void* const* qkv, int64_t ld_qkv, int64_t T, int n_heads,
+                          void* const* out, int64_t ldo, float scale_log2e, cudaStream_t stream) {
+  using D = FlashDims<kFD>;
   if (n_ranks < 1 || n_ranks > kMaxRanks)
     return fail(TP_ERR_UNSUPPORTED, "fused attention over %d ranks in one launch (at most %d)", n_ranks, kMaxRanks);
   unsigned int* status = status_word();
   if (status == nullptr) return fail(TP_ERR_CUDA, "cannot locate the kernel status word");
   FlashParams prm{};
-  const int64_t width = static_cast<int64_t>(n_heads) * FD;
+  const int64_t width = static_cast<int64_t>(n_heads) * kFD;
   for (int r = 0; r < n_ranks; ++r) {
     tp_status st = encode_bf16_2d(&prm.map_qk[r], qkv[r], 3 * width, T, ld_qkv, 64, 128, true);
     if (st == TP_OK) st = encode_bf16_2d(&prm.map_o[r], out[r], width, T, ldo, 64, 32, true);
@@ -485,21 +496,33 @@ tp_status flash_attention_d128(int n_ranks, const void* const* qkv, int64_t ld_q
   prm.n_heads = n_heads;
   prm.scale_log2e = scale_log2e;
   prm.status = status;
-  static std::once_flag once[64];
+  // The dynamic shared-memory limit, raised once per device (a failure is retried next time).
+  static std::atomic<bool> raised[64];
   int dev = 0;
   cudaGetDevice(&dev);
-  cudaError_t err = cudaSuccess;
-  std::call_once(once[dev & 63], [&] {
-    err = cudaFuncSetAttribute(tp_flash_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               static_cast<int>(kFlashSmem));
-  });
-  if (err != cudaSuccess) return cuda_fail(err, "cudaFuncSetAttribute(flash attention)");
+  if (!raised[dev & 63].load(std::memory_order_acquire)) {
+    cudaError_t err = cudaFuncSetAttribute(tp_flash_kernel<kFD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           static_cast<int>(D::SMEM));
+    if (err != cudaSuccess) return cuda_fail(err, "cudaFuncSetAttribute(flash attention)");
+    raised[dev & 63].store(true, std::memory_order_release);
+  }
   dim3 grid(static_cast<unsigned>((T + 2 * FQ - 1) / (2 * FQ)), static_cast<unsigned>(n_heads),
             static_cast<unsigned>(n_ranks));
-  cudaError_t e = launch_pdl(tp_flash_kernel, grid, dim3(kThreads), kFlashSmem, stream, prm);
+  cudaError_t e = launch_pdl(tp_flash_kernel<kFD>, grid, dim3(kThreads), D::SMEM, stream, prm);
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "flash attention launch");
   return TP_OK;
+}
+
+}  // namespace
+
+tp_status flash_attention_fused(int head_dim, int n_ranks, const void* const* qkv, int64_t ld_qkv, int64_t T,
+                                int n_heads, void* const* out, int64_t ldo, float scale_log2e, cudaStream_t stream) {
+  if (head_dim == 128)
+    return flash_attention<128>(n_ranks, qkv, ld_qkv, T, n_heads, out, ldo, scale_log2e, stream);
+  if (head_dim == 64)
+    return flash_attention<64>(n_ranks, qkv, ld_qkv, T, n_heads, out, ldo, scale_log2e, stream);
+  return fail(TP_ERR_UNSUPPORTED, "the fused attention covers head_dim 64 and 128, not %d", head_dim);
 }
 
 }  // namespace tp

@@ -87,8 +87,9 @@ namespace tp {
 // bf16 2-D tensor map over a row-major [outer, inner] matrix (row stride ld elements), cached (tp_gemm.cu).
 tp_status encode_bf16_2d(CUtensorMap* m, const void* ptr, int64_t inner, int64_t outer, int64_t ld, uint32_t box_inner,
                          uint32_t box_outer, bool swizzle128);
-// Fused attention for head_dim 128 over n_ranks ranks in one launch (tp_flash.cu), straight from
-// each rank's QKV buffer.
-tp_status flash_attention_d128(int n_ranks, const void* const* qkv, int64_t ld_qkv, int64_t T, int n_heads,
-                               void* const* out, int64_t ldo, float scale_log2e, cudaStream_t stream);
+// Fused attention for head_dim 64 or 128 over n_ranks ranks in one launch (tp_flash.cu), straight
+// from each rank's QKV buffer; TP_ERR_UNSUPPORTED for other head sizes.
+constexpr bool fused_attention_head_dim(int head_dim) { return head_dim == 64 || head_dim == 128; }
+tp_status flash_attention_fused(int head_dim, int n_ranks, const void* const* qkv, int64_t ld_qkv, int64_t T,
+                                int n_heads, void* const* out, int64_t ldo, float scale_log2e, cudaStream_t stream);
 }  // namespace tp

@@ -41,7 +41,7 @@ def _device_status_clean():
 # ----------------------------------------------------------------------------- attention core
 
 @pytest.mark.parametrize("T,heads,d", [(304, 3, 64), (520, 5, 128), (256, 18, 32), (8, 1, 8), (8, 2, 128),
-                                       (136, 3, 128), (1160, 1, 128)])
+                                       (136, 3, 128), (1160, 1, 128), (8, 2, 64), (1160, 2, 64), (296, 3, 96)])
 def test_attention_heads_within_tolerance(T, heads, d):
     qkv = tp_inputs.activation_bf16(150, heads * 1000 + T, (T, 3 * heads * d))
     out = tp.tp_attention_heads(dev(qkv), heads, d)
@@ -51,7 +51,8 @@ def test_attention_heads_within_tolerance(T, heads, d):
     assert_close(f64(out), ref, f"attention T={T} heads={heads} d={d}")
 
 
-@pytest.mark.parametrize("T,heads,d,n", [(520, 2, 128, 3), (136, 4, 128, 2), (200, 2, 64, 3)])
+@pytest.mark.parametrize("T,heads,d,n", [(520, 2, 128, 3), (136, 4, 128, 2), (200, 2, 64, 3), (392, 3, 64, 4),
+                                         (200, 2, 32, 3)])
 def test_attention_of_several_ranks_in_one_call(T, heads, d, n):
     # Every rank's heads in one call (one launch at head_dim 128): each rank's output equals
     # the single-rank call bit for bit and the oracle within tolerance.
@@ -67,17 +68,18 @@ def test_attention_of_several_ranks_in_one_call(T, heads, d, n):
 
 
 def test_attention_ranks_workspace_and_limits():
-    # head_dim 128 reads Q, K and V in place: no workspace; other sizes share one across ranks.
-    assert tp.tp_attention_ranks_workspace_bytes(4, 4608, 12, 128) == 0
-    assert tp.tp_attention_workspace_bytes(4608, 12, 128) == 0
-    assert tp.tp_attention_ranks_workspace_bytes(4, 300, 2, 64) == tp.tp_attention_workspace_bytes(300, 2, 64) > 0
+    # head_dim 64 and 128 read Q, K and V in place: no workspace; other sizes share one across ranks.
+    for d in (64, 128):
+        assert tp.tp_attention_ranks_workspace_bytes(4, 4608, 12, d) == 0
+        assert tp.tp_attention_workspace_bytes(4608, 12, d) == 0
+    assert tp.tp_attention_ranks_workspace_bytes(4, 300, 2, 32) == tp.tp_attention_workspace_bytes(300, 2, 32) > 0
     q = torch.zeros((16, 3 * 128), dtype=torch.bfloat16, device=DEV)
     with pytest.raises(tp.TPError) as e:
         tp.tp_attention_heads_ranks([q] * 17, 1, 128)
     assert e.value.name == "TP_ERR_UNSUPPORTED"
-    q64 = torch.zeros((16, 3 * 64), dtype=torch.bfloat16, device=DEV)
+    q32 = torch.zeros((16, 3 * 32), dtype=torch.bfloat16, device=DEV)
     with pytest.raises(tp.TPError) as e:
-        tp.tp_attention_heads_ranks([q64, q64], 1, 64, workspace=torch.empty(16, dtype=torch.uint8, device=DEV))
+        tp.tp_attention_heads_ranks([q32, q32], 1, 32, workspace=torch.empty(16, dtype=torch.uint8, device=DEV))
     assert e.value.name == "TP_ERR_WORKSPACE"
     out = tp.tp_attention_heads_ranks([q, q], 1, 128)   # no workspace at all
     torch.cuda.synchronize()
@@ -101,12 +103,13 @@ def test_attention_one_dominant_key_returns_its_value():
     assert_close(out, ref, "one-hot attention")
 
 
+@pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("T", [512, 1000])
-def test_attention_running_max_raised_in_some_rows(T):
+def test_attention_running_max_raised_in_some_rows(T, d):
     # Key tiles of growing magnitude (x1, x3, x9, ...): a query's scores jump between tiles
     # when it aligns with the keys (its running max is raised and its output rescaled) and
     # not when it does not -- rows of the same warp take different paths.
-    heads, d = 2, 128
+    heads = 2
     rng = np.random.default_rng(153)
     q = rng.standard_normal((T, heads * d))
     k = rng.standard_normal((T, heads * d)) * (3.0 ** (np.arange(T) // 128))[:, None] * 0.5
@@ -119,9 +122,11 @@ def test_attention_running_max_raised_in_some_rows(T):
     assert_close(out, ref, f"growing keys T={T}")
 
 
-def test_attention_writes_into_strided_output():
-    # The rank's attention output can land in a wider buffer (row stride ldo).
-    T, heads, d = 136, 2, 64
+@pytest.mark.parametrize("d", [32, 64])
+def test_attention_writes_into_strided_output(d):
+    # The rank's attention output can land in a wider buffer (row stride ldo): the unfused path
+    # (head_dim 32) and the fused one (64).
+    T, heads = 136, 2
     qkv = tp_inputs.activation_bf16(152, 0, (T, 3 * heads * d))
     wide = torch.zeros((T, 3 * heads * d), dtype=torch.bfloat16, device=DEV)
     tp.tp_attention_heads(dev(qkv), heads, d, out=wide[:, :heads * d])
