@@ -19,22 +19,25 @@
 //
 // Two tile shapes share one kernel template:
 //   single CTA  128 x 256 output tile per CTA, grid = min(#tiles, #SMs),
-//               4-stage ring of A (128 x 64) + B (256 x 64) bf16 boxes;
+//               2-stage ring of A (128 x 128) + B (256 x 128) bf16 per stage;
 //   CTA pair    256 x 256 output tile per cluster of two CTAs (used when the
 //               output has more than 128 rows): each CTA stages its 128 rows
-//               of A and 128 rows of B (6-stage ring, 32 KB per stage), and
+//               of A and 128 rows of B (3-stage ring, 64 KB per stage), and
 //               the even CTA issues cta_group::2 MMAs (M=256) that read both
 //               CTAs' shared memory -- half the B traffic per SM of the
 //               single-CTA tile, which is shared-memory-bandwidth bound.
 // CTA layout (192 threads, one CTA per SM):
-//   warp 0      TMA producer, 128-byte swizzled boxes into the ring.
+//   warp 0      TMA producer: a stage is K = 128, two 128-byte swizzled boxes
+//               of 64 columns per operand (eight K=16 MMAs per barrier round
+//               trip: measured 1.3-2.5 % faster than stages of one box, six
+//               deep, whose fixed cost per stage showed in the MMA issue).
 //   warp 1      MMA issuer: one thread issues tcgen05.mma (K=16 steps) into
 //               one of two TMEM accumulators (2 x 256 columns), so the
 //               epilogue of tile i overlaps the main loop of tile i+1.
 //   warps 2..5  epilogue: tcgen05.ld 32 columns at a time, bias, activation
 //               (GELU-tanh or SwiGLU) in fp32, round to bf16, store.
 // Chunked accumulation (EPI_BF16_CHUNKED, 320 threads): the MMA warp hands an
-// accumulator to the epilogue every 16 k-blocks, each chunk summed from zero,
+// accumulator to the epilogue every 1024 of K, each chunk summed from zero,
 // and warps 2..9 (two per TMEM lane quarter, half of the tile's columns each)
 // add the chunks into fp32 registers with round-to-nearest (epilogue_chunked).
 //
@@ -58,22 +61,23 @@ namespace {
 
 constexpr int BM = 128;        // accumulator rows per CTA (TMEM lanes)
 constexpr int BN = 256;        // accumulator columns per tile
-constexpr int BK = 64;         // K per stage: one 128-byte swizzle row of bf16
+constexpr int BK = 128;        // K per stage: two 128-byte swizzle boxes of 64 bf16
+constexpr int KBOX = 64;       // K per TMA box (one 128-byte swizzle row)
 constexpr int GROUP_M = 16;
 constexpr int kTmemCols = 512; // two accumulators of BN columns
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
-// EPI_BF16_CHUNKED: the K sum is formed on the tensor core in chunks of kChunkKBlocks k-blocks
+// EPI_BF16_CHUNKED: the K sum is formed on the tensor core in chunks of kChunkKBlocks stages
 // (K = 1024), each started from zero in one of the two accumulators, and the epilogue adds the
 // chunks in fp32 with round-to-nearest (see epilogue_chunked).  The chunk length is set by the
 // epilogue: pulling a chunk's 128 KB out of tensor memory while the tensor core runs takes each
 // epilogue warp about 2 us, so a chunk must hold more MMA work than that.  Measured on the
-// Q/K/V projection of the block (T 4608, K 6144, 4 x 4608 columns): chunks of 4 / 8 / 16 / 24
-// k-blocks took 1.51 / 1.14 / 1.09 / 1.10 times the plain launch, and 0.020 / 0.033 / 0.068 /
+// Q/K/V projection of the block (T 4608, K 6144, 4 x 4608 columns): chunks of K 256 / 512 / 1024 /
+// 1536 took 1.51 / 1.14 / 1.09 / 1.10 times the plain launch, and 0.020 / 0.033 / 0.068 /
 // 0.100 % of outputs differ from the correctly rounded value (0.35 % plain); one chunk per tile
 // takes 1.07 times as long, the cost of the 8-warp epilogue itself.
 enum Epi : int { EPI_BF16 = 0, EPI_GELU = 1, EPI_SWIGLU = 2, EPI_F32 = 3, EPI_WS_REDUCE = 4, EPI_BF16_CHUNKED = 5 };
-constexpr int kChunkKBlocks = 16;
+constexpr int kChunkKBlocks = 1024 / BK;
 
 // Epilogue warps: 4 (one per TMEM lane quarter), or 8 for the chunked sum (two per lane quarter,
 // each holding the running sums of half of the tile's columns in registers).
@@ -85,10 +89,12 @@ template <bool kPair>
 struct Cfg {
   static constexpr int TILE_M = kPair ? 2 * BM : BM;   // output rows per work tile
   static constexpr int B_ROWS = kPair ? BN / 2 : BN;   // B rows each CTA stages
-  static constexpr int STAGES = kPair ? 6 : 4;
+  static constexpr int STAGES = kPair ? 3 : 2;
   static constexpr uint32_t A_BYTES = BM * BK * 2;
   static constexpr uint32_t B_BYTES = B_ROWS * BK * 2;
   static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr uint32_t A_BOX = BM * KBOX * 2;        // one K box of A
+  static constexpr uint32_t B_BOX = B_ROWS * KBOX * 2;    // one K box of B
 };
 
 struct GemmParams {
@@ -108,7 +114,7 @@ struct GemmParams {
   int M, N;           // output rows; output columns per group
   int n_groups;       // independent outputs (ranks) -- 1 for ACCUM
   int n_ksegs;        // K segments per tile (ranks) -- >1 only for ACCUM
-  int kblocks;        // 64-wide K blocks per segment
+  int kblocks;        // K stages (BK wide) per segment
   int m_tiles, n_tiles;
   int bn;             // accumulator columns per tile: a multiple of 32, <= 256 (256 for SwiGLU)
   int n_counters;     // WS_REDUCE: counters per 128-row block (one per n-tile)
@@ -734,31 +740,38 @@ __global__ void __launch_bounds__(threads_of(kEpi), 1) tp_gemm_kernel(const __gr
               if (cta == 0) ptx::mbar_arrive_expect_tx(full, 2 * C::A_BYTES + static_cast<uint32_t>(p.bn) * (BK * 2));
               // quad: half of this CTA's shared operand rows, to the same position in both pairs.
               const uint16_t qmask = static_cast<uint16_t>((1u << cta) | (1u << (2 + cta)));
-              if (quad == 1)
-                ptx::tma_load_2d_pair_mc(sa + pq * (C::A_BYTES / 2), ma, full_leader, kb * BK,
-                                         a_row + static_cast<int>(pq) * (BM / 2), qmask);
-              else
-                ptx::tma_load_2d_pair(sa, ma, full_leader, kb * BK, a_row);
+              for (int bx = 0; bx < BK / KBOX; ++bx) {
+                if (quad == 1)
+                  ptx::tma_load_2d_pair_mc(sa + bx * C::A_BOX + pq * (C::A_BOX / 2), ma, full_leader,
+                                           kb * BK + bx * KBOX, a_row + static_cast<int>(pq) * (BM / 2), qmask);
+                else
+                  ptx::tma_load_2d_pair(sa + bx * C::A_BOX, ma, full_leader, kb * BK + bx * KBOX, a_row);
+              }
               int b_row;
               if (kEpi == EPI_SWIGLU)
                 b_row = (cta == 0 ? 0 : p.b_up_row) + nb * (BN / 2);  // leader: gate rows, peer: up rows
               else
                 b_row = nb * p.bn + static_cast<int>(cta) * (p.bn / 2);
-              if (quad == 2) {
-                const int half = ((kEpi == EPI_SWIGLU) ? BN : p.bn) / 4;  // rows of each pair's part
-                ptx::tma_load_2d_pair_mc(sb + pq * static_cast<uint32_t>(half * BK * 2), mbm, full_leader, kb * BK,
-                                         b_row + static_cast<int>(pq) * half, qmask);
-              } else {
-                ptx::tma_load_2d_pair(sb, mbm, full_leader, kb * BK, b_row);
+              for (int bx = 0; bx < BK / KBOX; ++bx) {
+                if (quad == 2) {
+                  const int half = ((kEpi == EPI_SWIGLU) ? BN : p.bn) / 4;  // rows of each pair's part
+                  ptx::tma_load_2d_pair_mc(sb + bx * C::B_BOX + pq * static_cast<uint32_t>(half * KBOX * 2), mbm,
+                                           full_leader, kb * BK + bx * KBOX, b_row + static_cast<int>(pq) * half, qmask);
+                } else {
+                  ptx::tma_load_2d_pair(sb + bx * C::B_BOX, mbm, full_leader, kb * BK + bx * KBOX, b_row);
+                }
               }
             } else {
               ptx::mbar_arrive_expect_tx(full, C::A_BYTES + static_cast<uint32_t>(p.bn) * (BK * 2));
-              ptx::tma_load_2d(sa, ma, full, kb * BK, a_row);
-              if (kEpi == EPI_SWIGLU) {
-                ptx::tma_load_2d(sb, mbm, full, kb * BK, nb * (BN / 2));
-                ptx::tma_load_2d(sb + C::B_BYTES / 2, mbm, full, kb * BK, p.b_up_row + nb * (BN / 2));
-              } else {
-                ptx::tma_load_2d(sb, mbm, full, kb * BK, nb * p.bn);
+              for (int bx = 0; bx < BK / KBOX; ++bx) {
+                const int kx = kb * BK + bx * KBOX;
+                ptx::tma_load_2d(sa + bx * C::A_BOX, ma, full, kx, a_row);
+                if (kEpi == EPI_SWIGLU) {
+                  ptx::tma_load_2d(sb + bx * C::B_BOX, mbm, full, kx, nb * (BN / 2));
+                  ptx::tma_load_2d(sb + bx * C::B_BOX + C::B_BOX / 2, mbm, full, kx, p.b_up_row + nb * (BN / 2));
+                } else {
+                  ptx::tma_load_2d(sb + bx * C::B_BOX, mbm, full, kx, nb * p.bn);
+                }
               }
             }
             ++it;
@@ -825,15 +838,16 @@ __global__ void __launch_bounds__(threads_of(kEpi), 1) tp_gemm_kernel(const __gr
             }
             ptx::tc_fence_after();
             const uint32_t sa = ptx::smem_addr(base + s * C::STAGE_BYTES);
-            const uint64_t adesc = ptx::sw128_kmajor_desc(sa);
-            const uint64_t bdesc = ptx::sw128_kmajor_desc(sa + C::A_BYTES);
 #pragma unroll
             for (int k = 0; k < BK / 16; ++k) {
-              // +32 bytes along K inside the 128-byte swizzled row = +2 in the >>4 address field.
+              // Box k / 4 of each operand; +32 bytes along K inside its 128-byte swizzled row = +2
+              // in the >>4 address field.
+              const uint64_t adesc = ptx::sw128_kmajor_desc(sa + (k >> 2) * C::A_BOX) + 2u * (k & 3);
+              const uint64_t bdesc = ptx::sw128_kmajor_desc(sa + C::A_BYTES + (k >> 2) * C::B_BOX) + 2u * (k & 3);
               if constexpr (kPair)
-                ptx::umma_bf16_pair(d_tmem, adesc + 2u * k, bdesc + 2u * k, idesc, accumulate);
+                ptx::umma_bf16_pair(d_tmem, adesc, bdesc, idesc, accumulate);
               else
-                ptx::umma_bf16(d_tmem, adesc + 2u * k, bdesc + 2u * k, idesc, accumulate);
+                ptx::umma_bf16(d_tmem, adesc, bdesc, idesc, accumulate);
               accumulate = 1;
             }
             if constexpr (kPair)  // (kQuad: the stage is free in all four CTAs once both pairs arrive)
@@ -983,7 +997,7 @@ tp_status encode_2d(CUtensorMap* m, const void* ptr, CUtensorMapDataType dtype, 
 // 2-D bf16 operand map over a row-major [outer, inner] matrix with row stride `ld`
 // elements: box = 64 (inner) x box_outer rows, 128-byte swizzle, out-of-range reads as zero.
 tp_status make_map(CUtensorMap* m, const void* ptr, int64_t inner, int64_t outer, int64_t ld, int box_outer) {
-  return encode_2d(m, ptr, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, inner, outer, ld, BK,
+  return encode_2d(m, ptr, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, inner, outer, ld, KBOX,
                    static_cast<uint32_t>(box_outer), CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
 }
 
@@ -1178,11 +1192,11 @@ int choose_group_m(int m_tiles, int64_t a_bytes) {
 
 // Accumulator width of a launch without SwiGLU: among the widths the epilogue
 // supports (multiples of 32 up to 256), the one whose tiles finish in the fewest
-// waves; ties go to the widest tile.  A k-block takes about the same time at every
-// width up to 256 (the operand ring's load round trip, not the MMA, sets it), so a
-// launch's time follows its wave count, not waves x width: a sweep of the 16 x N 3072
+// waves; ties go to the widest tile.  A stage takes about the same time at every
+// width up to 256 (the operand ring's round trip, not the MMA, sets it), so a launch's
+// time follows its wave count, not waves x width: a sweep of the 16 x N 3072
 // out-projection gave 60.6 / 60.1 / 73.2 / 86.1 / 100.2 us at widths 256 / 224 /
-// 192 / 160 / 128, i.e. 3 / 3 / 4 / 5 / 6 waves.
+// 192 / 160 / 128, i.e. 3 / 3 / 4 / 5 / 6 waves (stages of K 64, six deep).
 int choose_bn(int64_t n_out, int64_t groups_x_mtiles, int units, bool halves_of_32 = false) {
   static const int kWidths[] = {256, 224, 192, 160, 128};
   int best = 256;
