@@ -19,7 +19,7 @@
 //
 // Two tile shapes share one kernel template:
 //   single CTA  128 x 256 output tile per CTA, grid = min(#tiles, #SMs),
-//               2-stage ring of A (128 x 128) + B (256 x 128) bf16 per stage;
+//               4-stage ring of A (128 x 64) + B (256 x 64) bf16 boxes;
 //   CTA pair    256 x 256 output tile per cluster of two CTAs (used when the
 //               output has more than 128 rows): each CTA stages its 128 rows
 //               of A and 128 rows of B (3-stage ring, 64 KB per stage), and
@@ -27,10 +27,12 @@
 //               CTAs' shared memory -- half the B traffic per SM of the
 //               single-CTA tile, which is shared-memory-bandwidth bound.
 // CTA layout (192 threads, one CTA per SM):
-//   warp 0      TMA producer: a stage is K = 128, two 128-byte swizzled boxes
-//               of 64 columns per operand (eight K=16 MMAs per barrier round
-//               trip: measured 1.3-2.5 % faster than stages of one box, six
-//               deep, whose fixed cost per stage showed in the MMA issue).
+//   warp 0      TMA producer, 128-byte swizzled boxes of 64 columns into the
+//               ring.  A CTA pair's stage is K = 128, two boxes per operand
+//               (eight K=16 MMAs per barrier round trip: measured 1.3-2.5 %
+//               faster than six stages of one box, whose fixed cost per stage
+//               showed in the MMA issue); a single CTA's is one box (its two-box
+//               stages would leave two of them, 17 % slower at T 128).
 //   warp 1      MMA issuer: one thread issues tcgen05.mma (K=16 steps) into
 //               one of two TMEM accumulators (2 x 256 columns), so the
 //               epilogue of tile i overlaps the main loop of tile i+1.
@@ -61,13 +63,12 @@ namespace {
 
 constexpr int BM = 128;        // accumulator rows per CTA (TMEM lanes)
 constexpr int BN = 256;        // accumulator columns per tile
-constexpr int BK = 128;        // K per stage: two 128-byte swizzle boxes of 64 bf16
-constexpr int KBOX = 64;       // K per TMA box (one 128-byte swizzle row)
+constexpr int KBOX = 64;       // K per TMA box (one 128-byte swizzle row of bf16)
 constexpr int GROUP_M = 16;
 constexpr int kTmemCols = 512; // two accumulators of BN columns
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
-// EPI_BF16_CHUNKED: the K sum is formed on the tensor core in chunks of kChunkKBlocks stages
+// EPI_BF16_CHUNKED: the K sum is formed on the tensor core in chunks of Cfg::CHUNK_STAGES stages
 // (K = 1024), each started from zero in one of the two accumulators, and the epilogue adds the
 // chunks in fp32 with round-to-nearest (see epilogue_chunked).  The chunk length is set by the
 // epilogue: pulling a chunk's 128 KB out of tensor memory while the tensor core runs takes each
@@ -77,7 +78,6 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;
 // 0.100 % of outputs differ from the correctly rounded value (0.35 % plain); one chunk per tile
 // takes 1.07 times as long, the cost of the 8-warp epilogue itself.
 enum Epi : int { EPI_BF16 = 0, EPI_GELU = 1, EPI_SWIGLU = 2, EPI_F32 = 3, EPI_WS_REDUCE = 4, EPI_BF16_CHUNKED = 5 };
-constexpr int kChunkKBlocks = 1024 / BK;
 
 // Epilogue warps: 4 (one per TMEM lane quarter), or 8 for the chunked sum (two per lane quarter,
 // each holding the running sums of half of the tile's columns in registers).
@@ -89,7 +89,11 @@ template <bool kPair>
 struct Cfg {
   static constexpr int TILE_M = kPair ? 2 * BM : BM;   // output rows per work tile
   static constexpr int B_ROWS = kPair ? BN / 2 : BN;   // B rows each CTA stages
-  static constexpr int STAGES = kPair ? 3 : 2;
+  // K per stage: two boxes per operand for CTA pairs (eight K=16 MMAs per barrier round trip),
+  // one for a single CTA, whose larger B tile leaves room for only two stages of two boxes.
+  static constexpr int BK = kPair ? 2 * KBOX : KBOX;
+  static constexpr int STAGES = kPair ? 3 : 4;
+  static constexpr int CHUNK_STAGES = 1024 / BK;   // EPI_BF16_CHUNKED: stages per chunk (K 1024)
   static constexpr uint32_t A_BYTES = BM * BK * 2;
   static constexpr uint32_t B_BYTES = B_ROWS * BK * 2;
   static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
@@ -114,7 +118,7 @@ struct GemmParams {
   int M, N;           // output rows; output columns per group
   int n_groups;       // independent outputs (ranks) -- 1 for ACCUM
   int n_ksegs;        // K segments per tile (ranks) -- >1 only for ACCUM
-  int kblocks;        // K stages (BK wide) per segment
+  int kblocks;        // K stages (Cfg::BK wide) per segment
   int m_tiles, n_tiles;
   int bn;             // accumulator columns per tile: a multiple of 32, <= 256 (256 for SwiGLU)
   int n_counters;     // WS_REDUCE: counters per 128-row block (one per n-tile)
@@ -545,7 +549,7 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, SmemCtrl* ctl
 
 // Epilogue of EPI_BF16_CHUNKED: 8 warps, warp w (2..9) reading TMEM lane quarter w % 4 and
 // owning column half (w - 2) / 4 of the tile (p.bn / 2 = 64, 96 or 128 columns).  Each chunk of
-// kChunkKBlocks k-blocks arrives in one of the two accumulators, summed on the tensor core from
+// Cfg::CHUNK_STAGES stages arrives in one of the two accumulators, summed on the tensor core from
 // zero; the warp adds it to its running sums (fp32, round to nearest) and releases the
 // accumulator at once, so the MMA warp runs one chunk ahead.  After a tile's last chunk the sums
 // get the bias, are rounded to bf16 and stored (one 4 KB staging buffer per warp).
@@ -565,7 +569,7 @@ __device__ __forceinline__ void epilogue_chunked(const GemmParams& p, SmemCtrl* 
   const int h = (warp - 2) >> 2;     // column half of the tile
   const int half = p.bn / 2;
   const uint32_t wbuf = ptx::smem_addr(staging) + static_cast<uint32_t>(warp - 2) * kStageBuf;
-  const int nchunks = (p.n_ksegs * p.kblocks + kChunkKBlocks - 1) / kChunkKBlocks;
+  const int nchunks = (p.n_ksegs * p.kblocks + C::CHUNK_STAGES - 1) / C::CHUNK_STAGES;
   int nstore = 0;
   uint32_t ccount = 0;
   bool ok = true;
@@ -737,34 +741,34 @@ __global__ void __launch_bounds__(threads_of(kEpi), 1) tp_gemm_kernel(const __gr
             if constexpr (kPair) {
               // Both CTAs' copies complete on the leader's barrier; the leader expects all of them.
               const uint32_t full_leader = ptx::mapa_shared(full, leader);
-              if (cta == 0) ptx::mbar_arrive_expect_tx(full, 2 * C::A_BYTES + static_cast<uint32_t>(p.bn) * (BK * 2));
+              if (cta == 0) ptx::mbar_arrive_expect_tx(full, 2 * C::A_BYTES + static_cast<uint32_t>(p.bn) * (C::BK * 2));
               // quad: half of this CTA's shared operand rows, to the same position in both pairs.
               const uint16_t qmask = static_cast<uint16_t>((1u << cta) | (1u << (2 + cta)));
-              for (int bx = 0; bx < BK / KBOX; ++bx) {
+              for (int bx = 0; bx < C::BK / KBOX; ++bx) {
                 if (quad == 1)
                   ptx::tma_load_2d_pair_mc(sa + bx * C::A_BOX + pq * (C::A_BOX / 2), ma, full_leader,
-                                           kb * BK + bx * KBOX, a_row + static_cast<int>(pq) * (BM / 2), qmask);
+                                           kb * C::BK + bx * KBOX, a_row + static_cast<int>(pq) * (BM / 2), qmask);
                 else
-                  ptx::tma_load_2d_pair(sa + bx * C::A_BOX, ma, full_leader, kb * BK + bx * KBOX, a_row);
+                  ptx::tma_load_2d_pair(sa + bx * C::A_BOX, ma, full_leader, kb * C::BK + bx * KBOX, a_row);
               }
               int b_row;
               if (kEpi == EPI_SWIGLU)
                 b_row = (cta == 0 ? 0 : p.b_up_row) + nb * (BN / 2);  // leader: gate rows, peer: up rows
               else
                 b_row = nb * p.bn + static_cast<int>(cta) * (p.bn / 2);
-              for (int bx = 0; bx < BK / KBOX; ++bx) {
+              for (int bx = 0; bx < C::BK / KBOX; ++bx) {
                 if (quad == 2) {
                   const int half = ((kEpi == EPI_SWIGLU) ? BN : p.bn) / 4;  // rows of each pair's part
                   ptx::tma_load_2d_pair_mc(sb + bx * C::B_BOX + pq * static_cast<uint32_t>(half * KBOX * 2), mbm,
-                                           full_leader, kb * BK + bx * KBOX, b_row + static_cast<int>(pq) * half, qmask);
+                                           full_leader, kb * C::BK + bx * KBOX, b_row + static_cast<int>(pq) * half, qmask);
                 } else {
-                  ptx::tma_load_2d_pair(sb + bx * C::B_BOX, mbm, full_leader, kb * BK + bx * KBOX, b_row);
+                  ptx::tma_load_2d_pair(sb + bx * C::B_BOX, mbm, full_leader, kb * C::BK + bx * KBOX, b_row);
                 }
               }
             } else {
-              ptx::mbar_arrive_expect_tx(full, C::A_BYTES + static_cast<uint32_t>(p.bn) * (BK * 2));
-              for (int bx = 0; bx < BK / KBOX; ++bx) {
-                const int kx = kb * BK + bx * KBOX;
+              ptx::mbar_arrive_expect_tx(full, C::A_BYTES + static_cast<uint32_t>(p.bn) * (C::BK * 2));
+              for (int bx = 0; bx < C::BK / KBOX; ++bx) {
+                const int kx = kb * C::BK + bx * KBOX;
                 ptx::tma_load_2d(sa + bx * C::A_BOX, ma, full, kx, a_row);
                 if (kEpi == EPI_SWIGLU) {
                   ptx::tma_load_2d(sb + bx * C::B_BOX, mbm, full, kx, nb * (BN / 2));
@@ -797,7 +801,7 @@ __global__ void __launch_bounds__(threads_of(kEpi), 1) tp_gemm_kernel(const __gr
       const uint32_t idesc = ptx::idesc_bf16_f32(C::TILE_M, p.bn);
       // An accumulator is taken (wait until the epilogue has released it) and handed to the
       // epilogue (commit) once per tile -- or, for EPI_BF16_CHUNKED, once per chunk of
-      // kChunkKBlocks k-blocks, each chunk summed from zero; the two accumulators alternate.
+      // Cfg::CHUNK_STAGES stages (K 1024), each chunk summed from zero; the two accumulators alternate.
       uint32_t it = 0, ccount = 0;
       uint32_t acc = 0, accumulate = 0, d_tmem = tmem;
       bool ok = true;
@@ -823,7 +827,7 @@ __global__ void __launch_bounds__(threads_of(kEpi), 1) tp_gemm_kernel(const __gr
         int kdone = 0;
         for (int seg = 0; seg < p.n_ksegs && ok; ++seg) {
           for (int kb = 0; kb < p.kblocks; ++kb, ++kdone) {
-            if (kEpi == EPI_BF16_CHUNKED && kdone > 0 && kdone % kChunkKBlocks == 0) {
+            if (kEpi == EPI_BF16_CHUNKED && kdone > 0 && kdone % C::CHUNK_STAGES == 0) {
               hand_over();
               if (!take()) {
                 ok = false;
@@ -839,7 +843,7 @@ __global__ void __launch_bounds__(threads_of(kEpi), 1) tp_gemm_kernel(const __gr
             ptx::tc_fence_after();
             const uint32_t sa = ptx::smem_addr(base + s * C::STAGE_BYTES);
 #pragma unroll
-            for (int k = 0; k < BK / 16; ++k) {
+            for (int k = 0; k < C::BK / 16; ++k) {
               // Box k / 4 of each operand; +32 bytes along K inside its 128-byte swizzled row = +2
               // in the >>4 address field.
               const uint64_t adesc = ptx::sw128_kmajor_desc(sa + (k >> 2) * C::A_BOX) + 2u * (k & 3);
@@ -1214,6 +1218,7 @@ int choose_bn(int64_t n_out, int64_t groups_x_mtiles, int units, bool halves_of_
 }
 
 inline int ceil_div(int64_t a, int64_t b) { return static_cast<int>((a + b - 1) / b); }
+inline int stage_k(bool pair) { return pair ? Cfg<true>::BK : Cfg<false>::BK; }
 
 tp_status check_dims(int64_t T, int64_t K, int64_t N) {
   if (T < 0 || K < 0 || N < 0) return fail(TP_ERR_INVALID_ARG, "negative size");
@@ -1291,7 +1296,7 @@ tp_status tp_linear_colwise(const void* x, const void* const* w_shards, const vo
   p.N = static_cast<int>(n_out);
   p.n_groups = tp_degree;
   p.n_ksegs = 1;
-  p.kblocks = ceil_div(K, BK);
+  p.kblocks = ceil_div(K, stage_k(pair));
   p.m_tiles = ceil_div(T, pair ? 2 * BM : BM);
   p.group_m = choose_group_m(p.m_tiles, T * K * 2);  // A = X, shared by every rank
   p.n_tiles = ceil_div(n_out, (act == TP_ACT_SWIGLU) ? BN / 2 : bn);
@@ -1414,7 +1419,7 @@ tp_status rowwise_impl(const void* const* x_shards, int64_t ldx, const void* con
   p.tile_wait_ns = tile_wait_limit_ns();
   p.M = static_cast<int>(T);
   p.N = static_cast<int>(N);
-  p.kblocks = ceil_div(K_r, BK);
+  p.kblocks = ceil_div(K_r, stage_k(pair));
   p.m_tiles = ceil_div(T, pair ? 2 * BM : BM);
   // A of one tile sweep: every rank's X_r when the ranks are k-segments of one accumulator.
   p.group_m = choose_group_m(p.m_tiles, T * K_r * 2 * (mode == TP_REDUCE_ACCUM ? tp_degree : 1));
@@ -1573,7 +1578,7 @@ tp_status gemm_batched(int groups, const void* const* a, int64_t lda, const void
   p.N = static_cast<int>(N);
   p.n_groups = groups;
   p.n_ksegs = 1;
-  p.kblocks = ceil_div(K, BK);
+  p.kblocks = ceil_div(K, stage_k(pair));
   p.m_tiles = static_cast<int>(m_tiles);
   p.group_m = choose_group_m(p.m_tiles, M * K * 2);
   p.n_tiles = ceil_div(N, bn);
