@@ -1196,11 +1196,11 @@ int choose_group_m(int m_tiles, int64_t a_bytes) {
 
 // Accumulator width of a launch without SwiGLU: among the widths the epilogue
 // supports (multiples of 32 up to 256), the one whose tiles finish in the fewest
-// waves; ties go to the widest tile.  A stage takes about the same time at every
-// width up to 256 (the operand ring's round trip, not the MMA, sets it), so a launch's
-// time follows its wave count, not waves x width: a sweep of the 16 x N 3072
-// out-projection gave 60.6 / 60.1 / 73.2 / 86.1 / 100.2 us at widths 256 / 224 /
-// 192 / 160 / 128, i.e. 3 / 3 / 4 / 5 / 6 waves (stages of K 64, six deep).
+// waves; ties go to the narrowest tile.  A launch's time follows its wave count first
+// (a stage's fixed cost does not shrink with the width), then the width of its tiles:
+// the 16 x N 3072 out-projection (K 4 x 768) took 58.0 / 54.0 / 64.2 / 72.3 / 80.5 us at
+// widths 256 / 224 / 192 / 160 / 128 (3 / 3 / 4 / 5 / 6 waves of resident CTA pairs;
+// 224 runs as plain pairs on all 152 SMs, 256 as clusters of two pairs on 144).
 int choose_bn(int64_t n_out, int64_t groups_x_mtiles, int units, bool halves_of_32 = false) {
   static const int kWidths[] = {256, 224, 192, 160, 128};
   int best = 256;
@@ -1209,7 +1209,7 @@ int choose_bn(int64_t n_out, int64_t groups_x_mtiles, int units, bool halves_of_
     if (halves_of_32 && (bn / 2) % 32 != 0) continue;  // the chunked epilogue's halves: 128, 96 or 64 columns
     const int64_t tiles = groups_x_mtiles * ((n_out + bn - 1) / bn);
     const int64_t waves = (tiles + units - 1) / units;
-    if (best_waves < 0 || waves < best_waves) {
+    if (best_waves < 0 || waves <= best_waves) {
       best = bn;
       best_waves = waves;
     }
