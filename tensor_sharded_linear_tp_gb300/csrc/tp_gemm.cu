@@ -29,10 +29,14 @@
 // CTA layout (192 threads, one CTA per SM):
 //   warp 0      TMA producer, 128-byte swizzled boxes of 64 columns into the
 //               ring.  A CTA pair's stage is K = 128, two boxes per operand
-//               (eight K=16 MMAs per barrier round trip: measured 1.3-2.5 %
+//               (eight K=16 MMAs per wait on a full stage: measured 1.3-2.5 %
 //               faster than six stages of one box, whose fixed cost per stage
 //               showed in the MMA issue); a single CTA's is one box (its two-box
-//               stages would leave two of them, 17 % slower at T 128).
+//               stages would leave two of them, 17 % slower at T 128).  Each box
+//               has its own empty barrier: it is refilled as soon as its four
+//               MMAs are done, so the copy the MMAs next wait on is one box,
+//               not a whole stage (measured 4 % on the SwiGLU gate/up GEMM and
+//               7 % on a 3-wave out-projection, bit-identical).
 //   warp 1      MMA issuer: one thread issues tcgen05.mma (K=16 steps) into
 //               one of two TMEM accumulators (2 x 256 columns), so the
 //               epilogue of tile i overlaps the main loop of tile i+1.
@@ -89,7 +93,7 @@ template <bool kPair>
 struct Cfg {
   static constexpr int TILE_M = kPair ? 2 * BM : BM;   // output rows per work tile
   static constexpr int B_ROWS = kPair ? BN / 2 : BN;   // B rows each CTA stages
-  // K per stage: two boxes per operand for CTA pairs (eight K=16 MMAs per barrier round trip),
+  // K per stage: two boxes per operand for CTA pairs (eight K=16 MMAs per wait on a full stage),
   // one for a single CTA, whose larger B tile leaves room for only two stages of two boxes.
   static constexpr int BK = kPair ? 2 * KBOX : KBOX;
   static constexpr int STAGES = kPair ? 3 : 4;
@@ -133,11 +137,13 @@ struct GemmParams {
 
 constexpr int kMaxStages = 8;  // stage barriers held in SmemCtrl
 static_assert(Cfg<true>::STAGES <= kMaxStages && Cfg<false>::STAGES <= kMaxStages,
-              "the control block holds kMaxStages full/empty barrier pairs");
+              "the control block holds kMaxStages full barriers");
+static_assert(Cfg<true>::BK / KBOX <= 2 && Cfg<false>::BK / KBOX <= 2,
+              "the control block holds two empty barriers (one per K box) for each stage");
 
 struct alignas(8) SmemCtrl {
   uint64_t full[kMaxStages];
-  uint64_t empty[kMaxStages];
+  uint64_t empty[kMaxStages * 2];  // [stage * boxes + box]: a box is refilled once its MMAs are done
   uint64_t tfull[2];
   uint64_t tempty[2];
   uint64_t drain;
@@ -678,7 +684,8 @@ __global__ void __launch_bounds__(threads_of(kEpi), 1) tp_gemm_kernel(const __gr
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
       ptx::mbar_init(ptx::smem_addr(&ctl->full[s]), 1);
-      ptx::mbar_init(ptx::smem_addr(&ctl->empty[s]), kQuad ? 2 : 1);
+      for (int bx = 0; bx < C::BK / KBOX; ++bx)
+        ptx::mbar_init(ptx::smem_addr(&ctl->empty[s * (C::BK / KBOX) + bx]), kQuad ? 2 : 1);
     }
     for (int a = 0; a < 2; ++a) {
       ptx::mbar_init(ptx::smem_addr(&ctl->tfull[a]), 1);
@@ -731,44 +738,43 @@ __global__ void __launch_bounds__(threads_of(kEpi), 1) tp_gemm_kernel(const __gr
           for (int kb = 0; kb < p.kblocks; ++kb) {
             const uint32_t s = it % C::STAGES;
             const uint32_t ph = (it / C::STAGES) & 1u;
-            if (!wait_bounded(ptx::smem_addr(&ctl->empty[s]), ph ^ 1u, abort_flag, p.status, false)) {
-              ok = false;
-              break;
-            }
             const uint32_t full = ptx::smem_addr(&ctl->full[s]);
             const uint32_t sa = ptx::smem_addr(base + s * C::STAGE_BYTES);
             const uint32_t sb = sa + C::A_BYTES;
-            if constexpr (kPair) {
-              // Both CTAs' copies complete on the leader's barrier; the leader expects all of them.
-              const uint32_t full_leader = ptx::mapa_shared(full, leader);
-              if (cta == 0) ptx::mbar_arrive_expect_tx(full, 2 * C::A_BYTES + static_cast<uint32_t>(p.bn) * (C::BK * 2));
-              // quad: half of this CTA's shared operand rows, to the same position in both pairs.
-              const uint16_t qmask = static_cast<uint16_t>((1u << cta) | (1u << (2 + cta)));
-              for (int bx = 0; bx < C::BK / KBOX; ++bx) {
-                if (quad == 1)
-                  ptx::tma_load_2d_pair_mc(sa + bx * C::A_BOX + pq * (C::A_BOX / 2), ma, full_leader,
-                                           kb * C::BK + bx * KBOX, a_row + static_cast<int>(pq) * (BM / 2), qmask);
-                else
-                  ptx::tma_load_2d_pair(sa + bx * C::A_BOX, ma, full_leader, kb * C::BK + bx * KBOX, a_row);
+            for (int bx = 0; bx < C::BK / KBOX; ++bx) {
+              // Each box is free again once the MMAs that read it are done.
+              if (!wait_bounded(ptx::smem_addr(&ctl->empty[s * (C::BK / KBOX) + bx]), ph ^ 1u, abort_flag, p.status,
+                                false)) {
+                ok = false;
+                break;
               }
-              int b_row;
-              if (kEpi == EPI_SWIGLU)
-                b_row = (cta == 0 ? 0 : p.b_up_row) + nb * (BN / 2);  // leader: gate rows, peer: up rows
-              else
-                b_row = nb * p.bn + static_cast<int>(cta) * (p.bn / 2);
-              for (int bx = 0; bx < C::BK / KBOX; ++bx) {
+              const int kx = kb * C::BK + bx * KBOX;
+              if constexpr (kPair) {
+                // Both CTAs' copies complete on the leader's barrier; the leader expects all of them.
+                const uint32_t full_leader = ptx::mapa_shared(full, leader);
+                if (cta == 0 && bx == 0)
+                  ptx::mbar_arrive_expect_tx(full, 2 * C::A_BYTES + static_cast<uint32_t>(p.bn) * (C::BK * 2));
+                // quad: half of this CTA's shared operand rows, to the same position in both pairs.
+                const uint16_t qmask = static_cast<uint16_t>((1u << cta) | (1u << (2 + cta)));
+                if (quad == 1)
+                  ptx::tma_load_2d_pair_mc(sa + bx * C::A_BOX + pq * (C::A_BOX / 2), ma, full_leader, kx,
+                                           a_row + static_cast<int>(pq) * (BM / 2), qmask);
+                else
+                  ptx::tma_load_2d_pair(sa + bx * C::A_BOX, ma, full_leader, kx, a_row);
+                int b_row;
+                if (kEpi == EPI_SWIGLU)
+                  b_row = (cta == 0 ? 0 : p.b_up_row) + nb * (BN / 2);  // leader: gate rows, peer: up rows
+                else
+                  b_row = nb * p.bn + static_cast<int>(cta) * (p.bn / 2);
                 if (quad == 2) {
                   const int half = ((kEpi == EPI_SWIGLU) ? BN : p.bn) / 4;  // rows of each pair's part
                   ptx::tma_load_2d_pair_mc(sb + bx * C::B_BOX + pq * static_cast<uint32_t>(half * KBOX * 2), mbm,
-                                           full_leader, kb * C::BK + bx * KBOX, b_row + static_cast<int>(pq) * half, qmask);
+                                           full_leader, kx, b_row + static_cast<int>(pq) * half, qmask);
                 } else {
-                  ptx::tma_load_2d_pair(sb + bx * C::B_BOX, mbm, full_leader, kb * C::BK + bx * KBOX, b_row);
+                  ptx::tma_load_2d_pair(sb + bx * C::B_BOX, mbm, full_leader, kx, b_row);
                 }
-              }
-            } else {
-              ptx::mbar_arrive_expect_tx(full, C::A_BYTES + static_cast<uint32_t>(p.bn) * (C::BK * 2));
-              for (int bx = 0; bx < C::BK / KBOX; ++bx) {
-                const int kx = kb * C::BK + bx * KBOX;
+              } else {
+                if (bx == 0) ptx::mbar_arrive_expect_tx(full, C::A_BYTES + static_cast<uint32_t>(p.bn) * (C::BK * 2));
                 ptx::tma_load_2d(sa + bx * C::A_BOX, ma, full, kx, a_row);
                 if (kEpi == EPI_SWIGLU) {
                   ptx::tma_load_2d(sb + bx * C::B_BOX, mbm, full, kx, nb * (BN / 2));
@@ -778,6 +784,7 @@ __global__ void __launch_bounds__(threads_of(kEpi), 1) tp_gemm_kernel(const __gr
                 }
               }
             }
+            if (!ok) break;
             ++it;
           }
         }
@@ -853,11 +860,14 @@ __global__ void __launch_bounds__(threads_of(kEpi), 1) tp_gemm_kernel(const __gr
               else
                 ptx::umma_bf16(d_tmem, adesc, bdesc, idesc, accumulate);
               accumulate = 1;
+              if ((k & 3) == 3) {  // the box's last MMA: the box is free once these complete
+                const uint32_t eb = ptx::smem_addr(&ctl->empty[s * (C::BK / KBOX) + (k >> 2)]);
+                if constexpr (kPair)  // (kQuad: free in all four CTAs once both pairs arrive)
+                  ptx::umma_commit_pair(eb, kQuad ? 0xF : pair_mask);
+                else
+                  ptx::umma_commit(eb);
+              }
             }
-            if constexpr (kPair)  // (kQuad: the stage is free in all four CTAs once both pairs arrive)
-              ptx::umma_commit_pair(ptx::smem_addr(&ctl->empty[s]), kQuad ? 0xF : pair_mask);
-            else
-              ptx::umma_commit(ptx::smem_addr(&ctl->empty[s]));
             ++it;
           }
         }
