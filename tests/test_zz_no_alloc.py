@@ -12,6 +12,7 @@ claims no device memory.  The file sorts last, so a run that stops at the
 first failure has already run every other test.
 """
 import ctypes
+import gc
 
 import numpy as np
 import pytest
@@ -65,17 +66,25 @@ def test_noalloc_matches_workspace_entry_point_on_calls_in_a_row():
         ref = tp.tp_linear_rowwise(xs, ws, bias=b, mode="workspace")
         out = torch.full((T, N), float("nan"), dtype=torch.bfloat16, device="cuda")
         torch.cuda.synchronize()
-        free0, alloc0 = _device_free_bytes(), torch.cuda.memory_allocated()
-        if T <= 128:
-            tp.tp_linear_rowwise_noalloc(xs, ws, bias=b, out=out)
-        else:
-            assert _noalloc_raw(xs, ws, b, out) == "TP_OK", tp.tp_last_error()
-        tp.tp_device_status()
+        # Python's collector must not free other tests' tensors inside the measured call:
+        # that would change torch's count of allocated bytes without this call doing anything.
+        gc.collect()
+        gc.disable()
+        try:
+            free0, alloc0 = _device_free_bytes(), torch.cuda.memory_allocated()
+            if T <= 128:
+                tp.tp_linear_rowwise_noalloc(xs, ws, bias=b, out=out)
+            else:
+                assert _noalloc_raw(xs, ws, b, out) == "TP_OK", tp.tp_last_error()
+            tp.tp_device_status()
+            free1, alloc1 = _device_free_bytes(), torch.cuda.memory_allocated()
+        finally:
+            gc.enable()
         if k > 0:
             # After the first call on the device (which may load the module that holds the
             # array), a call claims no device memory at all.
-            assert _device_free_bytes() == free0
-            assert torch.cuda.memory_allocated() == alloc0
+            assert free1 == free0
+            assert alloc1 == alloc0
         assert torch.equal(out.view(torch.int16), ref.view(torch.int16)), f"case {k}: differs from the workspace call"
         assert_close(O.bf16_to_f64(tp.bits_from_bf16(out)), ref_o, f"noalloc call {k} (seed {seed})")
 
