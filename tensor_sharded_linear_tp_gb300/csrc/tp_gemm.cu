@@ -647,9 +647,9 @@ __device__ __forceinline__ void epilogue_chunked(const GemmParams& p, SmemCtrl* 
 // 128 rows.
 // kQuad (with kPair): clusters of two CTA pairs that work on n-adjacent tiles of the same 256
 // rows, so their A tiles are the same: each CTA loads half of its A rows and multicasts them to
-// the CTA in the same position of the other pair, halving the A traffic from L2.  A stage of
+// the CTA in the same position of the other pair, halving the A traffic from L2.  A box of
 // either pair is then written by both pairs' producers, so it is free again only once both
-// pairs' MMAs are done with it (two arrivals on every empty barrier).
+// pairs' MMAs are done with it (two arrivals on every box's empty barrier).
 template <int kEpi, bool kPair, bool kQuad = false>
 __global__ void __launch_bounds__(threads_of(kEpi), 1) tp_gemm_kernel(const __grid_constant__ GemmParams p) {
   using C = Cfg<kPair>;
@@ -1210,7 +1210,9 @@ int choose_group_m(int m_tiles, int64_t a_bytes) {
 // (a stage's fixed cost does not shrink with the width), then the width of its tiles:
 // the 16 x N 3072 out-projection (K 4 x 768) took 58.0 / 54.0 / 64.2 / 72.3 / 80.5 us at
 // widths 256 / 224 / 192 / 160 / 128 (3 / 3 / 4 / 5 / 6 waves of resident CTA pairs;
-// 224 runs as plain pairs on all 152 SMs, 256 as clusters of two pairs on 144).
+// 224 runs as plain pairs on all 152 SMs, 256 as clusters of two pairs on 144), and with a
+// box refilled as soon as its MMAs are done 55.9 / 52.9 us at 256 / 224 (each launch alone
+// after an L2 flush).
 int choose_bn(int64_t n_out, int64_t groups_x_mtiles, int units, bool halves_of_32 = false) {
   static const int kWidths[] = {256, 224, 192, 160, 128};
   int best = 256;
